@@ -1,0 +1,279 @@
+"""CPU oracle for the score -> select -> compact -> decode path (test infrastructure).
+
+This file is test infrastructure.  Only the test-suite, the package smoke
+check and the benchmark's CPU-baseline leg may import it; the library's
+product path never does.  It shares no code with the CUDA implementation:
+plain numpy, float64 arithmetic, one obvious loop per definition, no blocking,
+fusion or reordering beyond what each definition states.
+
+Sources (web pages on KV-cache compression; cited by title and section):
+
+* [Sculpt]  "KVSculpt: KV Cache Compression as Distillation"
+            §1 (eviction keeps a subset chosen by attention scores),
+            §2A (retention zone of the m most recent pairs),
+            §2B (loss with the log-sum-exp l of the attention scores),
+            §2D (budgets that differ per layer and per KV head).
+* [VECTOR]  "A Simple Plug-in for Improving Eviction-Based KV Cache
+            Compression", "Énoncé du Problème" (importance eviction: score
+            tokens, drop the low-score entries).
+* [KVTC]    "KV Cache Transform Coding for Compact Storage in LLM Inference" §2A
+            (attention sinks and the recent sliding window are kept as is).
+* [KVzap]   "KVzap: Fast, Adaptive, and Faithful KV Cache Pruning"
+            §1 (the T axis is the one left to compress; GQA on the H axis),
+            §2.1 (scores built from the attention weight a token receives),
+            §2.2 (linear surrogate h_t in R^{D_h} -> one score per KV head),
+            §2.3 (drop tokens whose score is below tau; keep the w most recent).
+
+Readings taken where the pages are silent (each is listed with its reason in
+the design notes of the repository):
+
+* attention-mass score = sum over the window rows of the row-softmax weight
+  a token receives (sum, not max); causal mask inside the window (window row
+  w sits at position T - W + w); no pooling or smoothing;
+* GQA: query head h belongs to kv head floor(h / G);
+* budget B = floor(keep_ratio * (Hkv * T)) in IEEE double, protected tokens
+  counted inside B, and when the protected set alone exceeds B only the
+  protected set is kept;
+* one pool per unit across its kv heads; order (score desc, token asc,
+  head asc), -0 == +0, NaN ranks below everything;
+* threshold rule: keep iff score >= tau (NaN never kept);
+* decode fidelity: KL(p_comp || p_full) = lse_full - lse_comp, the rel-L2
+  output error ||o_comp - o_full|| / ||o_full||.
+
+Parity pins: every function below is checked in ``tests/test_oracle_pins.py``
+against brute force on tiny inputs, closed forms, invariants and independent
+library routines; none of them is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+F64 = np.float64
+
+
+# ---------------------------------------------------------------- scoring
+def score_attn(q_win, k, scale, head_scale=None, causal=True):
+    """Attention-mass score of every cached token, per (unit, kv head).
+
+    q_win [U, Hq, W, d], k [U, Hkv, T, d] (any float dtype; computed in
+    float64).  For query head h of kv head g = h // G and window row w:
+        s[(h,w), t] = scale * f[u,h] * <q[u,h,w], k[u,g,t]>,  t <= T-W+w if causal
+        p[(h,w), :] = softmax_t(s[(h,w), :])
+        score[u,g,t] = sum_{h in g} sum_w p[(h,w), t]
+    The log-sum-exp lse = m + log(sum exp(s - m)) is the row normaliser
+    ([Sculpt] §2B); [VECTOR] "Énoncé du Problème" and [Sculpt] §1 rank tokens
+    by the attention they receive.  Returns float64 [U, Hkv, T].
+    """
+    q = np.asarray(q_win, dtype=F64)
+    kk = np.asarray(k, dtype=F64)
+    U, Hq, W, d = q.shape
+    _, Hkv, T, _ = kk.shape
+    G = Hq // Hkv
+    hs = None if head_scale is None else np.asarray(head_scale, dtype=F64)
+    out = np.zeros((U, Hkv, T), dtype=F64)
+    for u in range(U):
+        for g in range(Hkv):
+            for i in range(G):
+                h = g * G + i
+                c = scale * (1.0 if hs is None else hs[u, h])
+                logits = c * (q[u, h] @ kk[u, g].T)             # [W, T]
+                if causal:
+                    for w in range(W):
+                        logits[w, T - W + w + 1:] = -np.inf
+                m = logits.max(axis=1, keepdims=True)
+                lse = m + np.log(np.exp(logits - m).sum(axis=1, keepdims=True))
+                out[u, g] += np.exp(logits - lse).sum(axis=0)
+    return out
+
+
+def score_linear(hidden, weight, bias=None):
+    """Linear surrogate score ([KVzap] §2.2): score[u,g,t] = b_g + h[u,t,:] . W[:,g].
+
+    hidden [U, T, Dh], weight [Dh, Hkv], bias [Hkv] or None.  The raw linear
+    output is the score compared with tau (the pages' surrogate predicts a
+    log-score; the threshold is applied to that prediction).
+    Returns float64 [U, Hkv, T].
+    """
+    h = np.asarray(hidden, dtype=F64)
+    wt = np.asarray(weight, dtype=F64)
+    out = np.einsum("utj,jg->ugt", h, wt)
+    if bias is not None:
+        out = out + np.asarray(bias, dtype=F64)[None, :, None]
+    return out
+
+
+# -------------------------------------------------------------- selection
+def protected_mask(T, n_sink, n_recent):
+    """Tokens that are always kept: the first n_sink (attention sinks,
+    [KVTC] §2A) and the last n_recent (sliding window, [KVzap] §2.3 and the
+    retention zone of [Sculpt] §2A)."""
+    t = np.arange(T)
+    return (t < n_sink) | (t >= T - n_recent)
+
+
+def global_budget(keep_ratio, Hkv, T):
+    """B = floor(keep_ratio * (Hkv*T)) with one IEEE-double rounding."""
+    return int(math.floor(float(keep_ratio) * float(Hkv * T)))
+
+
+def _order_key(scores_f32, t_idx, g_idx):
+    """Sort keys for (score desc, token asc, head asc) with NaN last and
+    -0 == +0, suitable for np.lexsort (last key is primary)."""
+    s = scores_f32.astype(F64)
+    isnan = np.isnan(s)
+    neg = np.where(isnan, 0.0, -s) + 0.0      # + 0.0 turns -0.0 into +0.0
+    return (g_idx, t_idx, neg, isnan)
+
+
+def select(scores, mode, keep_ratio=0.0, tau=0.0, head_budget=None,
+           n_sink=0, n_recent=0):
+    """Budget selection over fp32 scores [U, Hkv, T].
+
+    mode "global": per unit, keep the protected set of every head, then fill
+    B_eff - Hkv*|P| slots with the highest non-protected (g, t) across heads
+    ([KVzap] §2.3 fixed budget; [Sculpt] §2D budgets that differ per head).
+    mode "per_head": the same inside each head with budget head_budget[i].
+    mode "threshold": keep t iff score >= tau or t protected ([KVzap] §2.3).
+
+    Returns (kept_idx int32 [U*Hkv, T] padded with -1, counts int32 [U*Hkv],
+    offsets int64 [U*Hkv + 1]); indices of each head are ascending.
+    """
+    s = np.asarray(scores, dtype=np.float32)
+    U, Hkv, T = s.shape
+    n = U * Hkv
+    P = protected_mask(T, n_sink, n_recent)
+    nP = int(P.sum())
+    free_t = np.nonzero(~P)[0]
+    kept = np.full((n, T), -1, dtype=np.int32)
+    counts = np.zeros(n, dtype=np.int32)
+
+    def emit(i, mask_t):
+        idx = np.nonzero(mask_t)[0].astype(np.int32)
+        kept[i, : idx.size] = idx
+        counts[i] = idx.size
+
+    if mode == "threshold":
+        for u in range(U):
+            for g in range(Hkv):
+                emit(u * Hkv + g, P | (s[u, g] >= np.float32(tau)))
+    elif mode == "global":
+        B = global_budget(keep_ratio, Hkv, T)
+        B_eff = min(max(B, Hkv * nP), Hkv * T)
+        need = B_eff - Hkv * nP
+        for u in range(U):
+            tt, gg = np.meshgrid(free_t, np.arange(Hkv), indexing="ij")
+            tt, gg = tt.ravel(), gg.ravel()
+            order = np.lexsort(_order_key(s[u, gg, tt], tt, gg))
+            take = order[:need]
+            chosen = np.zeros((Hkv, T), dtype=bool)
+            chosen[gg[take], tt[take]] = True
+            for g in range(Hkv):
+                emit(u * Hkv + g, P | chosen[g])
+    elif mode == "per_head":
+        hb = np.asarray(head_budget, dtype=np.int64).reshape(n)
+        for u in range(U):
+            for g in range(Hkv):
+                i = u * Hkv + g
+                B_eff = min(max(int(hb[i]), nP), T)
+                need = B_eff - nP
+                zeros = np.zeros(free_t.size, dtype=np.int64)
+                order = np.lexsort(_order_key(s[u, g, free_t], free_t, zeros))
+                chosen = np.zeros(T, dtype=bool)
+                chosen[free_t[order[:need]]] = True
+                emit(i, P | chosen)
+    else:
+        raise ValueError(mode)
+    offsets = np.zeros(n + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts.astype(np.int64))
+    return kept, counts, offsets
+
+
+# ------------------------------------------------------------- compaction
+def compact(k, v, kept_idx, counts, offsets, slack=0):
+    """Gather the kept rows into one variable-length cache.
+
+    Head i = u*Hkv + g owns rows [start_i, start_i + counts_i + slack) with
+    start_i = offsets_i + i*slack; row start_i + j is K[u, g, kept_idx[i, j]]
+    (same for V).  Slack rows are left zero.  Byte-exact copy.
+    Returns (kc, vc, start int64 [n], length int32 [n]).
+    """
+    k = np.asarray(k)
+    v = np.asarray(v)
+    U, Hkv, T, d = k.shape
+    n = U * Hkv
+    total = int(offsets[n]) + n * slack
+    kc = np.zeros((total, d), dtype=k.dtype)
+    vc = np.zeros((total, d), dtype=v.dtype)
+    start = np.zeros(n, dtype=np.int64)
+    for i in range(n):
+        u, g = divmod(i, Hkv)
+        start[i] = int(offsets[i]) + i * slack
+        for j in range(int(counts[i])):
+            kc[start[i] + j] = k[u, g, kept_idx[i, j]]
+            vc[start[i] + j] = v[u, g, kept_idx[i, j]]
+    return kc, vc, start, np.asarray(counts, dtype=np.int32).copy()
+
+
+# ----------------------------------------------------------------- decode
+def decode_attn(q, kc, vc, start, length, k_new=None, v_new=None, scale=1.0):
+    """One decode step over a variable-length cache (GQA).
+
+    If k_new/v_new [U, Hkv, d] are given they are first appended at row
+    start_i + length_i and length_i grows by one (the caller reserved the
+    slack).  Then for query head h of kv head g:
+        s_j = scale * <q[u,h], kc[start+j]>, j < length
+        lse = log sum_j exp(s_j),  o = sum_j exp(s_j - lse) * vc[start+j]
+    The lse is the log-sum-exp of [Sculpt] §2B.  Works on copies; returns
+    (out float64 [U, Hq, d], lse float64 [U, Hq], kc, vc, length).
+    """
+    qq = np.asarray(q, dtype=F64)
+    kc = np.array(kc, copy=True)
+    vc = np.array(vc, copy=True)
+    length = np.array(length, dtype=np.int64, copy=True)
+    U, Hq, d = qq.shape
+    Hkv = length.size // U
+    G = Hq // Hkv
+    out = np.zeros((U, Hq, d), dtype=F64)
+    lse = np.zeros((U, Hq), dtype=F64)
+    for u in range(U):
+        for g in range(Hkv):
+            i = u * Hkv + g
+            s0 = int(start[i])
+            if k_new is not None:
+                kc[s0 + length[i]] = np.asarray(k_new)[u, g]
+                vc[s0 + length[i]] = np.asarray(v_new)[u, g]
+                length[i] += 1
+            L = int(length[i])
+            K = kc[s0: s0 + L].astype(F64)
+            V = vc[s0: s0 + L].astype(F64)
+            for j in range(G):
+                h = g * G + j
+                if L == 0:
+                    lse[u, h] = -np.inf
+                    continue
+                logits = scale * (K @ qq[u, h])
+                m = logits.max()
+                e = np.exp(logits - m)
+                l = e.sum()
+                lse[u, h] = m + math.log(l)
+                out[u, h] = (e / l) @ V
+    return out, lse, kc, vc, length.astype(np.int32)
+
+
+def fidelity(out_comp, out_full, lse_comp, lse_full):
+    """Fidelity probe of a compressed cache against the full one.
+
+    rel_err[u,h] = ||o_comp - o_full||_2 / ||o_full||_2 and
+    kl[u,h] = KL(p_comp || p_full) = lse_full - lse_comp, which equals
+    -log(attention mass the full distribution puts on the kept rows) >= 0.
+    Returns float64 arrays (rel_err, kl) of shape [U, Hq].
+    """
+    oc = np.asarray(out_comp, dtype=F64)
+    of = np.asarray(out_full, dtype=F64)
+    num = np.sqrt(((oc - of) ** 2).sum(axis=-1))
+    den = np.sqrt((of ** 2).sum(axis=-1))
+    rel = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+    kl = np.asarray(lse_full, dtype=F64) - np.asarray(lse_comp, dtype=F64)
+    return rel, kl

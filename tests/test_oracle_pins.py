@@ -1,0 +1,414 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* brute force in pure Python (math.exp, explicit loops in another order),
+* hand-derived closed forms (tests/golden/closed_forms.json, with citations),
+* invariants the definitions imply (rows of a softmax add to one, kept count
+  equals the budget, protected tokens always kept, ...),
+* independent library routines (scipy softmax, torch SDPA in float64),
+* planted mistakes: wrong variants of the oracle must fail these pins.
+"""
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+# ----------------------------------------------------------- brute force
+def brute_score_attn(q, k, scale, head_scale=None, causal=True):
+    """Pure-Python attention mass: token-major loop, explicit normaliser."""
+    U, Hq, W, d = q.shape
+    Hkv, T = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    out = [[[0.0] * T for _ in range(Hkv)] for _ in range(U)]
+    for u in range(U):
+        for h in range(Hq):
+            g = h // G
+            c = scale * (1.0 if head_scale is None else float(head_scale[u][h]))
+            for w in range(W):
+                last = T - W + w if causal else T - 1
+                logit = []
+                for t in range(last + 1):
+                    acc = 0.0
+                    for x in range(d):
+                        acc += float(q[u][h][w][x]) * float(k[u][g][t][x])
+                    logit.append(c * acc)
+                mx = max(logit)
+                z = sum(math.exp(v - mx) for v in logit)
+                for t in range(last + 1):
+                    out[u][g][t] += math.exp(logit[t] - mx) / z
+    return np.array(out)
+
+
+def sort_key(score, t, g):
+    """(score desc, token asc, head asc) with NaN last, -0 == +0."""
+    s = float(score)
+    if math.isnan(s):
+        return (1, 0.0, t, g)
+    return (0, -(s + 0.0), t, g)
+
+
+def brute_select_global(s, keep_ratio, n_sink, n_recent):
+    U, Hkv, T = s.shape
+    prot = [t < n_sink or t >= T - n_recent for t in range(T)]
+    nP = sum(prot)
+    B = math.floor(keep_ratio * (Hkv * T))
+    need = min(max(B, Hkv * nP), Hkv * T) - Hkv * nP
+    res = []
+    for u in range(U):
+        cand = [(sort_key(s[u, g, t], t, g), g, t) for t in range(T) for g in range(Hkv)
+                if not prot[t]]
+        cand.sort()
+        chosen = {(g, t) for _, g, t in cand[:need]}
+        for g in range(Hkv):
+            res.append([t for t in range(T) if prot[t] or (g, t) in chosen])
+    return res
+
+
+def brute_select_per_head(s, budgets, n_sink, n_recent):
+    U, Hkv, T = s.shape
+    prot = [t < n_sink or t >= T - n_recent for t in range(T)]
+    nP = sum(prot)
+    res = []
+    for u in range(U):
+        for g in range(Hkv):
+            b = int(budgets[u * Hkv + g])
+            need = min(max(b, nP), T) - nP
+            cand = sorted((sort_key(s[u, g, t], t, 0), t) for t in range(T) if not prot[t])
+            chosen = {t for _, t in cand[:need]}
+            res.append([t for t in range(T) if prot[t] or t in chosen])
+    return res
+
+
+def kept_lists(kept, counts):
+    return [list(kept[i, : counts[i]]) for i in range(len(counts))]
+
+
+def rng_arrays(seed, *shapes):
+    r = np.random.default_rng(seed)
+    return [r.standard_normal(s) for s in shapes]
+
+
+# -------------------------------------------------------------- scoring
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("with_scale", [True, False])
+def test_score_attn_matches_brute_force(causal, with_scale):
+    q, k = rng_arrays(1, (2, 4, 3, 5), (2, 2, 9, 5))
+    hs = np.random.default_rng(2).uniform(0.5, 2.0, (2, 4)) if with_scale else None
+    got = O.score_attn(q, k, 0.7, hs, causal)
+    ref = brute_score_attn(q, k, 0.7, hs, causal)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("case", ["score_attn_softmax_row", "score_attn_causal_window"])
+def test_score_attn_golden(case):
+    c = GOLD[case]
+    got = O.score_attn(np.array(c["q_win"]), np.array(c["k"]), c["scale"], None, c["causal"])
+    np.testing.assert_allclose(got, np.array(c["score"]), rtol=1e-14)
+
+
+def test_score_attn_rows_sum_to_one():
+    q, k = rng_arrays(3, (3, 8, 16, 16), (3, 2, 200, 16))
+    for causal in (True, False):
+        s = O.score_attn(q, k, 0.25, None, causal)
+        # every window row is a probability distribution -> each kv head
+        # collects exactly G*W units of mass
+        np.testing.assert_allclose(s.sum(axis=-1), 4 * 16, rtol=1e-12)
+        assert (s >= 0).all()
+
+
+def test_score_attn_single_row_is_textbook_softmax():
+    from scipy.special import softmax
+    q, k = rng_arrays(4, (1, 1, 1, 8), (1, 1, 50, 8))
+    got = O.score_attn(q, k, 0.3, None, causal=False)[0, 0]
+    np.testing.assert_allclose(got, softmax(0.3 * (k[0, 0] @ q[0, 0, 0])), rtol=1e-12)
+
+
+def test_score_attn_identical_keys_give_uniform_rows():
+    U, Hq, Hkv, W, T, d = 1, 6, 2, 5, 17, 4
+    q = rng_arrays(5, (U, Hq, W, d))[0]
+    k = np.tile(rng_arrays(6, (d,))[0], (U, Hkv, T, 1))
+    G = Hq // Hkv
+    got = O.score_attn(q, k, 1.0, None, causal=True)
+    ref = np.zeros(T)
+    for w in range(W):
+        n = T - W + w + 1           # tokens visible to window row w
+        ref[:n] += G / n
+    for g in range(Hkv):
+        np.testing.assert_allclose(got[0, g], ref, rtol=1e-12)
+
+
+def test_score_attn_dominant_sink():
+    q = np.ones((1, 2, 4, 8))
+    k = np.zeros((1, 1, 32, 8))
+    k[0, 0, 0] = 10.0                    # logit 80 against 0 for the rest
+    s = O.score_attn(q, k, 1.0, None, causal=True)
+    assert abs(s[0, 0, 0] - 8.0) < 1e-12 and 0 < s[0, 0, 1:].sum() < 1e-30
+
+
+def test_score_linear_matches_loops_and_torch():
+    h, w, b = rng_arrays(7, (2, 11, 13), (13, 3), (3,))
+    got = O.score_linear(h, w, b)
+    for u in range(2):
+        for g in range(3):
+            for t in range(11):
+                ref = b[g] + sum(h[u, t, j] * w[j, g] for j in range(13))
+                assert abs(got[u, g, t] - ref) < 1e-12
+    th = torch.from_numpy(h) @ torch.from_numpy(w) + torch.from_numpy(b)
+    np.testing.assert_allclose(got, th.permute(0, 2, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_threshold_keep_fraction_matches_gaussian_tail():
+    # linear outputs with weight ~ N(0, 1/Dh) are ~ N(0, 1): P(x >= 0.5) = 0.3085
+    from kv_cache_compression_attention_b300 import inputs
+    wl = inputs.WORKLOADS["c4_qwen128k"].with_(T=8192, Dh=512)
+    hid, wt, bias = inputs.linear_scorer(wl)
+    s = O.score_linear(hid.float().numpy(), wt.float().numpy(), bias.numpy())
+    kept, counts, _ = O.select(s.astype(np.float32), "threshold", tau=0.5, n_sink=0, n_recent=0)
+    frac = counts.sum() / s.size
+    assert abs(frac - 0.30854) < 0.01
+
+
+# ------------------------------------------------------------ selection
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("ties,specials", [(False, False), (True, False), (True, True)])
+def test_select_global_matches_brute_force(seed, ties, specials):
+    from kv_cache_compression_attention_b300 import inputs
+    s = inputs.random_scores((2, 3, 23), seed=seed, ties=ties, specials=specials).numpy()
+    for ratio in (0.0, 0.1, 0.37, 0.5, 1.0):
+        kept, counts, offs = O.select(s, "global", keep_ratio=ratio, n_sink=2, n_recent=3)
+        assert kept_lists(kept, counts) == brute_select_global(s, ratio, 2, 3)
+        assert offs[0] == 0 and (np.diff(offs) == counts).all()
+
+
+@pytest.mark.parametrize("case", ["select_global_with_ties", "select_protected_overrides_budget"])
+def test_select_golden(case):
+    c = GOLD[case]
+    s = np.array(c["scores"], dtype=np.float32)
+    for cc in c["cases"]:
+        kept, counts, _ = O.select(s, "global", keep_ratio=cc["keep_ratio"],
+                                   n_sink=c.get("n_sink", 0), n_recent=c.get("n_recent", 0))
+        assert [list(map(int, x)) for x in kept_lists(kept, counts)] == cc["kept"]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_select_per_head_matches_brute_force(seed):
+    from kv_cache_compression_attention_b300 import inputs
+    s = inputs.random_scores((2, 3, 31), seed=10 + seed, ties=True, specials=seed == 2).numpy()
+    budgets = np.random.default_rng(seed).integers(-2, 35, size=6)
+    kept, counts, _ = O.select(s, "per_head", head_budget=budgets, n_sink=1, n_recent=4)
+    assert kept_lists(kept, counts) == brute_select_per_head(s, budgets, 1, 4)
+
+
+def test_select_threshold_exact_set():
+    from kv_cache_compression_attention_b300 import inputs
+    s = inputs.random_scores((2, 2, 40), seed=3, ties=True, specials=True).numpy()
+    tau = 0.5
+    kept, counts, _ = O.select(s, "threshold", tau=tau, n_sink=3, n_recent=5)
+    got = kept_lists(kept, counts)
+    for i in range(4):
+        u, g = divmod(i, 2)
+        ref = [t for t in range(40)
+               if t < 3 or t >= 35 or (not math.isnan(s[u, g, t]) and s[u, g, t] >= tau)]
+        assert got[i] == ref
+
+
+def test_select_invariants_large():
+    from kv_cache_compression_attention_b300 import inputs
+    U, Hkv, T = 3, 8, 4099
+    s = inputs.random_scores((U, Hkv, T), seed=9, ties=True).numpy()
+    n_sink, n_recent, ratio = 4, 64, 0.1
+    kept, counts, offs = O.select(s, "global", keep_ratio=ratio, n_sink=n_sink, n_recent=n_recent)
+    B = math.floor(ratio * Hkv * T)
+    P = set(range(n_sink)) | set(range(T - n_recent, T))
+    for u in range(U):
+        assert counts[u * Hkv:(u + 1) * Hkv].sum() == B
+        kept_free, dropped = [], []
+        for g in range(Hkv):
+            idx = list(kept[u * Hkv + g, : counts[u * Hkv + g]])
+            assert idx == sorted(set(idx))                     # ascending, unique
+            assert P <= set(idx)                                # protected kept
+            ks = set(idx)
+            for t in range(T):
+                if t in P:
+                    continue
+                (kept_free if t in ks else dropped).append(sort_key(s[u, g, t], t, g))
+        assert max(kept_free) < min(dropped)                  # nothing dropped outranks a kept one
+    # heads keep different counts (adaptive per-head budget)
+    assert len(set(counts.tolist())) > 1
+
+
+# ------------------------------------------------------------ compaction
+def test_compact_matches_fancy_indexing():
+    r = np.random.default_rng(11)
+    U, Hkv, T, d = 2, 3, 20, 6
+    k = r.standard_normal((U, Hkv, T, d)).astype(np.float32)
+    v = r.standard_normal((U, Hkv, T, d)).astype(np.float32)
+    s = r.random((U, Hkv, T)).astype(np.float32)
+    kept, counts, offs = O.select(s, "global", keep_ratio=0.3, n_sink=1, n_recent=2)
+    kc, vc, start, length = O.compact(k, v, kept, counts, offs, slack=2)
+    assert kc.shape[0] == offs[-1] + 2 * U * Hkv
+    for i in range(U * Hkv):
+        u, g = divmod(i, Hkv)
+        assert start[i] == offs[i] + 2 * i and length[i] == counts[i]
+        idx = kept[i, : counts[i]]
+        np.testing.assert_array_equal(kc[start[i]: start[i] + counts[i]], k[u, g][idx])
+        np.testing.assert_array_equal(vc[start[i]: start[i] + counts[i]], v[u, g][idx])
+        assert not kc[start[i] + counts[i]: start[i] + counts[i] + 2].any()
+
+
+# ---------------------------------------------------------------- decode
+def sdpa_ref(q, kc, vc, start, length, scale, G):
+    """torch float64 scaled_dot_product_attention per (unit, head)."""
+    U, Hq, d = q.shape
+    out = np.zeros((U, Hq, d))
+    lse = np.zeros((U, Hq))
+    for u in range(U):
+        for h in range(Hq):
+            i = u * (Hq // G) + h // G
+            K = torch.from_numpy(kc[start[i]: start[i] + length[i]].astype(np.float64))
+            V = torch.from_numpy(vc[start[i]: start[i] + length[i]].astype(np.float64))
+            qq = torch.from_numpy(q[u, h].astype(np.float64))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qq[None, None, None], K[None, None], V[None, None], scale=scale)
+            out[u, h] = o[0, 0, 0].numpy()
+            lse[u, h] = torch.logsumexp(scale * (K @ qq), 0).item()
+    return out, lse
+
+
+def test_decode_matches_sdpa_and_appends():
+    r = np.random.default_rng(12)
+    U, Hq, Hkv, d, slack = 2, 8, 2, 16, 1
+    lens = np.array([5, 17, 1, 40])
+    start = np.concatenate([[0], np.cumsum(lens + slack)[:-1]])
+    rows = int((lens + slack).sum())
+    kc = r.standard_normal((rows, d))
+    vc = r.standard_normal((rows, d))
+    q = r.standard_normal((U, Hq, d))
+    kn = r.standard_normal((U, Hkv, d))
+    vn = r.standard_normal((U, Hkv, d))
+    out, lse, kc2, vc2, len2 = O.decode_attn(q, kc, vc, start, lens, kn, vn, scale=0.25)
+    assert (len2 == lens + 1).all()
+    for i in range(U * Hkv):
+        u, g = divmod(i, Hkv)
+        np.testing.assert_array_equal(kc2[start[i] + lens[i]], kn[u, g])
+        np.testing.assert_array_equal(vc2[start[i] + lens[i]], vn[u, g])
+    ref_o, ref_l = sdpa_ref(q, kc2, vc2, start, len2, 0.25, Hq // Hkv)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-12)
+
+
+def test_decode_golden():
+    c = GOLD["decode_append"]
+    out, lse, _, _, len2 = O.decode_attn(np.array(c["q"]), np.array(c["kc"]), np.array(c["vc"]),
+                                         np.array(c["start"]), np.array(c["len"]),
+                                         np.array(c["k_new"]), np.array(c["v_new"]), scale=1.0)
+    np.testing.assert_allclose(out, np.array(c["out"]), rtol=1e-14)
+    np.testing.assert_allclose(lse, np.array(c["lse"]), rtol=1e-14)
+    assert len2[0] == 2
+
+
+def _full_cache(k, v, slack):
+    """Full cache laid out like a compacted one (every token kept)."""
+    U, Hkv, T, d = k.shape
+    kept = np.tile(np.arange(T, dtype=np.int32), (U * Hkv, 1))
+    counts = np.full(U * Hkv, T, dtype=np.int32)
+    offs = np.arange(U * Hkv + 1, dtype=np.int64) * T
+    return O.compact(k, v, kept, counts, offs, slack)
+
+
+def test_keep_ratio_one_is_the_full_cache_and_kl_is_zero():
+    r = np.random.default_rng(13)
+    U, Hq, Hkv, W, T, d = 1, 4, 2, 4, 30, 8
+    q_win = r.standard_normal((U, Hq, W, d))
+    k = r.standard_normal((U, Hkv, T, d))
+    v = r.standard_normal((U, Hkv, T, d))
+    s = O.score_attn(q_win, k, 0.3).astype(np.float32)
+    kept, counts, offs = O.select(s, "global", keep_ratio=1.0, n_sink=1, n_recent=2)
+    kc, vc, st, ln = O.compact(k, v, kept, counts, offs, slack=1)
+    kf, vf, sf, lf = _full_cache(k, v, 1)
+    np.testing.assert_array_equal(kc, kf)
+    q = r.standard_normal((U, Hq, d))
+    kn, vn = r.standard_normal((U, Hkv, d)), r.standard_normal((U, Hkv, d))
+    oc, lc, *_ = O.decode_attn(q, kc, vc, st, ln, kn, vn, 0.3)
+    of, lf2, *_ = O.decode_attn(q, kf, vf, sf, lf, kn, vn, 0.3)
+    np.testing.assert_array_equal(oc, of)
+    err, kl = O.fidelity(oc, of, lc, lf2)
+    assert (err == 0).all() and (kl == 0).all()
+
+
+def test_kl_is_minus_log_retained_mass():
+    r = np.random.default_rng(14)
+    U, Hq, Hkv, W, T, d = 1, 4, 2, 4, 60, 8
+    q_win = r.standard_normal((U, Hq, W, d))
+    k = r.standard_normal((U, Hkv, T, d))
+    v = r.standard_normal((U, Hkv, T, d))
+    s = O.score_attn(q_win, k, 0.3).astype(np.float32)
+    kept, counts, offs = O.select(s, "global", keep_ratio=0.3, n_sink=2, n_recent=4)
+    kc, vc, st, ln = O.compact(k, v, kept, counts, offs)
+    kf, vf, sf, lf = _full_cache(k, v, 0)
+    q = r.standard_normal((U, Hq, d))
+    oc, lc, *_ = O.decode_attn(q, kc, vc, st, ln, None, None, 0.3)
+    of, lfull, *_ = O.decode_attn(q, kf, vf, sf, lf, None, None, 0.3)
+    err, kl = O.fidelity(oc, of, lc, lfull)
+    for h in range(Hq):
+        g = h // 2
+        logits = 0.3 * (k[0, g] @ q[0, h])
+        p = np.exp(logits - logits.max())
+        p /= p.sum()
+        mass = p[kept[g, : counts[g]]].sum()
+        assert abs(kl[0, h] + math.log(mass)) < 1e-12
+        assert kl[0, h] >= 0 and err[0, h] > 0
+
+
+def test_fidelity_golden_and_scaling():
+    c = GOLD["fidelity_kl"]
+    _, kl = O.fidelity(np.ones((1, 1, 2)), np.ones((1, 1, 2)),
+                       np.array([[c["lse_comp"]]]), np.array([[c["lse_full"]]]))
+    assert abs(kl[0, 0] - c["kl"]) < 1e-15
+    o = np.random.default_rng(15).standard_normal((2, 3, 8))
+    err, _ = O.fidelity(1.5 * o, o, np.zeros((2, 3)), np.zeros((2, 3)))
+    np.testing.assert_allclose(err, 0.5, rtol=1e-14)
+
+
+# ------------------------------------------------------ planted mistakes
+def _score_attn_wrong_gqa(q, k, scale, head_scale=None, causal=True):
+    """Planted mistake: query head h read against kv head h % Hkv."""
+    q = np.asarray(q, float)
+    U, Hq, W, d = q.shape
+    Hkv = k.shape[1]
+    perm = [(h % Hkv) * (Hq // Hkv) + h // Hkv for h in range(Hq)]
+    return O.score_attn(q[:, np.argsort(perm)], k, scale, head_scale, causal)
+
+
+def _score_attn_no_causal(q, k, scale, head_scale=None, causal=True):
+    return O.score_attn(q, k, scale, head_scale, causal=False)
+
+
+def _score_attn_no_scale(q, k, scale, head_scale=None, causal=True):
+    return O.score_attn(q, k, 1.0, head_scale, causal)
+
+
+@pytest.mark.parametrize("bad", [_score_attn_wrong_gqa, _score_attn_no_causal, _score_attn_no_scale])
+def test_planted_score_mistakes_are_caught(bad):
+    q, k = rng_arrays(1, (2, 4, 3, 5), (2, 2, 9, 5))
+    ref = brute_score_attn(q, k, 0.7, None, True)
+    assert not np.allclose(bad(q, k, 0.7, None, True), ref, rtol=1e-6)
+
+
+def test_planted_tie_break_mistake_is_caught():
+    # head-asc before token-asc would pick (t1,g0) before (t0,g1)
+    c = GOLD["select_global_with_ties"]
+    s = np.array(c["scores"], dtype=np.float32)
+    U, Hkv, T = s.shape
+    cand = sorted(((-(float(s[0, g, t])), g, t) for g in range(Hkv) for t in range(T)))
+    chosen = {(g, t) for _, g, t in cand[:6]}
+    wrong = [[t for t in range(T) if (g, t) in chosen] for g in range(Hkv)]
+    assert wrong != c["cases"][1]["kept"]
