@@ -1,0 +1,247 @@
+/*
+ * kvc.h -- C ABI of the B300 (sm_103a) KV-cache compression hot path.
+ *
+ * One transformer layer's KV cache goes through four steps:
+ *   score   -> a per-(unit, kv head, token) importance score,
+ *   select  -> a budget (global top-k across heads, per-head top-k, or a
+ *              fixed threshold) that always keeps the sink and recent tokens,
+ *   compact -> a gather of the kept K/V rows into one variable-length cache,
+ *   decode  -> varlen decode attention over that cache (the consumer), plus a
+ *              fidelity probe against full-cache attention.
+ *
+ * Sources, cited by page title and section:
+ *   [Sculpt] "KVSculpt: KV Cache Compression as Distillation"
+ *   [VECTOR] "A Simple Plug-in for Improving Eviction-Based KV Cache Compression"
+ *   [KVTC]   "KV Cache Transform Coding for Compact Storage in LLM Inference"
+ *   [KVzap]  "KVzap: Fast, Adaptive, and Faithful KV Cache Pruning"
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *    library never allocates or frees device memory; steps that need scratch
+ *    take a caller-provided workspace whose size a *_workspace() query gives.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  Nothing synchronises except
+ *    kvc_device_status().
+ *  - Tensors are dense, row-major, innermost dimension last.  Index names:
+ *    U = independent units (batch x layers), Hq / Hkv = query / kv heads,
+ *    G = Hq / Hkv (query head h reads kv head h / G), T = cached tokens,
+ *    W = observation window, d = head dim.  Flat head index i = u*Hkv + g.
+ *  - Return value: KVC_OK, or a negative kvc_status.  Argument errors are
+ *    found on the host before any launch and leave every output untouched.
+ *    Conditions only the device can see (a row index beyond a capacity, a
+ *    bounded wait that gave up) are recorded in a per-device status word that
+ *    kvc_device_status() returns and clears; the kernel skips the bad access
+ *    and finishes.
+ *  - Thread safety: calls on different streams may overlap if their output
+ *    and workspace buffers are disjoint.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum kvc_dtype { KVC_F32 = 0, KVC_BF16 = 1 };
+
+enum kvc_status {
+  KVC_OK = 0,
+  KVC_ERR_INVALID = -1,      /* bad argument (null pointer, size, range)           */
+  KVC_ERR_UNSUPPORTED = -2,  /* valid but not implemented (dtype, head dim, size)  */
+  KVC_ERR_WORKSPACE = -3,    /* workspace smaller than the *_workspace() query     */
+  KVC_ERR_CUDA = -4,         /* a CUDA launch or attribute call failed             */
+  KVC_ERR_TIMEOUT = -5,      /* device: a bounded wait gave up                     */
+  KVC_ERR_RANGE = -6         /* device: an index fell outside a stated capacity    */
+};
+
+enum kvc_select_mode {
+  KVC_SEL_GLOBAL_TOPK = 0,   /* one budget per unit shared by its kv heads         */
+  KVC_SEL_THRESHOLD = 1,     /* keep iff score >= tau                              */
+  KVC_SEL_PER_HEAD = 2       /* one budget per (unit, kv head)                     */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+int kvc_version(void);
+
+/* Static text for a status code; never NULL. */
+const char* kvc_status_string(int status);
+
+/*
+ * Synchronises `stream`, then returns the first device-side error recorded
+ * on the current device since the last call (KVC_OK if none) and clears it.
+ * Returns KVC_ERR_CUDA if the synchronisation itself failed.
+ */
+int kvc_device_status(void* stream);
+
+/* ------------------------------------------------------------------ score */
+
+/* Bytes of workspace kvc_score_attn needs for these sizes (0 if none). */
+size_t kvc_score_attn_workspace(int U, int Hq, int Hkv, int T, int W, int d, int dtype);
+
+/*
+ * Attention-mass score of every cached token ([Sculpt] §1 and [VECTOR]
+ * "Énoncé du Problème": eviction ranks tokens by the attention they receive;
+ * [KVzap] §2.1: a token's score is built from the attention weight it
+ * receives; [Sculpt] §2B: the log-sum-exp normaliser of the attention row).
+ *
+ * For unit u, kv head g, query head h in g and window row w:
+ *   s[(h,w),t]   = scale * f[u,h] * <q_win[u,h,w,:], k[u,g,t,:]>
+ *                  (if causal, only t <= T - W + w: window row w is the
+ *                   query at position T - W + w)
+ *   scores[u,g,t] = sum over h in g, w < W of softmax_t(s[(h,w),:])[t]
+ *
+ * q_win      [U, Hq, W, d]  dtype
+ * k          [U, Hkv, T, d] dtype
+ * head_scale [U, Hq] fp32 temperature factor f, or NULL for all ones
+ * scores     [U, Hkv, T] fp32 (written)
+ * Requires 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}.
+ * dtype KVC_BF16 at d = 128 with G*W in {128, 256} runs on the tensor cores
+ * (tcgen05, TMEM accumulators, TMA); every other supported shape runs on the
+ * SIMT path.  Each unit of scores sums to G*W per kv head (rows are softmaxes).
+ */
+int kvc_score_attn(const void* q_win, const void* k, int dtype,
+                   int U, int Hq, int Hkv, int T, int W, int d,
+                   float scale, const float* head_scale, int causal,
+                   float* scores, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * Linear surrogate score ([KVzap] §2.2: a linear map from the hidden state
+ * h_t in R^{Dh} to one score per kv head):
+ *   scores[u,g,t] = bias[g] + sum_j hidden[u,t,j] * weight[j,g]
+ * hidden [U, T, Dh] dtype; weight [Dh, Hkv] dtype; bias [Hkv] fp32 or NULL;
+ * scores [U, Hkv, T] fp32.  Accumulates in fp32.  Requires Dh % 8 == 0 and
+ * 1 <= Hkv <= 8.
+ */
+int kvc_score_linear(const void* hidden, const void* weight, const float* bias,
+                     int dtype, int U, int T, int Dh, int Hkv,
+                     float* scores, void* stream);
+
+/* ----------------------------------------------------------------- select */
+
+/* Bytes of workspace kvc_select needs (currently 0 for every mode). */
+size_t kvc_select_workspace(int U, int Hkv, int T, int mode);
+
+/*
+ * Budget selection ([KVzap] §2.3: fixed budget "keep exactly x%" or a fixed
+ * threshold tau with the w most recent tokens always kept; [KVTC] §2A and
+ * [Sculpt] §2A: sinks and the recent window are never compressed; [Sculpt]
+ * §2D: heads of one layer end up with different budgets).
+ *
+ * Protected set P = {t < n_sink} U {t >= T - n_recent}, kept in every head.
+ *  GLOBAL_TOPK: per unit, B = floor(keep_ratio * (Hkv*T)) computed in IEEE
+ *    double; B_eff = min(max(B, Hkv*|P|), Hkv*T).  The unit keeps P in every
+ *    head plus the B_eff - Hkv*|P| highest non-protected (g, t), ordered by
+ *    (score desc, t asc, g asc); -0 == +0; NaN ranks below -inf.
+ *  PER_HEAD: the same inside each head with B_eff = min(max(head_budget[i],
+ *    |P|), T).
+ *  THRESHOLD: keep t iff t in P or scores[u,g,t] >= tau (NaN never kept).
+ *
+ * scores      [U, Hkv, T] fp32
+ * head_budget [U*Hkv] int32 (PER_HEAD only, else ignored / may be NULL)
+ * kept_idx    [U*Hkv, T] int32 (written): row i holds counts[i] ascending
+ *             token indices; entries past counts[i] are left untouched.
+ * counts      [U*Hkv] int32 (written)
+ * offsets     [U*Hkv + 1] int64 (written): exclusive prefix sum of counts.
+ * Requires 0 <= keep_ratio <= 1 (GLOBAL_TOPK), n_sink, n_recent >= 0,
+ * Hkv*T <= 2^20 per selection pool (GLOBAL_TOPK pools a unit's heads).
+ * Selection decisions are taken on the fp32 bits of the scores, so the
+ * result is exact and deterministic.
+ */
+int kvc_select(const float* scores, int U, int Hkv, int T, int mode,
+               double keep_ratio, float tau, const int32_t* head_budget,
+               int n_sink, int n_recent,
+               int32_t* kept_idx, int32_t* counts, int64_t* offsets,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------- compact */
+
+/*
+ * Gather-compaction of the kept rows into one variable-length cache
+ * ([Sculpt] §1: eviction keeps a subset of the original pairs).  Head i owns
+ * rows [start[i], start[i] + counts[i] + slack_per_head) of kc / vc with
+ *   start[i] = offsets[i] + i * slack_per_head,
+ *   kc[start[i] + j, :] = k[u, g, kept_idx[i, j], :]  (same for v), j < counts[i].
+ * Slack rows are not written: decode appends new tokens there.
+ *
+ * k, v     [U, Hkv, T, d] dtype (a byte copy: any dtype of the enum)
+ * kept_idx [U*Hkv, T] int32, counts [U*Hkv] int32, offsets [U*Hkv+1] int64
+ *          as written by kvc_select.
+ * kc, vc   [capacity_rows, d] dtype; capacity_rows must be at least
+ *          offsets[U*Hkv] + U*Hkv*slack_per_head (the device checks every
+ *          row and records KVC_ERR_RANGE instead of writing past it).
+ * start    [U*Hkv] int64 (written), len [U*Hkv] int32 (written = counts).
+ * Requires d * element size to be a multiple of 16 bytes and 16-byte aligned
+ * k, v, kc, vc.
+ */
+int kvc_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, int d,
+                const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
+                int slack_per_head, void* kc, void* vc, int64_t capacity_rows,
+                int64_t* start, int32_t* len, void* stream);
+
+/* ----------------------------------------------------------------- decode */
+
+/* Bytes of workspace kvc_decode_attn needs when no head holds more than
+ * max_len rows (counting the appended one). */
+size_t kvc_decode_workspace(int U, int Hq, int Hkv, int d, int max_len, int dtype);
+
+/*
+ * One decode step of varlen attention over a compressed cache, GQA
+ * ([KVzap] §2.3: pruning sits after attention and works in decode; [Sculpt]
+ * §2B: output and log-sum-exp of the attention row).
+ *
+ * If k_new and v_new are non-NULL they are appended first: row
+ * start[i] + len[i] of kc / vc receives k_new[u,g,:] / v_new[u,g,:] and
+ * len[i] grows by one (the caller reserved that slack row).  Then, with
+ * L = len[i] after the append and rows j < L of head i:
+ *   lse[u,h] = log sum_j exp(scale * <q[u,h,:], kc[start[i]+j,:]>)
+ *   out[u,h,:] = sum_j exp(scale * <q, kc_j> - lse[u,h]) * vc[start[i]+j,:]
+ * A head with L = 0 gets out = 0 and lse = -inf.
+ *
+ * q      [U, Hq, d] dtype; k_new, v_new [U, Hkv, d] dtype or both NULL
+ * kc, vc pool rows [*, d] dtype; start [U*Hkv] int64; len [U*Hkv] int32
+ *        (read, and incremented when appending)
+ * max_len upper bound on any len[i] after the append (sizes the split-K
+ *        grid; rows beyond it are reported as KVC_ERR_RANGE and ignored)
+ * out    [U, Hq, d] dtype (written, fp32 accumulate, round-to-nearest-even)
+ * lse    [U, Hq] fp32 natural-log log-sum-exp, or NULL
+ * Requires d in {64, 128}, G <= 8.
+ */
+int kvc_decode_attn(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len,
+                    const void* k_new, const void* v_new, int dtype,
+                    int U, int Hq, int Hkv, int d, int max_len, float scale,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Fidelity probe of a compressed cache against the full one, per (unit, q
+ * head) ([Sculpt] §4 measures fidelity as a KL divergence):
+ *   rel_err = ||out_comp - out_full||_2 / ||out_full||_2 (0/0 -> 0)
+ *   kl      = KL(p_comp || p_full) = lse_full - lse_comp
+ * (the second identity holds because the compressed rows are a subset of
+ * the full rows; it equals -log of the attention mass the full softmax puts
+ * on the kept rows).
+ * out_* [n, d] dtype; lse_* [n] fp32; rel_err, kl [n] fp32 (written).
+ */
+int kvc_fidelity(const void* out_comp, const void* out_full,
+                 const float* lse_comp, const float* lse_full, int dtype,
+                 int n, int d, float* rel_err, float* kl, void* stream);
+
+/* -------------------------------------------------------------- self-test */
+
+/*
+ * Runs one kernel whose bounded wait is made to run out: it waits on an
+ * mbarrier nothing arrives on, gives up after timeout_ns nanoseconds,
+ * records KVC_ERR_TIMEOUT in the device status word and returns.  Lets a
+ * test check the timeout path of the kernels' waits without hanging a GPU.
+ */
+int kvc_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */

@@ -1,0 +1,194 @@
+"""Thin ctypes binding of libkvc (C ABI in include/kvc.h).
+
+Functions carry the C names and only marshal arguments: torch tensors become
+device pointers, the current torch CUDA stream becomes the cudaStream_t, and
+a non-zero status becomes a ``KvcError``.  Every step of the path runs in the
+library's CUDA kernels; there is no fallback -- importing this module on a
+machine without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvc.so")
+
+KVC_F32, KVC_BF16 = 0, 1
+KVC_SEL_GLOBAL_TOPK, KVC_SEL_THRESHOLD, KVC_SEL_PER_HEAD = 0, 1, 2
+MODES = {"global": KVC_SEL_GLOBAL_TOPK, "threshold": KVC_SEL_THRESHOLD,
+         "per_head": KVC_SEL_PER_HEAD}
+
+STATUS = {0: "KVC_OK", -1: "KVC_ERR_INVALID", -2: "KVC_ERR_UNSUPPORTED",
+          -3: "KVC_ERR_WORKSPACE", -4: "KVC_ERR_CUDA", -5: "KVC_ERR_TIMEOUT",
+          -6: "KVC_ERR_RANGE"}
+
+# symbol -> (restype, argtypes)
+_P, _I, _I64, _SZ, _D, _F, _U64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                   ctypes.c_size_t, ctypes.c_double, ctypes.c_float,
+                                   ctypes.c_uint64)
+SIGNATURES = {
+    "kvc_version": (_I, []),
+    "kvc_status_string": (ctypes.c_char_p, [_I]),
+    "kvc_device_status": (_I, [_P]),
+    "kvc_score_attn_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "kvc_score_attn": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P]),
+    "kvc_score_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "kvc_select_workspace": (_SZ, [_I, _I, _I, _I]),
+    "kvc_select": (_I, [_P, _I, _I, _I, _I, _D, _F, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "kvc_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P]),
+    "kvc_decode_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "kvc_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                             _P, _SZ, _P]),
+    "kvc_fidelity": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "kvc_selftest_wait_timeout": (_I, [_U64, _P]),
+}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libkvc.so not built ({path}); run "
+                          "`python -m kv_cache_compression_attention_b300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load()
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("kvc kernels take CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("kvc kernels take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KVC_F32
+    if t.dtype == torch.bfloat16:
+        return KVC_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise KvcError(fn, rc)
+
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------- entry points
+def kvc_score_attn(q_win, k, scores, scale, head_scale=None, causal=True, workspace=None,
+                   stream=None):
+    U, Hq, W, d = q_win.shape
+    _, Hkv, T, _ = k.shape
+    dt = _dtype(k)
+    need = lib().kvc_score_attn_workspace(U, Hq, Hkv, T, W, d, dt)
+    if workspace is None:
+        workspace = _workspace(need, k.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_score_attn(_ptr(q_win), _ptr(k), dt, U, Hq, Hkv, T, W, d, float(scale),
+                              _ptr(head_scale), int(bool(causal)), _ptr(scores),
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _check("kvc_score_attn", rc)
+    return scores
+
+
+def kvc_score_linear(hidden, weight, bias, scores, stream=None):
+    U, T, Dh = hidden.shape
+    Hkv = weight.shape[1]
+    rc = lib().kvc_score_linear(_ptr(hidden), _ptr(weight), _ptr(bias), _dtype(hidden), U, T, Dh,
+                                Hkv, _ptr(scores), _stream(stream))
+    _check("kvc_score_linear", rc)
+    return scores
+
+
+def kvc_select(scores, mode, kept_idx, counts, offsets, keep_ratio=0.0, tau=0.0,
+               head_budget=None, n_sink=0, n_recent=0, stream=None):
+    U, Hkv, T = scores.shape
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    rc = lib().kvc_select(_ptr(scores), U, Hkv, T, m, float(keep_ratio), float(tau),
+                          _ptr(head_budget), int(n_sink), int(n_recent), _ptr(kept_idx),
+                          _ptr(counts), _ptr(offsets), None, 0, _stream(stream))
+    _check("kvc_select", rc)
+
+
+def kvc_compact(k, v, kept_idx, counts, offsets, kc, vc, start, length, slack=0, stream=None):
+    U, Hkv, T, d = k.shape
+    rc = lib().kvc_compact(_ptr(k), _ptr(v), _dtype(k), U, Hkv, T, d, _ptr(kept_idx),
+                           _ptr(counts), _ptr(offsets), int(slack), _ptr(kc), _ptr(vc),
+                           kc.shape[0], _ptr(start), _ptr(length), _stream(stream))
+    _check("kvc_compact", rc)
+
+
+def kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype=KVC_BF16) -> int:
+    return lib().kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype)
+
+
+def kvc_decode_attn(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,
+                    max_len=None, scale=None, workspace=None, stream=None):
+    U, Hq, d = q.shape
+    Hkv = start.numel() // U
+    if max_len is None:
+        raise ValueError("max_len is required (upper bound of any head's length)")
+    if scale is None:
+        scale = d ** -0.5
+    dt = _dtype(q)
+    need = lib().kvc_decode_workspace(U, Hq, Hkv, d, int(max_len), dt)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_decode_attn(_ptr(q), _ptr(kc), _ptr(vc), _ptr(start), _ptr(length),
+                               _ptr(k_new), _ptr(v_new), dt, U, Hq, Hkv, d, int(max_len),
+                               float(scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                               _stream(stream))
+    _check("kvc_decode_attn", rc)
+
+
+def kvc_fidelity(out_comp, out_full, lse_comp, lse_full, rel_err, kl, stream=None):
+    d = out_comp.shape[-1]
+    n = out_comp.numel() // d
+    rc = lib().kvc_fidelity(_ptr(out_comp), _ptr(out_full), _ptr(lse_comp), _ptr(lse_full),
+                            _dtype(out_comp), n, d, _ptr(rel_err), _ptr(kl), _stream(stream))
+    _check("kvc_fidelity", rc)
+
+
+def kvc_device_status(stream=None) -> int:
+    return lib().kvc_device_status(_stream(stream))
+
+
+def kvc_selftest_wait_timeout(timeout_ns: int, stream=None):
+    _check("kvc_selftest_wait_timeout", lib().kvc_selftest_wait_timeout(int(timeout_ns),
+                                                                        _stream(stream)))

@@ -1,0 +1,228 @@
+// C ABI entry points: host-side validation, workspace sizing and dispatch.
+#include <math.h>
+#include <mutex>
+
+#include "kvc_internal.cuh"
+
+namespace {
+
+__device__ int g_status_word;   // one per device that loads the library
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+kvc::Dev g_devs[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+namespace kvc {
+
+int device_info(Dev* out) {
+  int dev = 0;
+  KVC_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return KVC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_dev_ready[dev]) {
+    Dev d;
+    d.device = dev;
+    KVC_CUDA_TRY(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    KVC_CUDA_TRY(cudaDeviceGetAttribute(&d.max_smem_optin,
+                                        cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    void* p = nullptr;
+    KVC_CUDA_TRY(cudaGetSymbolAddress(&p, g_status_word));
+    d.status = static_cast<int*>(p);
+    g_devs[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  *out = g_devs[dev];
+  return KVC_OK;
+}
+
+}  // namespace kvc
+
+using kvc::Dev;
+
+extern "C" {
+
+int kvc_version(void) { return 100; }
+
+const char* kvc_status_string(int status) {
+  switch (status) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KVC_ERR_WORKSPACE: return "workspace too small";
+    case KVC_ERR_CUDA: return "CUDA error";
+    case KVC_ERR_TIMEOUT: return "device wait timed out";
+    case KVC_ERR_RANGE: return "device index outside the stated capacity";
+    default: return "unknown status";
+  }
+}
+
+int kvc_device_status(void* stream) {
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  KVC_CUDA_TRY(cudaStreamSynchronize(kvc::as_stream(stream)));
+  int v = 0;
+  KVC_CUDA_TRY(cudaMemcpy(&v, dev.status, sizeof(int), cudaMemcpyDeviceToHost));
+  int zero = 0;
+  KVC_CUDA_TRY(cudaMemcpy(dev.status, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  return v;
+}
+
+// ------------------------------------------------------------------ score
+size_t kvc_score_attn_workspace(int U, int Hq, int Hkv, int T, int W, int d, int dtype) {
+  if (U <= 0 || Hq <= 0 || W <= 0) return 0;
+  if (kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d)) return 0;
+  return kvc::score_attn_simt_ws(U, Hq, W);
+}
+
+int kvc_score_attn(const void* q_win, const void* k, int dtype, int U, int Hq, int Hkv,
+                   int T, int W, int d, float scale, const float* head_scale, int causal,
+                   float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q_win || !k || !scores) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || W <= 0 || Hq % Hkv) return KVC_ERR_INVALID;
+  if (W > T || !isfinite(scale)) return KVC_ERR_INVALID;
+  if (d != 64 && d != 128) return KVC_ERR_UNSUPPORTED;
+  if ((int64_t)U * Hkv > 65535 || (int64_t)U * Hq * W > (1ll << 31)) return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  if (kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d) && aligned16(q_win) && aligned16(k))
+    return kvc::score_attn_tc(q_win, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores,
+                              dev, kvc::as_stream(stream));
+  size_t need = kvc::score_attn_simt_ws(U, Hq, W);
+  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+  return kvc::score_attn_simt(q_win, k, dtype, U, Hq, Hkv, T, W, d, scale, head_scale, causal,
+                              scores, static_cast<float*>(workspace), dev,
+                              kvc::as_stream(stream));
+}
+
+int kvc_score_linear(const void* hidden, const void* weight, const float* bias, int dtype,
+                     int U, int T, int Dh, int Hkv, float* scores, void* stream) {
+  if (!hidden || !weight || !scores) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || T <= 0 || Dh <= 0 || Hkv <= 0) return KVC_ERR_INVALID;
+  if (Dh % 8 || Hkv > 8 || !aligned16(hidden)) return KVC_ERR_UNSUPPORTED;
+  if ((int64_t)Dh * Hkv * 4 > 96 * 1024) return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::score_linear_launch(hidden, weight, bias, dtype, U, T, Dh, Hkv, scores, dev,
+                                  kvc::as_stream(stream));
+}
+
+// ----------------------------------------------------------------- select
+size_t kvc_select_workspace(int U, int Hkv, int T, int mode) { return 0; }
+
+int kvc_select(const float* scores, int U, int Hkv, int T, int mode, double keep_ratio,
+               float tau, const int32_t* head_budget, int n_sink, int n_recent,
+               int32_t* kept_idx, int32_t* counts, int64_t* offsets, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (!scores || !kept_idx || !counts || !offsets) return KVC_ERR_INVALID;
+  if (U <= 0 || Hkv <= 0 || T <= 0 || n_sink < 0 || n_recent < 0) return KVC_ERR_INVALID;
+  if (mode != KVC_SEL_GLOBAL_TOPK && mode != KVC_SEL_THRESHOLD && mode != KVC_SEL_PER_HEAD)
+    return KVC_ERR_INVALID;
+  if (mode == KVC_SEL_GLOBAL_TOPK && !(keep_ratio >= 0.0 && keep_ratio <= 1.0))
+    return KVC_ERR_INVALID;
+  if (mode == KVC_SEL_PER_HEAD && !head_budget) return KVC_ERR_INVALID;
+  int64_t pool = (mode == KVC_SEL_GLOBAL_TOPK) ? (int64_t)Hkv * T : (int64_t)T;
+  if (pool > (1ll << 20) || (int64_t)U * Hkv > (1ll << 24)) return KVC_ERR_UNSUPPORTED;
+  // protected set size |P| (the two ranges may overlap when T is small)
+  int64_t ns = n_sink < T ? n_sink : T;
+  int64_t rs = T - (int64_t)n_recent;           // first recent token
+  if (rs < 0) rs = 0;
+  int64_t nP = ns + (T - rs) - (rs < ns ? ns - rs : 0);
+  int64_t need = 0;
+  if (mode == KVC_SEL_GLOBAL_TOPK) {
+    int64_t total = (int64_t)Hkv * T;
+    int64_t B = (int64_t)floor(keep_ratio * (double)total);
+    int64_t Beff = B < Hkv * nP ? Hkv * nP : B;
+    if (Beff > total) Beff = total;
+    need = Beff - Hkv * nP;
+  }
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::select_launch(scores, U, Hkv, T, mode, need, tau, head_budget, (int)ns,
+                            (int)(T - rs), kept_idx, counts, offsets, dev,
+                            kvc::as_stream(stream));
+}
+
+// ---------------------------------------------------------------- compact
+int kvc_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, int d,
+                const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
+                int slack_per_head, void* kc, void* vc, int64_t capacity_rows,
+                int64_t* start, int32_t* len, void* stream) {
+  if (!k || !v || !kept_idx || !counts || !offsets || !kc || !vc || !start || !len)
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hkv <= 0 || T <= 0 || d <= 0 || slack_per_head < 0 || capacity_rows < 0)
+    return KVC_ERR_INVALID;
+  int64_t row_bytes = (int64_t)d * (int64_t)kvc::elt_size(dtype);
+  if (row_bytes % 16 || row_bytes > 4096) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc))
+    return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::compact_launch(k, v, (int)row_bytes, U, Hkv, T, kept_idx, counts, offsets,
+                             slack_per_head, kc, vc, capacity_rows, start, len, dev,
+                             kvc::as_stream(stream));
+}
+
+// ----------------------------------------------------------------- decode
+size_t kvc_decode_workspace(int U, int Hq, int Hkv, int d, int max_len, int dtype) {
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || max_len < 0) return 0;
+  return kvc::decode_ws_bytes(U, Hq, Hkv, d, max_len);
+}
+
+int kvc_decode_attn(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len,
+                    const void* k_new, const void* v_new, int dtype, int U, int Hq, int Hkv,
+                    int d, int max_len, float scale, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!q || !kc || !vc || !start || !len || !out) return KVC_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_len < 0 || !isfinite(scale))
+    return KVC_ERR_INVALID;
+  if (d != 64 && d != 128) return KVC_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8 || (int64_t)U * Hkv > 65535) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(kc) || !aligned16(vc) || !aligned16(q)) return KVC_ERR_UNSUPPORTED;
+  size_t need = kvc::decode_ws_bytes(U, Hq, Hkv, d, max_len);
+  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::decode_launch(q, kc, vc, start, len, k_new, v_new, dtype, U, Hq, Hkv, d, max_len,
+                            scale, out, lse, static_cast<float*>(workspace), dev,
+                            kvc::as_stream(stream));
+}
+
+int kvc_fidelity(const void* out_comp, const void* out_full, const float* lse_comp,
+                 const float* lse_full, int dtype, int n, int d, float* rel_err, float* kl,
+                 void* stream) {
+  if (!out_comp || !out_full || !lse_comp || !lse_full || !rel_err || !kl)
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (n <= 0 || d <= 0 || d > 1024) return KVC_ERR_INVALID;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::fidelity_launch(out_comp, out_full, lse_comp, lse_full, dtype, n, d, rel_err, kl,
+                              dev, kvc::as_stream(stream));
+}
+
+int kvc_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns > 10000000000ull) return KVC_ERR_INVALID;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::selftest_wait_launch(timeout_ns, dev, kvc::as_stream(stream));
+}
+
+}  // extern "C"

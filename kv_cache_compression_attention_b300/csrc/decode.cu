@@ -1,0 +1,343 @@
+// Varlen split-K decode attention over a compressed cache, with append.
+//
+// Definition (KVSculpt §2B: attention output and its log-sum-exp; KVzap
+// §2.3: pruning sits after attention and also runs while decoding): for
+// head i = u*Hkv + g with rows j < L of the pool starting at start_i, and
+// each of its G query heads h,
+//   lse_h = log sum_j exp(scale <q_h, k_j>),  o_h = sum_j exp(scale <q_h,k_j> - lse_h) v_j.
+//
+// The step streams every cached K/V row once from HBM (bandwidth bound; the
+// G query heads of a kv head share each row, 4*d flops per 2*d bytes at
+// G = 4), so it runs on the SIMT cores:
+//   partial  grid (chunks of 512 rows, heads): each CTA's 4 warps take
+//            16-row groups; K rows are read by 8-lane teams (16-byte
+//            coalesced loads), the 8 partial dot products are reduced by
+//            xor-shuffles, an online softmax (base 2) keeps (m, l) per head,
+//            and each lane accumulates d/32 output columns of all G heads
+//            from the V rows.  The 4 warps merge through shared memory and
+//            the CTA writes (m, l, acc[d]) per query head to the workspace.
+//   combine  one CTA per kv head: merges the chunks by their maxima, adds
+//            the appended token (from k_new / v_new, not from the pool, so
+//            no CTA of this step reads a row another one writes), writes out
+//            and lse, then appends k_new / v_new at row start_i + L and
+//            bumps len.
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kChunk = 512;     // rows per partial CTA
+constexpr int kGroup = 16;      // rows per warp step
+constexpr int kWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename Tin> struct Elt;
+template <> struct Elt<float> {
+  static __device__ __forceinline__ float get(const float* p, int x) { return p[x]; }
+  static __device__ __forceinline__ void put(float* p, int x, float v) { p[x] = v; }
+};
+template <> struct Elt<uint16_t> {
+  static __device__ __forceinline__ float get(const uint16_t* p, int x) {
+    return __uint_as_float(((uint32_t)p[x]) << 16);
+  }
+  static __device__ __forceinline__ void put(uint16_t* p, int x, float v) { p[x] = f2bf16_rne(v); }
+};
+
+// N consecutive elements held packed in registers (bf16: two per word) and
+// loaded with 16/8/4-byte vector loads through the read-only path.
+template <typename Tin, int N>
+struct Raw {
+  static constexpr int kWords = N * (int)sizeof(Tin) / 4;
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const Tin* p) {
+    if constexpr (kWords % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < kWords / 4; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    } else if constexpr (kWords == 2) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+      w[0] = v.x; w[1] = v.y;
+    } else {
+      static_assert(kWords == 1, "vector width");
+      w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = 0u;
+  }
+  __device__ __forceinline__ float operator[](int x) const {
+    if constexpr (sizeof(Tin) == 2) return (x & 1) ? bf16hi(w[x >> 1]) : bf16lo(w[x >> 1]);
+    else return __uint_as_float(w[x]);
+  }
+};
+
+template <typename Tin, int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
+                      const Tin* __restrict__ vc, const int64_t* __restrict__ start,
+                      const int32_t* __restrict__ len, int Hkv, int max_chunks, float scale_log2,
+                      float* __restrict__ ws) {
+  constexpr int DPL = D / 8;     // q.k dims per lane (8 lanes per row)
+  constexpr int VPL = D / 32;    // output dims per lane
+  __shared__ float p_sm[kWarps][kGroup][G];
+  __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
+  __shared__ float acc_sm[kWarps][G][D];
+
+  const int i = blockIdx.y, c = blockIdx.x;
+  const int L = len[i];
+  const int rb = c * kChunk;
+  if (rb >= L) return;
+  const int re = min(L, rb + kChunk);
+  const int u = i / Hkv, g = i - u * Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r8 = lane >> 3, sub = lane & 7;
+  const Tin* kbase = kc + start[i] * D;
+  const Tin* vbase = vc + start[i] * D;
+
+  float qr[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    Raw<Tin, DPL> rq;
+    rq.load(q + ((int64_t)u * Hkv * G + (int64_t)g * G + h) * D + sub * DPL);
+#pragma unroll
+    for (int x = 0; x < DPL; ++x) qr[h][x] = rq[x];
+  }
+
+  float m[G], l[G], acc[G][VPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY; l[h] = 0.0f;
+#pragma unroll
+    for (int x = 0; x < VPL; ++x) acc[h][x] = 0.0f;
+  }
+
+  for (int g0 = rb + warp * kGroup; g0 < re; g0 += kWarps * kGroup) {
+    // issue every load of the 16-row group first: K by 8-lane teams (pass p
+    // covers rows g0 + 4p + r8), V by the whole warp (lane owns d/32 columns)
+    Raw<Tin, DPL> kr[4];
+    Raw<Tin, VPL> vr[kGroup];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int row = g0 + 4 * p + r8;
+      if (row < re) kr[p].load(kbase + (int64_t)row * D + sub * DPL);
+      else kr[p].zero();
+    }
+#pragma unroll
+    for (int rr = 0; rr < kGroup; ++rr) {
+      if (g0 + rr < re) vr[rr].load(vbase + (int64_t)(g0 + rr) * D + lane * VPL);
+      else vr[rr].zero();
+    }
+    float s[4][G];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int row = g0 + 4 * p + r8;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float a = 0.0f;
+#pragma unroll
+        for (int x = 0; x < DPL; ++x) a = fmaf(qr[h][x], kr[p][x], a);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        s[p][h] = (row < re) ? a * scale_log2 : -INFINITY;
+      }
+    }
+    // online softmax update (base 2), identical in all lanes
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float mx = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(m[h], mx);
+      const float alpha = exp2f(m[h] - mn);     // m = -inf at start -> 0
+      m[h] = mn;
+      l[h] *= alpha;
+#pragma unroll
+      for (int x = 0; x < VPL; ++x) acc[h][x] *= alpha;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float e = exp2f(s[p][h] - mn);
+        l[h] += e;                               // summed over the 4 row teams at the end
+        if (sub == 0) p_sm[warp][4 * p + r8][h] = e;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int rr = 0; rr < kGroup; ++rr) {
+      // rows past the end carry p = 0 and zeroed V
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pw = p_sm[warp][rr][h];
+#pragma unroll
+        for (int x = 0; x < VPL; ++x) acc[h][x] = fmaf(pw, vr[rr][x], acc[h][x]);
+      }
+    }
+    __syncwarp();
+  }
+  // l: each 8-lane team summed its own rows -> add the 4 teams
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) { m_sm[warp][h] = m[h]; l_sm[warp][h] = l[h]; }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int x = 0; x < VPL; ++x) acc_sm[warp][h][lane * VPL + x] = acc[h][x];
+  __syncthreads();
+  // merge the warps: thread -> (h, column block)
+  float* out = ws + ((int64_t)i * max_chunks + c) * G * (D + 2);
+  for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
+    const int h = e / D, x = e - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, m_sm[w][h]);
+    float a = 0.0f, lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = (m_sm[w][h] == -INFINITY) ? 0.0f : exp2f(m_sm[w][h] - M);
+      a += acc_sm[w][h][x] * f;
+      lsum += l_sm[w][h] * f;
+    }
+    out[h * (D + 2) + x] = a;
+    if (x == 0) { out[h * (D + 2) + D] = M; out[h * (D + 2) + D + 1] = lsum; }
+  }
+}
+
+template <typename Tin, int D, int G>
+__global__ void __launch_bounds__(D)
+decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __restrict__ vc,
+                      const int64_t* __restrict__ start, int32_t* __restrict__ len,
+                      const Tin* __restrict__ k_new, const Tin* __restrict__ v_new, int n_heads,
+                      int Hkv, int max_chunks, float scale_log2, const float* __restrict__ ws,
+                      Tin* __restrict__ out, float* __restrict__ lse, int* status) {
+  __shared__ float red[D / 32][G];
+  const int i = blockIdx.x;
+  const int u = i / Hkv, g = i - u * Hkv;
+  const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
+  const int L = len[i];
+  int nch = (L + kChunk - 1) / kChunk;
+  if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
+  const bool append = k_new != nullptr;
+  bool room = append;
+  if (append && i + 1 < n_heads && start[i] + L >= start[i + 1]) {
+    if (x == 0) report(status, KVC_ERR_RANGE);
+    room = false;
+  }
+  const int64_t nrow = (int64_t)u * Hkv + g;
+  const float kn = append ? Elt<Tin>::get(k_new + nrow * D, x) : 0.0f;
+  const float vn = append ? Elt<Tin>::get(v_new + nrow * D, x) : 0.0f;
+  // appended-token scores for the G heads
+  float snew[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float a = append ? Elt<Tin>::get(q + (nrow * G + h) * D, x) * kn : 0.0f;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (lane == 0) red[warp][h] = a;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) a += red[w][h];
+    snew[h] = a * scale_log2;
+  }
+  const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float M = append ? snew[h] : -INFINITY;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, base[(c * G + h) * (D + 2) + D]);
+    float a = 0.0f, lsum = 0.0f;
+    for (int c = 0; c < nch; ++c) {
+      const float* pc = base + (c * G + h) * (D + 2);
+      const float mc = pc[D];
+      const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
+      a += pc[x] * f;
+      lsum += pc[D + 1] * f;
+    }
+    if (append) {
+      const float f = exp2f(snew[h] - M);
+      a += vn * f;
+      lsum += f;
+    }
+    const int64_t orow = nrow * G + h;
+    Elt<Tin>::put(out + orow * D, x, lsum > 0.0f ? a / lsum : 0.0f);
+    if (lse && x == 0) lse[orow] = lsum > 0.0f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();                      // every thread has read len[i] and the pool
+  if (room) {
+    const int64_t row = start[i] + L;
+    if (sizeof(Tin) == 2) {
+      reinterpret_cast<uint16_t*>(kc)[row * D + x] = reinterpret_cast<const uint16_t*>(k_new)[nrow * D + x];
+      reinterpret_cast<uint16_t*>(vc)[row * D + x] = reinterpret_cast<const uint16_t*>(v_new)[nrow * D + x];
+    } else {
+      reinterpret_cast<float*>(kc)[row * D + x] = reinterpret_cast<const float*>(k_new)[nrow * D + x];
+      reinterpret_cast<float*>(vc)[row * D + x] = reinterpret_cast<const float*>(v_new)[nrow * D + x];
+    }
+    if (x == 0) len[i] = L + 1;
+  }
+}
+
+template <typename Tin, int D, int G>
+int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, const void* k_new,
+        const void* v_new, int U, int Hkv, int max_len, float scale, void* out, float* lse,
+        float* ws, const Dev& dev, cudaStream_t s) {
+  const int n = U * Hkv;
+  const int max_chunks = (max_len + kChunk - 1) / kChunk;
+  const float sl2 = scale * kLog2e;
+  if (max_chunks > 0) {
+    dim3 grid((unsigned)max_chunks, (unsigned)n);
+    decode_partial_kernel<Tin, D, G><<<grid, kWarps * 32, 0, s>>>(
+        static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
+        start, len, Hkv, max_chunks, sl2, ws);
+  }
+  decode_combine_kernel<Tin, D, G><<<n, D, 0, s>>>(
+      static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc), start, len,
+      static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new), n, Hkv, max_chunks, sl2,
+      ws, static_cast<Tin*>(out), lse, dev.status);
+  return launch_status();
+}
+
+template <typename Tin, int D>
+int dispatch_g(int G, const void* q, void* kc, void* vc, const int64_t* start, int32_t* len,
+               const void* kn, const void* vn, int U, int Hkv, int max_len, float scale,
+               void* out, float* lse, float* ws, const Dev& dev, cudaStream_t s) {
+  switch (G) {
+#define KVC_G(GG) \
+    case GG: return run<Tin, D, GG>(q, kc, vc, start, len, kn, vn, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+    KVC_G(1) KVC_G(2) KVC_G(3) KVC_G(4) KVC_G(5) KVC_G(6) KVC_G(7) KVC_G(8)
+#undef KVC_G
+  }
+  return KVC_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+size_t decode_ws_bytes(int U, int Hq, int Hkv, int d, int max_len) {
+  const int64_t chunks = (max_len + kChunk - 1) / kChunk;
+  return (size_t)U * Hkv * chunks * (Hq / Hkv) * (d + 2) * sizeof(float);
+}
+
+int decode_launch(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len,
+                  const void* k_new, const void* v_new, int dtype, int U, int Hq, int Hkv,
+                  int d, int max_len, float scale, void* out, float* lse, float* ws,
+                  const Dev& dev, cudaStream_t s) {
+  const int G = Hq / Hkv;
+  if (dtype == KVC_F32)
+    return d == 64 ? dispatch_g<float, 64>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
+                   : dispatch_g<float, 128>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+  return d == 64 ? dispatch_g<uint16_t, 64>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
+                 : dispatch_g<uint16_t, 128>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+}
+
+}  // namespace kvc

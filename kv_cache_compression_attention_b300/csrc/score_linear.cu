@@ -1,0 +1,166 @@
+// Linear surrogate scorer (KVzap §2.2): score[u,g,t] = bias[g] + h[u,t,:] . W[:,g].
+//
+// A streaming GEMV-like pass: every hidden row (Dh = 3584 bf16 = 7 KiB) is
+// read once from HBM with 16-byte coalesced loads and dotted with the Hkv
+// weight columns held in shared memory.  Work is 2*Hkv flops per hidden
+// element (8 per 16 bytes at Hkv = 4): bandwidth bound, so the kernel is
+// SIMT FFMA, not a tensor-core GEMM.
+//
+// Mapping: a warp owns 8 consecutive rows; lane L walks the 16-byte chunks
+// c = L, L+32, ... of those rows, loads the matching weight slice once from
+// shared memory (laid out chunk-interleaved so a warp's 32 loads hit 32
+// consecutive 16-byte words) and applies it to all 8 rows.  The 8 x Hkv
+// partial sums are reduced across the warp with xor-shuffles at the end.
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kRows = 8;        // rows per warp task
+constexpr int kWarps = 8;
+
+template <typename Tin> struct Vec;
+template <> struct Vec<uint16_t> { static constexpr int E = 8; };
+template <> struct Vec<float> { static constexpr int E = 4; };
+
+__device__ __forceinline__ void unpack(const uint4& v, float* x, uint16_t) {
+  x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
+  x[4] = bf16lo(v.z); x[5] = bf16hi(v.z); x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
+}
+__device__ __forceinline__ void unpack(const uint4& v, float* x, float) {
+  x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+  x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ float to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ float to_f(float f) { return f; }
+
+template <typename Tin, int HK>
+__global__ void __launch_bounds__(kWarps * 32)
+linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
+              const float* __restrict__ bias, int64_t rows, int T, int Dh,
+              float* __restrict__ scores) {
+  constexpr int E = Vec<Tin>::E;          // hidden elements per 16-byte chunk
+  constexpr int F4 = E * HK / 4;          // float4 words of weight per chunk
+  extern __shared__ float4 wsm[];         // [F4][NC] chunk-interleaved
+  const int NC = Dh / E;
+  // stage the weight: chunk c, element jj, head g -> float (jj*HK + g) of chunk c
+  for (int e = threadIdx.x; e < Dh * HK; e += blockDim.x) {
+    const int j = e / HK, g = e % HK;
+    const int c = j / E, jj = j % E;
+    const int f = jj * HK + g;
+    reinterpret_cast<float*>(&wsm[(f / 4) * NC + c])[f % 4] = to_f(weight[(int64_t)j * HK + g]);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int64_t warps_total = (int64_t)gridDim.x * kWarps;
+  const int64_t tasks = (rows + kRows - 1) / kRows;
+  for (int64_t task = warp_global; task < tasks; task += warps_total) {
+    const int64_t r0 = task * kRows;
+    float acc[kRows][HK];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+      for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
+    for (int c = lane; c < NC; c += 32) {
+      uint4 hv[kRows];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        if (r0 + r < rows) {
+          const uint4* p = reinterpret_cast<const uint4*>(hidden + (r0 + r) * (int64_t)Dh) + c;
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(hv[r].x), "=r"(hv[r].y), "=r"(hv[r].z), "=r"(hv[r].w)
+                       : "l"(p));
+        } else {
+          hv[r] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      float wv[E * HK];
+#pragma unroll
+      for (int f4 = 0; f4 < F4; ++f4) {
+        const float4 w4 = wsm[f4 * NC + c];
+        wv[4 * f4] = w4.x; wv[4 * f4 + 1] = w4.y; wv[4 * f4 + 2] = w4.z; wv[4 * f4 + 3] = w4.w;
+      }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        float x[E];
+        unpack(hv[r], x, Tin());
+#pragma unroll
+        for (int jj = 0; jj < E; ++jj)
+#pragma unroll
+          for (int g = 0; g < HK; ++g) acc[r][g] = fmaf(x[jj], wv[jj * HK + g], acc[r][g]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+      for (int g = 0; g < HK; ++g) {
+        float v = acc[r][g];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        acc[r][g] = v;
+      }
+    // lane (r*HK + g) writes (row r, head g)
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+      for (int g = 0; g < HK; ++g) {
+        if (lane == ((r * HK + g) & 31) && r0 + r < rows) {
+          const int64_t row = r0 + r;
+          const int64_t u = row / T, t = row % T;
+          scores[(u * HK + g) * (int64_t)T + t] = acc[r][g] + (bias ? bias[g] : 0.0f);
+        }
+      }
+  }
+}
+
+template <typename Tin, int HK>
+int run(const void* hidden, const void* weight, const float* bias, int U, int T, int Dh,
+        float* scores, const Dev& dev, cudaStream_t s) {
+  const size_t smem = (size_t)Dh * HK * sizeof(float);
+  auto kern = linear_kernel<Tin, HK>;
+  KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int per_sm = 0;
+  KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem));
+  if (per_sm < 1) return KVC_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)U * T;
+  const int64_t tasks = (rows + kRows - 1) / kRows;
+  int64_t blocks = (int64_t)dev.sms * per_sm;
+  const int64_t need = (tasks + kWarps - 1) / kWarps;
+  if (blocks > need) blocks = need;
+  kern<<<(unsigned)blocks, kWarps * 32, smem, s>>>(static_cast<const Tin*>(hidden),
+                                                   static_cast<const Tin*>(weight), bias, rows,
+                                                   T, Dh, scores);
+  return launch_status();
+}
+
+template <typename Tin>
+int dispatch(const void* h, const void* w, const float* b, int U, int T, int Dh, int Hkv,
+             float* sc, const Dev& dev, cudaStream_t s) {
+  switch (Hkv) {
+    case 1: return run<Tin, 1>(h, w, b, U, T, Dh, sc, dev, s);
+    case 2: return run<Tin, 2>(h, w, b, U, T, Dh, sc, dev, s);
+    case 3: return run<Tin, 3>(h, w, b, U, T, Dh, sc, dev, s);
+    case 4: return run<Tin, 4>(h, w, b, U, T, Dh, sc, dev, s);
+    case 5: return run<Tin, 5>(h, w, b, U, T, Dh, sc, dev, s);
+    case 6: return run<Tin, 6>(h, w, b, U, T, Dh, sc, dev, s);
+    case 7: return run<Tin, 7>(h, w, b, U, T, Dh, sc, dev, s);
+    case 8: return run<Tin, 8>(h, w, b, U, T, Dh, sc, dev, s);
+  }
+  return KVC_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int score_linear_launch(const void* hidden, const void* weight, const float* bias, int dtype,
+                        int U, int T, int Dh, int Hkv, float* scores, const Dev& dev,
+                        cudaStream_t s) {
+  if (dtype == KVC_F32) {
+    if (Dh % 4) return KVC_ERR_UNSUPPORTED;
+    return dispatch<float>(hidden, weight, bias, U, T, Dh, Hkv, scores, dev, s);
+  }
+  return dispatch<uint16_t>(hidden, weight, bias, U, T, Dh, Hkv, scores, dev, s);
+}
+
+}  // namespace kvc

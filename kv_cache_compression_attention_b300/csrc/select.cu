@@ -1,0 +1,395 @@
+// Budget selection: global top-k across heads, per-head top-k, or a fixed
+// threshold, always keeping the protected sinks and recent window.
+//
+// Sources: KVzap §2.3 (fixed budget "keep exactly x%", or a threshold tau on
+// the scores, with the w most recent tokens always kept); KV Cache Transform
+// Coding §2A and KVSculpt §2A (sinks and the recent window are not
+// compressed); KVSculpt §2D (heads of one layer end up with different
+// budgets -- the global pool gives exactly that).
+//
+// Design (one thread-block cluster per selection pool):
+//  * A pool is one unit's Hkv heads (global top-k) or one head (per-head
+//    budget, threshold).  The cluster's C CTAs split the pool's tokens into
+//    C contiguous ranges; each CTA keeps its range's order-preserving uint32
+//    keys in shared memory, token-major (element e = j*hps + head), so the
+//    element order inside a CTA, then across CTA ranks, is exactly the
+//    tie-break order (token asc, head asc).
+//  * Radix select, 4 passes of 8-bit digits, from the most significant
+//    digit: every CTA histograms its candidates that match the prefix found
+//    so far (warp-aggregated shared atomics), the cluster sums the C
+//    histograms through distributed shared memory, and every CTA picks the
+//    same digit.  After the last pass the exact key of the need-th largest
+//    candidate (thr) and the number of its equal-key elements to keep
+//    (need_eq) are known.
+//  * Ties (key == thr) are only ranked when not all of them are kept: a
+//    cluster prefix of per-CTA tie counts, then a block scan, gives the
+//    element index where kept ties stop.
+//  * Emission: per head, a cluster prefix of per-CTA kept counts gives each
+//    CTA's base; a block-wide ballot scan writes ascending token indices.
+//  * Offsets (exclusive scan of the counts) are a separate single-block
+//    kernel because threshold pools have data-dependent totals.
+// Every decision is an integer comparison on the fp32 bit patterns, so the
+// result is bit-exact and deterministic.
+#include <cooperative_groups.h>
+
+#include "kvc_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace kvc {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxHps = 8;                 // heads per pool kept in registers
+constexpr uint32_t kNoThr = 0xffffffffu;   // larger than every real key
+
+struct Args {
+  const float* scores;
+  int T, hps, mode;
+  int64_t need_global;
+  float tau;
+  const int32_t* head_budget;
+  int n_sink, n_recent, nP;
+  int32_t* kept;
+  int32_t* counts;
+};
+
+struct Shared {
+  uint32_t hist[2][256];
+  uint32_t tot[256];
+  uint32_t warp_tmp[kWarps];
+  uint32_t warp_tmp2[kWarps * kMaxHps];
+  uint32_t xchg_ties;                 // read remotely
+  uint32_t xchg_cnt[kMaxHps];         // read remotely
+  uint32_t head_base[kMaxHps];
+  uint32_t sel_bin, sel_above, sel_count, ecut;
+};
+
+__device__ __forceinline__ bool is_prot(int t, int T, int n_sink, int n_recent) {
+  return t < n_sink || t >= T - n_recent;
+}
+
+// Exclusive block scan of one flag per thread; returns the prefix and sets *total.
+__device__ __forceinline__ uint32_t block_excl_scan(bool flag, Shared& sh, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t ball = __ballot_sync(0xffffffffu, flag);
+  const uint32_t within = __popc(ball & ((1u << lane) - 1u));
+  if (lane == 0) sh.warp_tmp[warp] = __popc(ball);
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t v = sh.warp_tmp[lane];
+    uint32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      uint32_t n = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += n;
+    }
+    sh.warp_tmp[lane] = incl - v;                 // exclusive warp base
+    if (lane == 31) sh.warp_tmp2[0] = incl;       // block total
+  }
+  __syncthreads();
+  const uint32_t base = sh.warp_tmp[warp];
+  *total = sh.warp_tmp2[0];
+  __syncthreads();
+  return base + within;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+select_kernel(Args a) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = (int)cl.num_blocks();
+  const int rank = (int)cl.block_rank();
+  const int seg = blockIdx.y;
+  const int hps = a.hps;
+  const int T = a.T;
+  const int head0 = seg * hps;
+  const int t0 = (int)((int64_t)rank * T / C);
+  const int t1 = (int)((int64_t)(rank + 1) * T / C);
+  const int nt = t1 - t0;
+  const int nloc = nt * hps;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
+
+  // ---- phase A: keys of this CTA's token range (coalesced head-major reads)
+  for (int e = tid; e < nloc; e += kThreads) {
+    const int hh = e / nt, j = e - hh * nt;
+    const int t = t0 + j;
+    const float s = __ldg(a.scores + (int64_t)(head0 + hh) * T + t);
+    keys[j * hps + hh] = is_prot(t, T, a.n_sink, a.n_recent) ? 0u : score_key(s);
+  }
+  __syncthreads();
+
+  // ---- phase B: radix select of the need-th largest candidate key
+  int64_t need = 0;
+  if (a.mode == KVC_SEL_GLOBAL_TOPK) {
+    need = a.need_global;
+  } else if (a.mode == KVC_SEL_PER_HEAD) {
+    int64_t b = a.head_budget[head0];
+    if (b < a.nP) b = a.nP;
+    if (b > T) b = T;
+    need = b - a.nP;
+  }
+  uint32_t thr = kNoThr;
+  uint32_t ecut = 0;
+  if (a.mode == KVC_SEL_THRESHOLD) {
+    thr = (a.tau != a.tau) ? kNoThr : score_key(a.tau);
+  } else if (need > 0) {
+    uint32_t prefix = 0, pmask = 0;
+    uint32_t krem = (uint32_t)need;
+    uint32_t last_count = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      uint32_t* buf = sh.hist[pass & 1];
+      for (int b = tid; b < 256; b += kThreads) buf[b] = 0;
+      __syncthreads();
+      for (int e0 = 0; e0 < nloc; e0 += kThreads) {
+        const int e = e0 + tid;
+        uint32_t digit = 0xffffu;
+        if (e < nloc) {
+          const uint32_t key = keys[e];
+          if (key != 0u && (key & pmask) == prefix) digit = (key >> shift) & 255u;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+        if (digit != 0xffffu && lane == __ffs(peers) - 1) atomicAdd(&buf[digit], __popc(peers));
+      }
+      __syncthreads();
+      cl.sync();
+      if (tid < 256) {
+        uint32_t tot = 0;
+        for (int r = 0; r < C; ++r) tot += cl.map_shared_rank(buf, r)[tid];
+        sh.tot[tid] = tot;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t cnt[8];
+        uint32_t lsum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { cnt[i] = sh.tot[lane * 8 + i]; lsum += cnt[i]; }
+        uint32_t suffix = lsum;                  // sum over lanes >= lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          uint32_t n = __shfl_down_sync(0xffffffffu, suffix, off);
+          if (lane + off < 32) suffix += n;
+        }
+        uint32_t above = suffix - lsum;          // candidates in higher lanes' bins
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          if (above < krem && krem <= above + cnt[i]) {
+            sh.sel_bin = lane * 8 + i;
+            sh.sel_above = above;
+            sh.sel_count = cnt[i];
+          }
+          above += cnt[i];
+        }
+      }
+      __syncthreads();
+      const uint32_t bin = sh.sel_bin;
+      krem -= sh.sel_above;
+      last_count = sh.sel_count;
+      prefix |= bin << shift;
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+    thr = prefix;
+    // ---- ties: keep the first krem elements with key == thr in (t, g) order
+    if (krem < last_count) {
+      uint32_t mine = 0;
+      for (int e = tid; e < nloc; e += kThreads) mine += (keys[e] == thr);
+      mine = __reduce_add_sync(0xffffffffu, mine);
+      if (lane == 0) sh.warp_tmp[warp] = mine;
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t s = 0;
+        for (int w = 0; w < kWarps; ++w) s += sh.warp_tmp[w];
+        sh.xchg_ties = s;
+      }
+      __syncthreads();
+      cl.sync();
+      uint32_t base = 0;
+      for (int r = 0; r < rank; ++r) base += *cl.map_shared_rank(&sh.xchg_ties, r);
+      const uint32_t local_ties = sh.xchg_ties;
+      if (base >= krem) ecut = 0;
+      else if (base + local_ties <= krem) ecut = (uint32_t)nloc;
+      else {
+        const uint32_t want = krem - base;     // ties of this CTA to keep (>= 1)
+        if (tid == 0) sh.ecut = (uint32_t)nloc;
+        uint32_t carry = 0;
+        for (int e0 = 0; e0 < nloc; e0 += kThreads) {
+          const int e = e0 + tid;
+          const bool f = e < nloc && keys[e] == thr;
+          uint32_t total;
+          const uint32_t pos = block_excl_scan(f, sh, &total);
+          if (f && carry + pos == want) sh.ecut = (uint32_t)e;   // first dropped tie
+          carry += total;
+          if (carry > want) break;                              // uniform across the block
+        }
+        __syncthreads();
+        ecut = sh.ecut;
+      }
+    } else {
+      ecut = (uint32_t)nloc;
+    }
+  }
+
+  // kept(e): protected, strictly above thr, or a kept tie
+  auto kept = [&](int e) -> bool {
+    const uint32_t key = keys[e];
+    if (key == 0u) return true;
+    if (a.mode == KVC_SEL_THRESHOLD) return key >= thr;
+    return key > thr || (key == thr && (uint32_t)e < ecut);
+  };
+
+  // ---- phase D: per-head counts, cluster prefix, ascending emission
+  uint32_t cnt[kMaxHps];
+#pragma unroll
+  for (int hh = 0; hh < kMaxHps; ++hh) cnt[hh] = 0;
+  for (int e = tid; e < nloc; e += kThreads) {
+    const int hh = e % hps;
+    if (kept(e)) {
+#pragma unroll
+      for (int x = 0; x < kMaxHps; ++x) cnt[x] += (x == hh);
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMaxHps; ++hh) {
+    const uint32_t v = __reduce_add_sync(0xffffffffu, cnt[hh]);
+    if (lane == 0) sh.warp_tmp2[hh * kWarps + warp] = v;
+  }
+  __syncthreads();
+  if (tid < hps) {
+    uint32_t s = 0;
+    for (int w = 0; w < kWarps; ++w) s += sh.warp_tmp2[tid * kWarps + w];
+    sh.xchg_cnt[tid] = s;
+  }
+  __syncthreads();
+  cl.sync();
+  if (tid < hps) {
+    uint32_t base = 0, total = 0;
+    for (int r = 0; r < C; ++r) {
+      const uint32_t v = cl.map_shared_rank(sh.xchg_cnt, r)[tid];
+      if (r < rank) base += v;
+      total += v;
+    }
+    sh.head_base[tid] = base;
+    if (rank == 0) a.counts[head0 + tid] = (int32_t)total;
+  }
+  __syncthreads();
+  for (int hh = 0; hh < hps; ++hh) {
+    int32_t* out = a.kept + (int64_t)(head0 + hh) * T;
+    uint32_t carry = sh.head_base[hh];
+    for (int j0 = 0; j0 < nt; j0 += kThreads) {
+      const int j = j0 + tid;
+      const bool f = j < nt && kept(j * hps + hh);
+      uint32_t total;
+      const uint32_t pos = block_excl_scan(f, sh, &total);
+      if (f) out[carry + pos] = t0 + j;
+      carry += total;
+    }
+  }
+  // no CTA may leave while a peer can still read its shared memory
+  cl.sync();
+}
+
+// offsets[i] = sum_{j<i} counts[j], offsets[n] = total (one block).
+__global__ void __launch_bounds__(1024)
+offsets_kernel(const int32_t* __restrict__ counts, int n, int64_t* __restrict__ offsets) {
+  __shared__ int64_t warp_sum[32];
+  __shared__ int64_t carry_s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  for (int i0 = 0; i0 < n; i0 += 1024) {
+    const int i = i0 + threadIdx.x;
+    const int64_t v = i < n ? (int64_t)counts[i] : 0;
+    int64_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t ws = warp_sum[lane];
+      int64_t wi = ws;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, wi, off);
+        if (lane >= off) wi += y;
+      }
+      warp_sum[lane] = wi - ws;
+    }
+    __syncthreads();
+    const int64_t carry = carry_s;
+    if (i < n) offsets[i] = carry + warp_sum[warp] + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry_s = carry + warp_sum[warp] + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[n] = carry_s;
+}
+
+size_t shared_bytes(int keys) { return ((sizeof(Shared) + 15) & ~size_t(15)) + (size_t)keys * 4; }
+
+}  // namespace
+
+int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t need_global,
+                  float tau, const int32_t* head_budget, int n_sink, int n_recent,
+                  int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
+                  cudaStream_t s) {
+  const int hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1;
+  if (hps > kMaxHps) return KVC_ERR_UNSUPPORTED;
+  const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
+  const int64_t pool = (int64_t)hps * T;
+  const int cap = (int)((dev.max_smem_optin - (int)shared_bytes(0)) / 4);
+  // the smallest cluster that keeps <= 16K keys per CTA, else the smallest that fits
+  int C = 1;
+  while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
+  while (C < 16 && (pool + C - 1) / C > cap) C *= 2;
+  if ((pool + C - 1) / C > cap) return KVC_ERR_UNSUPPORTED;
+  Args a;
+  a.scores = scores; a.T = T; a.hps = hps; a.mode = mode; a.need_global = need_global;
+  a.tau = tau; a.head_budget = head_budget; a.n_sink = n_sink; a.n_recent = n_recent;
+  a.nP = 0;
+  {
+    int rs = T - n_recent;
+    a.nP = n_sink + (T - rs) - (rs < n_sink ? n_sink - rs : 0);
+  }
+  a.kept = kept_idx; a.counts = counts;
+  KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
+                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  // a cluster must fit one GPC: shrink it (while the keys still fit) until
+  // the occupancy query says at least one cluster can be resident
+  for (;;) {
+    const size_t smem = shared_bytes(((T + C - 1) / C) * hps);
+    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    cfg.gridDim = dim3((unsigned)C, (unsigned)nseg, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel, &cfg));
+    if (active > 0) break;
+    if (C == 1 || (pool + C / 2 - 1) / (C / 2) > cap) return KVC_ERR_UNSUPPORTED;
+    C /= 2;
+  }
+  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel, a));
+  offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
+  return launch_status();
+}
+
+}  // namespace kvc

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+* libkvc.so loads and exports every function include/kvc.h declares;
+* the ctypes signatures in the binding cover exactly those functions;
+* argument errors are rejected on the host with KVC_ERR_INVALID /
+  KVC_ERR_UNSUPPORTED before any CUDA call (so they work without a GPU);
+* the status strings are stable.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+LIB = os.path.join(ROOT, "kv_cache_compression_attention_b300", "libkvc.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kvc_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from kv_cache_compression_attention_b300 import build
+        build.build()
+    from kv_cache_compression_attention_b300 import binding
+    return binding.load(LIB)
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ("kvc_score_attn", "kvc_score_linear", "kvc_select", "kvc_compact",
+                     "kvc_decode_attn", "kvc_fidelity"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_match_header():
+    from kv_cache_compression_attention_b300 import binding
+    assert sorted(binding.SIGNATURES) == declared_functions()
+
+
+def test_status_strings(lib):
+    assert lib.kvc_status_string(0) == b"ok"
+    assert lib.kvc_status_string(-1) == b"invalid argument"
+    assert lib.kvc_status_string(-5) == b"device wait timed out"
+    assert lib.kvc_status_string(12345) == b"unknown status"
+    assert lib.kvc_version() >= 100
+
+
+P = ctypes.c_void_p(16)   # a non-null, 16-byte aligned dummy pointer (never dereferenced)
+
+
+def test_score_attn_rejects_bad_arguments(lib):
+    f = lib.kvc_score_attn
+    ok = dict(q=P, k=P, dt=1, U=1, Hq=8, Hkv=4, T=64, W=8, d=128, scale=0.1, hs=None, causal=1,
+              scores=P, ws=None, wsb=0, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["dt"], a["U"], a["Hq"], a["Hkv"], a["T"], a["W"], a["d"],
+                 a["scale"], a["hs"], a["causal"], a["scores"], a["ws"], a["wsb"], a["s"])
+
+    assert call(q=None) == -1
+    assert call(scores=None) == -1
+    assert call(dt=7) == -1
+    assert call(Hq=6) == -1              # Hq % Hkv
+    assert call(W=65) == -1              # W > T
+    assert call(T=0) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(d=96) == -2
+
+
+def test_select_rejects_bad_arguments(lib):
+    f = lib.kvc_select
+
+    def call(scores=P, U=1, Hkv=2, T=16, mode=0, ratio=0.5, tau=0.0, hb=None, ns=1, nr=1,
+             kept=P, counts=P, offs=P):
+        return f(scores, U, Hkv, T, mode, ratio, tau, hb, ns, nr, kept, counts, offs, None, 0, None)
+
+    assert call(scores=None) == -1
+    assert call(mode=3) == -1
+    assert call(ratio=1.5) == -1
+    assert call(ratio=float("nan")) == -1
+    assert call(ns=-1) == -1
+    assert call(mode=2, hb=None) == -1
+    assert call(T=1 << 21, mode=1) == -2   # pool larger than supported
+
+
+def test_compact_and_decode_reject_bad_arguments(lib):
+    c = lib.kvc_compact
+    assert c(None, P, 1, 1, 1, 8, 128, P, P, P, 0, P, P, 8, P, P, None) == -1
+    assert c(P, P, 1, 1, 1, 8, 128, P, P, P, -1, P, P, 8, P, P, None) == -1
+    assert c(P, P, 1, 1, 1, 8, 100, P, P, P, 0, P, P, 8, P, P, None) == -2   # 200-byte rows
+    dec = lib.kvc_decode_attn
+    args = [P, P, P, P, P, None, None, 1, 1, 8, 2, 128, 64, 0.1, P, P, P, 1 << 20, None]
+    bad = list(args); bad[0] = None
+    assert dec(*bad) == -1
+    bad = list(args); bad[5] = P              # k_new without v_new
+    assert dec(*bad) == -1
+    bad = list(args); bad[9] = 3              # Hq % Hkv
+    assert dec(*bad) == -1
+    bad = list(args); bad[11] = 80            # d
+    assert dec(*bad) == -2
+    bad = list(args); bad[17] = 0             # workspace too small
+    assert dec(*bad) == -3
+
+
+def test_workspace_queries_are_pure_host(lib):
+    assert lib.kvc_select_workspace(1, 8, 32768, 0) == 0
+    n = lib.kvc_decode_workspace(64, 32, 8, 128, 10086, 1)
+    chunks = (10086 + 511) // 512
+    assert n == 64 * 8 * chunks * 4 * (128 + 2) * 4
+    # tensor-core scoring path needs no workspace; the SIMT path keeps one lse per row
+    assert lib.kvc_score_attn_workspace(1, 32, 8, 32768, 64, 128, 1) == 0
+    assert lib.kvc_score_attn_workspace(1, 8, 4, 1024, 32, 64, 0) == 8 * 32 * 4

@@ -1,0 +1,125 @@
+"""GPU parity of the scoring kernels against the CPU oracle (through the C ABI).
+
+Attention-mass scoring: fp32 (SIMT path) and bf16 (tcgen05 path for d = 128,
+G*W in {128, 256}; SIMT path otherwise), causal and not, with and without a
+per-head temperature, on sizes that span several 128-token tiles and a ragged
+tail, then on the full workloads (Llama-3-8B-shaped 32k layer in full; the
+32-layer x batch-4 cache on sampled units).  Linear surrogate scoring on
+small shapes and on sampled rows of the 128k Qwen-shaped workload.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_compression_attention_b300 import inputs
+from oracle import kvc_oracle as O
+from tests.kvc_testutil import TOL, mass_rel_err, np64, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from kv_cache_compression_attention_b300 import binding
+    binding.lib()
+    return binding
+
+
+def gpu_scores(B, q, k, scale, hs=None, causal=True):
+    U, Hkv, T = k.shape[0], k.shape[1], k.shape[2]
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda", dtype=torch.float32)
+    B.kvc_score_attn(q, k, out, scale, head_scale=hs, causal=causal)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    return out
+
+
+def rand(shape, dtype, seed, scale=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (scale * torch.randn(shape, generator=g, device="cuda")).to(dtype)
+
+
+@pytest.mark.parametrize("dtype,d,G,W,T", [
+    (torch.float32, 64, 2, 32, 1024),     # the tiny fp32 workload's shape
+    (torch.float32, 128, 4, 16, 777),
+    (torch.bfloat16, 128, 4, 64, 1000),   # tcgen05, R = 256, ragged tail
+    (torch.bfloat16, 128, 2, 64, 1300),   # tcgen05, R = 128
+    (torch.bfloat16, 128, 4, 64, 300),    # tcgen05, fewer tiles than cluster ranks
+    (torch.bfloat16, 64, 4, 16, 500),     # SIMT bf16
+])
+@pytest.mark.parametrize("causal", [True, False])
+def test_score_attn_small(B, dtype, d, G, W, T, causal):
+    U, Hkv = 2, 2
+    q = rand((U, Hkv * G, W, d), dtype, 1)
+    k = rand((U, Hkv, T, d), dtype, 2)
+    hs = (0.5 + 1.5 * torch.rand((U, Hkv * G), generator=torch.Generator(device="cuda").manual_seed(3),
+                                 device="cuda")).float()
+    scale = d ** -0.5
+    got = np64(gpu_scores(B, q, k, scale, hs, causal))
+    ref = O.score_attn(np64(q), np64(k), scale, np64(hs), causal)
+    assert mass_rel_err(got, ref) <= TOL[dtype]
+    # every window row is a softmax: each kv head collects G*W
+    np.testing.assert_allclose(got.sum(-1), G * W, rtol=TOL[dtype])
+
+
+def test_score_attn_tiny_workload(B):
+    w = inputs.WORKLOADS["c1_tiny"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    got = np64(gpu_scores(B, q, k, w.scale))
+    ref = O.score_attn(np64(q), np64(k), w.scale)
+    assert mass_rel_err(got, ref) <= 1e-4
+
+
+def test_score_attn_llama32k_full(B):
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    got = np64(gpu_scores(B, q, k, w.scale))
+    ref = O.score_attn(np64(q), np64(k), w.scale)
+    assert mass_rel_err(got, ref) <= 2e-2
+    # the sinks dominate and every needle outranks the median token
+    assert (got[:, :, :4].min() > np.median(got))
+
+
+def test_score_attn_32layer_sampled_units(B):
+    w = inputs.WORKLOADS["c3_32layer"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    hs = inputs.head_scale(w, "cuda")
+    got = gpu_scores(B, q, k, w.scale, hs)
+    for u in (0, 77, 127):
+        ref = O.score_attn(np64(q[u:u + 1]), np64(k[u:u + 1]), w.scale, np64(hs[u:u + 1]))
+        assert mass_rel_err(np64(got[u:u + 1]), ref) <= 2e-2
+    del k
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("Hkv,Dh,T", [(4, 256, 1000), (3, 64, 37), (8, 128, 129)])
+def test_score_linear_small(B, dtype, Hkv, Dh, T):
+    U = 2
+    h = rand((U, T, Dh), dtype, 5)
+    wt = rand((Dh, Hkv), dtype, 6, scale=Dh ** -0.5)
+    bias = rand((Hkv,), torch.float32, 7)
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda")
+    B.kvc_score_linear(h, wt, bias, out)
+    ref = O.score_linear(np64(h), np64(wt), np64(bias))
+    assert row_rel_err(np64(out), ref) <= TOL[dtype]
+
+
+def test_score_linear_qwen128k_sampled_rows(B):
+    w = inputs.WORKLOADS["c4_qwen128k"]
+    hid, wt, bias = inputs.linear_scorer(w, "cuda")
+    out = torch.empty((w.U, w.Hkv, w.T), device="cuda")
+    B.kvc_score_linear(hid, wt, bias, out)
+    rows = torch.cat([torch.arange(0, 512), torch.arange(65536, 66048),
+                      torch.arange(w.T - 512, w.T)]).cuda()
+    ref = O.score_linear(np64(hid[:, rows]), np64(wt), np64(bias))
+    assert row_rel_err(np64(out[:, :, rows]), ref) <= 2e-2
+    # outputs ~ N(0,1): about 30.85% of the tokens score >= 0.5
+    frac = (out >= 0.5).float().mean().item()
+    assert abs(frac - 0.3085) < 0.01

@@ -1,0 +1,194 @@
+"""GPU selection and compaction, bit-exact against the oracle on the oracle's
+fp32 scores (through the C ABI).
+
+Covers global top-k across heads, per-head budgets and the threshold rule;
+ties, -0/+0, +-inf and NaN; protected sinks / recent windows that overlap or
+swallow the whole budget; one-token and ragged pools; and the full-size
+workloads (32k single layer, 32-layer x batch-4 cache, 128k threshold).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_compression_attention_b300 import inputs
+from oracle import kvc_oracle as O
+from tests.kvc_testutil import np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from kv_cache_compression_attention_b300 import binding
+    binding.lib()
+    return binding
+
+
+def gpu_select(B, scores, mode, **kw):
+    U, Hkv, T = scores.shape
+    kept = torch.full((U * Hkv, T), -7, dtype=torch.int32, device="cuda")
+    counts = torch.full((U * Hkv,), -7, dtype=torch.int32, device="cuda")
+    offs = torch.full((U * Hkv + 1,), -7, dtype=torch.int64, device="cuda")
+    hb = kw.pop("head_budget", None)
+    if hb is not None:
+        hb = torch.as_tensor(np.asarray(hb), dtype=torch.int32).cuda()
+    B.kvc_select(scores, mode, kept, counts, offs, head_budget=hb, **kw)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    return kept.cpu().numpy(), counts.cpu().numpy(), offs.cpu().numpy()
+
+
+def check_same(got, ref):
+    kept, counts, offs = got
+    rk, rc, ro = ref
+    np.testing.assert_array_equal(counts, rc)
+    np.testing.assert_array_equal(offs, ro)
+    for i in range(len(rc)):
+        np.testing.assert_array_equal(kept[i, : rc[i]], rk[i, : rc[i]])
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 1024), (2, 8, 5000), (3, 2, 1), (1, 1, 3), (2, 5, 40001)])
+@pytest.mark.parametrize("ties,specials", [(False, False), (True, False), (True, True)])
+def test_select_global_small(B, shape, ties, specials):
+    s = inputs.random_scores(shape, seed=sum(shape), ties=ties, specials=specials)
+    sc = s.numpy()
+    for ratio, ns, nr in [(0.25, 4, 32), (0.1, 0, 0), (0.0, 2, 2), (1.0, 4, 4), (0.5, 3000, 3000)]:
+        got = gpu_select(B, s.cuda(), "global", keep_ratio=ratio, n_sink=ns, n_recent=nr)
+        ref = O.select(sc, "global", keep_ratio=ratio, n_sink=ns, n_recent=nr)
+        check_same(got, ref)
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 777), (1, 8, 4096)])
+def test_select_per_head_and_threshold_small(B, shape):
+    s = inputs.random_scores(shape, seed=5, ties=True, specials=True)
+    sc = s.numpy()
+    U, Hkv, T = shape
+    hb = np.random.default_rng(1).integers(-5, T + 5, size=U * Hkv)
+    got = gpu_select(B, s.cuda(), "per_head", head_budget=hb, n_sink=2, n_recent=7)
+    check_same(got, O.select(sc, "per_head", head_budget=hb, n_sink=2, n_recent=7))
+    for tau in (0.5, -0.0, float("inf"), float("-inf"), float("nan")):
+        got = gpu_select(B, s.cuda(), "threshold", tau=tau, n_sink=1, n_recent=3)
+        check_same(got, O.select(sc, "threshold", tau=tau, n_sink=1, n_recent=3))
+
+
+def test_select_all_equal_scores_ties_by_token_then_head(B):
+    s = torch.zeros((1, 4, 1000))
+    got = gpu_select(B, s.cuda(), "global", keep_ratio=0.3, n_sink=1, n_recent=1)
+    check_same(got, O.select(s.numpy(), "global", keep_ratio=0.3, n_sink=1, n_recent=1))
+
+
+def test_select_llama32k_full(B):
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    ref_scores = O.score_attn(np64(q), np64(k), w.scale).astype(np.float32)
+    got = gpu_select(B, torch.from_numpy(ref_scores).cuda(), "global", keep_ratio=w.keep_ratio,
+                     n_sink=w.n_sink, n_recent=w.n_recent)
+    ref = O.select(ref_scores, "global", keep_ratio=w.keep_ratio, n_sink=w.n_sink,
+                   n_recent=w.n_recent)
+    check_same(got, ref)
+    assert got[2][-1] == math.floor(0.10 * 8 * 32768)
+    assert len(set(got[1].tolist())) > 1          # heads keep different counts
+
+
+def test_select_32layer_full_units(B):
+    w = inputs.WORKLOADS["c3_32layer"]
+    s = inputs.random_scores((w.U, w.Hkv, w.T), seed=33)
+    got = gpu_select(B, s.cuda(), "global", keep_ratio=w.keep_ratio, n_sink=w.n_sink,
+                     n_recent=w.n_recent)
+    ref = O.select(s.numpy(), "global", keep_ratio=w.keep_ratio, n_sink=w.n_sink,
+                   n_recent=w.n_recent)
+    check_same(got, ref)
+
+
+def test_select_threshold_qwen128k(B):
+    w = inputs.WORKLOADS["c4_qwen128k"]
+    g = torch.Generator().manual_seed(4)
+    s = torch.randn((w.U, w.Hkv, w.T), generator=g)
+    got = gpu_select(B, s.cuda(), "threshold", tau=w.tau, n_sink=w.n_sink, n_recent=w.n_recent)
+    check_same(got, O.select(s.numpy(), "threshold", tau=w.tau, n_sink=w.n_sink,
+                             n_recent=w.n_recent))
+
+
+# ------------------------------------------------------------- compaction
+def gpu_compact(B, k, v, kept, counts, offs, slack):
+    U, Hkv, T, d = k.shape
+    n = U * Hkv
+    rows = int(offs[-1]) + n * slack
+    kc = torch.zeros((max(rows, 1), d), dtype=k.dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    start = torch.full((n,), -1, dtype=torch.int64, device="cuda")
+    length = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    B.kvc_compact(k, v, torch.as_tensor(kept).cuda(), torch.as_tensor(counts).cuda(),
+                  torch.as_tensor(offs).cuda(), kc, vc, start, length, slack=slack)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    return kc[:rows], vc[:rows], start.cpu().numpy(), length.cpu().numpy()
+
+
+def as_bytes(t):
+    return t.cpu().contiguous().view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 128),
+                                     (torch.bfloat16, 64), (torch.float32, 64)])
+@pytest.mark.parametrize("slack", [0, 3])
+def test_compact_bit_exact_small(B, dtype, d, slack):
+    U, Hkv, T = 2, 3, 1001
+    g = torch.Generator().manual_seed(9)
+    k = torch.randn((U, Hkv, T, d), generator=g).to(dtype)
+    v = torch.randn((U, Hkv, T, d), generator=g).to(dtype)
+    s = inputs.random_scores((U, Hkv, T), seed=2).numpy()
+    kept, counts, offs = O.select(s, "global", keep_ratio=0.2, n_sink=4, n_recent=16)
+    kc, vc, start, length = gpu_compact(B, k.cuda(), v.cuda(), kept, counts, offs, slack)
+    rk, rv, rs, rl = O.compact(k.numpy() if dtype == torch.float32 else k.view(torch.int16).numpy(),
+                               v.numpy() if dtype == torch.float32 else v.view(torch.int16).numpy(),
+                               kept, counts, offs, slack)
+    np.testing.assert_array_equal(start, rs)
+    np.testing.assert_array_equal(length, rl)
+    kb = as_bytes(kc).reshape(kc.shape[0], -1)
+    vb = as_bytes(vc).reshape(vc.shape[0], -1)
+    rkb = rk.view(np.uint8).reshape(rk.shape[0], -1)
+    rvb = rv.view(np.uint8).reshape(rv.shape[0], -1)
+    for i in range(U * Hkv):           # written rows only (slack rows are not the kernel's)
+        sl = slice(rs[i], rs[i] + rl[i])
+        np.testing.assert_array_equal(kb[sl], rkb[sl])
+        np.testing.assert_array_equal(vb[sl], rvb[sl])
+
+
+def test_compact_llama32k_full(B):
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, v = inputs.keys_values(w, q, "cuda")
+    s = O.score_attn(np64(q), np64(k), w.scale).astype(np.float32)
+    kept, counts, offs = O.select(s, "global", keep_ratio=w.keep_ratio, n_sink=w.n_sink,
+                                  n_recent=w.n_recent)
+    kc, vc, start, length = gpu_compact(B, k, v, kept, counts, offs, 0)
+    kh = k.cpu().view(torch.int16).numpy()
+    vh = v.cpu().view(torch.int16).numpy()
+    rk, rv, rs, rl = O.compact(kh, vh, kept, counts, offs, 0)
+    np.testing.assert_array_equal(kc.cpu().view(torch.int16).numpy(), rk)
+    np.testing.assert_array_equal(vc.cpu().view(torch.int16).numpy(), rv)
+
+
+def test_compact_reports_capacity_overflow_without_writing_past(B):
+    U, Hkv, T, d = 1, 2, 64, 128
+    k = torch.randn((U, Hkv, T, d), device="cuda").to(torch.bfloat16)
+    v = torch.randn_like(k)
+    kept = np.tile(np.arange(T, dtype=np.int32), (2, 1))
+    counts = np.array([T, T], dtype=np.int32)
+    offs = np.array([0, T, 2 * T], dtype=np.int64)
+    guard = torch.zeros((2 * T + 8, d), dtype=torch.bfloat16, device="cuda")
+    kc = guard[: T + 5]                     # too small on purpose: rows >= T+5 must be skipped
+    vc = torch.zeros_like(guard)[: T + 5]
+    start = torch.empty(2, dtype=torch.int64, device="cuda")
+    length = torch.empty(2, dtype=torch.int32, device="cuda")
+    B.kvc_compact(k, v, torch.as_tensor(kept).cuda(), torch.as_tensor(counts).cuda(),
+                  torch.as_tensor(offs).cuda(), kc, vc, start, length)
+    assert B.kvc_device_status() == -6            # KVC_ERR_RANGE
+    assert B.kvc_device_status() == 0             # cleared
+    assert guard[T + 5:].abs().sum().item() == 0  # nothing written past the capacity
