@@ -253,7 +253,8 @@ def fidelity_probe(B, L):
     n = L.n
     dev = L.k.device
     g = torch.Generator(device=dev).manual_seed(2026)
-    q = torch.randn((w.U, w.Hq, w.d), generator=g, device=dev).to(L.k.dtype)
+    # the probe query is the last observation-window query of every q head
+    q = L.q[:, :, -1, :].contiguous()
     kn = torch.randn((w.U, w.Hkv, w.d), generator=g, device=dev).to(L.k.dtype)
     vn = torch.randn((w.U, w.Hkv, w.d), generator=g, device=dev).to(L.k.dtype)
     L.score(); L.select(); L.compact()
