@@ -217,6 +217,39 @@ int kvc_decode_attn(const void* q, void* kc, void* vc, const int64_t* start, int
                     void* stream);
 
 /*
+ * kvc_decode_attn without a workspace, for callers that cannot allocate
+ * device memory (a plug-in inside a host engine that owns every allocation
+ * and offers no workspace; a caller whose device-memory budget is fixed at
+ * start-up).  The pages have no counterpart: this is an interface choice.
+ *
+ * Same arguments, semantics and results as kvc_decode_attn, minus the
+ * workspace.  The split-K scratch is a fixed array of
+ * KVC_DECODE_NOALLOC_SCRATCH_BYTES in the library's device memory, reserved
+ * on every GPU that loads the library until the process exits.  Nothing is
+ * allocated or freed by the call.
+ *  - Limit: sizes with kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype) >
+ *    KVC_DECODE_NOALLOC_SCRATCH_BYTES are refused with KVC_ERR_WORKSPACE
+ *    before any CUDA call (e.g. 64 x 8 kv heads, G = 4, d = 128 fit up to
+ *    max_len = 7680).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make it before any
+ *    stream capture.
+ *  - All calls on a device share the array: calls whose kernels can overlap
+ *    on the GPU race and must be serialised by the caller.  The array keeps
+ *    the last call's contents; nothing in it needs clearing, since each step
+ *    writes every record it reads.
+ */
+#define KVC_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* The scratch size of kvc_decode_attn_noalloc in bytes (a constant). */
+size_t kvc_decode_noalloc_scratch_bytes(void);
+
+int kvc_decode_attn_noalloc(const void* q, void* kc, void* vc, const int64_t* start,
+                            int32_t* len, const void* k_new, const void* v_new, int dtype,
+                            int U, int Hq, int Hkv, int d, int max_len, float scale,
+                            void* out, float* lse, void* stream);
+
+/*
  * Fidelity probe of a compressed cache against the full one, per (unit, q
  * head) ([Sculpt] §4 measures fidelity as a KL divergence):
  *   rel_err = ||out_comp - out_full||_2 / ||out_full||_2 (0/0 -> 0)

@@ -42,6 +42,9 @@ SIGNATURES = {
     "kvc_decode_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvc_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                              _P, _SZ, _P]),
+    "kvc_decode_noalloc_scratch_bytes": (_SZ, []),
+    "kvc_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                                     _P, _P]),
     "kvc_fidelity": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
     "kvc_selftest_wait_timeout": (_I, [_U64, _P]),
 }
@@ -175,6 +178,24 @@ def kvc_decode_attn(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=N
                                float(scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                _stream(stream))
     _check("kvc_decode_attn", rc)
+
+
+def kvc_decode_attn_noalloc(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,
+                            max_len=None, scale=None, stream=None):
+    """kvc_decode_attn for callers that cannot allocate device memory: the
+    split-K scratch is the library's fixed device array, so no workspace is
+    allocated here either.  Calls that overlap on the GPU race on that array."""
+    U, Hq, d = q.shape
+    Hkv = start.numel() // U
+    if max_len is None:
+        raise ValueError("max_len is required (upper bound of any head's length)")
+    if scale is None:
+        scale = d ** -0.5
+    rc = lib().kvc_decode_attn_noalloc(_ptr(q), _ptr(kc), _ptr(vc), _ptr(start), _ptr(length),
+                                       _ptr(k_new), _ptr(v_new), _dtype(q), U, Hq, Hkv, d,
+                                       int(max_len), float(scale), _ptr(out), _ptr(lse),
+                                       _stream(stream))
+    _check("kvc_decode_attn_noalloc", rc)
 
 
 def kvc_fidelity(out_comp, out_full, lse_comp, lse_full, rel_err, kl, stream=None):
