@@ -121,6 +121,9 @@ class LayerWorkload:
         n = w.U * w.Hkv
         self.n = n
         self.scores = torch.empty((w.U, w.Hkv, w.T), device=device)
+        self.score_ws = torch.empty(B.lib().kvc_score_attn_workspace(
+            w.U, w.Hq, w.Hkv, w.T, w.W, w.d, B.KVC_BF16 if w.dtype == "bf16" else B.KVC_F32),
+            dtype=torch.uint8, device=device)
         self.kept = torch.empty((n, w.T), dtype=torch.int32, device=device)
         self.counts = torch.empty(n, dtype=torch.int32, device=device)
         self.offs = torch.empty(n + 1, dtype=torch.int64, device=device)
@@ -131,7 +134,7 @@ class LayerWorkload:
         self.len = torch.empty(n, dtype=torch.int32, device=device)
 
     def score(self):
-        self.B.kvc_score_attn(self.q, self.k, self.scores, self.w.scale)
+        self.B.kvc_score_attn(self.q, self.k, self.scores, self.w.scale, workspace=self.score_ws)
 
     def select(self):
         w = self.w

@@ -95,9 +95,12 @@ size_t kvc_score_attn_workspace(int U, int Hq, int Hkv, int T, int W, int d, int
  *
  * q_win      [U, Hq, W, d]  dtype
  * k          [U, Hkv, T, d] dtype
- * head_scale [U, Hq] fp32 temperature factor f, or NULL for all ones
+ * head_scale [U, Hq] fp32 temperature factor f, or NULL for all ones; every
+ *            entry must be finite and > 0 (a kernel that meets another value
+ *            records KVC_ERR_INVALID in the device status word and the scores
+ *            of that call are unspecified)
  * scores     [U, Hkv, T] fp32 (written)
- * Requires 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}.
+ * Requires 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}, finite scale > 0.
  * dtype KVC_BF16 at d = 128 with G*W in {128, 256} runs on the tensor cores
  * (tcgen05, TMEM accumulators, TMA); every other supported shape runs on the
  * SIMT path.  Each unit of scores sums to G*W per kv head (rows are softmaxes).

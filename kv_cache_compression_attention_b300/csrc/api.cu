@@ -74,9 +74,15 @@ int kvc_device_status(void* stream) {
 }
 
 // ------------------------------------------------------------------ score
+namespace kvc {
+size_t kvc_score_ws_need(bool tc, int U, int Hq, int Hkv, int W) {
+  return tc ? score_attn_tc_ws(Hq, Hkv, W) : score_attn_simt_ws(U, Hq, W);
+}
+}  // namespace kvc
+
 size_t kvc_score_attn_workspace(int U, int Hq, int Hkv, int T, int W, int d, int dtype) {
   if (U <= 0 || Hq <= 0 || W <= 0) return 0;
-  if (kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d)) return 0;
+  if (kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d)) return kvc::score_attn_tc_ws(Hq, Hkv, W);
   return kvc::score_attn_simt_ws(U, Hq, W);
 }
 
@@ -86,17 +92,20 @@ int kvc_score_attn(const void* q_win, const void* k, int dtype, int U, int Hq, i
   if (!q_win || !k || !scores) return KVC_ERR_INVALID;
   if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
   if (U <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || W <= 0 || Hq % Hkv) return KVC_ERR_INVALID;
-  if (W > T || !isfinite(scale)) return KVC_ERR_INVALID;
+  if (W > T || !(scale > 0.0f) || !isfinite(scale)) return KVC_ERR_INVALID;
   if (d != 64 && d != 128) return KVC_ERR_UNSUPPORTED;
   if ((int64_t)U * Hkv > 65535 || (int64_t)U * Hq * W > (1ll << 31)) return KVC_ERR_UNSUPPORTED;
+  const bool tc = kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d);
+  size_t need = kvc::kvc_score_ws_need(tc, U, Hq, Hkv, W);
+  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+  if (tc && (!aligned16(q_win) || !aligned16(k) || !aligned16(workspace)))
+    return KVC_ERR_UNSUPPORTED;
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
-  if (kvc::score_attn_tc_supported(dtype, Hq, Hkv, W, d) && aligned16(q_win) && aligned16(k))
+  if (tc)
     return kvc::score_attn_tc(q_win, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores,
-                              dev, kvc::as_stream(stream));
-  size_t need = kvc::score_attn_simt_ws(U, Hq, W);
-  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+                              workspace, dev, kvc::as_stream(stream));
   return kvc::score_attn_simt(q_win, k, dtype, U, Hq, Hkv, T, W, d, scale, head_scale, causal,
                               scores, static_cast<float*>(workspace), dev,
                               kvc::as_stream(stream));

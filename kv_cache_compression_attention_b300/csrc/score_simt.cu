@@ -57,7 +57,7 @@ template <typename Tin, int D>
 __global__ void __launch_bounds__(kRowWarps * 32)
 row_lse_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int Hq, int Hkv,
                int T, int W, float scale, const float* __restrict__ head_scale, int causal,
-               float* __restrict__ lse) {
+               float* __restrict__ lse, int* status) {
   __shared__ float qs[kRowWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kRowWarps + warp;
@@ -67,7 +67,9 @@ row_lse_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int 
   const int h = (int)((row / W) % Hq);
   const int u = (int)(row / ((int64_t)W * Hq));
   const int G = Hq / Hkv, g = h / G;
-  const float c = scale * (head_scale ? head_scale[(int64_t)u * Hq + h] : 1.0f);
+  const float f = head_scale ? head_scale[(int64_t)u * Hq + h] : 1.0f;
+  if (lane == 0 && !(f > 0.0f && f < INFINITY)) report(status, KVC_ERR_INVALID);
+  const float c = scale * f;
   for (int x = lane; x < D; x += 32) qs[warp][x] = load_elem<Tin>(q + row * D, x);
   __syncwarp();
   const int last = causal ? (T - W + w) : (T - 1);
@@ -151,12 +153,12 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
 
 template <typename Tin, int D>
 int run(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W, float scale,
-        const float* hs, int causal, float* scores, float* lse, cudaStream_t s) {
+        const float* hs, int causal, float* scores, float* lse, int* status, cudaStream_t s) {
   const int64_t rows = (int64_t)U * Hq * W;
   dim3 g1((unsigned)((rows + kRowWarps - 1) / kRowWarps));
   row_lse_kernel<Tin, D><<<g1, kRowWarps * 32, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), U, Hq, Hkv, T, W, scale, hs,
-      causal, lse);
+      causal, lse, status);
   dim3 g2((unsigned)((T + kColThreads - 1) / kColThreads), (unsigned)(U * Hkv));
   col_mass_kernel<Tin, D><<<g2, kColThreads, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), U, Hq, Hkv, T, W, scale, hs,
@@ -173,13 +175,12 @@ size_t score_attn_simt_ws(int U, int Hq, int W) {
 int score_attn_simt(const void* q, const void* k, int dtype, int U, int Hq, int Hkv, int T,
                     int W, int d, float scale, const float* head_scale, int causal,
                     float* scores, float* lse_ws, const Dev& dev, cudaStream_t s) {
-  (void)dev;
   if (dtype == KVC_F32) {
-    return d == 64 ? run<float, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, s)
-                   : run<float, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, s);
+    return d == 64 ? run<float, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s)
+                   : run<float, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s);
   }
-  return d == 64 ? run<uint16_t, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, s)
-                 : run<uint16_t, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, s);
+  return d == 64 ? run<uint16_t, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s)
+                 : run<uint16_t, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s);
 }
 
 }  // namespace kvc

@@ -7,27 +7,36 @@
 //
 // The contraction Q_g (R x 128) . K_g^T (128 x T) is a real dense GEMM, so it
 // runs on tcgen05 with fp32 accumulators in TMEM.  The column mass needs
-// every row's normaliser first, so the kernel makes two passes over the
-// CTA's K tiles (the second pass finds them in L2):
+// every row's normaliser first, so each CTA makes two passes over its K
+// (the second pass finds it in L2).  K streams in super-tiles of 256 tokens;
+// every MMA item is 8 MMAs with N = 256 into one 256-column TMEM buffer:
 //
-//   pass 1  S = Q . K_tile^T  (rows on TMEM lanes, M = 128 per m-tile,
-//           N = 128 tokens): each epilogue thread owns one window row and
-//           keeps an online (max, sum) in base 2;
-//   merge   the cluster's CTAs (one cluster per (u, g), each CTA a token
-//           range) exchange their per-row partial (max, sum) through
-//           distributed shared memory -> lse_r for all R rows;
-//   pass 2  S^T = K_tile . Q^T (tokens on TMEM lanes, M = 128, N = R): each
-//           epilogue thread owns one token and sums exp2(s*c_r - lse2_r)
-//           over its half of the R columns; the two halves add in shared
-//           memory and the token's score is stored (coalesced).
+//   pass 1  S = Q_m . K_super^T, one item per 128-row m-tile (rows on TMEM
+//           lanes, 256 tokens on columns): each epilogue thread owns one
+//           window row and 64 of the tokens and keeps a running (max, sum)
+//           in base 2;
+//   merge   the CTAs that share a (u, g) publish their per-row partial
+//           (max, sum) in global memory, count themselves in on a per-group
+//           counter and wait (bounded) for the others -> lse_r of every row;
+//   pass 2  S^T = K_tile . Q^T, one item per 128-token tile (tokens on TMEM
+//           lanes, N = R): each epilogue thread owns one token and a quarter
+//           of the R columns and sums exp2(c_r * s - lse2_r); the quarters
+//           add in shared memory and the token's score is stored (coalesced).
 //
-// Warp roles (320 threads): warps 0-7 epilogue (warp w reads TMEM lanes
-// 32*(w%4)..+31, half w/4 of the columns), warp 8 TMA producer, warp 9 MMA
-// issuer and TMEM owner.  K tiles stream through a 4-stage TMA ring
-// (128 tokens x 128 dims, two 128-byte-swizzled boxes per stage); the
+// Work split: one persistent CTA per SM (cooperative launch, so every CTA
+// of a group is resident while its peers wait for it).  The (u, g) pairs
+// are processed in rounds; in a round, group i of gs CTAs owns one (u, g)
+// and CTA j of the group a contiguous range of about 8 super-tiles (1 MiB
+// of K), so that the second pass re-reads K from L2 while every SM is busy.
+//
+// Warp roles (576 threads): warps 0-15 epilogue (warp w reads TMEM lanes
+// 32*(w%4)..+31; w/4 picks its column slice), warp 16 TMA producer, warp 17
+// MMA issuer and TMEM owner.  Super-tiles stream through a 2-stage TMA ring
+// (256 tokens x 128 dims, four 128-byte-swizzled boxes per stage); the
 // accumulator is double-buffered in TMEM (2 x 256 of the 512 columns), so
-// the MMA of tile j+1 overlaps the epilogue of tile j.  Every mbarrier wait
-// is bounded (2 s); on expiry the status word records KVC_ERR_TIMEOUT and
+// the MMA of item j+1 overlaps the epilogue of item j.  The window queries
+// of the round's (u, g) sit in shared memory for both passes.  Every wait
+// is bounded (2 s): on expiry the status word records KVC_ERR_TIMEOUT and
 // the kernel runs to completion without hanging.
 #include <cudaTypedefs.h>
 
@@ -40,15 +49,20 @@ namespace {
 
 constexpr int kD = 128;              // head dim handled here
 constexpr int kTile = 128;           // tokens per K tile
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = (kEpiWarps + 2) * 32;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;         // super-stages of 256 tokens
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = kEpiThreads + 64;
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kStageBytes = kTile * kD * 2;          // 32 KiB
-constexpr uint32_t kHalfBytes = kTile * 64 * 2;           // one 64-dim box: 16 KiB
+constexpr uint32_t kBoxBytes = kTile * 64 * 2;            // one 128 x 64 box: 16 KiB
+constexpr uint32_t kHalfBytes = 2 * kBoxBytes;            // 256 tokens x 64 dims: 32 KiB
+constexpr uint32_t kStageBytes = 2 * kHalfBytes;          // 256 tokens x 128 dims: 64 KiB
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxGroup = 32;        // CTAs sharing one (u, g)
+constexpr int kMaxCtas = 1024;       // grid bound (workspace sizing)
+constexpr int kSupersPerCta = 8;     // target super-tiles (256 tokens) per CTA and round
 
 struct Params {
   int T, W, R, Hq, Hkv, G;
@@ -56,24 +70,47 @@ struct Params {
   const float* head_scale;
   int causal;
   float* scores;
-  int n_tiles;       // tiles of T
+  int n_super;       // super-tiles (256 tokens) of T
+  int heads;         // U * Hkv
+  int gs;            // CTAs per (u, g)
+  int hpr;           // (u, g) pairs per round
+  int rounds;
+  float2* parts;     // [2][grid][R] per-CTA row partials (max2, sum)
+  int* cnt;          // [hpr] arrivals per group slot, zeroed before the launch
   int* status;
 };
 
 struct SmemSmall {
   uint64_t full[kStages], empty[kStages];
   uint64_t tmem_full[2], tmem_empty[2];
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint32_t tmem_base;
   int abort_flag;
-  float m_part[256], l_part[256];      // read by the other CTAs of the cluster
-  float2 cl[256];                      // (c_r, lse2_r) for pass 2
-  float coef[256];
-  float psum[2][kTile];                // pass-2 half sums
-  float mh[2][128], lh[2][128];        // R = 128: the two column halves' stats
+  float4 cl4[128];                     // column pairs (c, c', -lse2, -lse2') for pass 2
+  float coef[256];                     // c_r = scale * f * log2(e) per window row
+  float nlse[256];                     // -lse2 per window row
+  float mpart[4][256], lpart[4][256];  // per column slice (max2, sum) of each row
+  float psum[2][4][kTile];             // pass-2 quarter sums per token
 };
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Merge of two base-2 (max, sum) pairs.
+__device__ __forceinline__ void merge_ms(float& M, float& L, float m, float l) {
+  if (m == -INFINITY) return;
+  if (m > M) { L = L * tc::ex2(M - m) + l; M = m; }
+  else       { L += l * tc::ex2(m - M); }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -86,13 +123,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t k_smem = q_smem + 2u * q_half_bytes;        // 1024-aligned (R % 8 == 0)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = tc::cluster_ctarank();
-  const uint32_t csize = tc::cluster_nctarank();
-  const int ug = blockIdx.y;                                  // u * Hkv + g
-  const int u = ug / p.Hkv, g = ug - u * p.Hkv;
-  const int tile_lo = (int)((int64_t)crank * p.n_tiles / csize);
-  const int tile_hi = (int)((int64_t)(crank + 1) * p.n_tiles / csize);
-  const int nt = tile_hi - tile_lo;
+  const int cta = blockIdx.x;
+  const int grp = cta / p.gs, slot = cta - grp * p.gs;
+  const bool in_group = grp < p.hpr;
+  // this CTA's super-tiles (pairs of 128-token K tiles) of its (u, g)
+  const int st_lo = (int)((int64_t)slot * p.n_super / p.gs);
+  const int st_hi = (int)((int64_t)(slot + 1) * p.n_super / p.gs);
+  const int ns = st_hi - st_lo;
   const int R = p.R, W = p.W, T = p.T;
   const int n_mt = R / 128;
 
@@ -100,9 +137,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], 1); }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.tmem_full[b], 1);
-      mbar_init(&sm.tmem_empty[b], kEpiWarps * 32);
+      mbar_init(&sm.tmem_empty[b], kEpiThreads);
     }
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -114,182 +152,278 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
-    tc::cluster_arrive();                       // phase 0 needs no producer work
-    if (lane == 0) {
+    // Stage layout (64 KiB): [dims 0-63 of tokens 0-255 | dims 64-127 of
+    // tokens 0-255], so each 64-dim half of a super-tile is one contiguous
+    // 256-row swizzled operand.
+    if (lane == 0 && in_group && ns > 0) {
       tc::prefetch_tmap(&tm_q);
       tc::prefetch_tmap(&tm_k);
-      const int qrow = (u * p.Hq + g * p.G) * W;
-      mbar_arrive_expect_tx(&sm.q_full, 2u * q_half_bytes);
-      tc::tma_load_2d(q_smem, &tm_q, 0, qrow, &sm.q_full);
-      tc::tma_load_2d(q_smem + q_half_bytes, &tm_q, 64, qrow, &sm.q_full);
-      for (int J = 0; J < 2 * nt; ++J) {
-        const int s = J % kStages;
-        if (J >= kStages) mbar_wait(&sm.empty[s], ((J / kStages) - 1) & 1, p.status, abort_flag);
-        const int t0 = (tile_lo + J % nt) * kTile;
-        const uint32_t dst = k_smem + (uint32_t)s * kStageBytes;
-        mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
-        tc::tma_load_3d(dst, &tm_k, 0, t0, ug, &sm.full[s]);
-        tc::tma_load_3d(dst + kHalfBytes, &tm_k, 64, t0, ug, &sm.full[s]);
+      int J = 0, qk = 0;
+      for (int k = 0; k < p.rounds; ++k) {
+        const int head = k * p.hpr + grp;
+        if (head >= p.heads) break;
+        const int u = head / p.Hkv, g = head - u * p.Hkv;
+        if (qk > 0) mbar_wait(&sm.q_empty, (qk - 1) & 1, p.status, abort_flag);
+        const int qrow = (u * p.Hq + g * p.G) * W;
+        mbar_arrive_expect_tx(&sm.q_full, 2u * q_half_bytes);
+        tc::tma_load_2d(q_smem, &tm_q, 0, qrow, &sm.q_full);
+        tc::tma_load_2d(q_smem + q_half_bytes, &tm_q, 64, qrow, &sm.q_full);
+        for (int i = 0; i < 2 * ns; ++i, ++J) {
+          const int s = J % kStages;
+          if (J >= kStages) mbar_wait(&sm.empty[s], ((J / kStages) - 1) & 1, p.status, abort_flag);
+          const int t0 = (st_lo + i % ns) * (2 * kTile);
+          const uint32_t dst = k_smem + (uint32_t)s * kStageBytes;
+          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+              tc::tma_load_3d(dst + h * kHalfBytes + tt * kBoxBytes, &tm_k, 64 * h,
+                              t0 + tt * kTile, head, &sm.full[s]);
+        }
+        ++qk;
       }
     }
-    __syncwarp();
-    tc::cluster_wait();
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
-    tc::cluster_arrive();
-    if (lane == 0) {
-      mbar_wait(&sm.q_full, 0, p.status, abort_flag);
-      tc::fence_after_sync();
-      const uint32_t idesc1 = tc::idesc_bf16_f32(128, kTile);   // pass 1: N = tokens
-      const uint32_t idesc2 = tc::idesc_bf16_f32(128, R);       // pass 2: N = rows
-      for (int J = 0; J < 2 * nt; ++J) {
-        const int s = J % kStages, b = J & 1;
-        mbar_wait(&sm.full[s], (J / kStages) & 1, p.status, abort_flag);
-        if (J >= 2) mbar_wait(&sm.tmem_empty[b], ((J >> 1) - 1) & 1, p.status, abort_flag);
+    // pass 1 items: (super-tile, m-tile), D = Q_mtile . K_super^T, N = 256
+    // pass 2 items: (super-tile, tile),   D = K_tile . Q^T,        N = R
+    // every item is 8 MMAs (K = 16 each) into one 256-column TMEM buffer
+    if (lane == 0 && in_group && ns > 0) {
+      const uint32_t idesc1 = tc::idesc_bf16_f32(128, 2 * kTile);
+      const uint32_t idesc2 = tc::idesc_bf16_f32(128, R);
+      int J = 0, item = 0, qk = 0;
+      for (int k = 0; k < p.rounds; ++k) {
+        const int head = k * p.hpr + grp;
+        if (head >= p.heads) break;
+        mbar_wait(&sm.q_full, qk & 1, p.status, abort_flag);
         tc::fence_after_sync();
-        const uint32_t kst = k_smem + (uint32_t)s * kStageBytes;
-        const uint32_t dcol = tmem + (uint32_t)b * 256u;
-        if (J < nt) {
-          for (int mt = 0; mt < n_mt; ++mt) {
+        for (int i = 0; i < 2 * ns; ++i, ++J) {
+          const int s = J % kStages;
+          mbar_wait(&sm.full[s], (J / kStages) & 1, p.status, abort_flag);
+          tc::fence_after_sync();
+          const uint32_t kst = k_smem + (uint32_t)s * kStageBytes;
+          const int n_items = (i < ns) ? n_mt : 2;
+          for (int x = 0; x < n_items; ++x, ++item) {
+            const int b = item & 1;
+            if (item >= 2) mbar_wait(&sm.tmem_empty[b], ((item >> 1) - 1) & 1, p.status, abort_flag);
+            tc::fence_after_sync();
+            const uint32_t dcol = tmem + (uint32_t)b * 256u;
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t kh = kk >> 2, ko = (kk & 3) * 32u;
-              const uint64_t a = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + mt * 128u * 128u + ko);
-              const uint64_t bd = tc::smem_desc_sw128(kst + kh * kHalfBytes + ko);
-              tc::mma_bf16(dcol + (uint32_t)mt * 128u, a, bd, idesc1, kk > 0);
+              uint64_t a, bd;
+              if (i < ns) {
+                a = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + x * 128u * 128u + ko);
+                bd = tc::smem_desc_sw128(kst + kh * kHalfBytes + ko);
+                tc::mma_bf16(dcol, a, bd, idesc1, kk > 0);
+              } else {
+                a = tc::smem_desc_sw128(kst + kh * kHalfBytes + x * kBoxBytes + ko);
+                bd = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + ko);
+                tc::mma_bf16(dcol, a, bd, idesc2, kk > 0);
+              }
+            }
+            tc::mma_commit(&sm.tmem_full[b]);
+          }
+          tc::mma_commit(&sm.empty[s]);
+        }
+        tc::mma_commit(&sm.q_empty);       // the queries are free once these MMAs finish
+        ++qk;
+      }
+    }
+  } else if (in_group && ns > 0) {
+    // ---------------------------------------------------------- epilogue
+    // Per element the inner loops issue one ex2 plus about one and a half
+    // other instructions (packed f32x2 FMA / add, three-input max trees,
+    // several independent accumulators); four epilogue warps per SM
+    // sub-partition keep the exponential unit busy across TMEM-load waits.
+    const int q4 = warp & 3, wq = warp >> 2;     // lane quadrant, column slice
+    const int et = threadIdx.x;                  // 0..511
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    // pass 1: rows on lanes; this thread owns row mt*128 + 32*q4 + lane of
+    // each m-tile and tokens [64*wq, 64*wq + 64) of every super-tile
+    const int lrow = 32 * q4 + lane;
+    // pass 2: tokens on lanes; this thread owns a quarter of the R columns
+    const int qcols = R / 4;
+    const int rc0 = wq * qcols;
+    int item = 0, kr = 0;
+    for (int k = 0; k < p.rounds; ++k, ++kr) {
+      const int head = k * p.hpr + grp;
+      if (head >= p.heads) break;
+      const int u = head / p.Hkv, g = head - u * p.Hkv;
+      for (int r = et; r < R; r += kEpiThreads) {
+        const int h = g * p.G + r / W;
+        const float f = p.head_scale ? p.head_scale[(int64_t)u * p.Hq + h] : 1.0f;
+        if (!(f > 0.0f && f < INFINITY)) report(p.status, KVC_ERR_INVALID);
+        sm.coef[r] = p.scale * f * kLog2e;
+      }
+      tc::named_sync(1, kEpiThreads);
+      // ---- pass 1: running (max, sum) of this thread's row slices
+      float c_r[2], m[2];
+      uint64_t acc[2][4];
+      int tlim[2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int row = mt * 128 + lrow;
+        c_r[mt] = (mt < n_mt) ? sm.coef[row] : 0.0f;
+        m[mt] = -INFINITY;
+        tlim[mt] = p.causal ? (T - W + row % W) : (T - 1);   // last visible token
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[mt][x] = 0ull;
+      }
+      for (int i = 0; i < ns; ++i) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          if (mt >= n_mt) break;
+          const int b = item & 1;
+          mbar_wait(&sm.tmem_full[b], (item >> 1) & 1, p.status, abort_flag);
+          tc::fence_after_sync();
+          const uint64_t c2 = tc::pk2(c_r[mt], c_r[mt]);
+          const int t0 = (st_lo + i) * (2 * kTile) + 64 * wq;
+#pragma unroll 1
+          for (int c = 0; c < 64; c += 32) {
+            float v[32];
+            tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + (uint32_t)(64 * wq + c), v);
+            const int tc0 = t0 + c;
+            if (tc0 + 31 > tlim[mt]) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = (tc0 + j <= tlim[mt]) ? v[j] : -INFINITY;
+            }
+            const float cm = tc::max32(v);
+            if (cm > m[mt]) {
+              const float sc = (m[mt] == -INFINITY) ? 0.0f : tc::ex2(c_r[mt] * (m[mt] - cm));
+              const uint64_t sc2 = tc::pk2(sc, sc);
+#pragma unroll
+              for (int x = 0; x < 4; ++x) acc[mt][x] = tc::ffma2(acc[mt][x], sc2, 0ull);
+              m[mt] = cm;
+            }
+            if (m[mt] != -INFINITY) {
+              const float nm = -c_r[mt] * m[mt];
+              const uint64_t nm2 = tc::pk2(nm, nm);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float2 x = tc::upk2(tc::ffma2(tc::pk2(v[2 * j], v[2 * j + 1]), c2, nm2));
+                acc[mt][j & 3] = tc::fadd2(acc[mt][j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+              }
             }
           }
-        } else {
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t kh = kk >> 2, ko = (kk & 3) * 32u;
-            const uint64_t a = tc::smem_desc_sw128(kst + kh * kHalfBytes + ko);
-            const uint64_t bd = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + ko);
-            tc::mma_bf16(dcol, a, bd, idesc2, kk > 0);
-          }
-        }
-        tc::mma_commit(&sm.empty[s]);
-        tc::mma_commit(&sm.tmem_full[b]);
-      }
-    }
-    __syncwarp();
-    tc::cluster_wait();
-  } else {
-    // ---------------------------------------------------------- epilogue
-    const int q4 = warp & 3, hf = warp >> 2;
-    const int et = threadIdx.x;                 // 0..255
-    for (int r = et; r < R; r += kEpiWarps * 32) {
-      const int h = g * p.G + r / W;
-      const float f = p.head_scale ? p.head_scale[(int64_t)u * p.Hq + h] : 1.0f;
-      sm.coef[r] = p.scale * f * kLog2e;
-    }
-    tc::named_sync(1, kEpiWarps * 32);
-    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    // pass 1: this thread's window row and column range
-    const int row = (R == 256) ? hf * 128 + 32 * q4 + lane : 32 * q4 + lane;
-    const int col0 = (R == 256) ? 0 : hf * 64;
-    const int ncol = (R == 256) ? 128 : 64;
-    const uint32_t mcol = (R == 256) ? (uint32_t)hf * 128u : 0u;
-    const float c_r = sm.coef[row];
-    const int tlim = p.causal ? (T - W + row % W) : (T - 1);   // last visible token
-    float m = -INFINITY, l = 0.0f;
-    for (int J = 0; J < nt; ++J) {
-      const int b = J & 1;
-      mbar_wait(&sm.tmem_full[b], (J >> 1) & 1, p.status, abort_flag);
-      tc::fence_after_sync();
-      const int t0 = (tile_lo + J) * kTile + col0;
-      for (int c = 0; c < ncol; c += 32) {
-        float v[32];
-        tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + mcol + (uint32_t)(col0 + c), v);
-        const int tc0 = t0 + c;
-        float cmax = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = (tc0 + j <= tlim) ? v[j] * c_r : -INFINITY;
-          cmax = fmaxf(cmax, v[j]);
-        }
-        const float mn = fmaxf(m, cmax);
-        if (mn != -INFINITY) {
-          float sum = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sum += tc::ex2(v[j] - mn);
-          l = l * tc::ex2(m - mn) + sum;
-          m = mn;
+          tc::fence_before_sync();
+          mbar_arrive(&sm.tmem_empty[b]);
+          ++item;
         }
       }
-      tc::fence_before_sync();
-      mbar_arrive(&sm.tmem_empty[b]);
-    }
-    if (R == 256) {
-      sm.m_part[row] = m;
-      sm.l_part[row] = l;
-    } else {
-      sm.mh[hf][row] = m;
-      sm.lh[hf][row] = l;
-      tc::named_sync(1, kEpiWarps * 32);
-      if (hf == 0) {
-        const float m2 = sm.mh[1][row], l2 = sm.lh[1][row];
-        const float mn = fmaxf(m, m2);
-        float ls = 0.0f;
-        if (mn != -INFINITY) ls = l * tc::ex2(m - mn) + l2 * tc::ex2(m2 - mn);
-        sm.m_part[row] = mn;
-        sm.l_part[row] = ls;
-      }
-    }
-    // cluster-wide merge of the per-row partials -> lse2 per row
-    tc::cluster_arrive();
-    tc::cluster_wait();
-    for (int r = et; r < R; r += kEpiWarps * 32) {
-      float M = -INFINITY;
-      const uint32_t ma = smem_u32(&sm.m_part[r]), la = smem_u32(&sm.l_part[r]);
-      for (uint32_t c = 0; c < csize; ++c) M = fmaxf(M, tc::ld_cluster_f32(tc::map_rank(ma, c)));
-      float L = 0.0f;
-      for (uint32_t c = 0; c < csize; ++c) {
-        const float mc = tc::ld_cluster_f32(tc::map_rank(ma, c));
-        if (mc != -INFINITY) L += tc::ld_cluster_f32(tc::map_rank(la, c)) * tc::ex2(mc - M);
-      }
-      sm.cl[r] = make_float2(sm.coef[r], M + __log2f(L));
-    }
-    tc::named_sync(1, kEpiWarps * 32);
-    // pass 2: this thread's token and half of the R columns
-    const int half_cols = R / 2;
-    const int rc0 = hf * half_cols;
-    for (int J = nt; J < 2 * nt; ++J) {
-      const int b = J & 1;
-      mbar_wait(&sm.tmem_full[b], (J >> 1) & 1, p.status, abort_flag);
-      tc::fence_after_sync();
-      const int tok = (tile_lo + J - nt) * kTile + 32 * q4 + lane;
-      // causal: window row w sees token tok iff w >= tok - (T - W)
-      const int wmin = p.causal ? tok - (T - W) : 0;
-      float sum = 0.0f;
-      for (int c = 0; c < half_cols; c += 32) {
-        float v[32];
-        tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + (uint32_t)(rc0 + c), v);
-        if (wmin <= 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float2 cl = sm.cl[rc0 + c + j];
-            sum += tc::ex2(fmaf(v[j], cl.x, -cl.y));
-          }
-        } else {
+      for (int mt = 0; mt < 2; ++mt) {
+        if (mt >= n_mt) break;
+        const float2 a = tc::upk2(tc::fadd2(tc::fadd2(acc[mt][0], acc[mt][1]),
+                                            tc::fadd2(acc[mt][2], acc[mt][3])));
+        sm.mpart[wq][mt * 128 + lrow] = (m[mt] == -INFINITY) ? -INFINITY : c_r[mt] * m[mt];
+        sm.lpart[wq][mt * 128 + lrow] = a.x + a.y;
+      }
+      tc::named_sync(1, kEpiThreads);
+      // ---- publish this CTA's row partials, then gather the group's
+      float2* pub = p.parts + ((size_t)(kr & 1) * gridDim.x + cta) * R;
+      if (et < R) {
+        float M = -INFINITY, L = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = rc0 + c + j;
-            const float2 cl = sm.cl[r];
-            if (r % W >= wmin) sum += tc::ex2(fmaf(v[j], cl.x, -cl.y));
+        for (int x = 0; x < 4; ++x) merge_ms(M, L, sm.mpart[x][et], sm.lpart[x][et]);
+        __stcg(pub + et, make_float2(M, L));
+        __threadfence();
+      }
+      tc::named_sync(1, kEpiThreads);
+      if (et == 0) {
+        red_release_add(&p.cnt[grp], 1);
+        const int want = p.gs * (kr + 1);
+        if (ld_acquire(&p.cnt[grp]) < want) {
+          const uint64_t t_start = globaltimer_ns();
+          for (uint32_t it = 0;; ++it) {
+            if (ld_acquire(&p.cnt[grp]) >= want) break;
+            if ((it & 15u) == 15u) {
+              if (*abort_flag) break;
+              if (globaltimer_ns() - t_start > kWaitTimeoutNs) {
+                report(p.status, KVC_ERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+              }
+            }
           }
         }
       }
-      tc::fence_before_sync();
-      mbar_arrive(&sm.tmem_empty[b]);
-      if (hf == 1) sm.psum[J & 1][32 * q4 + lane] = sum;
-      tc::named_sync(2, kEpiWarps * 32);
-      if (hf == 0 && tok < T)
-        p.scores[(int64_t)ug * T + tok] = sum + sm.psum[J & 1][32 * q4 + lane];
+      tc::named_sync(1, kEpiThreads);
+      // gather: thread (row, quarter) merges a quarter of the group's
+      // partials with all its loads in flight at once
+      {
+        const int gr = et & 255, gq = et >> 8;       // row, half of the group
+        float M = -INFINITY, L = 0.0f;
+        if (gr < R) {
+          const float2* gp = p.parts + ((size_t)(kr & 1) * gridDim.x + grp * p.gs) * R + gr;
+          const int x0 = gq * ((p.gs + 1) >> 1), x1 = min(p.gs, x0 + ((p.gs + 1) >> 1));
+          float2 q[kMaxGroup / 2];
+#pragma unroll
+          for (int y = 0; y < kMaxGroup / 2; ++y)
+            q[y] = (x0 + y < x1) ? __ldcg(gp + (size_t)(x0 + y) * R) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+          for (int y = 0; y < kMaxGroup / 2; ++y) merge_ms(M, L, q[y].x, q[y].y);
+          sm.mpart[gq][gr] = M;
+          sm.lpart[gq][gr] = L;
+        }
+      }
+      tc::named_sync(1, kEpiThreads);
+      if (et < R) {
+        float M = sm.mpart[0][et], L = sm.lpart[0][et];
+        merge_ms(M, L, sm.mpart[1][et], sm.lpart[1][et]);
+        sm.nlse[et] = -(M + __log2f(L));   // -lse2 of row et
+      }
+      tc::named_sync(1, kEpiThreads);
+      if (et < R / 2)
+        sm.cl4[et] = make_float4(sm.coef[2 * et], sm.coef[2 * et + 1], sm.nlse[2 * et],
+                                 sm.nlse[2 * et + 1]);
+      tc::named_sync(1, kEpiThreads);
+      // ---- pass 2: this thread's token and quarter of the R columns
+      for (int i = 0; i < 2 * ns; ++i, ++item) {
+        const int b = item & 1;
+        mbar_wait(&sm.tmem_full[b], (item >> 1) & 1, p.status, abort_flag);
+        tc::fence_after_sync();
+        const int tl = 32 * q4 + lane;
+        const int tok = (2 * st_lo + i) * kTile + tl;
+        // causal: window row w sees token tok iff w >= tok - (T - W)
+        const int wmin = p.causal ? tok - (T - W) : 0;
+        uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
+        for (int c = 0; c < qcols; c += 32) {
+          float v[32];
+          tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + (uint32_t)(rc0 + c), v);
+          const float4* cp = &sm.cl4[(rc0 + c) >> 1];
+          if (wmin <= 0) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float4 q = cp[j];
+              const float2 x = tc::upk2(tc::ffma2(tc::pk2(v[2 * j], v[2 * j + 1]),
+                                                  tc::pk2(q.x, q.y), tc::pk2(q.z, q.w)));
+              s2[j & 3] = tc::fadd2(s2[j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = rc0 + c + 2 * j;
+              const float4 q = cp[j];
+              const float e0 = (r % W >= wmin) ? tc::ex2(fmaf(v[2 * j], q.x, q.z)) : 0.0f;
+              const float e1 = ((r + 1) % W >= wmin) ? tc::ex2(fmaf(v[2 * j + 1], q.y, q.w)) : 0.0f;
+              s2[j & 3] = tc::fadd2(s2[j & 3], tc::pk2(e0, e1));
+            }
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&sm.tmem_empty[b]);
+        const float2 a = tc::upk2(tc::fadd2(tc::fadd2(s2[0], s2[1]), tc::fadd2(s2[2], s2[3])));
+        sm.psum[item & 1][wq][tl] = a.x + a.y;
+        tc::named_sync(2, kEpiThreads);
+        if (wq == 0 && tok < T) {
+          const float* ps = &sm.psum[item & 1][0][tl];
+          p.scores[(int64_t)head * T + tok] = (ps[0] + ps[kTile]) + (ps[2 * kTile] + ps[3 * kTile]);
+        }
+      }
     }
   }
-  // no CTA may leave while a peer still reads its shared memory
-  __syncwarp();
-  tc::cluster_arrive();
-  tc::cluster_wait();
+  __syncthreads();
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -316,6 +450,8 @@ size_t smem_bytes(int R) {
   return sizeof(SmemSmall) + 1024 /*alignment slack*/ + 2ull * R * 128 + (size_t)kStages * kStageBytes;
 }
 
+size_t parts_bytes(int R) { return 2ull * kMaxCtas * R * sizeof(float2); }
+
 }  // namespace
 
 bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d) {
@@ -324,8 +460,13 @@ bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d) {
   return R == 128 || R == 256;
 }
 
+size_t score_attn_tc_ws(int Hq, int Hkv, int W) {
+  const int R = (Hq / Hkv) * W;
+  return parts_bytes(R) + kMaxCtas * sizeof(int);
+}
+
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
-                  float scale, const float* head_scale, int causal, float* scores,
+                  float scale, const float* head_scale, int causal, float* scores, void* ws,
                   const Dev& dev, cudaStream_t s) {
   int rc = get_encoder();
   if (rc) return rc;
@@ -354,37 +495,46 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   Params p;
   p.T = T; p.W = W; p.R = R; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.scale = scale;
   p.head_scale = head_scale; p.causal = causal; p.scores = scores;
-  p.n_tiles = (T + kTile - 1) / kTile; p.status = dev.status;
+  p.n_super = (T + 2 * kTile - 1) / (2 * kTile); p.status = dev.status;
+  p.heads = U * Hkv;
   const size_t smem = smem_bytes(R);
   if ((int)smem > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
   KVC_CUDA_TRY(cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem));
-  KVC_CUDA_TRY(cudaFuncSetAttribute(score_tc_kernel,
-                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-  // cluster size: about 16 tiles (512 KiB of K) per CTA, so that the second
-  // pass re-reads K from L2; at most 16; shrink until a cluster fits a GPC
-  int C = 1;
-  while (C < 16 && (p.n_tiles + C - 1) / C > 16) C *= 2;
-  while (C > 1 && (int64_t)U * Hkv * C > 4ll * dev.sms && (p.n_tiles + C / 2 - 1) / (C / 2) <= 32) C /= 2;
+  int per_sm = 0;
+  KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel, kThreads,
+                                                             smem));
+  if (per_sm < 1) return KVC_ERR_UNSUPPORTED;
+  // work split: P resident CTAs; gs CTAs per (u, g), hpr pairs per round
+  const int P = dev.sms < kMaxCtas ? dev.sms : kMaxCtas;
+  int gs;
+  if (p.heads <= P) {
+    gs = P / p.heads;
+  } else {
+    gs = (p.n_super + kSupersPerCta - 1) / kSupersPerCta;
+    if (gs > P) gs = P;
+  }
+  if (gs > p.n_super) gs = p.n_super;
+  if (gs > kMaxGroup) gs = kMaxGroup;
+  if (gs < 1) gs = 1;
+  p.gs = gs;
+  p.hpr = P / gs;
+  if (p.hpr > p.heads) p.hpr = p.heads;
+  p.rounds = (p.heads + p.hpr - 1) / p.hpr;
+  p.parts = static_cast<float2*>(ws);
+  p.cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + parts_bytes(R));
+  const int grid = p.hpr * gs;
+  KVC_CUDA_TRY(cudaMemsetAsync(p.cnt, 0, sizeof(int) * (size_t)p.hpr, s));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  for (;;) {
-    cfg.gridDim = dim3((unsigned)C, (unsigned)(U * Hkv), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, score_tc_kernel, &cfg));
-    if (active > 0) break;
-    if (C == 1) return KVC_ERR_UNSUPPORTED;
-    C /= 2;
-  }
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: peers wait on each other
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, score_tc_kernel, tm_q, tm_k, p));
   return launch_status();
 }

@@ -11,21 +11,22 @@
 //  * A pool is one unit's Hkv heads (global top-k) or one head (per-head
 //    budget, threshold).  The cluster's C CTAs split the pool's tokens into
 //    C contiguous ranges; each CTA keeps its range's order-preserving uint32
-//    keys in shared memory, token-major (element e = j*hps + head), so the
-//    element order inside a CTA, then across CTA ranks, is exactly the
-//    tie-break order (token asc, head asc).
+//    keys in shared memory, head-major (keys[head][token]), so every pass
+//    over them is a conflict-free sweep of consecutive words.
 //  * Radix select, 4 passes of 8-bit digits, from the most significant
 //    digit: every CTA histograms its candidates that match the prefix found
-//    so far (warp-aggregated shared atomics), the cluster sums the C
-//    histograms through distributed shared memory, and every CTA picks the
-//    same digit.  After the last pass the exact key of the need-th largest
-//    candidate (thr) and the number of its equal-key elements to keep
-//    (need_eq) are known.
+//    so far (warp-aggregated shared atomics into 8 sub-histograms), adds its
+//    histogram into rank 0's with distributed-shared-memory atomics, and
+//    after one cluster barrier every CTA reads the totals and picks the same
+//    digit.  After the last pass the exact key of the need-th largest
+//    candidate (thr) and how many of its equal-key elements to keep are known.
 //  * Ties (key == thr) are only ranked when not all of them are kept: a
-//    cluster prefix of per-CTA tie counts, then a block scan, gives the
-//    element index where kept ties stop.
-//  * Emission: per head, a cluster prefix of per-CTA kept counts gives each
-//    CTA's base; a block-wide ballot scan writes ascending token indices.
+//    cluster prefix of per-CTA tie counts, then a block scan over tokens of
+//    the per-token tie counts, gives the first dropped tie in the tie-break
+//    order (token asc, head asc), as an element index e = t * hps + head.
+//  * Emission: a counting sweep and a cluster prefix give each CTA its base
+//    per head; a block-wide ballot scan over consecutive tokens then writes
+//    the ascending token indices of each head.
 //  * Offsets (exclusive scan of the counts) are a separate single-block
 //    kernel because threshold pools have data-dependent totals.
 // Every decision is an integer comparison on the fp32 bit patterns, so the
@@ -55,44 +56,54 @@ struct Args {
   int32_t* counts;
 };
 
+constexpr int kSubHist = 8;              // sub-histograms (4 warps each)
+
 struct Shared {
-  uint32_t hist[2][256];
-  uint32_t tot[256];
-  uint32_t warp_tmp[kWarps];
-  uint32_t warp_tmp2[kWarps * kMaxHps];
+  uint32_t hist[kSubHist][256];       // this CTA's sub-histograms of the current pass
+  uint32_t tot[4][256];               // cluster totals per pass (summed into rank 0)
+  uint32_t totl[256];                 // this CTA's copy of the pass totals
+  uint32_t warp_tmp[2][kWarps];       // block scans (double-buffered)
+  uint32_t warp_tot[2];
+  uint32_t hcnt[kWarps][kMaxHps];     // per-warp kept counts per head
   uint32_t xchg_ties;                 // read remotely
   uint32_t xchg_cnt[kMaxHps];         // read remotely
   uint32_t head_base[kMaxHps];
-  uint32_t sel_bin, sel_above, sel_count, ecut;
+  uint32_t sel_bin, sel_above, sel_count, ecut, tie_base;
 };
 
 __device__ __forceinline__ bool is_prot(int t, int T, int n_sink, int n_recent) {
   return t < n_sink || t >= T - n_recent;
 }
 
-// Exclusive block scan of one flag per thread; returns the prefix and sets *total.
-__device__ __forceinline__ uint32_t block_excl_scan(bool flag, Shared& sh, uint32_t* total) {
+// Exclusive block scan of one value per thread; returns the prefix and sets
+// *total.  Two barriers; consecutive calls alternate scratch buffers.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, Shared& sh, int& buf, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t ball = __ballot_sync(0xffffffffu, flag);
-  const uint32_t within = __popc(ball & ((1u << lane) - 1u));
-  if (lane == 0) sh.warp_tmp[warp] = __popc(ball);
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  uint32_t* wt = sh.warp_tmp[buf];
+  if (lane == 31) wt[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    uint32_t v = sh.warp_tmp[lane];
-    uint32_t incl = v;
+    const uint32_t x = wt[lane];
+    uint32_t y = x;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      uint32_t n = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += n;
+      const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) y += n;
     }
-    sh.warp_tmp[lane] = incl - v;                 // exclusive warp base
-    if (lane == 31) sh.warp_tmp2[0] = incl;       // block total
+    wt[lane] = y - x;
+    if (lane == 31) sh.warp_tot[buf] = y;
   }
   __syncthreads();
-  const uint32_t base = sh.warp_tmp[warp];
-  *total = sh.warp_tmp2[0];
-  __syncthreads();
-  return base + within;
+  const uint32_t r = wt[warp] + incl - v;
+  *total = sh.warp_tot[buf];
+  buf ^= 1;
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -109,19 +120,37 @@ select_kernel(Args a) {
   const int nt = t1 - t0;
   const int nloc = nt * hps;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int sbuf = 0;
 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
 
-  // ---- phase A: keys of this CTA's token range (coalesced head-major reads)
-  for (int e = tid; e < nloc; e += kThreads) {
-    const int hh = e / nt, j = e - hh * nt;
-    const int t = t0 + j;
-    const float s = __ldg(a.scores + (int64_t)(head0 + hh) * T + t);
-    keys[j * hps + hh] = is_prot(t, T, a.n_sink, a.n_recent) ? 0u : score_key(s);
+  for (int i = tid; i < 4 * 256; i += kThreads) (&sh.tot[0][0])[i] = 0u;
+  for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
+
+  // ---- phase A: keys of this CTA's token range, head-major (coalesced
+  // global reads, conflict-free shared stores, eight loads in flight)
+  for (int hh = 0; hh < hps; ++hh) {
+    const float* src = a.scores + (int64_t)(head0 + hh) * T + t0;
+    uint32_t* dst = keys + hh * nt;
+    for (int j0 = 0; j0 < nt; j0 += 8 * kThreads) {
+      float sv[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + x * kThreads + tid;
+        if (j < nt) sv[x] = __ldg(src + j);
+      }
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + x * kThreads + tid;
+        if (j < nt) dst[j] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x]);
+      }
+    }
   }
-  __syncthreads();
+  // every CTA of the cluster is running and its totals are zero before any
+  // remote update
+  cl.sync();
 
   // ---- phase B: radix select of the need-th largest candidate key
   int64_t need = 0;
@@ -141,12 +170,14 @@ select_kernel(Args a) {
     uint32_t prefix = 0, pmask = 0;
     uint32_t krem = (uint32_t)need;
     uint32_t last_count = 0;
+    uint32_t* myhist = sh.hist[warp & (kSubHist - 1)];
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      uint32_t* buf = sh.hist[pass & 1];
-      for (int b = tid; b < 256; b += kThreads) buf[b] = 0;
-      __syncthreads();
+      if (pass > 0) {
+        for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
+        __syncthreads();
+      }
       for (int e0 = 0; e0 < nloc; e0 += kThreads) {
         const int e = e0 + tid;
         uint32_t digit = 0xffffu;
@@ -155,21 +186,24 @@ select_kernel(Args a) {
           if (key != 0u && (key & pmask) == prefix) digit = (key >> shift) & 255u;
         }
         const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (digit != 0xffffu && lane == __ffs(peers) - 1) atomicAdd(&buf[digit], __popc(peers));
+        if (digit != 0xffffu && lane == __ffs(peers) - 1) atomicAdd(&myhist[digit], __popc(peers));
       }
       __syncthreads();
-      cl.sync();
+      // every CTA adds its histogram into rank 0's totals of this pass
       if (tid < 256) {
-        uint32_t tot = 0;
-        for (int r = 0; r < C; ++r) tot += cl.map_shared_rank(buf, r)[tid];
-        sh.tot[tid] = tot;
+        uint32_t h = 0;
+#pragma unroll
+        for (int x = 0; x < kSubHist; ++x) h += sh.hist[x][tid];
+        if (h) atomicAdd(cl.map_shared_rank(&sh.tot[pass][tid], 0), h);
       }
+      cl.sync();
+      if (tid < 256) sh.totl[tid] = *cl.map_shared_rank(&sh.tot[pass][tid], 0);
       __syncthreads();
       if (warp == 0) {
         uint32_t cnt[8];
         uint32_t lsum = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { cnt[i] = sh.tot[lane * 8 + i]; lsum += cnt[i]; }
+        for (int i = 0; i < 8; ++i) { cnt[i] = sh.totl[lane * 8 + i]; lsum += cnt[i]; }
         uint32_t suffix = lsum;                  // sum over lanes >= lane
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -193,7 +227,6 @@ select_kernel(Args a) {
       last_count = sh.sel_count;
       prefix |= bin << shift;
       pmask |= 255u << shift;
-      __syncthreads();
     }
     thr = prefix;
     // ---- ties: keep the first krem elements with key == thr in (t, g) order
@@ -201,32 +234,45 @@ select_kernel(Args a) {
       uint32_t mine = 0;
       for (int e = tid; e < nloc; e += kThreads) mine += (keys[e] == thr);
       mine = __reduce_add_sync(0xffffffffu, mine);
-      if (lane == 0) sh.warp_tmp[warp] = mine;
+      if (lane == 0) sh.warp_tmp[0][warp] = mine;
       __syncthreads();
       if (tid == 0) {
         uint32_t s = 0;
-        for (int w = 0; w < kWarps; ++w) s += sh.warp_tmp[w];
+        for (int w = 0; w < kWarps; ++w) s += sh.warp_tmp[0][w];
         sh.xchg_ties = s;
       }
       __syncthreads();
       cl.sync();
-      uint32_t base = 0;
-      for (int r = 0; r < rank; ++r) base += *cl.map_shared_rank(&sh.xchg_ties, r);
+      if (tid == 0) {
+        uint32_t b = 0;
+        for (int r = 0; r < rank; ++r) b += *cl.map_shared_rank(&sh.xchg_ties, r);
+        sh.tie_base = b;
+      }
+      __syncthreads();
+      const uint32_t base = sh.tie_base;
       const uint32_t local_ties = sh.xchg_ties;
       if (base >= krem) ecut = 0;
       else if (base + local_ties <= krem) ecut = (uint32_t)nloc;
       else {
-        const uint32_t want = krem - base;     // ties of this CTA to keep (>= 1)
-        if (tid == 0) sh.ecut = (uint32_t)nloc;
+        // the first dropped tie has local rank `want` in (token, head) order
+        const uint32_t want = krem - base;     // 1 <= want < local_ties
         uint32_t carry = 0;
-        for (int e0 = 0; e0 < nloc; e0 += kThreads) {
-          const int e = e0 + tid;
-          const bool f = e < nloc && keys[e] == thr;
+        for (int j0 = 0; j0 < nt; j0 += kThreads) {
+          const int j = j0 + tid;
+          uint32_t c = 0;
+          if (j < nt)
+            for (int hh = 0; hh < hps; ++hh) c += (keys[hh * nt + j] == thr);
           uint32_t total;
-          const uint32_t pos = block_excl_scan(f, sh, &total);
-          if (f && carry + pos == want) sh.ecut = (uint32_t)e;   // first dropped tie
+          const uint32_t excl = carry + block_scan(c, sh, sbuf, &total);
+          if (c && excl <= want && want < excl + c) {
+            uint32_t k = want - excl;          // 0-based tie index inside token j
+            int hh = 0;
+            for (; hh < hps; ++hh)
+              if (keys[hh * nt + j] == thr) { if (k == 0) break; --k; }
+            sh.ecut = (uint32_t)(j * hps + hh);
+          }
           carry += total;
-          if (carry > want) break;                              // uniform across the block
+          if (carry > want) break;             // uniform across the block
         }
         __syncthreads();
         ecut = sh.ecut;
@@ -236,37 +282,27 @@ select_kernel(Args a) {
     }
   }
 
-  // kept(e): protected, strictly above thr, or a kept tie
-  auto kept = [&](int e) -> bool {
-    const uint32_t key = keys[e];
+  // kept(hh, j): protected, strictly above thr, or a kept tie
+  auto kept = [&](int hh, int j) -> bool {
+    const uint32_t key = keys[hh * nt + j];
     if (key == 0u) return true;
     if (a.mode == KVC_SEL_THRESHOLD) return key >= thr;
-    return key > thr || (key == thr && (uint32_t)e < ecut);
+    return key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut);
   };
 
   // ---- phase D: per-head counts, cluster prefix, ascending emission
-  uint32_t cnt[kMaxHps];
-#pragma unroll
-  for (int hh = 0; hh < kMaxHps; ++hh) cnt[hh] = 0;
-  for (int e = tid; e < nloc; e += kThreads) {
-    const int hh = e % hps;
-    if (kept(e)) {
-#pragma unroll
-      for (int x = 0; x < kMaxHps; ++x) cnt[x] += (x == hh);
-    }
-  }
-#pragma unroll
-  for (int hh = 0; hh < kMaxHps; ++hh) {
-    const uint32_t v = __reduce_add_sync(0xffffffffu, cnt[hh]);
-    if (lane == 0) sh.warp_tmp2[hh * kWarps + warp] = v;
+  for (int hh = 0; hh < hps; ++hh) {
+    uint32_t c = 0;
+    for (int j = tid; j < nt; j += kThreads) c += kept(hh, j);
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) sh.hcnt[warp][hh] = c;
   }
   __syncthreads();
   if (tid < hps) {
     uint32_t s = 0;
-    for (int w = 0; w < kWarps; ++w) s += sh.warp_tmp2[tid * kWarps + w];
+    for (int w = 0; w < kWarps; ++w) s += sh.hcnt[w][tid];
     sh.xchg_cnt[tid] = s;
   }
-  __syncthreads();
   cl.sync();
   if (tid < hps) {
     uint32_t base = 0, total = 0;
@@ -284,11 +320,26 @@ select_kernel(Args a) {
     uint32_t carry = sh.head_base[hh];
     for (int j0 = 0; j0 < nt; j0 += kThreads) {
       const int j = j0 + tid;
-      const bool f = j < nt && kept(j * hps + hh);
-      uint32_t total;
-      const uint32_t pos = block_excl_scan(f, sh, &total);
-      if (f) out[carry + pos] = t0 + j;
-      carry += total;
+      const bool f = j < nt && kept(hh, j);
+      const uint32_t ball = __ballot_sync(0xffffffffu, f);
+      uint32_t* wt = sh.warp_tmp[sbuf];
+      if (lane == 0) wt[warp] = __popc(ball);
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t x = wt[lane];
+        uint32_t y = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
+          if (lane >= off) y += n;
+        }
+        wt[lane] = y - x;
+        if (lane == 31) sh.warp_tot[sbuf] = y;
+      }
+      __syncthreads();
+      if (f) out[carry + wt[warp] + __popc(ball & ((1u << lane) - 1u))] = t0 + j;
+      carry += sh.warp_tot[sbuf];
+      sbuf ^= 1;
     }
   }
   // no CTA may leave while a peer can still read its shared memory

@@ -78,6 +78,8 @@ def test_score_attn_rejects_bad_arguments(lib):
     assert call(W=65) == -1              # W > T
     assert call(T=0) == -1
     assert call(scale=float("nan")) == -1
+    assert call(scale=0.0) == -1
+    assert call(scale=-0.1) == -1
     assert call(d=96) == -2
 
 
@@ -121,6 +123,10 @@ def test_workspace_queries_are_pure_host(lib):
     n = lib.kvc_decode_workspace(64, 32, 8, 128, 10086, 1)
     chunks = (10086 + 511) // 512
     assert n == 64 * 8 * chunks * 4 * (128 + 2) * 4
-    # tensor-core scoring path needs no workspace; the SIMT path keeps one lse per row
-    assert lib.kvc_score_attn_workspace(1, 32, 8, 32768, 64, 128, 1) == 0
+    # tensor-core scoring path: per-CTA row partials (2 buffers x 1024 CTAs x G*W rows of
+    # (max, sum)) + 1024 group counters, independent of U and T; the SIMT path keeps one
+    # lse per window row
+    tc = 2 * 1024 * 256 * 8 + 1024 * 4
+    assert lib.kvc_score_attn_workspace(1, 32, 8, 32768, 64, 128, 1) == tc
+    assert lib.kvc_score_attn_workspace(128, 32, 8, 16384, 64, 128, 1) == tc
     assert lib.kvc_score_attn_workspace(1, 8, 4, 1024, 32, 64, 0) == 8 * 32 * 4

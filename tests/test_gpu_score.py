@@ -123,3 +123,16 @@ def test_score_linear_qwen128k_sampled_rows(B):
     # outputs ~ N(0,1): about 30.85% of the tokens score >= 0.5
     frac = (out >= 0.5).float().mean().item()
     assert abs(frac - 0.3085) < 0.01
+
+
+@pytest.mark.parametrize("dtype,d,G,W", [(torch.bfloat16, 128, 4, 64), (torch.float32, 64, 2, 32)])
+def test_score_attn_rejects_non_positive_temperature_on_device(B, dtype, d, G, W):
+    U, Hkv, T = 1, 2, 300
+    q = rand((U, Hkv * G, W, d), dtype, 1)
+    k = rand((U, Hkv, T, d), dtype, 2)
+    hs = torch.ones((U, Hkv * G), device="cuda")
+    hs[0, 3] = 0.0
+    out = torch.empty((U, Hkv, T), device="cuda")
+    B.kvc_score_attn(q, k, out, d ** -0.5, head_scale=hs)
+    assert B.kvc_device_status() == -1            # KVC_ERR_INVALID, recorded on the device
+    assert B.kvc_device_status() == 0
