@@ -11,6 +11,8 @@
 // -- one binary search over the offsets per block, then a forward walk --
 // and the warp copies the block's rows with 16-byte non-caching loads and
 // streaming stores, several vectors in flight per lane.
+#include <atomic>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -18,7 +20,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBlockRows = 16;    // output rows per warp task
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane and tensor
 constexpr int kMaxCachedHeads = 6144;   // offsets kept in shared memory up to this many heads
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -126,9 +128,16 @@ int compact_launch(const void* k, const void* v, int row_bytes, int U, int Hkv, 
   while ((1 << shift) < vpr) ++shift;
   const int n_heads = U * Hkv;
   const size_t smem = n_heads < kMaxCachedHeads ? (size_t)(n_heads + 1) * sizeof(int64_t) : 0;
-  int per_sm = 0;
-  KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_kernel, kThreads, smem));
-  if (per_sm < 1) per_sm = 1;
+  // resident blocks per SM at the largest shared-memory size (a lower bound
+  // for every launch), once per device
+  static std::atomic<int> per_sm_memo[64];
+  int per_sm = per_sm_memo[dev.device & 63].load();
+  if (per_sm == 0) {
+    KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, compact_kernel, kThreads, (size_t)kMaxCachedHeads * sizeof(int64_t)));
+    if (per_sm < 1) per_sm = 1;
+    per_sm_memo[dev.device & 63].store(per_sm);
+  }
   const int blocks = dev.sms * per_sm;
   compact_kernel<<<blocks, kThreads, smem, s>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), shift, T, U * Hkv, kept_idx,

@@ -21,14 +21,17 @@
 //            no CTA of this step reads a row another one writes), writes out
 //            and lse, then appends k_new / v_new at row start_i + L and
 //            bumps len.
+#include <atomic>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
 namespace {
 
 constexpr int kChunk = 512;     // rows per partial CTA
-constexpr int kGroup = 16;      // rows per warp step
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;       // compute warps per partial CTA
+constexpr int kStageRows = 32;  // rows per shared-memory stage (8 per compute warp)
+constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -75,15 +78,72 @@ struct Raw {
   }
 };
 
+// N consecutive elements of a shared-memory row, loaded with 16/8/4-byte
+// vector loads.
+template <typename Tin, int N>
+struct SRaw {
+  static constexpr int kWords = N * (int)sizeof(Tin) / 4;
+  uint32_t w[kWords];
+  __device__ __forceinline__ void load(const Tin* p) {
+    if constexpr (kWords % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < kWords / 4; ++i) {
+        const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    } else if constexpr (kWords == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x; w[1] = v.y;
+    } else {
+      static_assert(kWords == 1, "vector width");
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) w[i] = 0u;
+  }
+  __device__ __forceinline__ float operator[](int x) const {
+    if constexpr (sizeof(Tin) == 2) return (x & 1) ? bf16hi(w[x >> 1]) : bf16lo(w[x >> 1]);
+    else return __uint_as_float(w[x]);
+  }
+};
+
+// Bulk asynchronous copy global -> shared, completing on an mbarrier
+// (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <typename Tin, int D>
+constexpr size_t partial_smem_bytes() {
+  return 2ull * kStages * kStageRows * D * sizeof(Tin);
+}
+
+// One CTA per (kv head, 512-row chunk).  A producer warp streams the chunk's
+// K and V rows (contiguous in the pool) into a 4-stage shared-memory ring
+// with bulk asynchronous copies; four compute warps take 8 rows of every
+// stage each.
 template <typename Tin, int D, int G>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__((kWarps + 1) * 32)
 decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
                       const Tin* __restrict__ vc, const int64_t* __restrict__ start,
                       const int32_t* __restrict__ len, int Hkv, int max_chunks, float scale_log2,
-                      float* __restrict__ ws) {
+                      float* __restrict__ ws, int* status) {
   constexpr int DPL = D / 8;     // q.k dims per lane (8 lanes per row)
   constexpr int VPL = D / 32;    // output dims per lane
-  __shared__ float p_sm[kWarps][kGroup][G];
+  constexpr int RPW = kStageRows / kWarps;   // rows per warp and stage
+  constexpr uint32_t RB = D * sizeof(Tin);   // bytes per row
+  extern __shared__ __align__(128) uint8_t smem_dec[];
+  Tin* ks = reinterpret_cast<Tin*>(smem_dec);
+  Tin* vs = ks + kStages * kStageRows * D;
+  __shared__ uint64_t full[kStages], empty[kStages];
+  __shared__ float p_sm[kWarps][RPW][G];
   __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
   __shared__ float acc_sm[kWarps][G][D];
 
@@ -91,13 +151,39 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
   const int L = len[i];
   const int rb = c * kChunk;
   if (rb >= L) return;
-  const int re = min(L, rb + kChunk);
+  const int nrows = min(L, rb + kChunk) - rb;
+  const int nst = (nrows + kStageRows - 1) / kStageRows;
   const int u = i / Hkv, g = i - u * Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r8 = lane >> 3, sub = lane & 7;
-  const Tin* kbase = kc + start[i] * D;
-  const Tin* vbase = vc + start[i] * D;
 
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kWarps); }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const Tin* kb = kc + (start[i] + rb) * D;
+      const Tin* vb = vc + (start[i] + rb) * D;
+      for (int st = 0; st < nst; ++st) {
+        const int slot = st % kStages;
+        if (st >= kStages) mbar_wait(&empty[slot], ((st / kStages) - 1) & 1, status, nullptr);
+        const int n = min(kStageRows, nrows - st * kStageRows);
+        const uint32_t bytes = (uint32_t)n * RB;
+        mbar_arrive_expect_tx(&full[slot], 2u * bytes);
+        bulk_g2s(smem_u32(ks + (size_t)slot * kStageRows * D), kb + (size_t)st * kStageRows * D,
+                 bytes, &full[slot]);
+        bulk_g2s(smem_u32(vs + (size_t)slot * kStageRows * D), vb + (size_t)st * kStageRows * D,
+                 bytes, &full[slot]);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const int r8 = lane >> 3, sub = lane & 7;
   float qr[G][DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -106,7 +192,6 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
 #pragma unroll
     for (int x = 0; x < DPL; ++x) qr[h][x] = rq[x];
   }
-
   float m[G], l[G], acc[G][VPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -114,60 +199,67 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
 #pragma unroll
     for (int x = 0; x < VPL; ++x) acc[h][x] = 0.0f;
   }
-
-  for (int g0 = rb + warp * kGroup; g0 < re; g0 += kWarps * kGroup) {
-    // issue every load of the 16-row group first: K by 8-lane teams (pass p
-    // covers rows g0 + 4p + r8), V by the whole warp (lane owns d/32 columns)
-    Raw<Tin, DPL> kr[4];
-    Raw<Tin, VPL> vr[kGroup];
+  const int r0 = warp * RPW;                   // this warp's rows inside a stage
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kStages;
+    mbar_wait(&full[slot], (st / kStages) & 1, status, nullptr);
+    const int n = min(kStageRows, nrows - st * kStageRows);
+    const Tin* kst = ks + ((size_t)slot * kStageRows + r0) * D;
+    const Tin* vst = vs + ((size_t)slot * kStageRows + r0) * D;
+    // K rows by 8-lane teams (pass p covers rows 4p + r8), V rows by the
+    // whole warp (lane owns d/32 columns)
+    SRaw<Tin, DPL> kr[RPW / 4];
+    SRaw<Tin, VPL> vr[RPW];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const int row = g0 + 4 * p + r8;
-      if (row < re) kr[p].load(kbase + (int64_t)row * D + sub * DPL);
-      else kr[p].zero();
+    for (int pp = 0; pp < RPW / 4; ++pp) {
+      const int row = 4 * pp + r8;
+      if (r0 + row < n) kr[pp].load(kst + row * D + sub * DPL);
+      else kr[pp].zero();
     }
 #pragma unroll
-    for (int rr = 0; rr < kGroup; ++rr) {
-      if (g0 + rr < re) vr[rr].load(vbase + (int64_t)(g0 + rr) * D + lane * VPL);
+    for (int rr = 0; rr < RPW; ++rr) {
+      if (r0 + rr < n) vr[rr].load(vst + rr * D + lane * VPL);
       else vr[rr].zero();
     }
-    float s[4][G];
+    float sc[RPW / 4][G];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const int row = g0 + 4 * p + r8;
+    for (int pp = 0; pp < RPW / 4; ++pp) {
+      const int row = 4 * pp + r8;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float a = 0.0f;
 #pragma unroll
-        for (int x = 0; x < DPL; ++x) a = fmaf(qr[h][x], kr[p][x], a);
+        for (int x = 0; x < DPL; ++x) a = fmaf(qr[h][x], kr[pp][x], a);
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
         a += __shfl_xor_sync(0xffffffffu, a, 4);
-        s[p][h] = (row < re) ? a * scale_log2 : -INFINITY;
+        sc[pp][h] = (r0 + row < n) ? a * scale_log2 : -INFINITY;
       }
     }
     // online softmax update (base 2), identical in all lanes
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float mx = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
+      float mx = sc[0][h];
+#pragma unroll
+      for (int pp = 1; pp < RPW / 4; ++pp) mx = fmaxf(mx, sc[pp][h]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float mn = fmaxf(m[h], mx);
-      const float alpha = exp2f(m[h] - mn);     // m = -inf at start -> 0
+      const float alpha = (mn == -INFINITY) ? 1.0f : exp2f(m[h] - mn);   // m = -inf -> 0
       m[h] = mn;
       l[h] *= alpha;
 #pragma unroll
       for (int x = 0; x < VPL; ++x) acc[h][x] *= alpha;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float e = exp2f(s[p][h] - mn);
+      for (int pp = 0; pp < RPW / 4; ++pp) {
+        const float e = (mn == -INFINITY) ? 0.0f : exp2f(sc[pp][h] - mn);
         l[h] += e;                               // summed over the 4 row teams at the end
-        if (sub == 0) p_sm[warp][4 * p + r8][h] = e;
+        if (sub == 0) p_sm[warp][4 * pp + r8][h] = e;
       }
     }
     __syncwarp();
 #pragma unroll
-    for (int rr = 0; rr < kGroup; ++rr) {
+    for (int rr = 0; rr < RPW; ++rr) {
       // rows past the end carry p = 0 and zeroed V
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -176,7 +268,9 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
         for (int x = 0; x < VPL; ++x) acc[h][x] = fmaf(pw, vr[rr][x], acc[h][x]);
       }
     }
+    // every lane has consumed its shared-memory reads of this stage
     __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
   }
   // l: each 8-lane team summed its own rows -> add the 4 teams
 #pragma unroll
@@ -192,7 +286,7 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int x = 0; x < VPL; ++x) acc_sm[warp][h][lane * VPL + x] = acc[h][x];
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");   // compute warps only
   // merge the warps: thread -> (h, column block)
   float* out = ws + ((int64_t)i * max_chunks + c) * G * (D + 2);
   for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
@@ -297,9 +391,16 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
   const float sl2 = scale * kLog2e;
   if (max_chunks > 0) {
     dim3 grid((unsigned)max_chunks, (unsigned)n);
-    decode_partial_kernel<Tin, D, G><<<grid, kWarps * 32, 0, s>>>(
+    const size_t smem = partial_smem_bytes<Tin, D>();
+    auto kern = decode_partial_kernel<Tin, D, G>;
+    static std::atomic<uint64_t> attr_done{0};          // one bit per device
+    if (!(attr_done.load() & (1ull << (dev.device & 63)))) {
+      KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      attr_done.fetch_or(1ull << (dev.device & 63));
+    }
+    kern<<<grid, (kWarps + 1) * 32, smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
-        start, len, Hkv, max_chunks, sl2, ws);
+        start, len, Hkv, max_chunks, sl2, ws, dev.status);
   }
   decode_combine_kernel<Tin, D, G><<<n, D, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc), start, len,

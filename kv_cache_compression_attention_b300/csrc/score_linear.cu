@@ -11,6 +11,8 @@
 // shared memory (laid out chunk-interleaved so a warp's 32 loads hit 32
 // consecutive 16-byte words) and applies it to all 8 rows.  The 8 x Hkv
 // partial sums are reduced across the warp with xor-shuffles at the end.
+#include <atomic>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -120,7 +122,13 @@ int run(const void* hidden, const void* weight, const float* bias, int U, int T,
         float* scores, const Dev& dev, cudaStream_t s) {
   const size_t smem = (size_t)Dh * HK * sizeof(float);
   auto kern = linear_kernel<Tin, HK>;
-  KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  // shared-memory attribute at the largest supported weight size, once per
+  // device and instantiation
+  static std::atomic<uint64_t> attr_done{0};
+  if (!(attr_done.load() & (1ull << (dev.device & 63)))) {
+    KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024));
+    attr_done.fetch_or(1ull << (dev.device & 63));
+  }
   int per_sm = 0;
   KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem));
   if (per_sm < 1) return KVC_ERR_UNSUPPORTED;

@@ -16,12 +16,13 @@
 //           window row and 64 of the tokens and keeps a running (max, sum)
 //           in base 2;
 //   merge   the CTAs that share a (u, g) publish their per-row partial
-//           (max, sum) in global memory, count themselves in on a per-group
-//           counter and wait (bounded) for the others -> lse_r of every row;
+//           (max, sum) in global memory with a per-launch tag and wait
+//           (bounded) for the others' tags -> lse_r of every row;
 //   pass 2  S^T = K_tile . Q^T, one item per 128-token tile (tokens on TMEM
 //           lanes, N = R): each epilogue thread owns one token and a quarter
-//           of the R columns and sums exp2(c_r * s - lse2_r); the quarters
-//           add in shared memory and the token's score is stored (coalesced).
+//           of the R columns and sums exp2(c_r * s - lse2_r); quarters 1-3
+//           hand their sums to quarter 0 through double-buffered shared slots
+//           guarded by mbarriers, and quarter 0 stores the token's score.
 //
 // Work split: one persistent CTA per SM (cooperative launch, so every CTA
 // of a group is resident while its peers wait for it).  The (u, g) pairs
@@ -40,6 +41,8 @@
 // the kernel runs to completion without hanging.
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -76,7 +79,8 @@ struct Params {
   int hpr;           // (u, g) pairs per round
   int rounds;
   float2* parts;     // [2][grid][R] per-CTA row partials (max2, sum)
-  int* cnt;          // [hpr] arrivals per group slot, zeroed before the launch
+  uint64_t* tags;    // [2][kMaxCtas] per-CTA publication tags
+  uint64_t tag0;     // this launch's tag base (unique per launch)
   int* status;
 };
 
@@ -84,6 +88,7 @@ struct SmemSmall {
   uint64_t full[kStages], empty[kStages];
   uint64_t tmem_full[2], tmem_empty[2];
   uint64_t q_full, q_empty;
+  uint64_t psum_full[2], psum_empty[2];  // pass-2 quarter sums: written / consumed
   uint32_t tmem_base;
   int abort_flag;
   float4 cl4[128];                     // column pairs (c, c', -lse2, -lse2') for pass 2
@@ -95,14 +100,14 @@ struct SmemSmall {
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Merge of two base-2 (max, sum) pairs.
@@ -141,6 +146,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.psum_full[b], 12);    // the 12 warps of quarters 1-3
+      mbar_init(&sm.psum_empty[b], 4);    // the 4 warps of quarter 0
+    }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -245,7 +254,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // pass 2: tokens on lanes; this thread owns a quarter of the R columns
     const int qcols = R / 4;
     const int rc0 = wq * qcols;
-    int item = 0, kr = 0;
+    int item = 0, kr = 0, p2 = 0;
     for (int k = 0; k < p.rounds; ++k, ++kr) {
       const int head = k * p.hpr + grp;
       if (head >= p.heads) break;
@@ -330,13 +339,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __threadfence();
       }
       tc::named_sync(1, kEpiThreads);
-      if (et == 0) {
-        red_release_add(&p.cnt[grp], 1);
-        const int want = p.gs * (kr + 1);
-        if (ld_acquire(&p.cnt[grp]) < want) {
+      // tag this CTA's partials as published for this launch and round, then
+      // thread x waits (bounded) for group member x's tag
+      {
+        const uint64_t tag = p.tag0 + (uint64_t)kr;
+        uint64_t* tags = p.tags + (size_t)(kr & 1) * kMaxCtas;
+        if (et == 0) st_release_u64(tags + cta, tag);
+        if (et < p.gs && ld_acquire_u64(tags + grp * p.gs + et) != tag) {
           const uint64_t t_start = globaltimer_ns();
           for (uint32_t it = 0;; ++it) {
-            if (ld_acquire(&p.cnt[grp]) >= want) break;
+            if (ld_acquire_u64(tags + grp * p.gs + et) == tag) break;
             if ((it & 15u) == 15u) {
               if (*abort_flag) break;
               if (globaltimer_ns() - t_start > kWaitTimeoutNs) {
@@ -414,12 +426,23 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc::fence_before_sync();
         mbar_arrive(&sm.tmem_empty[b]);
         const float2 a = tc::upk2(tc::fadd2(tc::fadd2(s2[0], s2[1]), tc::fadd2(s2[2], s2[3])));
-        sm.psum[item & 1][wq][tl] = a.x + a.y;
-        tc::named_sync(2, kEpiThreads);
-        if (wq == 0 && tok < T) {
-          const float* ps = &sm.psum[item & 1][0][tl];
-          p.scores[(int64_t)head * T + tok] = (ps[0] + ps[kTile]) + (ps[2 * kTile] + ps[3 * kTile]);
+        // quarters 1-3 hand their sums to quarter 0 through a double-buffered
+        // slot; only the two quarters involved wait, never the whole epilogue
+        const int pb = p2 & 1, use = p2 >> 1;
+        if (wq != 0) {
+          if (use > 0) mbar_wait(&sm.psum_empty[pb], (use - 1) & 1, p.status, abort_flag);
+          sm.psum[pb][wq][tl] = a.x + a.y;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.psum_full[pb]);
+        } else {
+          mbar_wait(&sm.psum_full[pb], use & 1, p.status, abort_flag);
+          const float* ps = &sm.psum[pb][0][tl];
+          if (tok < T)
+            p.scores[(int64_t)head * T + tok] = (a.x + a.y + ps[kTile]) + (ps[2 * kTile] + ps[3 * kTile]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.psum_empty[pb]);
         }
+        ++p2;
       }
     }
   }
@@ -452,6 +475,14 @@ size_t smem_bytes(int R) {
 
 size_t parts_bytes(int R) { return 2ull * kMaxCtas * R * sizeof(float2); }
 
+// Launch tags: a process-wide counter seeded from the clock, in steps of
+// 2^16 (a launch uses tag_base + round, rounds < 2^16).
+uint64_t next_tag_base() {
+  static std::atomic<uint64_t> counter{
+      (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() << 20};
+  return counter.fetch_add(1ull << 16) + (1ull << 16);
+}
+
 }  // namespace
 
 bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d) {
@@ -462,7 +493,7 @@ bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d) {
 
 size_t score_attn_tc_ws(int Hq, int Hkv, int W) {
   const int R = (Hq / Hkv) * W;
-  return parts_bytes(R) + kMaxCtas * sizeof(int);
+  return parts_bytes(R) + 2ull * kMaxCtas * sizeof(uint64_t);
 }
 
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
@@ -499,12 +530,24 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   p.heads = U * Hkv;
   const size_t smem = smem_bytes(R);
   if ((int)smem > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
-  KVC_CUDA_TRY(cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem));
-  int per_sm = 0;
-  KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel, kThreads,
-                                                             smem));
-  if (per_sm < 1) return KVC_ERR_UNSUPPORTED;
+  // attribute set-up and occupancy check, once per device and row count
+  {
+    static std::mutex mu;
+    static int per_sm_memo[64][2];
+    std::lock_guard<std::mutex> lock(mu);
+    int& per_sm = per_sm_memo[dev.device & 63][R == 256];
+    if (per_sm == 0) {
+      // the attribute is the kernel's, shared by both row counts: the larger
+      const size_t smax = smem_bytes(256);
+      if ((int)smax > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
+      KVC_CUDA_TRY(cudaFuncSetAttribute(score_tc_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
+      KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel,
+                                                                 kThreads, smem));
+      if (per_sm < 1) per_sm = -1;
+    }
+    if (per_sm < 1) return KVC_ERR_UNSUPPORTED;
+  }
   // work split: P resident CTAs; gs CTAs per (u, g), hpr pairs per round
   const int P = dev.sms < kMaxCtas ? dev.sms : kMaxCtas;
   int gs;
@@ -522,9 +565,11 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   if (p.hpr > p.heads) p.hpr = p.heads;
   p.rounds = (p.heads + p.hpr - 1) / p.hpr;
   p.parts = static_cast<float2*>(ws);
-  p.cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + parts_bytes(R));
+  p.tags = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + parts_bytes(R));
+  // tags are unique per launch (and per round inside it), so the workspace
+  // needs no clearing: stale tags of earlier launches never match
+  p.tag0 = next_tag_base();
   const int grid = p.hpr * gs;
-  KVC_CUDA_TRY(cudaMemsetAsync(p.cnt, 0, sizeof(int) * (size_t)p.hpr, s));
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3((unsigned)grid, 1, 1);

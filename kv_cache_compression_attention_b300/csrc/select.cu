@@ -15,7 +15,8 @@
 //    over them is a conflict-free sweep of consecutive words.
 //  * Radix select, 4 passes of 8-bit digits, from the most significant
 //    digit: every CTA histograms its candidates that match the prefix found
-//    so far (warp-aggregated shared atomics into 8 sub-histograms), adds its
+//    so far (into 8 sub-histograms; one atomic per warp when all its
+//    candidates share the digit, as in the first pass), adds its
 //    histogram into rank 0's with distributed-shared-memory atomics, and
 //    after one cluster barrier every CTA reads the totals and picks the same
 //    digit.  After the last pass the exact key of the need-th largest
@@ -32,6 +33,10 @@
 // Every decision is an integer comparison on the fp32 bit patterns, so the
 // result is bit-exact and deterministic.
 #include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "kvc_internal.cuh"
 
@@ -57,6 +62,7 @@ struct Args {
 };
 
 constexpr int kSubHist = 8;              // sub-histograms (4 warps each)
+constexpr int kList2 = 4096;             // capacity of the second candidate list
 
 struct Shared {
   uint32_t hist[kSubHist][256];       // this CTA's sub-histograms of the current pass
@@ -65,10 +71,13 @@ struct Shared {
   uint32_t warp_tmp[2][kWarps];       // block scans (double-buffered)
   uint32_t warp_tot[2];
   uint32_t hcnt[kWarps][kMaxHps];     // per-warp kept counts per head
+  uint32_t emit_tmp[2][kMaxHps][kWarps];  // emission scans (double-buffered)
+  uint32_t emit_tot[2][kMaxHps];
   uint32_t xchg_ties;                 // read remotely
   uint32_t xchg_cnt[kMaxHps];         // read remotely
   uint32_t head_base[kMaxHps];
-  uint32_t sel_bin, sel_above, sel_count, ecut, tie_base;
+  uint32_t sel_bin, sel_above, sel_count, ecut, tie_base, nlist;
+  uint32_t list2[kList2];             // candidates of the last two passes
 };
 
 __device__ __forceinline__ bool is_prot(int t, int T, int n_sink, int n_recent) {
@@ -125,26 +134,33 @@ select_kernel(Args a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
+  // (the first candidate list follows the keys: nloc more words)
 
   for (int i = tid; i < 4 * 256; i += kThreads) (&sh.tot[0][0])[i] = 0u;
   for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
 
   // ---- phase A: keys of this CTA's token range, head-major (coalesced
-  // global reads, conflict-free shared stores, eight loads in flight)
-  for (int hh = 0; hh < hps; ++hh) {
-    const float* src = a.scores + (int64_t)(head0 + hh) * T + t0;
-    uint32_t* dst = keys + hh * nt;
-    for (int j0 = 0; j0 < nt; j0 += 8 * kThreads) {
-      float sv[8];
+  // global reads, conflict-free shared stores, sixteen loads in flight);
+  // item q covers head q / nch, tokens (q % nch) * 1024 + tid
+  {
+    const int nch = (nt + kThreads - 1) / kThreads;
+    const int nq = hps * nch;
+    for (int q0 = 0; q0 < nq; q0 += 16) {
+      float sv[16];
+      int hh = q0 / nch, jc = q0 - (q0 / nch) * nch;
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int j = j0 + x * kThreads + tid;
-        if (j < nt) sv[x] = __ldg(src + j);
+      for (int x = 0; x < 16; ++x) {
+        const int j = jc * kThreads + tid;
+        if (q0 + x < nq && j < nt) sv[x] = __ldg(a.scores + (int64_t)(head0 + hh) * T + t0 + j);
+        if (++jc == nch) { jc = 0; ++hh; }
       }
+      hh = q0 / nch; jc = q0 - hh * nch;
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int j = j0 + x * kThreads + tid;
-        if (j < nt) dst[j] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x]);
+      for (int x = 0; x < 16; ++x) {
+        const int j = jc * kThreads + tid;
+        if (q0 + x < nq && j < nt)
+          keys[hh * nt + j] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x]);
+        if (++jc == nch) { jc = 0; ++hh; }
       }
     }
   }
@@ -171,6 +187,13 @@ select_kernel(Args a) {
     uint32_t krem = (uint32_t)need;
     uint32_t last_count = 0;
     uint32_t* myhist = sh.hist[warp & (kSubHist - 1)];
+    // candidates of the later passes: after pass 0 the keys whose top byte
+    // matches are copied to list1; after pass 1 those matching 16 bits go to
+    // list2 when they fit (otherwise pass 2 and 3 scan list1 again)
+    uint32_t* list1 = keys + nloc;
+    uint32_t* list2 = sh.list2;
+    const uint32_t* src = keys;
+    int nsrc = nloc;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
@@ -178,15 +201,26 @@ select_kernel(Args a) {
         for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
         __syncthreads();
       }
-      for (int e0 = 0; e0 < nloc; e0 += kThreads) {
+      for (int e0 = 0; e0 < nsrc; e0 += kThreads) {
         const int e = e0 + tid;
-        uint32_t digit = 0xffffu;
-        if (e < nloc) {
-          const uint32_t key = keys[e];
-          if (key != 0u && (key & pmask) == prefix) digit = (key >> shift) & 255u;
+        bool cand = false;
+        uint32_t digit = 0u;
+        if (e < nsrc) {
+          const uint32_t key = src[e];
+          cand = key != 0u && (key & pmask) == prefix;
+          digit = (key >> shift) & 255u;
         }
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (digit != 0xffffu && lane == __ffs(peers) - 1) atomicAdd(&myhist[digit], __popc(peers));
+        // one atomic per warp when all its candidates share a digit (the
+        // common case in the first pass), else one per candidate
+        const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
+        if (cmask) {
+          const uint32_t d0 = __shfl_sync(0xffffffffu, digit, __ffs(cmask) - 1);
+          if (__all_sync(0xffffffffu, !cand || digit == d0)) {
+            if (lane == 0) atomicAdd(&myhist[d0], (uint32_t)__popc(cmask));
+          } else if (cand) {
+            atomicAdd(&myhist[digit], 1u);
+          }
+        }
       }
       __syncthreads();
       // every CTA adds its histogram into rank 0's totals of this pass
@@ -227,6 +261,31 @@ select_kernel(Args a) {
       last_count = sh.sel_count;
       prefix |= bin << shift;
       pmask |= 255u << shift;
+      if (pass < 2) {
+        // compact this CTA's candidates of the next pass (warp-aggregated appends)
+        uint32_t* dst = (pass == 0) ? list1 : list2;
+        const int cap = (pass == 0) ? nloc : kList2;
+        if (tid == 0) sh.nlist = 0u;
+        __syncthreads();
+        for (int e0 = 0; e0 < nsrc; e0 += kThreads) {
+          const int e = e0 + tid;
+          uint32_t key = 0u;
+          bool keep = false;
+          if (e < nsrc) {
+            key = src[e];
+            keep = key != 0u && (key & pmask) == prefix;
+          }
+          const uint32_t bm = __ballot_sync(0xffffffffu, keep);
+          uint32_t base = 0u;
+          if (lane == 0 && bm) base = atomicAdd(&sh.nlist, (uint32_t)__popc(bm));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const uint32_t at = base + __popc(bm & ((1u << lane) - 1u));
+          if (keep && at < (uint32_t)cap) dst[at] = key;
+        }
+        __syncthreads();
+        if (sh.nlist <= (uint32_t)cap) { src = dst; nsrc = (int)sh.nlist; }
+        __syncthreads();
+      }
     }
     thr = prefix;
     // ---- ties: keep the first krem elements with key == thr in (t, g) order
@@ -315,32 +374,43 @@ select_kernel(Args a) {
     if (rank == 0) a.counts[head0 + tid] = (int32_t)total;
   }
   __syncthreads();
-  for (int hh = 0; hh < hps; ++hh) {
-    int32_t* out = a.kept + (int64_t)(head0 + hh) * T;
-    uint32_t carry = sh.head_base[hh];
-    for (int j0 = 0; j0 < nt; j0 += kThreads) {
-      const int j = j0 + tid;
-      const bool f = j < nt && kept(hh, j);
-      const uint32_t ball = __ballot_sync(0xffffffffu, f);
-      uint32_t* wt = sh.warp_tmp[sbuf];
-      if (lane == 0) wt[warp] = __popc(ball);
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t x = wt[lane];
-        uint32_t y = x;
+  // one block scan per 1024-token chunk covers every head: flags by ballot,
+  // per-warp counts scanned by one warp per head, positions by popcount
+  uint32_t carry[kMaxHps];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
-          if (lane >= off) y += n;
-        }
-        wt[lane] = y - x;
-        if (lane == 31) sh.warp_tot[sbuf] = y;
-      }
-      __syncthreads();
-      if (f) out[carry + wt[warp] + __popc(ball & ((1u << lane) - 1u))] = t0 + j;
-      carry += sh.warp_tot[sbuf];
-      sbuf ^= 1;
+  for (int hh = 0; hh < kMaxHps; ++hh) carry[hh] = (hh < hps) ? sh.head_base[hh] : 0u;
+  for (int j0 = 0; j0 < nt; j0 += kThreads) {
+    const int j = j0 + tid;
+    uint32_t ball[kMaxHps];
+    uint32_t (*wt)[kWarps] = sh.emit_tmp[sbuf];
+#pragma unroll
+    for (int hh = 0; hh < kMaxHps; ++hh) {
+      const bool f = hh < hps && j < nt && kept(hh, j);
+      ball[hh] = __ballot_sync(0xffffffffu, f);
+      if (lane == 0 && hh < hps) wt[hh][warp] = __popc(ball[hh]);
     }
+    __syncthreads();
+    if (warp < hps) {
+      const uint32_t x = wt[warp][lane];
+      uint32_t y = x;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
+        if (lane >= off) y += n;
+      }
+      wt[warp][lane] = y - x;
+      if (lane == 31) sh.emit_tot[sbuf][warp] = y;
+    }
+    __syncthreads();
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int hh = 0; hh < kMaxHps; ++hh) {
+      if (hh >= hps) break;
+      if (ball[hh] & (1u << lane))
+        a.kept[(int64_t)(head0 + hh) * T + carry[hh] + wt[hh][warp] + __popc(ball[hh] & below)] = t0 + j;
+      carry[hh] += sh.emit_tot[sbuf][hh];
+    }
+    sbuf ^= 1;
   }
   // no CTA may leave while a peer can still read its shared memory
   cl.sync();
@@ -385,7 +455,8 @@ offsets_kernel(const int32_t* __restrict__ counts, int n, int64_t* __restrict__ 
   if (threadIdx.x == 0) offsets[n] = carry_s;
 }
 
-size_t shared_bytes(int keys) { return ((sizeof(Shared) + 15) & ~size_t(15)) + (size_t)keys * 4; }
+// keys of the CTA's range plus the same capacity for the first candidate list
+size_t shared_bytes(int keys) { return ((sizeof(Shared) + 15) & ~size_t(15)) + 2ull * keys * 4; }
 
 }  // namespace
 
@@ -397,7 +468,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   if (hps > kMaxHps) return KVC_ERR_UNSUPPORTED;
   const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
   const int64_t pool = (int64_t)hps * T;
-  const int cap = (int)((dev.max_smem_optin - (int)shared_bytes(0)) / 4);
+  const int cap = (int)((dev.max_smem_optin - (int)shared_bytes(0)) / 8);
   // the smallest cluster that keeps <= 16K keys per CTA, else the smallest that fits
   int C = 1;
   while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
@@ -412,16 +483,24 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     a.nP = n_sink + (T - rs) - (rs < n_sink ? n_sink - rs : 0);
   }
   a.kept = kept_idx; a.counts = counts;
-  KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
-                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  static std::mutex mu;
+  static bool attr_done[64];
+  static std::map<std::tuple<int, int, size_t>, int> active_memo;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!attr_done[dev.device & 63]) {
+    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
+                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      dev.max_smem_optin));
+    attr_done[dev.device & 63] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   // a cluster must fit one GPC: shrink it (while the keys still fit) until
-  // the occupancy query says at least one cluster can be resident
+  // the occupancy query says at least one cluster can be resident (the
+  // answer is remembered per device, cluster size and shared memory)
   for (;;) {
     const size_t smem = shared_bytes(((T + C - 1) / C) * hps);
-    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     cfg.gridDim = dim3((unsigned)C, (unsigned)nseg, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
@@ -433,7 +512,14 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int active = 0;
-    KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel, &cfg));
+    const auto key = std::make_tuple(dev.device, C, smem);
+    auto it = active_memo.find(key);
+    if (it != active_memo.end()) {
+      active = it->second;
+    } else {
+      KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel, &cfg));
+      active_memo[key] = active;
+    }
     if (active > 0) break;
     if (C == 1 || (pool + C / 2 - 1) / (C / 2) > cap) return KVC_ERR_UNSUPPORTED;
     C /= 2;
