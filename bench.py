@@ -250,6 +250,124 @@ def bench_decode(B, steps, warmup, device):
                 gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2, rows_at_start=rows0)
 
 
+def compact_bytes(rows, d, elt):
+    """Algorithmic bytes of one compaction: every kept K and V row read once
+    and written once, plus its int32 source index."""
+    return rows * (2 * 2 * d * elt + 4)
+
+
+def bench_c4(B, steps, warmup, device):
+    """Threshold pruning with the linear surrogate scorer on the 128k-token
+    Qwen-shaped layer (28 q / 4 kv heads, hidden 3584): kvc_score_linear ->
+    kvc_select (tau = 0.5, 4 sinks + 128 recent) -> kvc_compact, each stage
+    timed with CUDA events; the 940 MB hidden-state read flushes L2 itself."""
+    w = inputs.WORKLOADS["c4_qwen128k"]
+    hidden, weight, bias = inputs.linear_scorer(w, device)
+    k, v = inputs.keys_values(w, None, device)
+    n = w.U * w.Hkv
+    scores = torch.empty((w.U, w.Hkv, w.T), device=device)
+    kept = torch.empty((n, w.T), dtype=torch.int32, device=device)
+    counts = torch.empty(n, dtype=torch.int32, device=device)
+    offs = torch.empty(n + 1, dtype=torch.int64, device=device)
+    kc = torch.empty((n * w.T, w.d), dtype=k.dtype, device=device)
+    vc = torch.empty_like(kc)
+    start = torch.empty(n, dtype=torch.int64, device=device)
+    length = torch.empty(n, dtype=torch.int32, device=device)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream()
+
+    def step(ev=None):
+        flush_l2(flush)
+        if ev: ev[0].record(s)
+        B.kvc_score_linear(hidden, weight, bias, scores)
+        if ev: ev[1].record(s)
+        B.kvc_select(scores, "threshold", kept, counts, offs, tau=w.tau, n_sink=w.n_sink,
+                     n_recent=w.n_recent)
+        if ev: ev[2].record(s)
+        B.kvc_compact(k, v, kept, counts, offs, kc, vc, start, length)
+        if ev: ev[3].record(s)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    t_sel = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    t_comp = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    rows = int(offs[-1].item())
+    score_bytes = hidden.numel() * 2 + weight.numel() * 2 + scores.numel() * 4
+    comp_bytes = compact_bytes(rows, w.d, 2)
+    out = dict(workload="c4_qwen128k", score_us=t_score, select_us=t_sel, compact_us=t_comp,
+               kept_rows=rows, keep_fraction=rows / (n * w.T),
+               score_linear_gbs=score_bytes / (t_score * 1e-6) / 1e9,
+               score_linear_bytes=score_bytes,
+               compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
+               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
+    del hidden, k, v, kc, vc, kept, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_c3(B, steps, warmup, device):
+    """The 32-layer x batch-4 cache (U = 128 units, 8 kv heads, T = 16384):
+    score (per-(layer, kv head) temperature) -> global top-k per unit at keep
+    0.20 -> compact, each stage timed; 4.3 GB of K, so L2 holds none of it."""
+    w = inputs.WORKLOADS["c3_32layer"]
+    q = inputs.window_queries(w, device)
+    k, v = inputs.keys_values(w, q, device)
+    hs = inputs.head_scale(w, device)
+    n = w.U * w.Hkv
+    scores = torch.empty((w.U, w.Hkv, w.T), device=device)
+    ws = torch.empty(B.lib().kvc_score_attn_workspace(w.U, w.Hq, w.Hkv, w.T, w.W, w.d, B.KVC_BF16),
+                     dtype=torch.uint8, device=device)
+    kept = torch.empty((n, w.T), dtype=torch.int32, device=device)
+    counts = torch.empty(n, dtype=torch.int32, device=device)
+    offs = torch.empty(n + 1, dtype=torch.int64, device=device)
+    cap = w.U * math.floor(w.keep_ratio * w.Hkv * w.T) + n * (w.n_sink + w.n_recent)
+    kc = torch.empty((cap, w.d), dtype=k.dtype, device=device)
+    vc = torch.empty_like(kc)
+    start = torch.empty(n, dtype=torch.int64, device=device)
+    length = torch.empty(n, dtype=torch.int32, device=device)
+    s = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(s)
+        B.kvc_score_attn(q, k, scores, w.scale, head_scale=hs, workspace=ws)
+        if ev: ev[1].record(s)
+        B.kvc_select(scores, "global", kept, counts, offs, keep_ratio=w.keep_ratio,
+                     n_sink=w.n_sink, n_recent=w.n_recent)
+        if ev: ev[2].record(s)
+        B.kvc_compact(k, v, kept, counts, offs, kc, vc, start, length)
+        if ev: ev[3].record(s)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    t_sel = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    t_comp = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    rows = int(offs[-1].item())
+    per_head = counts.view(w.U, w.Hkv).float()
+    score_bytes = k.numel() * 2 + q.numel() * 2 + scores.numel() * 4
+    comp_bytes = compact_bytes(rows, w.d, 2)
+    out = dict(workload="c3_32layer", score_us=t_score, select_us=t_sel, compact_us=t_comp,
+               kept_rows=rows,
+               per_head_count_min=int(per_head.min()), per_head_count_max=int(per_head.max()),
+               score_gbs=score_bytes / (t_score * 1e-6) / 1e9, score_bytes=score_bytes,
+               compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
+               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
+    del q, k, v, kc, vc, kept, scores, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def fidelity_probe(B, L):
     """One decode step over the compacted cache and over the full cache."""
     w = L.w
@@ -353,8 +471,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "decode"], default=None,
-                    help="profiling runs: time only the layer pass or only decode")
+    ap.add_argument("--only", choices=["layer", "decode", "c4", "c3"], default=None,
+                    help="profiling runs: time only one workload")
     args = ap.parse_args()
     world, rank, local = dist_setup(args.gpus)
     w = inputs.WORKLOADS[WORKLOAD]
@@ -398,6 +516,12 @@ def main():
         dec = bench_decode(B, args.steps, args.warmup, device)
         print(json.dumps({"decode": dec, "frac": dec["gbs"] / hbm}))
         return
+    if args.only == "c4":
+        print(json.dumps(bench_c4(B, args.steps, args.warmup, device)))
+        return
+    if args.only == "c3":
+        print(json.dumps(bench_c3(B, args.steps, args.warmup, device)))
+        return
 
     # ---- timed region: exactly K steps of the layer pass
     if world > 1:
@@ -430,6 +554,10 @@ def main():
     dec = bench_decode(B, max(16, args.steps), max(3, args.warmup), device)
     dec["frac"] = dec["gbs"] / hbm
     dec["peak_gbs"] = hbm
+    c4 = bench_c4(B, max(3, args.steps // 4), 3, device)
+    c3 = bench_c3(B, 3, 3, device)
+    comp_c2 = compact_bytes(r["kept_rows"], w.d, 2)
+    comp_c2_us = statistics.mean(r["compact_ms"]) * 1e3
 
     score_bytes = (w.U * w.Hkv * w.T * w.d * 2 + w.U * w.Hq * w.W * w.d * 2 + w.U * w.Hkv * w.T * 4)
     score_flops = 2.0 * w.U * w.Hq * w.W * w.T * w.d
@@ -454,6 +582,24 @@ def main():
                      "tensor_tflops": score_flops / (score_ms * 1e-3) / 1e12,
                      "tensor_frac": score_flops / (score_ms * 1e-3) / 1e12 / bf16},
         "decode": dec,
+        "c4_qwen128k": c4,
+        "c3_32layer": c3,
+        "rooflines": [
+            {"kernel": "score_tc_kernel", "workload": WORKLOAD, "bound": "hbm",
+             "achieved_gbs": achieved, "frac": achieved / hbm},
+            {"kernel": "compact_kernel", "workload": WORKLOAD, "bound": "hbm",
+             "achieved_gbs": comp_c2 / (comp_c2_us * 1e-6) / 1e9,
+             "frac": comp_c2 / (comp_c2_us * 1e-6) / 1e9 / hbm},
+            {"kernel": "linear_kernel", "workload": "c4_qwen128k", "bound": "hbm",
+             "achieved_gbs": c4["score_linear_gbs"], "frac": c4["score_linear_gbs"] / hbm},
+            {"kernel": "compact_kernel", "workload": "c4_qwen128k", "bound": "hbm",
+             "achieved_gbs": c4["compact_gbs"], "frac": c4["compact_gbs"] / hbm},
+            {"kernel": "score_tc_kernel", "workload": "c3_32layer", "bound": "hbm",
+             "achieved_gbs": c3["score_gbs"], "frac": c3["score_gbs"] / hbm},
+            {"kernel": "compact_kernel", "workload": "c3_32layer", "bound": "hbm",
+             "achieved_gbs": c3["compact_gbs"], "frac": c3["compact_gbs"] / hbm},
+            {"kernel": "decode_partial_kernel+decode_combine_kernel", "workload": DECODE_WORKLOAD,
+             "bound": "hbm", "achieved_gbs": dec["gbs"], "frac": dec["gbs"] / hbm}],
         "fidelity": fid,
         "e2e": {"value": world * w.U * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -382,6 +382,222 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 partial kernel on the tensor cores.  Per row of the cache the G query
+// heads need G * d multiply-adds for q.k and again for p.v; done on the SIMT
+// cores that is ~50-100 instructions per 512-byte row, which caps the kernel
+// below the HBM rate.  Warp-level bf16 MMAs (m16n8k16, fp32 accumulate) do
+// the same work in ~4 instructions per row: S = Q . K^T with the (<= 8)
+// query heads as the M rows and 8 tokens per N tile, then O += P . V with P
+// taken straight from the S accumulators.  The contraction is tiny (M = G
+// padded to 16), so the warp-level MMA is the right size; the rows stream
+// through a 3-stage cp.async ring whose 16-byte-padded rows make every
+// ldmatrix conflict-free.
+namespace mma {
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D = A (16x16 bf16, row) . B (16x8 bf16, col) + C, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+constexpr int kRows = 64;      // rows per stage (16 per warp)
+constexpr int kStg = 3;
+
+template <int D>
+constexpr size_t smem_bytes() { return (size_t)kStg * 2 * kRows * (D + 8) * 2; }
+
+}  // namespace mma
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc,
+                          const uint16_t* __restrict__ vc, const int64_t* __restrict__ start,
+                          const int32_t* __restrict__ len, int Hkv, int max_chunks,
+                          float scale_log2, float* __restrict__ ws) {
+  static_assert(G <= 8, "query heads per kv head");
+  constexpr int RS = D + 8;                  // padded row stride (elements)
+  constexpr int CPR = D * 2 / 16;            // 16-byte chunks per row
+  constexpr int NT = D / 8;                  // 8-wide output tiles
+  extern __shared__ __align__(128) uint16_t smem_m[];
+  __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
+  __shared__ float acc_sm[kWarps][G][D];
+
+  const int i = blockIdx.y, c = blockIdx.x;
+  const int L = len[i];
+  const int rb = c * kChunk;
+  if (rb >= L) return;
+  const int nrows = min(L, rb + kChunk) - rb;
+  const int nst = (nrows + mma::kRows - 1) / mma::kRows;
+  const int u = i / Hkv, g = i - u * Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t* kb = kc + (start[i] + rb) * D;
+  const uint16_t* vb = vc + (start[i] + rb) * D;
+  const uint32_t sbase = smem_u32(smem_m);
+
+  // stage st -> slot: K rows then V rows, each kRows x RS elements
+  auto issue = [&](int st) {
+    const int slot = st % mma::kStg;
+    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    const int r0 = st * mma::kRows;
+    for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
+      const int r = x / CPR, ch = x - r * CPR;
+      const bool ok = r0 + r < nrows;
+      const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
+      const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
+      mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
+      mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+    }
+  };
+  for (int st = 0; st < mma::kStg - 1; ++st) {
+    if (st < nst) issue(st);
+    mma::cp_commit();
+  }
+
+  // Q as the A operand: rows = query heads (lane / 4), 8 dims per register pair
+  uint32_t qa[D / 16][2];
+  {
+    const int h = lane >> 2;
+    const int d0 = (lane & 3) * 2;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      if (h < G) {
+        const uint16_t* qp = q + ((int64_t)u * Hkv * G + (int64_t)g * G + h) * D + kk * 16 + d0;
+        qa[kk][0] = *reinterpret_cast<const uint32_t*>(qp);
+        qa[kk][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+      } else {
+        qa[kk][0] = qa[kk][1] = 0u;
+      }
+    }
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
+  float m = -INFINITY, l = 0.0f;                  // for head lane / 4 (lanes of a quad agree)
+
+  for (int st = 0; st < nst; ++st) {
+    mma::cp_wait<mma::kStg - 2>();
+    __syncthreads();                              // stage st landed; slot st-1 is free
+    if (st + mma::kStg - 1 < nst) issue(st + mma::kStg - 1);
+    mma::cp_commit();
+    const int slot = st % mma::kStg;
+    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    const int wr = warp * 16;                     // this warp's 16 rows of the stage
+    // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int j = lane >> 3, r = lane & 7;
+      const uint32_t rowaddr = ks + (uint32_t)((wr + (j >> 1) * 8 + r) * RS + (j & 1) * 8) * 2u;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t b[4];
+        mma::ldsm_x4(rowaddr + kk * 32u, b);
+        mma::mma_bf16(s0, qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
+        mma::mma_bf16(s1, qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+      }
+    }
+    // ---- online softmax in base 2 over the 16 tokens (row = head lane / 4)
+    const int tcol = (lane & 3) * 2;
+    const int base_row = st * mma::kRows + wr;
+    float x0 = (base_row + tcol < nrows) ? s0[0] * scale_log2 : -INFINITY;
+    float x1 = (base_row + tcol + 1 < nrows) ? s0[1] * scale_log2 : -INFINITY;
+    float x2 = (base_row + 8 + tcol < nrows) ? s1[0] * scale_log2 : -INFINITY;
+    float x3 = (base_row + 8 + tcol + 1 < nrows) ? s1[1] * scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    if (mn != -INFINITY) {
+      const float alpha = mma::ex2(m - mn);        // m = -inf -> 0
+      l *= alpha;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) { o[nt][0] *= alpha; o[nt][1] *= alpha; }
+      p0 = mma::ex2(x0 - mn); p1 = mma::ex2(x1 - mn); p2 = mma::ex2(x2 - mn); p3 = mma::ex2(x3 - mn);
+      l += (p0 + p1) + (p2 + p3);
+      m = mn;
+    }
+    // ---- O += P . V: P (heads x 16 tokens) is the A operand
+    const uint32_t pa0 = mma::pack_bf16(p0, p1), pa2 = mma::pack_bf16(p2, p3);
+    {
+      const int j = lane >> 3, r = lane & 7;
+      const uint32_t rowaddr = vs + (uint32_t)((wr + (j & 1) * 8 + r) * RS + (j >> 1) * 8) * 2u;
+#pragma unroll
+      for (int dn = 0; dn < D / 16; ++dn) {
+        uint32_t b[4];
+        mma::ldsm_x4_t(rowaddr + dn * 32u, b);
+        mma::mma_bf16(o[2 * dn], pa0, 0u, pa2, 0u, b[0], b[1]);
+        mma::mma_bf16(o[2 * dn + 1], pa0, 0u, pa2, 0u, b[2], b[3]);
+      }
+    }
+  }
+  mma::cp_wait<0>();
+  // quad sum of l, then per-warp partials to shared memory
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  const int h = lane >> 2;
+  if (h < G) {
+    if ((lane & 3) == 0) { m_sm[warp][h] = m; l_sm[warp][h] = l; }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      acc_sm[warp][h][nt * 8 + (lane & 3) * 2] = o[nt][0];
+      acc_sm[warp][h][nt * 8 + (lane & 3) * 2 + 1] = o[nt][1];
+    }
+  }
+  __syncthreads();
+  float* out = ws + ((int64_t)i * max_chunks + c) * G * (D + 2);
+  for (int e = tid; e < G * D; e += kWarps * 32) {
+    const int hh = e / D, x = e - hh * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, m_sm[w][hh]);
+    float a = 0.0f, lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = (m_sm[w][hh] == -INFINITY) ? 0.0f : exp2f(m_sm[w][hh] - M);
+      a += acc_sm[w][hh][x] * f;
+      lsum += l_sm[w][hh] * f;
+    }
+    out[hh * (D + 2) + x] = a;
+    if (x == 0) { out[hh * (D + 2) + D] = M; out[hh * (D + 2) + D + 1] = lsum; }
+  }
+}
+
 template <typename Tin, int D, int G>
 int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, const void* k_new,
         const void* v_new, int U, int Hkv, int max_len, float scale, void* out, float* lse,
@@ -391,16 +607,29 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
   const float sl2 = scale * kLog2e;
   if (max_chunks > 0) {
     dim3 grid((unsigned)max_chunks, (unsigned)n);
-    const size_t smem = partial_smem_bytes<Tin, D>();
-    auto kern = decode_partial_kernel<Tin, D, G>;
     static std::atomic<uint64_t> attr_done{0};          // one bit per device
-    if (!(attr_done.load() & (1ull << (dev.device & 63)))) {
-      KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-      attr_done.fetch_or(1ull << (dev.device & 63));
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if constexpr (sizeof(Tin) == 2 && G <= 8) {
+      const size_t smem = mma::smem_bytes<D>();
+      auto kern = decode_partial_mma_kernel<D, G>;
+      if (!(attr_done.load() & bit)) {
+        KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        attr_done.fetch_or(bit);
+      }
+      kern<<<grid, kWarps * 32, smem, s>>>(
+          static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kc),
+          static_cast<const uint16_t*>(vc), start, len, Hkv, max_chunks, sl2, ws);
+    } else {
+      const size_t smem = partial_smem_bytes<Tin, D>();
+      auto kern = decode_partial_kernel<Tin, D, G>;
+      if (!(attr_done.load() & bit)) {
+        KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        attr_done.fetch_or(bit);
+      }
+      kern<<<grid, (kWarps + 1) * 32, smem, s>>>(
+          static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
+          start, len, Hkv, max_chunks, sl2, ws, dev.status);
     }
-    kern<<<grid, (kWarps + 1) * 32, smem, s>>>(
-        static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
-        start, len, Hkv, max_chunks, sl2, ws, dev.status);
   }
   decode_combine_kernel<Tin, D, G><<<n, D, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc), start, len,

@@ -9,7 +9,9 @@
 // Mapping: a warp owns 8 consecutive rows; lane L walks the 16-byte chunks
 // c = L, L+32, ... of those rows, loads the matching weight slice once from
 // shared memory (laid out chunk-interleaved so a warp's 32 loads hit 32
-// consecutive 16-byte words) and applies it to all 8 rows.  The 8 x Hkv
+// consecutive 16-byte words) and applies it to all 8 rows.  The loads of
+// chunk c+32 are issued before chunk c is multiplied (two register
+// buffers), and three 4-warp blocks per SM keep ~96 KB of reads in flight.  The 8 x Hkv
 // partial sums are reduced across the warp with xor-shuffles at the end.
 #include <atomic>
 
@@ -19,7 +21,8 @@ namespace kvc {
 namespace {
 
 constexpr int kRows = 8;        // rows per warp task
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
+constexpr int kBlocksPerSm = 3;
 
 template <typename Tin> struct Vec;
 template <> struct Vec<uint16_t> { static constexpr int E = 8; };
@@ -38,7 +41,7 @@ __device__ __forceinline__ float to_f(uint16_t b) { return __uint_as_float(((uin
 __device__ __forceinline__ float to_f(float f) { return f; }
 
 template <typename Tin, int HK>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
 linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
               const float* __restrict__ bias, int64_t rows, int T, int Dh,
               float* __restrict__ scores) {
@@ -65,11 +68,12 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
     for (int r = 0; r < kRows; ++r)
 #pragma unroll
       for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
-    for (int c = lane; c < NC; c += 32) {
-      uint4 hv[kRows];
+    // two register buffers: the next chunk's 8 row loads are in flight
+    // while the current chunk is multiplied
+    auto load = [&](uint4* hv, int c) {
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
-        if (r0 + r < rows) {
+        if (c < NC && r0 + r < rows) {
           const uint4* p = reinterpret_cast<const uint4*>(hidden + (r0 + r) * (int64_t)Dh) + c;
           asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(hv[r].x), "=r"(hv[r].y), "=r"(hv[r].z), "=r"(hv[r].w)
@@ -78,6 +82,8 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
           hv[r] = make_uint4(0, 0, 0, 0);
         }
       }
+    };
+    auto mac = [&](const uint4* hv, int c) {
       float wv[E * HK];
 #pragma unroll
       for (int f4 = 0; f4 < F4; ++f4) {
@@ -93,6 +99,15 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
 #pragma unroll
           for (int g = 0; g < HK; ++g) acc[r][g] = fmaf(x[jj], wv[jj * HK + g], acc[r][g]);
       }
+    };
+    uint4 ha[kRows], hb[kRows];
+    load(ha, lane);
+    for (int c = lane; c < NC; c += 64) {
+      load(hb, c + 32);
+      mac(ha, c);
+      if (c + 32 >= NC) break;
+      load(ha, c + 64);
+      mac(hb, c + 32);
     }
 #pragma unroll
     for (int r = 0; r < kRows; ++r)
