@@ -9,9 +9,10 @@
 // Mapping: a warp owns 8 consecutive rows; lane L walks the 16-byte chunks
 // c = L, L+32, ... of those rows, loads the matching weight slice once from
 // shared memory (laid out chunk-interleaved so a warp's 32 loads hit 32
-// consecutive 16-byte words) and applies it to all 8 rows.  The loads of
-// chunk c+32 are issued before chunk c is multiplied (two register
-// buffers), and three 4-warp blocks per SM keep ~96 KB of reads in flight.  The 8 x Hkv
+// consecutive 16-byte words) and applies it to all 8 rows.  Each lane
+// streams its 16-byte pieces of the next three column blocks into a private
+// shared-memory ring with cp.async, so 12 warps keep ~144 KB of reads per SM
+// in flight without holding them in registers.  The 8 x Hkv
 // partial sums are reduced across the warp with xor-shuffles at the end.
 #include <atomic>
 
@@ -21,8 +22,9 @@ namespace kvc {
 namespace {
 
 constexpr int kRows = 8;        // rows per warp task
-constexpr int kWarps = 4;
-constexpr int kBlocksPerSm = 3;
+constexpr int kWarps = 12;      // one block per SM
+constexpr int kStages = 3;      // column blocks in flight per warp
+constexpr int kBlockBytes = 32 * 16;   // one row's column block: 32 lanes x 16 bytes
 
 template <typename Tin> struct Vec;
 template <> struct Vec<uint16_t> { static constexpr int E = 8; };
@@ -40,15 +42,24 @@ __device__ __forceinline__ void unpack(const uint4& v, float* x, float) {
 __device__ __forceinline__ float to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 __device__ __forceinline__ float to_f(float f) { return f; }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
 template <typename Tin, int HK>
-__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
+__global__ void __launch_bounds__(kWarps * 32, 1)
 linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
               const float* __restrict__ bias, int64_t rows, int T, int Dh,
               float* __restrict__ scores) {
   constexpr int E = Vec<Tin>::E;          // hidden elements per 16-byte chunk
   constexpr int F4 = E * HK / 4;          // float4 words of weight per chunk
-  extern __shared__ float4 wsm[];         // [F4][NC] chunk-interleaved
+  extern __shared__ __align__(128) uint8_t smem_lin[];
   const int NC = Dh / E;
+  const int NIT = (NC + 31) / 32;         // 512-byte column blocks per row
+  float4* wsm = reinterpret_cast<float4*>(smem_lin);                    // [F4][NC]
+  uint8_t* ring = smem_lin + (((size_t)F4 * NC * 16 + 127) & ~size_t(127));
   // stage the weight: chunk c, element jj, head g -> float (jj*HK + g) of chunk c
   for (int e = threadIdx.x; e < Dh * HK; e += blockDim.x) {
     const int j = e / HK, g = e % HK;
@@ -57,33 +68,59 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
     reinterpret_cast<float*>(&wsm[(f / 4) * NC + c])[f % 4] = to_f(weight[(int64_t)j * HK + g]);
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t warp_global = (int64_t)blockIdx.x * kWarps + warp;
   const int64_t warps_total = (int64_t)gridDim.x * kWarps;
   const int64_t tasks = (rows + kRows - 1) / kRows;
-  for (int64_t task = warp_global; task < tasks; task += warps_total) {
+  const int64_t my_tasks =
+      (warp_global < tasks) ? (tasks - warp_global + warps_total - 1) / warps_total : 0;
+  const int64_t nq = my_tasks * NIT;      // this warp's (task, column block) iterations
+  // lane's 16 bytes of row r in ring slot `slot` (each lane reads back only
+  // what it copied itself, so its own cp.async wait is enough)
+  const uint32_t lane_ring =
+      smem_u32(ring) + (uint32_t)((warp * kStages * kRows) * kBlockBytes + lane * 16);
+  auto issue = [&](int64_t q) {
+    const int64_t task = warp_global + (q / NIT) * warps_total;
+    const int k = (int)(q % NIT);
+    const int slot = (int)(q % kStages);
     const int64_t r0 = task * kRows;
-    float acc[kRows][HK];
+    const int c = k * 32 + lane;
 #pragma unroll
-    for (int r = 0; r < kRows; ++r)
+    for (int r = 0; r < kRows; ++r) {
+      const bool ok = c < NC && r0 + r < rows;
+      const Tin* src = ok ? hidden + (r0 + r) * (int64_t)Dh + (int64_t)c * E : hidden;
+      cp_async16(lane_ring + (uint32_t)((slot * kRows + r) * kBlockBytes), src, ok ? 16u : 0u);
+    }
+  };
 #pragma unroll
-      for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
-    // two register buffers: the next chunk's 8 row loads are in flight
-    // while the current chunk is multiplied
-    auto load = [&](uint4* hv, int c) {
+  for (int x = 0; x < kStages; ++x) {
+    if (x < nq) issue(x);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  float acc[kRows][HK];
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        if (c < NC && r0 + r < rows) {
-          const uint4* p = reinterpret_cast<const uint4*>(hidden + (r0 + r) * (int64_t)Dh) + c;
-          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(hv[r].x), "=r"(hv[r].y), "=r"(hv[r].z), "=r"(hv[r].w)
-                       : "l"(p));
-        } else {
-          hv[r] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    };
-    auto mac = [&](const uint4* hv, int c) {
+  for (int r = 0; r < kRows; ++r)
+#pragma unroll
+    for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
+  for (int64_t q = 0; q < nq; ++q) {
+    const int64_t task = warp_global + (q / NIT) * warps_total;
+    const int k = (int)(q % NIT);
+    const int slot = (int)(q % kStages);
+    const int64_t r0 = task * kRows;
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+    const int c = k * 32 + lane;
+    uint4 hv[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const uint32_t a = lane_ring + (uint32_t)((slot * kRows + r) * kBlockBytes);
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(hv[r].x), "=r"(hv[r].y), "=r"(hv[r].z), "=r"(hv[r].w)
+                   : "r"(a));
+    }
+    // the slot is now in registers: refill it with iteration q + kStages
+    if (q + kStages < nq) issue(q + kStages);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (c < NC) {
       float wv[E * HK];
 #pragma unroll
       for (int f4 = 0; f4 < F4; ++f4) {
@@ -99,57 +136,57 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
 #pragma unroll
           for (int g = 0; g < HK; ++g) acc[r][g] = fmaf(x[jj], wv[jj * HK + g], acc[r][g]);
       }
-    };
-    uint4 ha[kRows], hb[kRows];
-    load(ha, lane);
-    for (int c = lane; c < NC; c += 64) {
-      load(hb, c + 32);
-      mac(ha, c);
-      if (c + 32 >= NC) break;
-      load(ha, c + 64);
-      mac(hb, c + 32);
     }
+    if (k == NIT - 1) {
 #pragma unroll
-    for (int r = 0; r < kRows; ++r)
+      for (int r = 0; r < kRows; ++r)
 #pragma unroll
-      for (int g = 0; g < HK; ++g) {
-        float v = acc[r][g];
+        for (int g = 0; g < HK; ++g) {
+          float v = acc[r][g];
 #pragma unroll
-        for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        acc[r][g] = v;
-      }
-    // lane (r*HK + g) writes (row r, head g)
-#pragma unroll
-    for (int r = 0; r < kRows; ++r)
-#pragma unroll
-      for (int g = 0; g < HK; ++g) {
-        if (lane == ((r * HK + g) & 31) && r0 + r < rows) {
-          const int64_t row = r0 + r;
-          const int64_t u = row / T, t = row % T;
-          scores[(u * HK + g) * (int64_t)T + t] = acc[r][g] + (bias ? bias[g] : 0.0f);
+          for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          acc[r][g] = v;
         }
-      }
+      // lane (r*HK + g) writes (row r, head g)
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int g = 0; g < HK; ++g) {
+          if (lane == ((r * HK + g) & 31) && r0 + r < rows) {
+            const int64_t row = r0 + r;
+            const int64_t u = row / T, t = row % T;
+            scores[(u * HK + g) * (int64_t)T + t] = acc[r][g] + (bias ? bias[g] : 0.0f);
+          }
+          acc[r][g] = 0.0f;
+        }
+    }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <typename Tin, int HK>
+size_t smem_bytes(int Dh) {
+  const int NC = Dh / Vec<Tin>::E;
+  const size_t wbytes = (((size_t)(Vec<Tin>::E * HK / 4) * NC * 16) + 127) & ~size_t(127);
+  return wbytes + (size_t)kWarps * kStages * kRows * kBlockBytes;
 }
 
 template <typename Tin, int HK>
 int run(const void* hidden, const void* weight, const float* bias, int U, int T, int Dh,
         float* scores, const Dev& dev, cudaStream_t s) {
-  const size_t smem = (size_t)Dh * HK * sizeof(float);
+  const size_t smem = smem_bytes<Tin, HK>(Dh);
+  if ((int)smem > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
   auto kern = linear_kernel<Tin, HK>;
-  // shared-memory attribute at the largest supported weight size, once per
-  // device and instantiation
-  static std::atomic<uint64_t> attr_done{0};
-  if (!(attr_done.load() & (1ull << (dev.device & 63)))) {
-    KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024));
-    attr_done.fetch_or(1ull << (dev.device & 63));
+  // raise the kernel's dynamic shared-memory limit when a call needs more
+  // than any earlier one on this device
+  static std::atomic<int> attr_bytes[64];
+  if ((int)smem > attr_bytes[dev.device & 63].load()) {
+    KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr_bytes[dev.device & 63].store((int)smem);
   }
-  int per_sm = 0;
-  KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem));
-  if (per_sm < 1) return KVC_ERR_UNSUPPORTED;
   const int64_t rows = (int64_t)U * T;
   const int64_t tasks = (rows + kRows - 1) / kRows;
-  int64_t blocks = (int64_t)dev.sms * per_sm;
+  int64_t blocks = dev.sms;
   const int64_t need = (tasks + kWarps - 1) / kWarps;
   if (blocks > need) blocks = need;
   kern<<<(unsigned)blocks, kWarps * 32, smem, s>>>(static_cast<const Tin*>(hidden),
