@@ -336,11 +336,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int x = 0; x < 4; ++x) merge_ms(M, L, sm.mpart[x][et], sm.lpart[x][et]);
         __stcg(pub + et, make_float2(M, L));
-        __threadfence();
       }
       tc::named_sync(1, kEpiThreads);
-      // tag this CTA's partials as published for this launch and round, then
-      // thread x waits (bounded) for group member x's tag
+      // tag this CTA's partials as published for this launch and round (the
+      // release store is cumulative over the partials the barrier ordered
+      // before it), then thread x waits (bounded) for group member x's tag
       {
         const uint64_t tag = p.tag0 + (uint64_t)kr;
         uint64_t* tags = p.tags + (size_t)(kr & 1) * kMaxCtas;
