@@ -28,8 +28,9 @@
 //  * Emission: a counting sweep and a cluster prefix give each CTA its base
 //    per head; a block-wide ballot scan over consecutive tokens then writes
 //    the ascending token indices of each head.
-//  * Offsets (exclusive scan of the counts) are a separate single-block
-//    kernel because threshold pools have data-dependent totals.
+//  * Offsets (exclusive scan of the counts): a launch with a single pool
+//    writes them from rank 0; otherwise a separate single-block kernel scans
+//    the counts of all pools (threshold pools have data-dependent totals).
 // Every decision is an integer comparison on the fp32 bit patterns, so the
 // result is bit-exact and deterministic.
 #include <cooperative_groups.h>
@@ -59,6 +60,7 @@ struct Args {
   int n_sink, n_recent, nP;
   int32_t* kept;
   int32_t* counts;
+  int64_t* offsets;   // written here when the launch has a single pool, else NULL
 };
 
 constexpr int kSubHist = 8;              // sub-histograms (4 warps each)
@@ -76,6 +78,7 @@ struct Shared {
   uint32_t xchg_ties;                 // read remotely
   uint32_t xchg_cnt[kMaxHps];         // read remotely
   uint32_t head_base[kMaxHps];
+  uint32_t head_total[kMaxHps];
   uint32_t sel_bin, sel_above, sel_count, ecut, tie_base, nlist;
   uint32_t list2[kList2];             // candidates of the last two passes
 };
@@ -141,25 +144,45 @@ select_kernel(Args a) {
 
   // ---- phase A: keys of this CTA's token range, head-major (coalesced
   // global reads, conflict-free shared stores, sixteen loads in flight);
-  // item q covers head q / nch, tokens (q % nch) * 1024 + tid
+  // item q covers head q / nch, vector slots (q % nch) * 1024 + tid.  When the
+  // rows and the range are 16-byte aligned every slot is a float4 of 4 tokens.
   {
-    const int nch = (nt + kThreads - 1) / kThreads;
+    const bool vec = ((T | t0 | nt) & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0;
+    const int per = vec ? 4 : 1;                       // tokens per slot
+    const int nslot = nt / per;
+    const int nch = (nslot + kThreads - 1) / kThreads;
     const int nq = hps * nch;
-    for (int q0 = 0; q0 < nq; q0 += 16) {
-      float sv[16];
+    for (int q0 = 0; q0 < nq; q0 += 8) {
+      float4 sv[8];
       int hh = q0 / nch, jc = q0 - (q0 / nch) * nch;
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const int j = jc * kThreads + tid;
-        if (q0 + x < nq && j < nt) sv[x] = __ldg(a.scores + (int64_t)(head0 + hh) * T + t0 + j);
+      for (int x = 0; x < 8; ++x) {
+        const int js = jc * kThreads + tid;
+        if (q0 + x < nq && js < nslot) {
+          const float* row = a.scores + (int64_t)(head0 + hh) * T + t0;
+          if (vec) sv[x] = __ldg(reinterpret_cast<const float4*>(row) + js);
+          else sv[x].x = __ldg(row + js);
+        }
         if (++jc == nch) { jc = 0; ++hh; }
       }
       hh = q0 / nch; jc = q0 - hh * nch;
 #pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        const int j = jc * kThreads + tid;
-        if (q0 + x < nq && j < nt)
-          keys[hh * nt + j] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x]);
+      for (int x = 0; x < 8; ++x) {
+        const int js = jc * kThreads + tid;
+        if (q0 + x < nq && js < nslot) {
+          const int j = js * per;
+          uint32_t* dst = keys + hh * nt + j;
+          if (vec) {
+            uint4 kk;
+            kk.x = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].x);
+            kk.y = is_prot(t0 + j + 1, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].y);
+            kk.z = is_prot(t0 + j + 2, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].z);
+            kk.w = is_prot(t0 + j + 3, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].w);
+            *reinterpret_cast<uint4*>(dst) = kk;
+          } else {
+            dst[0] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].x);
+          }
+        }
         if (++jc == nch) { jc = 0; ++hh; }
       }
     }
@@ -372,8 +395,15 @@ select_kernel(Args a) {
     }
     sh.head_base[tid] = base;
     if (rank == 0) a.counts[head0 + tid] = (int32_t)total;
+    sh.head_total[tid] = total;
   }
   __syncthreads();
+  // a launch with a single pool writes the offsets itself (no second kernel)
+  if (a.offsets && rank == 0 && tid == 0) {
+    int64_t o = 0;
+    for (int hh = 0; hh < hps; ++hh) { a.offsets[hh] = o; o += sh.head_total[hh]; }
+    a.offsets[hps] = o;
+  }
   // one block scan per 1024-token chunk covers every head: flags by ballot,
   // per-warp counts scanned by one warp per head, positions by popcount
   uint32_t carry[kMaxHps];
@@ -483,6 +513,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     a.nP = n_sink + (T - rs) - (rs < n_sink ? n_sink - rs : 0);
   }
   a.kept = kept_idx; a.counts = counts;
+  a.offsets = (nseg == 1) ? offsets : nullptr;
   static std::mutex mu;
   static bool attr_done[64];
   static std::map<std::tuple<int, int, size_t>, int> active_memo;
@@ -525,7 +556,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     C /= 2;
   }
   KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel, a));
-  offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
+  if (nseg > 1) offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
   return launch_status();
 }
 
