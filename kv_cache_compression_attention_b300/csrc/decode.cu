@@ -32,6 +32,7 @@ constexpr int kChunk = 512;     // rows per partial CTA
 constexpr int kWarps = 4;       // compute warps per partial CTA
 constexpr int kStageRows = 32;  // rows per shared-memory stage (8 per compute warp)
 constexpr int kStages = 4;
+constexpr int kStagedChunks = 256;  // chunks whose statistics the combine stages in smem
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -347,26 +348,78 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
     snew[h] = a * scale_log2;
   }
   const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
+  if (nch <= kStagedChunks) {
+    // every chunk's (max, sum) of every head into shared memory (all loads
+    // in flight), one warp per head for the maxima and the normalisers, then
+    // each thread sums its column over the chunks with the staged weights
+    __shared__ float s_w[kStagedChunks * G], s_l[kStagedChunks * G];
+    __shared__ float s_M[G], s_L[G];
+    for (int e = x; e < nch * G; e += D) {
+      const float* pc = base + (int64_t)e * (D + 2);
+      s_w[e] = pc[D];
+      s_l[e] = pc[D + 1];
+    }
+    __syncthreads();
+    for (int h = warp; h < G; h += D / 32) {
+      float M = append ? snew[h] : -INFINITY;
+      for (int c = lane; c < nch; c += 32) M = fmaxf(M, s_w[c * G + h]);
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float M = append ? snew[h] : -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, base[(c * G + h) * (D + 2) + D]);
-    float a = 0.0f, lsum = 0.0f;
-    for (int c = 0; c < nch; ++c) {
-      const float* pc = base + (c * G + h) * (D + 2);
-      const float mc = pc[D];
-      const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
-      a += pc[x] * f;
-      lsum += pc[D + 1] * f;
+      for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      if (lane == 0) s_M[h] = M;
     }
-    if (append) {
-      const float f = exp2f(snew[h] - M);
-      a += vn * f;
-      lsum += f;
+    __syncthreads();
+    for (int e = x; e < nch * G; e += D) {
+      const float mc = s_w[e];
+      s_w[e] = (mc == -INFINITY) ? 0.0f : exp2f(mc - s_M[e % G]);
     }
-    const int64_t orow = nrow * G + h;
-    Elt<Tin>::put(out + orow * D, x, lsum > 0.0f ? a / lsum : 0.0f);
-    if (lse && x == 0) lse[orow] = lsum > 0.0f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+    __syncthreads();
+    for (int h = warp; h < G; h += D / 32) {
+      float Ls = 0.0f;
+      for (int c = lane; c < nch; c += 32) Ls += s_w[c * G + h] * s_l[c * G + h];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+      if (lane == 0) s_L[h] = Ls;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float M = s_M[h];
+      float a = 0.0f, lsum = s_L[h];
+#pragma unroll 4
+      for (int c = 0; c < nch; ++c) a += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
+      if (append) {
+        const float f = exp2f(snew[h] - M);
+        a += vn * f;
+        lsum += f;
+      }
+      const int64_t orow = nrow * G + h;
+      Elt<Tin>::put(out + orow * D, x, lsum > 0.0f ? a / lsum : 0.0f);
+      if (lse && x == 0) lse[orow] = lsum > 0.0f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+    }
+  } else {
+    // more chunks than the staging holds: per head, a pass for the maximum
+    // and a pass for the weighted sums
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = append ? snew[h] : -INFINITY;
+      for (int c = 0; c < nch; ++c) M = fmaxf(M, base[(int64_t)(c * G + h) * (D + 2) + D]);
+      float a = 0.0f, lsum = 0.0f;
+      for (int c = 0; c < nch; ++c) {
+        const float* pc = base + (int64_t)(c * G + h) * (D + 2);
+        const float mc = pc[D];
+        const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
+        a += pc[x] * f;
+        lsum += pc[D + 1] * f;
+      }
+      if (append) {
+        const float f = exp2f(snew[h] - M);
+        a += vn * f;
+        lsum += f;
+      }
+      const int64_t orow = nrow * G + h;
+      Elt<Tin>::put(out + orow * D, x, lsum > 0.0f ? a / lsum : 0.0f);
+      if (lse && x == 0) lse[orow] = lsum > 0.0f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+    }
   }
   __syncthreads();                      // every thread has read len[i] and the pool
   if (room) {

@@ -79,34 +79,42 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
   // what it copied itself, so its own cp.async wait is enough)
   const uint32_t lane_ring =
       smem_u32(ring) + (uint32_t)((warp * kStages * kRows) * kBlockBytes + lane * 16);
-  auto issue = [&](int64_t q) {
-    const int64_t task = warp_global + (q / NIT) * warps_total;
-    const int k = (int)(q % NIT);
-    const int slot = (int)(q % kStages);
-    const int64_t r0 = task * kRows;
-    const int c = k * 32 + lane;
+  // iteration cursors, advanced without divisions: (task, column block, slot)
+  struct Cursor {
+    int64_t task;
+    int k, slot;
+  };
+  auto advance = [&](Cursor& cu) {
+    if (++cu.k == NIT) { cu.k = 0; cu.task += warps_total; }
+    if (++cu.slot == kStages) cu.slot = 0;
+  };
+  auto issue = [&](const Cursor& cu) {
+    const int64_t r0 = cu.task * kRows;
+    const int c = cu.k * 32 + lane;
+    const Tin* rowp = hidden + r0 * (int64_t)Dh + (int64_t)c * E;
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
       const bool ok = c < NC && r0 + r < rows;
-      const Tin* src = ok ? hidden + (r0 + r) * (int64_t)Dh + (int64_t)c * E : hidden;
-      cp_async16(lane_ring + (uint32_t)((slot * kRows + r) * kBlockBytes), src, ok ? 16u : 0u);
+      cp_async16(lane_ring + (uint32_t)((cu.slot * kRows + r) * kBlockBytes),
+                 ok ? rowp + (int64_t)r * Dh : hidden, ok ? 16u : 0u);
     }
   };
+  Cursor ahead{warp_global, 0, 0};          // the next iteration to fetch
 #pragma unroll
   for (int x = 0; x < kStages; ++x) {
-    if (x < nq) issue(x);
+    if (x < nq) { issue(ahead); advance(ahead); }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
+  Cursor cur{warp_global, 0, 0};            // the iteration being multiplied
   float acc[kRows][HK];
 #pragma unroll
   for (int r = 0; r < kRows; ++r)
 #pragma unroll
     for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
   for (int64_t q = 0; q < nq; ++q) {
-    const int64_t task = warp_global + (q / NIT) * warps_total;
-    const int k = (int)(q % NIT);
-    const int slot = (int)(q % kStages);
-    const int64_t r0 = task * kRows;
+    const int k = cur.k;
+    const int slot = cur.slot;
+    const int64_t r0 = cur.task * kRows;
     asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
     const int c = k * 32 + lane;
     uint4 hv[kRows];
@@ -118,7 +126,7 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
                    : "r"(a));
     }
     // the slot is now in registers: refill it with iteration q + kStages
-    if (q + kStages < nq) issue(q + kStages);
+    if (q + kStages < nq) { issue(ahead); advance(ahead); }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (c < NC) {
       float wv[E * HK];
@@ -147,19 +155,23 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
           for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
           acc[r][g] = v;
         }
-      // lane (r*HK + g) writes (row r, head g)
+      // lane (r*HK + g) mod 32 writes (row r, head g); one division per task
+      const int64_t u0 = r0 / T;
+      int64_t uu = u0, tt = r0 - u0 * T;
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        if (r > 0 && ++tt == T) { tt = 0; ++uu; }
+#pragma unroll
+        for (int g = 0; g < HK; ++g)
+          if (lane == ((r * HK + g) & 31) && r0 + r < rows)
+            scores[(uu * HK + g) * (int64_t)T + tt] = acc[r][g] + (bias ? bias[g] : 0.0f);
+      }
 #pragma unroll
       for (int r = 0; r < kRows; ++r)
 #pragma unroll
-        for (int g = 0; g < HK; ++g) {
-          if (lane == ((r * HK + g) & 31) && r0 + r < rows) {
-            const int64_t row = r0 + r;
-            const int64_t u = row / T, t = row % T;
-            scores[(u * HK + g) * (int64_t)T + t] = acc[r][g] + (bias ? bias[g] : 0.0f);
-          }
-          acc[r][g] = 0.0f;
-        }
+        for (int g = 0; g < HK; ++g) acc[r][g] = 0.0f;
     }
+    advance(cur);
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
