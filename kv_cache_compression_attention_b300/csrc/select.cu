@@ -10,24 +10,32 @@
 // Design (one thread-block cluster per selection pool):
 //  * A pool is one unit's Hkv heads (global top-k) or one head (per-head
 //    budget, threshold).  The cluster's C CTAs split the pool's tokens into
-//    C contiguous ranges; each CTA keeps its range's order-preserving uint32
-//    keys in shared memory, head-major (keys[head][token]), so every pass
-//    over them is a conflict-free sweep of consecutive words.
-//  * Radix select, 4 passes of 8-bit digits, from the most significant
-//    digit: every CTA histograms its candidates that match the prefix found
-//    so far (into 8 sub-histograms; one atomic per warp when all its
-//    candidates share the digit, as in the first pass), adds its
-//    histogram into rank 0's with distributed-shared-memory atomics, and
-//    after one cluster barrier every CTA reads the totals and picks the same
-//    digit.  After the last pass the exact key of the need-th largest
-//    candidate (thr) and how many of its equal-key elements to keep are known.
+//    C contiguous ranges; each CTA copies its range of every head's score
+//    row into shared memory (bulk asynchronous copies when the rows are
+//    16-byte aligned), keys[head][token], and turns the scores into
+//    order-preserving uint32 keys in place, V = 4 consecutive keys per
+//    thread and step when the range allows (1 otherwise).
+//  * Radix select, 4 passes of 8-bit digits from the most significant one.
+//    Every warp histograms into a private shared-memory histogram (one
+//    atomic per warp when its candidates share a digit, else one per
+//    candidate).  The first pass is counted while the keys are made;
+//    the second sweeps the keys once more and appends the candidates that
+//    match the first digit to the warp's own list; the third and fourth
+//    sweep only that list, compacting it in place.  After each pass every
+//    CTA adds its histogram into the bins' owners (bin b lives in CTA
+//    b * C / 256) with distributed-shared-memory atomics, and after one
+//    cluster barrier every CTA reads the 256 totals and picks the same
+//    digit.  When the chosen bin is kept whole, selection stops early:
+//    every key at or above the bin's smallest prefix is kept.
 //  * Ties (key == thr) are only ranked when not all of them are kept: a
 //    cluster prefix of per-CTA tie counts, then a block scan over tokens of
 //    the per-token tie counts, gives the first dropped tie in the tie-break
 //    order (token asc, head asc), as an element index e = t * hps + head.
-//  * Emission: a counting sweep and a cluster prefix give each CTA its base
-//    per head; a block-wide ballot scan over consecutive tokens then writes
-//    the ascending token indices of each head.
+//  * Emission: warp w owns a contiguous 1/32 of the range's tokens; per head
+//    it writes its kept tokens, ascending, into its own staging segment
+//    (ballot + popcount, no block barrier), then one scan over the warps
+//    and a cluster prefix of the per-head counts place every segment in the
+//    output with coalesced stores.
 //  * Offsets (exclusive scan of the counts): a launch with a single pool
 //    writes them from rank 0; otherwise a separate single-block kernel scans
 //    the counts of all pools (threshold pools have data-dependent totals).
@@ -61,31 +69,78 @@ struct Args {
   int32_t* kept;
   int32_t* counts;
   int64_t* offsets;   // written here when the launch has a single pool, else NULL
+  int* status;
 };
 
-constexpr int kSubHist = 8;              // sub-histograms (4 warps each)
-constexpr int kList2 = 4096;             // capacity of the second candidate list
-
 struct Shared {
-  uint32_t hist[kSubHist][256];       // this CTA's sub-histograms of the current pass
-  uint32_t tot[4][256];               // cluster totals per pass (summed into rank 0)
+  uint32_t whist[kWarps][256];        // per-warp histograms of the current pass
+  uint32_t part[4][256];              // partial sums of the warp histograms
+  uint32_t tot[4][256];               // per pass: totals of the bins this CTA owns
   uint32_t totl[256];                 // this CTA's copy of the pass totals
   uint32_t warp_tmp[2][kWarps];       // block scans (double-buffered)
   uint32_t warp_tot[2];
-  uint32_t hcnt[kWarps][kMaxHps];     // per-warp kept counts per head
-  uint32_t emit_tmp[2][kMaxHps][kWarps];  // emission scans (double-buffered)
-  uint32_t emit_tot[2][kMaxHps];
+  uint32_t wcnt[kMaxHps][kWarps];     // emission: kept tokens per head and warp
+  uint32_t wexcl[kMaxHps][kWarps];    // ... their exclusive prefix over warps
   uint32_t xchg_ties;                 // read remotely
   uint32_t xchg_cnt[kMaxHps];         // read remotely
+  uint32_t xall[16][kMaxHps];         // every CTA's per-head counts
   uint32_t head_base[kMaxHps];
   uint32_t head_total[kMaxHps];
-  uint32_t sel_bin, sel_above, sel_count, ecut, tie_base, nlist;
-  uint32_t list2[kList2];             // candidates of the last two passes
+  uint32_t sel_bin, sel_above, sel_count, ecut, tie_base;
+  uint64_t bar;                       // completion of the bulk score copies
 };
 
-__device__ __forceinline__ bool is_prot(int t, int T, int n_sink, int n_recent) {
-  return t < n_sink || t >= T - n_recent;
+// Shared-memory layout after Shared: the keys (nt * hps words, rounded up to
+// 4), then one region that first holds the warps' candidate lists and later
+// the emission staging segments.
+struct Layout {
+  int nloc, cap_w, per_w, region;
+  __host__ __device__ Layout(int nt, int hps, int V) {
+    nloc = nt * hps;
+    // a warp visits at most ceil(nloc / (1024 V)) groups of 32 V keys
+    cap_w = 32 * V * ((nloc + kThreads * V - 1) / (kThreads * V));
+    per_w = (nt + kWarps - 1) / kWarps;          // emission tokens per warp
+    const int lists = kWarps * cap_w, stage = hps * kWarps * per_w;
+    region = lists > stage ? lists : stage;
+  }
+  __host__ __device__ size_t keys_words() const { return ((size_t)nloc + 3) & ~size_t(3); }
+};
+
+// Adds the warp's candidates' digits into its private histogram: one
+// atomic for the warp when all its candidates share a digit, else one per
+// candidate (lanes with equal digits serialise on one address, which costs
+// less than grouping them first).  Returns the ballot of candidates.
+__device__ __forceinline__ uint32_t hist_add(uint32_t* wh, bool cand, uint32_t digit, int lane) {
+  const uint32_t cm = __ballot_sync(0xffffffffu, cand);
+  if (cm) {
+    const int first = __ffs(cm) - 1;
+    const uint32_t d0 = __shfl_sync(0xffffffffu, digit, first);
+    if (__all_sync(0xffffffffu, !cand || digit == d0)) {
+      if (lane == first) atomicAdd(&wh[d0], (uint32_t)__popc(cm));
+    } else if (cand) {
+      atomicAdd(&wh[digit], 1u);
+    }
+  }
+  return cm;
 }
+
+// V consecutive keys.
+template <int V> struct Vec;
+template <> struct Vec<1> {
+  uint32_t k[1];
+  __device__ __forceinline__ void load(const uint32_t* p) { k[0] = *p; }
+  __device__ __forceinline__ void store(uint32_t* p) const { *p = k[0]; }
+};
+template <> struct Vec<4> {
+  uint32_t k[4];
+  __device__ __forceinline__ void load(const uint32_t* p) {
+    const uint4 x = *reinterpret_cast<const uint4*>(p);
+    k[0] = x.x; k[1] = x.y; k[2] = x.z; k[3] = x.w;
+  }
+  __device__ __forceinline__ void store(uint32_t* p) const {
+    *reinterpret_cast<uint4*>(p) = make_uint4(k[0], k[1], k[2], k[3]);
+  }
+};
 
 // Exclusive block scan of one value per thread; returns the prefix and sets
 // *total.  Two barriers; consecutive calls alternate scratch buffers.
@@ -118,6 +173,31 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, Shared& sh, int& buf,
   return r;
 }
 
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_plain() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// V = 4 requires every CTA's range to start and end on a multiple of 4
+// tokens and 16-byte aligned score rows (then the rows are bulk-copied).
+template <int V>
 __global__ void __launch_bounds__(kThreads, 1)
 select_kernel(Args a) {
   cg::cluster_group cl = cg::this_cluster();
@@ -130,68 +210,28 @@ select_kernel(Args a) {
   const int t0 = (int)((int64_t)rank * T / C);
   const int t1 = (int)((int64_t)(rank + 1) * T / C);
   const int nt = t1 - t0;
-  const int nloc = nt * hps;
+  const Layout lay(nt, hps, V);
+  const int nloc = lay.nloc;
+  const int nvec = nloc / V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
   int sbuf = 0;
 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
-  // (the first candidate list follows the keys: nloc more words)
+  uint32_t* region = keys + lay.keys_words();
 
   for (int i = tid; i < 4 * 256; i += kThreads) (&sh.tot[0][0])[i] = 0u;
-  for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
-
-  // ---- phase A: keys of this CTA's token range, head-major (coalesced
-  // global reads, conflict-free shared stores, sixteen loads in flight);
-  // item q covers head q / nch, vector slots (q % nch) * 1024 + tid.  When the
-  // rows and the range are 16-byte aligned every slot is a float4 of 4 tokens.
-  {
-    const bool vec = ((T | t0 | nt) & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15u) == 0;
-    const int per = vec ? 4 : 1;                       // tokens per slot
-    const int nslot = nt / per;
-    const int nch = (nslot + kThreads - 1) / kThreads;
-    const int nq = hps * nch;
-    for (int q0 = 0; q0 < nq; q0 += 8) {
-      float4 sv[8];
-      int hh = q0 / nch, jc = q0 - (q0 / nch) * nch;
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int js = jc * kThreads + tid;
-        if (q0 + x < nq && js < nslot) {
-          const float* row = a.scores + (int64_t)(head0 + hh) * T + t0;
-          if (vec) sv[x] = __ldg(reinterpret_cast<const float4*>(row) + js);
-          else sv[x].x = __ldg(row + js);
-        }
-        if (++jc == nch) { jc = 0; ++hh; }
-      }
-      hh = q0 / nch; jc = q0 - hh * nch;
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int js = jc * kThreads + tid;
-        if (q0 + x < nq && js < nslot) {
-          const int j = js * per;
-          uint32_t* dst = keys + hh * nt + j;
-          if (vec) {
-            uint4 kk;
-            kk.x = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].x);
-            kk.y = is_prot(t0 + j + 1, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].y);
-            kk.z = is_prot(t0 + j + 2, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].z);
-            kk.w = is_prot(t0 + j + 3, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].w);
-            *reinterpret_cast<uint4*>(dst) = kk;
-          } else {
-            dst[0] = is_prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(sv[x].x);
-          }
-        }
-        if (++jc == nch) { jc = 0; ++hh; }
-      }
-    }
+  for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.whist[0][0])[i] = 0u;
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_barrier_init();
   }
-  // every CTA of the cluster is running and its totals are zero before any
-  // remote update
-  cl.sync();
+  __syncthreads();
+  // the totals are zero: peers may add into them once this barrier completes
+  cluster_arrive_release();
 
-  // ---- phase B: radix select of the need-th largest candidate key
   int64_t need = 0;
   if (a.mode == KVC_SEL_GLOBAL_TOPK) {
     need = a.need_global;
@@ -201,6 +241,71 @@ select_kernel(Args a) {
     if (b > T) b = T;
     need = b - a.nP;
   }
+  const bool radix = a.mode != KVC_SEL_THRESHOLD && need > 0;
+  uint32_t* wh = sh.whist[warp];
+
+  // ---- phase A: the range's scores into shared memory, keys made in place
+  // while the first pass's digits (bits 31-24) are counted
+  if (V == 4) {
+    if (nt > 0) {
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&sh.bar, (uint32_t)nloc * 4u);
+        for (int hh = 0; hh < hps; ++hh)
+          bulk_g2s(smem_u32(keys + hh * nt), a.scores + (int64_t)(head0 + hh) * T + t0,
+                   (uint32_t)nt * 4u, &sh.bar);
+      }
+      mbar_wait(&sh.bar, 0, a.status, nullptr);
+    }
+    for (int q0 = warp * 32; q0 < nvec; q0 += kThreads) {
+      const int q = q0 + lane;
+      Vec<V> x;
+#pragma unroll
+      for (int i = 0; i < V; ++i) x.k[i] = 0u;
+      const bool ok = q < nvec;
+      if (ok) x.load(keys + (size_t)q * V);
+#pragma unroll
+      for (int i = 0; i < V; ++i) x.k[i] = score_key(__uint_as_float(x.k[i]));
+      if (ok) x.store(keys + (size_t)q * V);
+      if (radix) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) hist_add(wh, ok, x.k[i] >> 24, lane);
+      }
+    }
+  } else {
+    for (int hh = 0; hh < hps; ++hh) {
+      const float* row = a.scores + (int64_t)(head0 + hh) * T + t0;
+      uint32_t* kr = keys + hh * nt;
+      for (int j0 = warp * 32; j0 < nt; j0 += kThreads) {
+        const int j = j0 + lane;
+        const bool ok = j < nt;
+        const uint32_t key = ok ? score_key(__ldg(row + j)) : 0u;
+        if (ok) kr[j] = key;
+        if (radix) hist_add(wh, ok, key >> 24, lane);
+      }
+    }
+  }
+  __syncthreads();
+  // protected tokens of this range: key 0 (not a candidate), taken back out
+  // of the first pass's histogram.  The sink range and the part of the
+  // recent window past it are disjoint, so no key is visited twice.
+  {
+    const int s_hi = min(t1, a.n_sink);                        // sinks [t0, s_hi)
+    const int r_lo = max(max(t0, T - a.n_recent), a.n_sink);   // recent [r_lo, t1)
+    const int ns = max(0, s_hi - t0), nr = max(0, t1 - r_lo);
+    const int np = ns + nr;
+    for (int i = tid; i < np * hps; i += kThreads) {
+      const int hh = i / np, x = i - hh * np;
+      const int t = x < ns ? t0 + x : r_lo + (x - ns);
+      uint32_t* kp = keys + hh * nt + (t - t0);
+      const uint32_t key = *kp;
+      *kp = 0u;
+      if (radix) atomicSub(&sh.whist[0][key >> 24], 1u);
+    }
+  }
+  __syncthreads();
+  cluster_wait_acquire();
+
+  // ---- phase B: radix select of the need-th largest candidate key
   uint32_t thr = kNoThr;
   uint32_t ecut = 0;
   if (a.mode == KVC_SEL_THRESHOLD) {
@@ -209,52 +314,65 @@ select_kernel(Args a) {
     uint32_t prefix = 0, pmask = 0;
     uint32_t krem = (uint32_t)need;
     uint32_t last_count = 0;
-    uint32_t* myhist = sh.hist[warp & (kSubHist - 1)];
-    // candidates of the later passes: after pass 0 the keys whose top byte
-    // matches are copied to list1; after pass 1 those matching 16 bits go to
-    // list2 when they fit (otherwise pass 2 and 3 scan list1 again)
-    uint32_t* list1 = keys + nloc;
-    uint32_t* list2 = sh.list2;
-    const uint32_t* src = keys;
-    int nsrc = nloc;
+    bool whole_bin = false;
+    uint32_t* wl = region + warp * lay.cap_w;   // this warp's candidate list
+    int nl = 0;                                 // its length (warp-uniform)
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      if (pass > 0) {
-        for (int i = tid; i < kSubHist * 256; i += kThreads) (&sh.hist[0][0])[i] = 0u;
-        __syncthreads();
-      }
-      for (int e0 = 0; e0 < nsrc; e0 += kThreads) {
-        const int e = e0 + tid;
-        bool cand = false;
-        uint32_t digit = 0u;
-        if (e < nsrc) {
-          const uint32_t key = src[e];
-          cand = key != 0u && (key & pmask) == prefix;
-          digit = (key >> shift) & 255u;
-        }
-        // one atomic per warp when all its candidates share a digit (the
-        // common case in the first pass), else one per candidate
-        const uint32_t cmask = __ballot_sync(0xffffffffu, cand);
-        if (cmask) {
-          const uint32_t d0 = __shfl_sync(0xffffffffu, digit, __ffs(cmask) - 1);
-          if (__all_sync(0xffffffffu, !cand || digit == d0)) {
-            if (lane == 0) atomicAdd(&myhist[d0], (uint32_t)__popc(cmask));
-          } else if (cand) {
-            atomicAdd(&myhist[digit], 1u);
+      if (pass == 1) {
+        // keys matching the first digit: histogram the second, append to the list
+        for (int q0 = warp * 32; q0 < nvec; q0 += kThreads) {
+          const int q = q0 + lane;
+          Vec<V> x;
+          if (q < nvec) x.load(keys + (size_t)q * V);
+          else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) x.k[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            const bool cand = x.k[i] != 0u && (x.k[i] & pmask) == prefix;
+            const uint32_t cm = hist_add(wh, cand, (x.k[i] >> shift) & 255u, lane);
+            if (cand) wl[nl + __popc(cm & lt_mask)] = x.k[i];
+            nl += __popc(cm);
           }
         }
+      } else if (pass > 1) {
+        // the warp's list, compacted in place to the candidates of this pass
+        // (a lane writes at or below the slot it read; all reads of a group
+        // precede its ballot)
+        int nn = 0;
+        for (int e0 = 0; e0 < nl; e0 += 32) {
+          const int e = e0 + lane;
+          const uint32_t key = (e < nl) ? wl[e] : 0u;
+          const bool cand = key != 0u && (key & pmask) == prefix;
+          const uint32_t cm = hist_add(wh, cand, (key >> shift) & 255u, lane);
+          if (cand) wl[nn + __popc(cm & lt_mask)] = key;
+          nn += __popc(cm);
+        }
+        nl = nn;
       }
       __syncthreads();
-      // every CTA adds its histogram into rank 0's totals of this pass
-      if (tid < 256) {
-        uint32_t h = 0;
+      // reduce the warp histograms (and clear them for the next pass); every
+      // CTA adds its histogram into the bins' owners
+      {
+        const int b = tid & 255, qq = tid >> 8;
+        uint32_t s = 0;
 #pragma unroll
-        for (int x = 0; x < kSubHist; ++x) h += sh.hist[x][tid];
-        if (h) atomicAdd(cl.map_shared_rank(&sh.tot[pass][tid], 0), h);
+        for (int w = 0; w < kWarps / 4; ++w) {
+          s += sh.whist[qq * (kWarps / 4) + w][b];
+          sh.whist[qq * (kWarps / 4) + w][b] = 0u;
+        }
+        sh.part[qq][b] = s;
+      }
+      __syncthreads();
+      if (tid < 256) {
+        const uint32_t h = sh.part[0][tid] + sh.part[1][tid] + sh.part[2][tid] + sh.part[3][tid];
+        if (h) atomicAdd(cl.map_shared_rank(&sh.tot[pass][tid], (tid * C) >> 8), h);
       }
       cl.sync();
-      if (tid < 256) sh.totl[tid] = *cl.map_shared_rank(&sh.tot[pass][tid], 0);
+      if (tid < 256) sh.totl[tid] = *cl.map_shared_rank(&sh.tot[pass][tid], (tid * C) >> 8);
       __syncthreads();
       if (warp == 0) {
         uint32_t cnt[8];
@@ -284,35 +402,18 @@ select_kernel(Args a) {
       last_count = sh.sel_count;
       prefix |= bin << shift;
       pmask |= 255u << shift;
-      if (pass < 2) {
-        // compact this CTA's candidates of the next pass (warp-aggregated appends)
-        uint32_t* dst = (pass == 0) ? list1 : list2;
-        const int cap = (pass == 0) ? nloc : kList2;
-        if (tid == 0) sh.nlist = 0u;
-        __syncthreads();
-        for (int e0 = 0; e0 < nsrc; e0 += kThreads) {
-          const int e = e0 + tid;
-          uint32_t key = 0u;
-          bool keep = false;
-          if (e < nsrc) {
-            key = src[e];
-            keep = key != 0u && (key & pmask) == prefix;
-          }
-          const uint32_t bm = __ballot_sync(0xffffffffu, keep);
-          uint32_t base = 0u;
-          if (lane == 0 && bm) base = atomicAdd(&sh.nlist, (uint32_t)__popc(bm));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          const uint32_t at = base + __popc(bm & ((1u << lane) - 1u));
-          if (keep && at < (uint32_t)cap) dst[at] = key;
-        }
-        __syncthreads();
-        if (sh.nlist <= (uint32_t)cap) { src = dst; nsrc = (int)sh.nlist; }
-        __syncthreads();
-      }
+      if (krem == last_count) { whole_bin = true; break; }   // uniform across the cluster
     }
-    thr = prefix;
+    if (whole_bin) {
+      // keep every key >= prefix: key > prefix - 1 with no tie list (prefix 0
+      // keeps every candidate; no candidate key is 0)
+      thr = prefix ? prefix - 1u : 0u;
+      ecut = 0;
+    } else {
+      thr = prefix;
+    }
     // ---- ties: keep the first krem elements with key == thr in (t, g) order
-    if (krem < last_count) {
+    if (!whole_bin && krem < last_count) {
       uint32_t mine = 0;
       for (int e = tid; e < nloc; e += kThreads) mine += (keys[e] == thr);
       mine = __reduce_add_sync(0xffffffffu, mine);
@@ -359,43 +460,70 @@ select_kernel(Args a) {
         __syncthreads();
         ecut = sh.ecut;
       }
-    } else {
+    } else if (!whole_bin) {
       ecut = (uint32_t)nloc;
     }
   }
 
-  // kept(hh, j): protected, strictly above thr, or a kept tie
-  auto kept = [&](int hh, int j) -> bool {
-    const uint32_t key = keys[hh * nt + j];
-    if (key == 0u) return true;
-    if (a.mode == KVC_SEL_THRESHOLD) return key >= thr;
-    return key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut);
+  // ---- phase D: warp w emits the kept tokens of its slice [j_lo, j_hi) of
+  // the range, per head, ascending, into its staging segment
+  const int per_w = lay.per_w;
+  const int j_lo = min(nt, warp * per_w), j_hi = min(nt, j_lo + per_w);
+  const bool thr_mode = a.mode == KVC_SEL_THRESHOLD;
+  auto keep = [&](uint32_t key, int j, int hh) -> bool {
+    return key == 0u || (thr_mode ? key >= thr
+                                  : (key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut)));
   };
-
-  // ---- phase D: per-head counts, cluster prefix, ascending emission
   for (int hh = 0; hh < hps; ++hh) {
-    uint32_t c = 0;
-    for (int j = tid; j < nt; j += kThreads) c += kept(hh, j);
-    c = __reduce_add_sync(0xffffffffu, c);
-    if (lane == 0) sh.hcnt[warp][hh] = c;
+    const uint32_t* kr = keys + hh * nt;
+    uint32_t* sg = region + (size_t)(hh * kWarps + warp) * per_w;
+    uint32_t n = 0;
+    for (int j0 = j_lo; j0 < j_hi; j0 += 64) {
+      const int ja = j0 + lane, jb = ja + 32;
+      const uint32_t ka = ja < j_hi ? kr[ja] : 0u;
+      const uint32_t kb = jb < j_hi ? kr[jb] : 0u;
+      const bool fa = ja < j_hi && keep(ka, ja, hh);
+      const bool fb = jb < j_hi && keep(kb, jb, hh);
+      const uint32_t ba = __ballot_sync(0xffffffffu, fa);
+      const uint32_t bb = __ballot_sync(0xffffffffu, fb);
+      if (fa) sg[n + __popc(ba & lt_mask)] = (uint32_t)(t0 + ja);
+      n += __popc(ba);
+      if (fb) sg[n + __popc(bb & lt_mask)] = (uint32_t)(t0 + jb);
+      n += __popc(bb);
+    }
+    if (lane == 0) sh.wcnt[hh][warp] = n;
   }
   __syncthreads();
-  if (tid < hps) {
-    uint32_t s = 0;
-    for (int w = 0; w < kWarps; ++w) s += sh.hcnt[w][tid];
-    sh.xchg_cnt[tid] = s;
+  // per head: exclusive prefix over the warps, CTA total
+  if (warp < hps) {
+    const uint32_t x = sh.wcnt[warp][lane];
+    uint32_t y = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) y += n;
+    }
+    sh.wexcl[warp][lane] = y - x;
+    if (lane == 31) sh.xchg_cnt[warp] = y;
   }
   cl.sync();
+  if (tid < C * hps) {
+    const int r = tid / hps, hh = tid - r * hps;
+    sh.xall[r][hh] = cl.map_shared_rank(sh.xchg_cnt, r)[hh];
+  }
+  __syncthreads();
+  // every remote read of this CTA's counts is done once all CTAs pass here
+  cluster_arrive_relaxed();
   if (tid < hps) {
     uint32_t base = 0, total = 0;
     for (int r = 0; r < C; ++r) {
-      const uint32_t v = cl.map_shared_rank(sh.xchg_cnt, r)[tid];
+      const uint32_t v = sh.xall[r][tid];
       if (r < rank) base += v;
       total += v;
     }
     sh.head_base[tid] = base;
-    if (rank == 0) a.counts[head0 + tid] = (int32_t)total;
     sh.head_total[tid] = total;
+    if (rank == 0) a.counts[head0 + tid] = (int32_t)total;
   }
   __syncthreads();
   // a launch with a single pool writes the offsets itself (no second kernel)
@@ -404,46 +532,15 @@ select_kernel(Args a) {
     for (int hh = 0; hh < hps; ++hh) { a.offsets[hh] = o; o += sh.head_total[hh]; }
     a.offsets[hps] = o;
   }
-  // one block scan per 1024-token chunk covers every head: flags by ballot,
-  // per-warp counts scanned by one warp per head, positions by popcount
-  uint32_t carry[kMaxHps];
-#pragma unroll
-  for (int hh = 0; hh < kMaxHps; ++hh) carry[hh] = (hh < hps) ? sh.head_base[hh] : 0u;
-  for (int j0 = 0; j0 < nt; j0 += kThreads) {
-    const int j = j0 + tid;
-    uint32_t ball[kMaxHps];
-    uint32_t (*wt)[kWarps] = sh.emit_tmp[sbuf];
-#pragma unroll
-    for (int hh = 0; hh < kMaxHps; ++hh) {
-      const bool f = hh < hps && j < nt && kept(hh, j);
-      ball[hh] = __ballot_sync(0xffffffffu, f);
-      if (lane == 0 && hh < hps) wt[hh][warp] = __popc(ball[hh]);
-    }
-    __syncthreads();
-    if (warp < hps) {
-      const uint32_t x = wt[warp][lane];
-      uint32_t y = x;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t n = __shfl_up_sync(0xffffffffu, y, off);
-        if (lane >= off) y += n;
-      }
-      wt[warp][lane] = y - x;
-      if (lane == 31) sh.emit_tot[sbuf][warp] = y;
-    }
-    __syncthreads();
-    const uint32_t below = (1u << lane) - 1u;
-#pragma unroll
-    for (int hh = 0; hh < kMaxHps; ++hh) {
-      if (hh >= hps) break;
-      if (ball[hh] & (1u << lane))
-        a.kept[(int64_t)(head0 + hh) * T + carry[hh] + wt[hh][warp] + __popc(ball[hh] & below)] = t0 + j;
-      carry[hh] += sh.emit_tot[sbuf][hh];
-    }
-    sbuf ^= 1;
+  // the staging segments into place (each warp its own, coalesced)
+  for (int hh = 0; hh < hps; ++hh) {
+    const uint32_t n = sh.wcnt[hh][warp];
+    int32_t* dst = a.kept + (int64_t)(head0 + hh) * T + sh.head_base[hh] + sh.wexcl[hh][warp];
+    const uint32_t* sg = region + (size_t)(hh * kWarps + warp) * per_w;
+    for (uint32_t i = lane; i < n; i += 32) dst[i] = (int32_t)sg[i];
   }
   // no CTA may leave while a peer can still read its shared memory
-  cl.sync();
+  cluster_wait_plain();
 }
 
 // offsets[i] = sum_{j<i} counts[j], offsets[n] = total (one block).
@@ -485,8 +582,10 @@ offsets_kernel(const int32_t* __restrict__ counts, int n, int64_t* __restrict__ 
   if (threadIdx.x == 0) offsets[n] = carry_s;
 }
 
-// keys of the CTA's range plus the same capacity for the first candidate list
-size_t shared_bytes(int keys) { return ((sizeof(Shared) + 15) & ~size_t(15)) + 2ull * keys * 4; }
+size_t shared_bytes(int nt, int hps, int V) {
+  const Layout lay(nt, hps, V);
+  return ((sizeof(Shared) + 15) & ~size_t(15)) + (lay.keys_words() + (size_t)lay.region) * 4;
+}
 
 }  // namespace
 
@@ -498,12 +597,16 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   if (hps > kMaxHps) return KVC_ERR_UNSUPPORTED;
   const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
   const int64_t pool = (int64_t)hps * T;
-  const int cap = (int)((dev.max_smem_optin - (int)shared_bytes(0)) / 8);
+  const size_t smem_max = (size_t)dev.max_smem_optin;
+  const bool aligned = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
+  // four keys per thread and step when every CTA's range is a multiple of 4
+  auto vec_for = [&](int c) { return (aligned && T % (4 * c) == 0) ? 4 : 1; };
+  auto smem_for = [&](int c) { return shared_bytes((T + c - 1) / c, hps, vec_for(c)); };
   // the smallest cluster that keeps <= 16K keys per CTA, else the smallest that fits
   int C = 1;
   while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
-  while (C < 16 && (pool + C - 1) / C > cap) C *= 2;
-  if ((pool + C - 1) / C > cap) return KVC_ERR_UNSUPPORTED;
+  while (C < 16 && smem_for(C) > smem_max) C *= 2;
+  if (smem_for(C) > smem_max) return KVC_ERR_UNSUPPORTED;
   Args a;
   a.scores = scores; a.T = T; a.hps = hps; a.mode = mode; a.need_global = need_global;
   a.tau = tau; a.head_budget = head_budget; a.n_sink = n_sink; a.n_recent = n_recent;
@@ -514,15 +617,17 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   }
   a.kept = kept_idx; a.counts = counts;
   a.offsets = (nseg == 1) ? offsets : nullptr;
+  a.status = dev.status;
   static std::mutex mu;
   static bool attr_done[64];
   static std::map<std::tuple<int, int, size_t>, int> active_memo;
   std::lock_guard<std::mutex> lock(mu);
   if (!attr_done[dev.device & 63]) {
-    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel,
-                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-    KVC_CUDA_TRY(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      dev.max_smem_optin));
+    for (auto fn : {select_kernel<1>, select_kernel<4>}) {
+      KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+      KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        dev.max_smem_optin));
+    }
     attr_done[dev.device & 63] = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -531,7 +636,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   // the occupancy query says at least one cluster can be resident (the
   // answer is remembered per device, cluster size and shared memory)
   for (;;) {
-    const size_t smem = shared_bytes(((T + C - 1) / C) * hps);
+    const size_t smem = smem_for(C);
     cfg.gridDim = dim3((unsigned)C, (unsigned)nseg, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
@@ -548,14 +653,15 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     if (it != active_memo.end()) {
       active = it->second;
     } else {
-      KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel, &cfg));
+      KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel<1>, &cfg));
       active_memo[key] = active;
     }
     if (active > 0) break;
-    if (C == 1 || (pool + C / 2 - 1) / (C / 2) > cap) return KVC_ERR_UNSUPPORTED;
+    if (C == 1 || smem_for(C / 2) > smem_max) return KVC_ERR_UNSUPPORTED;
     C /= 2;
   }
-  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel, a));
+  if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
+  else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
   if (nseg > 1) offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
   return launch_status();
 }

@@ -231,3 +231,21 @@ def test_bounded_wait_times_out_and_context_survives(B):
     assert B.kvc_device_status() == 0
     x = torch.ones(4, device="cuda") * 2          # the context is still usable
     assert x.sum().item() == 8
+
+
+def test_decode_more_chunks_than_the_combine_stages(B):
+    """A head of 140 000 rows has 274 chunks of 512, more than the combine
+    kernel stages in shared memory (256): the second merge path runs."""
+    L = 140000
+    kc, vc, start, lens = pool([L], 1, 128, torch.bfloat16, 17)
+    g = torch.Generator().manual_seed(18)
+    q = torch.randn((1, 2, 128), generator=g).to(torch.bfloat16)
+    kn = torch.randn((1, 1, 128), generator=g).to(torch.bfloat16)
+    vn = torch.randn((1, 1, 128), generator=g).to(torch.bfloat16)
+    kcg, vcg = kc.cuda(), vc.cuda()
+    st, ln = torch.from_numpy(start).cuda(), torch.from_numpy(lens).cuda()
+    out, lse = run_decode(B, q.cuda(), kcg, vcg, st, ln, kn.cuda(), vn.cuda(), L + 1, 128 ** -0.5)
+    ro, rl, *_ = O.decode_attn(np64(q), kc.float().numpy(), vc.float().numpy(), start, lens,
+                               np64(kn), np64(vn), 128 ** -0.5)
+    assert row_rel_err(np64(out).reshape(-1, 128), ro.reshape(-1, 128)) <= 2e-2
+    assert lse_err(np64(lse), rl) <= 2e-2
