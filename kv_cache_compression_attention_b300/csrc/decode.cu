@@ -669,6 +669,7 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
         KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         attr_done.fetch_or(bit);
       }
+      if (int rc = prefer_max_shared(kern, dev.device)) return rc;
       kern<<<grid, kWarps * 32, smem, s>>>(
           static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kc),
           static_cast<const uint16_t*>(vc), start, len, Hkv, max_chunks, sl2, ws);
@@ -679,11 +680,13 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
         KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         attr_done.fetch_or(bit);
       }
+      if (int rc = prefer_max_shared(kern, dev.device)) return rc;
       kern<<<grid, (kWarps + 1) * 32, smem, s>>>(
           static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
           start, len, Hkv, max_chunks, sl2, ws, dev.status);
     }
   }
+  if (int rc = prefer_max_shared(decode_combine_kernel<Tin, D, G>, dev.device)) return rc;
   decode_combine_kernel<Tin, D, G><<<n, D, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc), start, len,
       static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new), n, Hkv, max_chunks, sl2,

@@ -5,6 +5,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "kvc.h"
 
 namespace kvc {
@@ -34,6 +38,24 @@ inline int launch_status() {
 }
 
 inline size_t elt_size(int dtype) { return dtype == KVC_F32 ? 4 : 2; }
+
+// Asks for the largest shared-memory carve-out for a kernel, once per
+// device, so that back-to-back launches of the library's shared-memory
+// kernels (score -> select, decode partial -> combine) need no
+// reconfiguration of the SMs in between.  The gather-compaction keeps the
+// default split: its streams run faster with the larger L1.
+template <typename K>
+inline int prefer_max_shared(K* kernel, int device) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), device);
+  if (done.count(key)) return KVC_OK;
+  KVC_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                    (int)cudaSharedmemCarveoutMaxShared));
+  done.insert(key);
+  return KVC_OK;
+}
 
 // Launchers (one per translation unit).  Arguments are already validated.
 int score_attn_simt(const void* q, const void* k, int dtype, int U, int Hq, int Hkv, int T,

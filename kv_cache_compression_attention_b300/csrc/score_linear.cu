@@ -201,6 +201,7 @@ int run(const void* hidden, const void* weight, const float* bias, int U, int T,
   int64_t blocks = dev.sms;
   const int64_t need = (tasks + kWarps - 1) / kWarps;
   if (blocks > need) blocks = need;
+  if (int rc = prefer_max_shared(kern, dev.device)) return rc;
   kern<<<(unsigned)blocks, kWarps * 32, smem, s>>>(static_cast<const Tin*>(hidden),
                                                    static_cast<const Tin*>(weight), bias, rows,
                                                    T, Dh, scores);

@@ -8,16 +8,18 @@
 // The contraction Q_g (R x 128) . K_g^T (128 x T) is a real dense GEMM, so it
 // runs on tcgen05 with fp32 accumulators in TMEM.  The column mass needs
 // every row's normaliser first, so each CTA makes two passes over its K
-// (the second pass finds it in L2).  K streams in super-tiles of 256 tokens;
-// every MMA item is 8 MMAs with N = 256 into one 256-column TMEM buffer:
+// (the second pass finds it in L2).  K streams in stages of two 128-token
+// tiles (a range's last stage holds one when its tile count is odd); every
+// MMA item is 8 MMAs (K = 16 each) into one 256-column TMEM buffer:
 //
-//   pass 1  S = Q_m . K_super^T, one item per 128-row m-tile (rows on TMEM
-//           lanes, 256 tokens on columns): each epilogue thread owns one
-//           window row and 64 of the tokens and keeps a running (max, sum)
-//           in base 2;
+//   pass 1  S = Q_m . K_stage^T, one item per 128-row m-tile (rows on TMEM
+//           lanes, the stage's tokens on columns, N = 256 or 128): each
+//           epilogue thread owns one window row and 64 of the columns and
+//           keeps a running (max, sum) in base 2;
 //   merge   the CTAs that share a (u, g) publish their per-row partial
-//           (max, sum) in global memory with a per-launch tag and wait
-//           (bounded) for the others' tags -> lse_r of every row;
+//           (max, sum) in global memory, each 32-bit value paired with a
+//           per-launch tag in one 64-bit word, and poll (bounded) the
+//           others' partials until the tags match -> lse_r of every row;
 //   pass 2  S^T = K_tile . Q^T, one item per 128-token tile (tokens on TMEM
 //           lanes, N = R): each epilogue thread owns one token and a quarter
 //           of the R columns and sums exp2(c_r * s - lse2_r); quarters 1-3
@@ -27,12 +29,13 @@
 // Work split: one persistent CTA per SM (cooperative launch, so every CTA
 // of a group is resident while its peers wait for it).  The (u, g) pairs
 // are processed in rounds; in a round, group i of gs CTAs owns one (u, g)
-// and CTA j of the group a contiguous range of about 8 super-tiles (1 MiB
-// of K), so that the second pass re-reads K from L2 while every SM is busy.
+// and CTA j of the group a contiguous range of 128-token tiles (about 16,
+// 512 KiB of K; ranges differ by at most one tile), so that the second pass
+// re-reads K from L2 while every SM is busy.
 //
 // Warp roles (576 threads): warps 0-15 epilogue (warp w reads TMEM lanes
 // 32*(w%4)..+31; w/4 picks its column slice), warp 16 TMA producer, warp 17
-// MMA issuer and TMEM owner.  Super-tiles stream through a 2-stage TMA ring
+// MMA issuer and TMEM owner.  Stages stream through a 2-stage TMA ring
 // (256 tokens x 128 dims, four 128-byte-swizzled boxes per stage); the
 // accumulator is double-buffered in TMEM (2 x 256 of the 512 columns), so
 // the MMA of item j+1 overlaps the epilogue of item j.  The window queries
@@ -73,13 +76,12 @@ struct Params {
   const float* head_scale;
   int causal;
   float* scores;
-  int n_super;       // super-tiles (256 tokens) of T
+  int n_tiles;       // 128-token tiles of T
   int heads;         // U * Hkv
   int gs;            // CTAs per (u, g)
   int hpr;           // (u, g) pairs per round
   int rounds;
-  float2* parts;     // [2][grid][R] per-CTA row partials (max2, sum)
-  uint64_t* tags;    // [2][kMaxCtas] per-CTA publication tags
+  ulonglong2* parts; // [2][grid][R] per-CTA row partials: (max2 | tag, sum | tag)
   uint64_t tag0;     // this launch's tag base (unique per launch)
   int* status;
 };
@@ -100,14 +102,19 @@ struct SmemSmall {
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+// A row partial travels as two 64-bit words, each a 32-bit value and the
+// round's 32-bit tag; a 64-bit access is single-copy atomic, so a reader
+// that sees the tag in both words has the value too (no fence, no flag).
+__device__ __forceinline__ ulonglong2 ld_relaxed_v2(const ulonglong2* p) {
+  ulonglong2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];"
+               : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_v2(ulonglong2* p, uint64_t a, uint64_t b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
+               : "memory");
 }
 
 // Merge of two base-2 (max, sum) pairs.
@@ -131,10 +138,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int cta = blockIdx.x;
   const int grp = cta / p.gs, slot = cta - grp * p.gs;
   const bool in_group = grp < p.hpr;
-  // this CTA's super-tiles (pairs of 128-token K tiles) of its (u, g)
-  const int st_lo = (int)((int64_t)slot * p.n_super / p.gs);
-  const int st_hi = (int)((int64_t)(slot + 1) * p.n_super / p.gs);
-  const int ns = st_hi - st_lo;
+  // this CTA's 128-token K tiles [tl_lo, tl_hi) of its (u, g), streamed as
+  // ns stages of two tiles (the last stage holds one when ntl is odd)
+  const int tl_lo = (int)((int64_t)slot * p.n_tiles / p.gs);
+  const int tl_hi = (int)((int64_t)(slot + 1) * p.n_tiles / p.gs);
+  const int ntl = tl_hi - tl_lo;
+  const int ns = (ntl + 1) >> 1;
   const int R = p.R, W = p.W, T = p.T;
   const int n_mt = R / 128;
 
@@ -180,13 +189,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int i = 0; i < 2 * ns; ++i, ++J) {
           const int s = J % kStages;
           if (J >= kStages) mbar_wait(&sm.empty[s], ((J / kStages) - 1) & 1, p.status, abort_flag);
-          const int t0 = (st_lo + i % ns) * (2 * kTile);
+          const int si = i % ns, nti = min(2, ntl - 2 * si);   // tiles in this stage
+          const int t0 = (tl_lo + 2 * si) * kTile;
           const uint32_t dst = k_smem + (uint32_t)s * kStageBytes;
-          mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+          mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nti * 2u * kBoxBytes);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt)
+            for (int tt = 0; tt < nti; ++tt)
               tc::tma_load_3d(dst + h * kHalfBytes + tt * kBoxBytes, &tm_k, 64 * h,
                               t0 + tt * kTile, head, &sm.full[s]);
         }
@@ -195,11 +204,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
-    // pass 1 items: (super-tile, m-tile), D = Q_mtile . K_super^T, N = 256
-    // pass 2 items: (super-tile, tile),   D = K_tile . Q^T,        N = R
+    // pass 1 items: (stage, m-tile), D = Q_mtile . K_stage^T, N = 128 x tiles
+    // pass 2 items: (stage, tile),   D = K_tile . Q^T,         N = R
     // every item is 8 MMAs (K = 16 each) into one 256-column TMEM buffer
     if (lane == 0 && in_group && ns > 0) {
       const uint32_t idesc1 = tc::idesc_bf16_f32(128, 2 * kTile);
+      const uint32_t idesc1h = tc::idesc_bf16_f32(128, kTile);    // a one-tile stage
       const uint32_t idesc2 = tc::idesc_bf16_f32(128, R);
       int J = 0, item = 0, qk = 0;
       for (int k = 0; k < p.rounds; ++k) {
@@ -212,7 +222,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mbar_wait(&sm.full[s], (J / kStages) & 1, p.status, abort_flag);
           tc::fence_after_sync();
           const uint32_t kst = k_smem + (uint32_t)s * kStageBytes;
-          const int n_items = (i < ns) ? n_mt : 2;
+          const int nti = min(2, ntl - 2 * (i < ns ? i : i - ns));
+          const int n_items = (i < ns) ? n_mt : nti;
           for (int x = 0; x < n_items; ++x, ++item) {
             const int b = item & 1;
             if (item >= 2) mbar_wait(&sm.tmem_empty[b], ((item >> 1) - 1) & 1, p.status, abort_flag);
@@ -224,7 +235,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (i < ns) {
                 a = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + x * 128u * 128u + ko);
                 bd = tc::smem_desc_sw128(kst + kh * kHalfBytes + ko);
-                tc::mma_bf16(dcol, a, bd, idesc1, kk > 0);
+                tc::mma_bf16(dcol, a, bd, nti == 2 ? idesc1 : idesc1h, kk > 0);
               } else {
                 a = tc::smem_desc_sw128(kst + kh * kHalfBytes + x * kBoxBytes + ko);
                 bd = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + ko);
@@ -280,6 +291,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int x = 0; x < 4; ++x) acc[mt][x] = 0ull;
       }
       for (int i = 0; i < ns; ++i) {
+        // a one-tile stage fills columns 0-127 only: slices 2 and 3 idle
+        const bool cols = 64 * wq < min(2, ntl - 2 * i) * kTile;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           if (mt >= n_mt) break;
@@ -287,9 +300,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mbar_wait(&sm.tmem_full[b], (item >> 1) & 1, p.status, abort_flag);
           tc::fence_after_sync();
           const uint64_t c2 = tc::pk2(c_r[mt], c_r[mt]);
-          const int t0 = (st_lo + i) * (2 * kTile) + 64 * wq;
+          const int t0 = (tl_lo + 2 * i) * kTile + 64 * wq;
 #pragma unroll 1
-          for (int c = 0; c < 64; c += 32) {
+          for (int c = 0; c < (cols ? 64 : 0); c += 32) {
             float v[32];
             tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + (uint32_t)(64 * wq + c), v);
             const int tc0 = t0 + c;
@@ -329,52 +342,59 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         sm.lpart[wq][mt * 128 + lrow] = a.x + a.y;
       }
       tc::named_sync(1, kEpiThreads);
-      // ---- publish this CTA's row partials, then gather the group's
-      float2* pub = p.parts + ((size_t)(kr & 1) * gridDim.x + cta) * R;
+      // ---- publish this CTA's row partials, then gather the group's: every
+      // partial carries the round's tag, so readers poll the data itself
+      const uint64_t tg = (uint64_t)(uint32_t)((p.tag0 + (uint64_t)kr) ^ ((p.tag0 + (uint64_t)kr) >> 32)) << 32;
+      ulonglong2* parts = p.parts + (size_t)(kr & 1) * gridDim.x * R;
       if (et < R) {
         float M = -INFINITY, L = 0.0f;
 #pragma unroll
         for (int x = 0; x < 4; ++x) merge_ms(M, L, sm.mpart[x][et], sm.lpart[x][et]);
-        __stcg(pub + et, make_float2(M, L));
+        st_relaxed_v2(parts + (size_t)cta * R + et, tg | __float_as_uint(M), tg | __float_as_uint(L));
       }
       tc::named_sync(1, kEpiThreads);
-      // tag this CTA's partials as published for this launch and round (the
-      // release store is cumulative over the partials the barrier ordered
-      // before it), then thread x waits (bounded) for group member x's tag
-      {
-        const uint64_t tag = p.tag0 + (uint64_t)kr;
-        uint64_t* tags = p.tags + (size_t)(kr & 1) * kMaxCtas;
-        if (et == 0) st_release_u64(tags + cta, tag);
-        if (et < p.gs && ld_acquire_u64(tags + grp * p.gs + et) != tag) {
-          const uint64_t t_start = globaltimer_ns();
-          for (uint32_t it = 0;; ++it) {
-            if (ld_acquire_u64(tags + grp * p.gs + et) == tag) break;
-            if ((it & 15u) == 15u) {
-              if (*abort_flag) break;
-              if (globaltimer_ns() - t_start > kWaitTimeoutNs) {
-                report(p.status, KVC_ERR_TIMEOUT);
-                *abort_flag = 1;
-                break;
-              }
-            }
-          }
-        }
-      }
-      tc::named_sync(1, kEpiThreads);
-      // gather: thread (row, quarter) merges a quarter of the group's
-      // partials with all its loads in flight at once
+      // gather: thread (row, half) polls its half of the group's partials
+      // (bounded), eight members at a time with all loads in flight, and
+      // merges them in member order
       {
         const int gr = et & 255, gq = et >> 8;       // row, half of the group
         float M = -INFINITY, L = 0.0f;
         if (gr < R) {
-          const float2* gp = p.parts + ((size_t)(kr & 1) * gridDim.x + grp * p.gs) * R + gr;
+          const ulonglong2* gp = parts + (size_t)grp * p.gs * R + gr;
           const int x0 = gq * ((p.gs + 1) >> 1), x1 = min(p.gs, x0 + ((p.gs + 1) >> 1));
-          float2 q[kMaxGroup / 2];
+          uint64_t t_start = 0;
+#pragma unroll 1
+          for (int xb = x0; xb < x1; xb += 8) {
+            const int nx = min(8, x1 - xb);
+            float mv[8], lv[8];
+            uint32_t pending = 0xffu >> (8 - nx);
+            for (uint32_t it = 0; pending; ++it) {
 #pragma unroll
-          for (int y = 0; y < kMaxGroup / 2; ++y)
-            q[y] = (x0 + y < x1) ? __ldcg(gp + (size_t)(x0 + y) * R) : make_float2(-INFINITY, 0.0f);
+              for (int y = 0; y < 8; ++y) {
+                if ((pending >> y) & 1u) {
+                  const ulonglong2 w = ld_relaxed_v2(gp + (size_t)(xb + y) * R);
+                  if ((w.x & 0xffffffff00000000ull) == tg && (w.y & 0xffffffff00000000ull) == tg) {
+                    mv[y] = __uint_as_float((uint32_t)w.x);
+                    lv[y] = __uint_as_float((uint32_t)w.y);
+                    pending &= ~(1u << y);
+                  }
+                }
+              }
+              if (pending && (it & 7u) == 7u) {
+                if (*abort_flag) break;
+                const uint64_t now = globaltimer_ns();
+                if (t_start == 0) t_start = now;
+                else if (now - t_start > kWaitTimeoutNs) {
+                  report(p.status, KVC_ERR_TIMEOUT);
+                  *abort_flag = 1;
+                  break;
+                }
+              }
+            }
 #pragma unroll
-          for (int y = 0; y < kMaxGroup / 2; ++y) merge_ms(M, L, q[y].x, q[y].y);
+            for (int y = 0; y < 8; ++y)
+              if (y < nx && !((pending >> y) & 1u)) merge_ms(M, L, mv[y], lv[y]);
+          }
           sm.mpart[gq][gr] = M;
           sm.lpart[gq][gr] = L;
         }
@@ -391,12 +411,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                  sm.nlse[2 * et + 1]);
       tc::named_sync(1, kEpiThreads);
       // ---- pass 2: this thread's token and quarter of the R columns
-      for (int i = 0; i < 2 * ns; ++i, ++item) {
+      for (int i = 0; i < ntl; ++i, ++item) {
         const int b = item & 1;
         mbar_wait(&sm.tmem_full[b], (item >> 1) & 1, p.status, abort_flag);
         tc::fence_after_sync();
         const int tl = 32 * q4 + lane;
-        const int tok = (2 * st_lo + i) * kTile + tl;
+        const int tok = (tl_lo + i) * kTile + tl;
         // causal: window row w sees token tok iff w >= tok - (T - W)
         const int wmin = p.causal ? tok - (T - W) : 0;
         uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
@@ -473,7 +493,7 @@ size_t smem_bytes(int R) {
   return sizeof(SmemSmall) + 1024 /*alignment slack*/ + 2ull * R * 128 + (size_t)kStages * kStageBytes;
 }
 
-size_t parts_bytes(int R) { return 2ull * kMaxCtas * R * sizeof(float2); }
+size_t parts_bytes(int R) { return 2ull * kMaxCtas * R * sizeof(ulonglong2); }
 
 // Launch tags: a process-wide counter seeded from the clock, in steps of
 // 2^16 (a launch uses tag_base + round, rounds < 2^16).
@@ -493,7 +513,7 @@ bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d) {
 
 size_t score_attn_tc_ws(int Hq, int Hkv, int W) {
   const int R = (Hq / Hkv) * W;
-  return parts_bytes(R) + 2ull * kMaxCtas * sizeof(uint64_t);
+  return parts_bytes(R);
 }
 
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
@@ -526,7 +546,7 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   Params p;
   p.T = T; p.W = W; p.R = R; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.scale = scale;
   p.head_scale = head_scale; p.causal = causal; p.scores = scores;
-  p.n_super = (T + 2 * kTile - 1) / (2 * kTile); p.status = dev.status;
+  p.n_tiles = (T + kTile - 1) / kTile; p.status = dev.status;
   p.heads = U * Hkv;
   const size_t smem = smem_bytes(R);
   if ((int)smem > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
@@ -554,20 +574,19 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   if (p.heads <= P) {
     gs = P / p.heads;
   } else {
-    gs = (p.n_super + kSupersPerCta - 1) / kSupersPerCta;
+    gs = (p.n_tiles + 2 * kSupersPerCta - 1) / (2 * kSupersPerCta);
     if (gs > P) gs = P;
   }
-  if (gs > p.n_super) gs = p.n_super;
+  if (gs > p.n_tiles) gs = p.n_tiles;
   if (gs > kMaxGroup) gs = kMaxGroup;
   if (gs < 1) gs = 1;
   p.gs = gs;
   p.hpr = P / gs;
   if (p.hpr > p.heads) p.hpr = p.heads;
   p.rounds = (p.heads + p.hpr - 1) / p.hpr;
-  p.parts = static_cast<float2*>(ws);
-  p.tags = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + parts_bytes(R));
+  p.parts = static_cast<ulonglong2*>(ws);
   // tags are unique per launch (and per round inside it), so the workspace
-  // needs no clearing: stale tags of earlier launches never match
+  // needs no clearing: stale partials of earlier launches never match
   p.tag0 = next_tag_base();
   const int grid = p.hpr * gs;
   cudaLaunchConfig_t cfg = {};
@@ -580,6 +599,7 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (int rc2 = prefer_max_shared(score_tc_kernel, dev.device)) return rc2;
   KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, score_tc_kernel, tm_q, tm_k, p));
   return launch_status();
 }

@@ -630,6 +630,8 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     }
     attr_done[dev.device & 63] = true;
   }
+  if (int rc = prefer_max_shared(select_kernel<1>, dev.device)) return rc;
+  if (int rc = prefer_max_shared(select_kernel<4>, dev.device)) return rc;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   // a cluster must fit one GPC: shrink it (while the keys still fit) until
@@ -662,7 +664,10 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   }
   if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
   else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
-  if (nseg > 1) offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
+  if (nseg > 1) {
+    if (int rc = prefer_max_shared(offsets_kernel, dev.device)) return rc;
+    offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
+  }
   return launch_status();
 }
 

@@ -123,10 +123,10 @@ def test_workspace_queries_are_pure_host(lib):
     n = lib.kvc_decode_workspace(64, 32, 8, 128, 10086, 1)
     chunks = (10086 + 511) // 512
     assert n == 64 * 8 * chunks * 4 * (128 + 2) * 4
-    # tensor-core scoring path: per-CTA row partials (2 buffers x 1024 CTAs x G*W rows of
-    # (max, sum)) + 2 x 1024 publication tags, independent of U and T; the SIMT path
-    # keeps one lse per window row
-    tc = 2 * 1024 * 256 * 8 + 2 * 1024 * 8
+    # tensor-core scoring path: per-CTA row partials (2 buffers x 1024 CTAs x G*W rows,
+    # each (max, sum) as two tagged 64-bit words), independent of U and T; the SIMT
+    # path keeps one lse per window row
+    tc = 2 * 1024 * 256 * 16
     assert lib.kvc_score_attn_workspace(1, 32, 8, 32768, 64, 128, 1) == tc
     assert lib.kvc_score_attn_workspace(128, 32, 8, 16384, 64, 128, 1) == tc
     assert lib.kvc_score_attn_workspace(1, 8, 4, 1024, 32, 64, 0) == 8 * 32 * 4
