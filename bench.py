@@ -168,6 +168,12 @@ def flush_l2(buf):
 
 
 def bench_layer(B, w, steps, warmup, device):
+    """`warmup` untimed steps, then `steps` timed steps: each one score ->
+    select -> compact with CUDA events around the three launches only (the
+    L2 flush before it stays outside).  Nothing is recorded between the
+    kernels, so each may start while its predecessor drains (programmatic
+    dependent launch).  A second run of the same steps with events between
+    the kernels gives the per-stage split (it serialises the stages)."""
     L = LayerWorkload(B, w, device)
     flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
     s = torch.cuda.current_stream()
@@ -175,6 +181,13 @@ def bench_layer(B, w, steps, warmup, device):
         flush_l2(flush)
         L.score(); L.select(); L.compact()
     torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush)
+        ev[i][0].record(s); L.score(); L.select(); L.compact(); ev[i][1].record(s)
+    torch.cuda.synchronize()
+    t_step = [e[0].elapsed_time(e[1]) for e in ev]
+    # per-stage split (outside the timed steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for i in range(steps):
         flush_l2(flush)
@@ -185,7 +198,6 @@ def bench_layer(B, w, steps, warmup, device):
     t_score = [e[0].elapsed_time(e[1]) for e in ev]
     t_sel = [e[1].elapsed_time(e[2]) for e in ev]
     t_comp = [e[2].elapsed_time(e[3]) for e in ev]
-    t_step = [e[0].elapsed_time(e[3]) for e in ev]
     kept_rows = int(L.offs[-1].item())
     return L, dict(score_ms=t_score, select_ms=t_sel, compact_ms=t_comp, step_ms=t_step,
                    kept_rows=kept_rows)
@@ -602,6 +614,7 @@ def main():
                    "T": w.T, "W": w.W, "keep_ratio": w.keep_ratio, "n_sink": w.n_sink,
                    "n_recent": w.n_recent, "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
+        # stage times from a separate run with events between the kernels
         "stages_us": {"score": score_ms * 1e3,
                       "select": statistics.mean(r["select_ms"]) * 1e3,
                       "compact": statistics.mean(r["compact_ms"]) * 1e3,

@@ -46,6 +46,8 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int vpr
                int* status) {
   extern __shared__ int64_t offs_sm[];      // offsets cached when they fit
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const bool cached = n_heads < kMaxCachedHeads;
   if (cached) {
     for (int i = threadIdx.x; i <= n_heads; i += kThreads) offs_sm[i] = offsets[i];
@@ -139,11 +141,10 @@ int compact_launch(const void* k, const void* v, int row_bytes, int U, int Hkv, 
     per_sm_memo[dev.device & 63].store(per_sm);
   }
   const int blocks = dev.sms * per_sm;
-  compact_kernel<<<blocks, kThreads, smem, s>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), shift, T, U * Hkv, kept_idx,
-      counts, offsets, slack, static_cast<uint4*>(kc), static_cast<uint4*>(vc), capacity_rows,
-      start, len, dev.status);
-  return launch_status();
+  return launch_pdl(compact_kernel, dim3((unsigned)blocks), dim3(kThreads), smem, s,
+                    static_cast<const uint4*>(k), static_cast<const uint4*>(v), shift, T,
+                    U * Hkv, kept_idx, counts, offsets, slack, static_cast<uint4*>(kc),
+                    static_cast<uint4*>(vc), capacity_rows, start, len, dev.status);
 }
 
 }  // namespace kvc

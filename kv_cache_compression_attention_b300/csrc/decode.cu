@@ -147,6 +147,8 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
   __shared__ float p_sm[kWarps][RPW][G];
   __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
   __shared__ float acc_sm[kWarps][G][D];
+  pdl_wait();
+  pdl_trigger();
 
   const int i = blockIdx.y, c = blockIdx.x;
   const int L = len[i];
@@ -315,6 +317,8 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
                       int Hkv, int max_chunks, float scale_log2, const float* __restrict__ ws,
                       Tin* __restrict__ out, float* __restrict__ lse, int* status) {
   __shared__ float red[D / 32][G];
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int u = i / Hkv, g = i - u * Hkv;
   const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
@@ -508,6 +512,8 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   extern __shared__ __align__(128) uint16_t smem_m[];
   __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
   __shared__ float acc_sm[kWarps][G][D];
+  pdl_wait();
+  pdl_trigger();
 
   const int i = blockIdx.y, c = blockIdx.x;
   const int L = len[i];
@@ -670,9 +676,11 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
         attr_done.fetch_or(bit);
       }
       if (int rc = prefer_max_shared(kern, dev.device)) return rc;
-      kern<<<grid, kWarps * 32, smem, s>>>(
-          static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kc),
-          static_cast<const uint16_t*>(vc), start, len, Hkv, max_chunks, sl2, ws);
+      if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
+                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kc),
+                              static_cast<const uint16_t*>(vc), start, (const int32_t*)len, Hkv,
+                              max_chunks, sl2, ws))
+        return rc;
     } else {
       const size_t smem = partial_smem_bytes<Tin, D>();
       auto kern = decode_partial_kernel<Tin, D, G>;
@@ -681,17 +689,19 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
         attr_done.fetch_or(bit);
       }
       if (int rc = prefer_max_shared(kern, dev.device)) return rc;
-      kern<<<grid, (kWarps + 1) * 32, smem, s>>>(
-          static_cast<const Tin*>(q), static_cast<const Tin*>(kc), static_cast<const Tin*>(vc),
-          start, len, Hkv, max_chunks, sl2, ws, dev.status);
+      if (int rc = launch_pdl(kern, grid, dim3((kWarps + 1) * 32), smem, s,
+                              static_cast<const Tin*>(q), static_cast<const Tin*>(kc),
+                              static_cast<const Tin*>(vc), start, (const int32_t*)len, Hkv,
+                              max_chunks, sl2, ws, dev.status))
+        return rc;
     }
   }
   if (int rc = prefer_max_shared(decode_combine_kernel<Tin, D, G>, dev.device)) return rc;
-  decode_combine_kernel<Tin, D, G><<<n, D, 0, s>>>(
-      static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc), start, len,
-      static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new), n, Hkv, max_chunks, sl2,
-      ws, static_cast<Tin*>(out), lse, dev.status);
-  return launch_status();
+  return launch_pdl(decode_combine_kernel<Tin, D, G>, dim3((unsigned)n), dim3(D), 0, s,
+                    static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc),
+                    start, len, static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new),
+                    n, Hkv, max_chunks, sl2, (const float*)ws, static_cast<Tin*>(out), lse,
+                    dev.status);
 }
 
 template <typename Tin, int D>

@@ -39,6 +39,33 @@ inline int launch_status() {
 
 inline size_t elt_size(int dtype) { return dtype == KVC_F32 ? 4 : 2; }
 
+// Launch attribute for programmatic dependent launch: the kernel may start
+// while the previous kernel of the stream still runs (its prologue overlaps
+// that kernel's tail); every such kernel calls pdl_wait() before it touches
+// memory the previous kernel reads or writes.
+inline cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+// Launches `kernel` with programmatic dependent launch enabled.
+template <typename... P, typename... A>
+inline int launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...));
+  return KVC_OK;
+}
+
 // Asks for the largest shared-memory carve-out for a kernel, once per
 // device, so that back-to-back launches of the library's shared-memory
 // kernels (score -> select, decode partial -> combine) need no
@@ -108,6 +135,13 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 __device__ __forceinline__ void report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
+
+// Programmatic dependent launch, device side: pdl_wait() returns once the
+// previous kernel of the stream has completed and its memory is visible (at
+// once when the kernel was launched without the attribute); pdl_trigger()
+// lets the next kernel's CTAs be scheduled before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

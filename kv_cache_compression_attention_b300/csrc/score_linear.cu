@@ -56,6 +56,8 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
   constexpr int E = Vec<Tin>::E;          // hidden elements per 16-byte chunk
   constexpr int F4 = E * HK / 4;          // float4 words of weight per chunk
   extern __shared__ __align__(128) uint8_t smem_lin[];
+  pdl_wait();
+  pdl_trigger();
   const int NC = Dh / E;
   const int NIT = (NC + 31) / 32;         // 512-byte column blocks per row
   float4* wsm = reinterpret_cast<float4*>(smem_lin);                    // [F4][NC]
@@ -202,10 +204,9 @@ int run(const void* hidden, const void* weight, const float* bias, int U, int T,
   const int64_t need = (tasks + kWarps - 1) / kWarps;
   if (blocks > need) blocks = need;
   if (int rc = prefer_max_shared(kern, dev.device)) return rc;
-  kern<<<(unsigned)blocks, kWarps * 32, smem, s>>>(static_cast<const Tin*>(hidden),
-                                                   static_cast<const Tin*>(weight), bias, rows,
-                                                   T, Dh, scores);
-  return launch_status();
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kWarps * 32), smem, s,
+                    static_cast<const Tin*>(hidden), static_cast<const Tin*>(weight), bias, rows,
+                    T, Dh, scores);
 }
 
 template <typename Tin>

@@ -410,6 +410,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         sm.cl4[et] = make_float4(sm.coef[2 * et], sm.coef[2 * et + 1], sm.nlse[2 * et],
                                  sm.nlse[2 * et + 1]);
       tc::named_sync(1, kEpiThreads);
+      // the next kernel of the stream may be scheduled once every CTA is here
+      if (et == 0 && kr == 0) pdl_trigger();
       // ---- pass 2: this thread's token and quarter of the R columns
       for (int i = 0; i < ntl; ++i, ++item) {
         const int b = item & 1;

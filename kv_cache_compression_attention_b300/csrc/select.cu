@@ -228,9 +228,12 @@ select_kernel(Args a) {
     mbar_init(&sh.bar, 1);
     fence_barrier_init();
   }
+  pdl_trigger();
   __syncthreads();
   // the totals are zero: peers may add into them once this barrier completes
   cluster_arrive_release();
+  // the scores (and every output) belong to the previous kernel until here
+  pdl_wait();
 
   int64_t need = 0;
   if (a.mode == KVC_SEL_GLOBAL_TOPK) {
@@ -548,6 +551,7 @@ __global__ void __launch_bounds__(1024)
 offsets_kernel(const int32_t* __restrict__ counts, int n, int64_t* __restrict__ offsets) {
   __shared__ int64_t warp_sum[32];
   __shared__ int64_t carry_s;
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
@@ -633,7 +637,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   if (int rc = prefer_max_shared(select_kernel<1>, dev.device)) return rc;
   if (int rc = prefer_max_shared(select_kernel<4>, dev.device)) return rc;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   // a cluster must fit one GPC: shrink it (while the keys still fit) until
   // the occupancy query says at least one cluster can be resident (the
   // answer is remembered per device, cluster size and shared memory)
@@ -648,7 +652,7 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;                 // the occupancy query sees the cluster shape only
     int active = 0;
     const auto key = std::make_tuple(dev.device, C, smem);
     auto it = active_memo.find(key);
@@ -662,11 +666,14 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     if (C == 1 || smem_for(C / 2) > smem_max) return KVC_ERR_UNSUPPORTED;
     C /= 2;
   }
+  attr[1] = pdl_attr();
+  cfg.numAttrs = 2;
   if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
   else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
   if (nseg > 1) {
     if (int rc = prefer_max_shared(offsets_kernel, dev.device)) return rc;
-    offsets_kernel<<<1, 1024, 0, s>>>(counts, U * Hkv, offsets);
+    return launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)counts,
+                      U * Hkv, offsets);
   }
   return launch_status();
 }
