@@ -17,15 +17,14 @@
 //    thread and step when the range allows (1 otherwise).
 //  * Radix select, 4 passes of 8-bit digits from the most significant one.
 //    Every warp histograms into a private shared-memory histogram (one
-//    atomic per warp when its candidates share a digit, else one per
-//    candidate).  The first pass is counted while the keys are made;
-//    the second sweeps the keys once more and appends the candidates that
-//    match the first digit to the warp's own list; the third and fourth
-//    sweep only that list, compacting it in place.  After each pass every
-//    CTA adds its histogram into the bins' owners (bin b lives in CTA
-//    b * C / 256) with distributed-shared-memory atomics, and after one
-//    cluster barrier every CTA reads the 256 totals and picks the same
-//    digit.  When the chosen bin is kept whole, selection stops early:
+//    shared atomic per candidate).  The first pass is counted while the
+//    keys are made; the second sweeps the keys once more and appends the
+//    candidates that match the first digit to the warp's own list; the
+//    third and fourth sweep only that list, compacting it in place.  After
+//    each pass every CTA adds its histogram into the bins' owners (bin b
+//    lives in CTA b * C / 256) with distributed-shared-memory atomics, and
+//    after one cluster barrier every CTA reads the 256 totals and picks the
+//    same digit.  When the chosen bin is kept whole, selection stops early:
 //    every key at or above the bin's smallest prefix is kept.
 //  * Ties (key == thr) are only ranked when not all of them are kept: a
 //    cluster prefix of per-CTA tie counts, then a block scan over tokens of
@@ -106,21 +105,13 @@ struct Layout {
   __host__ __device__ size_t keys_words() const { return ((size_t)nloc + 3) & ~size_t(3); }
 };
 
-// Adds the warp's candidates' digits into its private histogram: one
-// atomic for the warp when all its candidates share a digit, else one per
-// candidate (lanes with equal digits serialise on one address, which costs
-// less than grouping them first).  Returns the ballot of candidates.
-__device__ __forceinline__ uint32_t hist_add(uint32_t* wh, bool cand, uint32_t digit, int lane) {
+// Adds a candidate's digit into the warp's private histogram (lanes with
+// equal digits serialise on one address, which costs less than grouping
+// them first, or than testing whether the warp's digits agree); returns the
+// ballot of candidates.
+__device__ __forceinline__ uint32_t hist_add(uint32_t* wh, bool cand, uint32_t digit) {
   const uint32_t cm = __ballot_sync(0xffffffffu, cand);
-  if (cm) {
-    const int first = __ffs(cm) - 1;
-    const uint32_t d0 = __shfl_sync(0xffffffffu, digit, first);
-    if (__all_sync(0xffffffffu, !cand || digit == d0)) {
-      if (lane == first) atomicAdd(&wh[d0], (uint32_t)__popc(cm));
-    } else if (cand) {
-      atomicAdd(&wh[digit], 1u);
-    }
-  }
+  if (cand) atomicAdd(&wh[digit], 1u);
   return cm;
 }
 
@@ -271,7 +262,7 @@ select_kernel(Args a) {
       if (ok) x.store(keys + (size_t)q * V);
       if (radix) {
 #pragma unroll
-        for (int i = 0; i < V; ++i) hist_add(wh, ok, x.k[i] >> 24, lane);
+        for (int i = 0; i < V; ++i) hist_add(wh, ok, x.k[i] >> 24);
       }
     }
   } else {
@@ -283,7 +274,7 @@ select_kernel(Args a) {
         const bool ok = j < nt;
         const uint32_t key = ok ? score_key(__ldg(row + j)) : 0u;
         if (ok) kr[j] = key;
-        if (radix) hist_add(wh, ok, key >> 24, lane);
+        if (radix) hist_add(wh, ok, key >> 24);
       }
     }
   }
@@ -336,7 +327,7 @@ select_kernel(Args a) {
 #pragma unroll
           for (int i = 0; i < V; ++i) {
             const bool cand = x.k[i] != 0u && (x.k[i] & pmask) == prefix;
-            const uint32_t cm = hist_add(wh, cand, (x.k[i] >> shift) & 255u, lane);
+            const uint32_t cm = hist_add(wh, cand, (x.k[i] >> shift) & 255u);
             if (cand) wl[nl + __popc(cm & lt_mask)] = x.k[i];
             nl += __popc(cm);
           }
@@ -350,7 +341,7 @@ select_kernel(Args a) {
           const int e = e0 + lane;
           const uint32_t key = (e < nl) ? wl[e] : 0u;
           const bool cand = key != 0u && (key & pmask) == prefix;
-          const uint32_t cm = hist_add(wh, cand, (key >> shift) & 255u, lane);
+          const uint32_t cm = hist_add(wh, cand, (key >> shift) & 255u);
           if (cand) wl[nn + __popc(cm & lt_mask)] = key;
           nn += __popc(cm);
         }
@@ -477,9 +468,10 @@ select_kernel(Args a) {
     return key == 0u || (thr_mode ? key >= thr
                                   : (key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut)));
   };
+#pragma unroll 2
   for (int hh = 0; hh < hps; ++hh) {
-    const uint32_t* kr = keys + hh * nt;
-    uint32_t* sg = region + (size_t)(hh * kWarps + warp) * per_w;
+    const uint32_t* __restrict__ kr = keys + hh * nt;                       // keys and staging
+    uint32_t* __restrict__ sg = region + (size_t)(hh * kWarps + warp) * per_w;   // never overlap
     uint32_t n = 0;
     for (int j0 = j_lo; j0 < j_hi; j0 += 64) {
       const int ja = j0 + lane, jb = ja + 32;
