@@ -81,6 +81,19 @@ def test_select_all_equal_scores_ties_by_token_then_head(B):
     check_same(got, O.select(s.numpy(), "global", keep_ratio=0.3, n_sink=1, n_recent=1))
 
 
+def test_select_largest_pools(B):
+    """A pool is one cluster's shared memory: 8 heads x 40 960 tokens (327 680
+    keys) is selected exactly; 8 x 65 536 (524 288 keys) is refused before
+    any kernel runs, and the context stays usable."""
+    s = inputs.random_scores((1, 8, 40960), seed=77)
+    got = gpu_select(B, s.cuda(), "global", keep_ratio=0.1, n_sink=4, n_recent=64)
+    check_same(got, O.select(s.numpy(), "global", keep_ratio=0.1, n_sink=4, n_recent=64))
+    with pytest.raises(B.KvcError) as e:
+        gpu_select(B, torch.zeros((1, 8, 65536), device="cuda"), "global", keep_ratio=0.1)
+    assert e.value.status == -2
+    assert B.kvc_device_status() == 0
+
+
 def test_select_llama32k_full(B):
     w = inputs.WORKLOADS["c2_llama32k"]
     q = inputs.window_queries(w, "cuda")
