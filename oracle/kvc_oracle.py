@@ -54,18 +54,25 @@ F64 = np.float64
 
 
 # ---------------------------------------------------------------- scoring
-def score_attn(q_win, k, scale, head_scale=None, causal=True):
-    """Attention-mass score of every cached token, per (unit, kv head).
+def score_attn(q_win, k, scale, head_scale=None, causal=True, aggregation="sum"):
+    """Attention-based score of every cached token, per (unit, kv head).
 
     q_win [U, Hq, W, d], k [U, Hkv, T, d] (any float dtype; computed in
     float64).  For query head h of kv head g = h // G and window row w:
         s[(h,w), t] = scale * f[u,h] * <q[u,h,w], k[u,g,t]>,  t <= T-W+w if causal
         p[(h,w), :] = softmax_t(s[(h,w), :])
+    aggregation "sum" (attention mass):
         score[u,g,t] = sum_{h in g} sum_w p[(h,w), t]
+    aggregation "max" (the largest attention weight the token receives from
+    any window row of the group, the KVzip score of [KVzap] §2.1 without its
+    KVzip+ normalisation):
+        score[u,g,t] = max_{h in g, w} p[(h,w), t]
     The log-sum-exp lse = m + log(sum exp(s - m)) is the row normaliser
     ([Sculpt] §2B); [VECTOR] "Énoncé du Problème" and [Sculpt] §1 rank tokens
     by the attention they receive.  Returns float64 [U, Hkv, T].
     """
+    if aggregation not in ("sum", "max"):
+        raise ValueError(aggregation)
     q = np.asarray(q_win, dtype=F64)
     kk = np.asarray(k, dtype=F64)
     U, Hq, W, d = q.shape
@@ -84,7 +91,11 @@ def score_attn(q_win, k, scale, head_scale=None, causal=True):
                         logits[w, T - W + w + 1:] = -np.inf
                 m = logits.max(axis=1, keepdims=True)
                 lse = m + np.log(np.exp(logits - m).sum(axis=1, keepdims=True))
-                out[u, g] += np.exp(logits - lse).sum(axis=0)
+                p = np.exp(logits - lse)
+                if aggregation == "sum":
+                    out[u, g] += p.sum(axis=0)
+                else:
+                    out[u, g] = np.maximum(out[u, g], p.max(axis=0))
     return out
 
 

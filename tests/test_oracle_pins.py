@@ -22,8 +22,9 @@ GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_
 
 
 # ----------------------------------------------------------- brute force
-def brute_score_attn(q, k, scale, head_scale=None, causal=True):
-    """Pure-Python attention mass: token-major loop, explicit normaliser."""
+def brute_score_attn(q, k, scale, head_scale=None, causal=True, aggregation="sum"):
+    """Pure-Python attention mass (or maximum attention weight): token-major
+    loop, explicit normaliser."""
     U, Hq, W, d = q.shape
     Hkv, T = k.shape[1], k.shape[2]
     G = Hq // Hkv
@@ -43,7 +44,11 @@ def brute_score_attn(q, k, scale, head_scale=None, causal=True):
                 mx = max(logit)
                 z = sum(math.exp(v - mx) for v in logit)
                 for t in range(last + 1):
-                    out[u][g][t] += math.exp(logit[t] - mx) / z
+                    p = math.exp(logit[t] - mx) / z
+                    if aggregation == "sum":
+                        out[u][g][t] += p
+                    else:
+                        out[u][g][t] = max(out[u][g][t], p)
     return np.array(out)
 
 
@@ -151,6 +156,53 @@ def test_score_attn_dominant_sink():
     k[0, 0, 0] = 10.0                    # logit 80 against 0 for the rest
     s = O.score_attn(q, k, 1.0, None, causal=True)
     assert abs(s[0, 0, 0] - 8.0) < 1e-12 and 0 < s[0, 0, 1:].sum() < 1e-30
+
+
+# ------------------------------------------- max aggregation ([KVzap] §2.1)
+@pytest.mark.parametrize("causal", [True, False])
+def test_score_max_matches_brute_force(causal):
+    q, k = rng_arrays(11, (2, 4, 3, 5), (2, 2, 9, 5))
+    hs = np.random.default_rng(12).uniform(0.5, 2.0, (2, 4))
+    got = O.score_attn(q, k, 0.7, hs, causal, aggregation="max")
+    ref = brute_score_attn(q, k, 0.7, hs, causal, aggregation="max")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_score_max_identical_keys_closed_form():
+    """Uniform rows: token t is seen by rows w >= t - (T - W), the one with
+    the fewest visible tokens gives it 1 / (T - W + w_min + 1)."""
+    U, Hq, Hkv, W, T, d = 1, 6, 2, 5, 17, 4
+    q = rng_arrays(13, (U, Hq, W, d))[0]
+    k = np.tile(rng_arrays(14, (d,))[0], (U, Hkv, T, 1))
+    got = O.score_attn(q, k, 1.0, None, causal=True, aggregation="max")
+    ref = np.array([1.0 / (T - W + max(0, t - (T - W)) + 1) for t in range(T)])
+    for g in range(Hkv):
+        np.testing.assert_allclose(got[0, g], ref, rtol=1e-12)
+
+
+def test_score_max_bounds_and_single_row():
+    q, k = rng_arrays(15, (2, 8, 16, 16), (2, 2, 200, 16))
+    G, W = 4, 16
+    smax = O.score_attn(q, k, 0.25, None, True, aggregation="max")
+    ssum = O.score_attn(q, k, 0.25, None, True)
+    assert (smax <= ssum * (1 + 1e-12)).all() and (ssum <= G * W * smax * (1 + 1e-12)).all()
+    assert (smax <= 1.0).all() and (smax > 0).all()
+    q1, k1 = rng_arrays(16, (1, 1, 1, 8), (1, 1, 50, 8))
+    np.testing.assert_allclose(O.score_attn(q1, k1, 0.3, None, False, aggregation="max"),
+                               O.score_attn(q1, k1, 0.3, None, False), rtol=1e-14)
+
+
+def _score_max_first_head_only(q, k, scale, head_scale=None, causal=True):
+    """A planted mistake: the maximum over the first query head of each group only."""
+    G = q.shape[1] // k.shape[1]
+    return O.score_attn(q[:, ::G], k, scale, None, causal, "max")
+
+
+def test_planted_max_mistake_is_caught():
+    q, k = rng_arrays(17, (1, 4, 3, 5), (1, 2, 9, 5))
+    ref = brute_score_attn(q, k, 0.7, None, True, aggregation="max")
+    assert not np.allclose(_score_max_first_head_only(q, k, 0.7), ref, rtol=1e-6)
+    assert not np.allclose(O.score_attn(q, k, 0.7, None, True), ref, rtol=1e-6)
 
 
 def test_score_linear_matches_loops_and_torch():
