@@ -150,8 +150,9 @@ class LayerWorkload:
         self.start = torch.empty(n, dtype=torch.int64, device=device)
         self.len = torch.empty(n, dtype=torch.int32, device=device)
 
-    def score(self):
-        self.B.kvc_score_attn(self.q, self.k, self.scores, self.w.scale, workspace=self.score_ws)
+    def score(self, aggregation="sum"):
+        self.B.kvc_score_attn(self.q, self.k, self.scores, self.w.scale, workspace=self.score_ws,
+                              aggregation=aggregation)
 
     def select(self):
         w = self.w
@@ -201,6 +202,25 @@ def bench_layer(B, w, steps, warmup, device):
     kept_rows = int(L.offs[-1].item())
     return L, dict(score_ms=t_score, select_ms=t_sel, compact_ms=t_comp, step_ms=t_step,
                    kept_rows=kept_rows)
+
+
+def bench_score_max(L, steps, warmup):
+    """The scoring kernel with max aggregation over the window rows (KVzip's
+    score) on the same layer: mean CUDA-event time per launch, L2 flushed
+    before each."""
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=L.k.device)
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush_l2(flush)
+        L.score("max")
+    ts = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s); L.score("max"); e1.record(s)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts)
 
 
 def bench_e2e(B, L, steps, warmup):
@@ -609,6 +629,7 @@ def main():
 
     # ---- sub-measurements (outside the headline timed region)
     e2e_ms, h2d, d2h = bench_e2e(B, L, max(6, args.steps // 2), 2)
+    score_max_ms = bench_score_max(L, max(5, args.steps // 2), 3)
     fid = fidelity_probe(B, L)
     del L
     torch.cuda.empty_cache()
@@ -650,6 +671,10 @@ def main():
         "rooflines": [
             {"kernel": "score_tc_kernel", "workload": WORKLOAD, "bound": "hbm",
              "achieved_gbs": achieved, "frac": achieved / hbm},
+            {"kernel": "score_tc_kernel (max aggregation)", "workload": WORKLOAD, "bound": "hbm",
+             "time_us": score_max_ms * 1e3,
+             "achieved_gbs": score_bytes / (score_max_ms * 1e-3) / 1e9,
+             "frac": score_bytes / (score_max_ms * 1e-3) / 1e9 / hbm},
             {"kernel": "compact_kernel", "workload": WORKLOAD, "bound": "hbm",
              "achieved_gbs": comp_c2 / (comp_c2_us * 1e-6) / 1e9,
              "frac": comp_c2 / (comp_c2_us * 1e-6) / 1e9 / hbm},

@@ -111,6 +111,28 @@ int kvc_score_attn(const void* q_win, const void* k, int dtype,
                    float* scores, void* workspace, size_t workspace_bytes,
                    void* stream);
 
+/* Aggregation of a token's attention weights over the G*W window rows. */
+typedef enum {
+  KVC_AGG_SUM = 0,   /* attention mass (kvc_score_attn)                     */
+  KVC_AGG_MAX = 1    /* largest attention weight received from any row      */
+} kvc_aggregation;
+
+/*
+ * kvc_score_attn with the aggregation over the window rows chosen.
+ * KVC_AGG_SUM is kvc_score_attn; KVC_AGG_MAX gives
+ *   scores[u,g,t] = max over h in g, w < W of softmax_t(s[(h,w),:])[t]
+ * ([KVzap] §2.1: KVzip scores a token by the largest attention weight it
+ * receives; the KVzip+ normalisation by value and hidden-state norms needs
+ * model weights and is not applied here).  Same arguments, layouts,
+ * workspace, limits and paths as kvc_score_attn; aggregation outside the
+ * enum is KVC_ERR_INVALID.  Each max score lies in (0, 1].
+ */
+int kvc_score_attn_agg(const void* q_win, const void* k, int dtype,
+                       int U, int Hq, int Hkv, int T, int W, int d,
+                       float scale, const float* head_scale, int causal,
+                       int aggregation, float* scores,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Linear surrogate score ([KVzap] §2.2: a linear map from the hidden state
  * h_t in R^{Dh} to one score per kv head):

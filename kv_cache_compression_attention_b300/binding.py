@@ -21,6 +21,9 @@ KVC_SEL_GLOBAL_TOPK, KVC_SEL_THRESHOLD, KVC_SEL_PER_HEAD = 0, 1, 2
 MODES = {"global": KVC_SEL_GLOBAL_TOPK, "threshold": KVC_SEL_THRESHOLD,
          "per_head": KVC_SEL_PER_HEAD}
 
+KVC_AGG_SUM, KVC_AGG_MAX = 0, 1
+AGGREGATIONS = {"sum": KVC_AGG_SUM, "max": KVC_AGG_MAX}
+
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_INVALID", -2: "KVC_ERR_UNSUPPORTED",
           -3: "KVC_ERR_WORKSPACE", -4: "KVC_ERR_CUDA", -5: "KVC_ERR_TIMEOUT",
           -6: "KVC_ERR_RANGE"}
@@ -35,6 +38,8 @@ SIGNATURES = {
     "kvc_device_status": (_I, [_P]),
     "kvc_score_attn_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "kvc_score_attn": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P]),
+    "kvc_score_attn_agg": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _I, _P, _P, _SZ,
+                                _P]),
     "kvc_score_linear": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "kvc_select_workspace": (_SZ, [_I, _I, _I, _I]),
     "kvc_select": (_I, [_P, _I, _I, _I, _I, _D, _F, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -114,7 +119,9 @@ def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
 
 # ----------------------------------------------------------------- entry points
 def kvc_score_attn(q_win, k, scores, scale, head_scale=None, causal=True, workspace=None,
-                   stream=None):
+                   stream=None, aggregation="sum"):
+    """aggregation "sum" (attention mass) calls kvc_score_attn, "max" calls
+    kvc_score_attn_agg with KVC_AGG_MAX."""
     U, Hq, W, d = q_win.shape
     _, Hkv, T, _ = k.shape
     dt = _dtype(k)
@@ -122,10 +129,17 @@ def kvc_score_attn(q_win, k, scores, scale, head_scale=None, causal=True, worksp
     if workspace is None:
         workspace = _workspace(need, k.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().kvc_score_attn(_ptr(q_win), _ptr(k), dt, U, Hq, Hkv, T, W, d, float(scale),
-                              _ptr(head_scale), int(bool(causal)), _ptr(scores),
-                              _ptr(workspace), ws_bytes, _stream(stream))
-    _check("kvc_score_attn", rc)
+    if aggregation == "sum":
+        rc = lib().kvc_score_attn(_ptr(q_win), _ptr(k), dt, U, Hq, Hkv, T, W, d, float(scale),
+                                  _ptr(head_scale), int(bool(causal)), _ptr(scores),
+                                  _ptr(workspace), ws_bytes, _stream(stream))
+        _check("kvc_score_attn", rc)
+    else:
+        rc = lib().kvc_score_attn_agg(_ptr(q_win), _ptr(k), dt, U, Hq, Hkv, T, W, d,
+                                      float(scale), _ptr(head_scale), int(bool(causal)),
+                                      AGGREGATIONS[aggregation], _ptr(scores), _ptr(workspace),
+                                      ws_bytes, _stream(stream))
+        _check("kvc_score_attn_agg", rc)
     return scores
 
 

@@ -86,11 +86,13 @@ size_t kvc_score_attn_workspace(int U, int Hq, int Hkv, int T, int W, int d, int
   return kvc::score_attn_simt_ws(U, Hq, W);
 }
 
-int kvc_score_attn(const void* q_win, const void* k, int dtype, int U, int Hq, int Hkv,
-                   int T, int W, int d, float scale, const float* head_scale, int causal,
-                   float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+int kvc_score_attn_agg(const void* q_win, const void* k, int dtype, int U, int Hq, int Hkv,
+                       int T, int W, int d, float scale, const float* head_scale, int causal,
+                       int aggregation, float* scores, void* workspace, size_t workspace_bytes,
+                       void* stream) {
   if (!q_win || !k || !scores) return KVC_ERR_INVALID;
   if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (aggregation != KVC_AGG_SUM && aggregation != KVC_AGG_MAX) return KVC_ERR_INVALID;
   if (U <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || W <= 0 || Hq % Hkv) return KVC_ERR_INVALID;
   if (W > T || !(scale > 0.0f) || !isfinite(scale)) return KVC_ERR_INVALID;
   if (d != 64 && d != 128) return KVC_ERR_UNSUPPORTED;
@@ -104,11 +106,18 @@ int kvc_score_attn(const void* q_win, const void* k, int dtype, int U, int Hq, i
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
   if (tc)
-    return kvc::score_attn_tc(q_win, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores,
-                              workspace, dev, kvc::as_stream(stream));
+    return kvc::score_attn_tc(q_win, k, U, Hq, Hkv, T, W, scale, head_scale, causal, aggregation,
+                              scores, workspace, dev, kvc::as_stream(stream));
   return kvc::score_attn_simt(q_win, k, dtype, U, Hq, Hkv, T, W, d, scale, head_scale, causal,
-                              scores, static_cast<float*>(workspace), dev,
+                              aggregation, scores, static_cast<float*>(workspace), dev,
                               kvc::as_stream(stream));
+}
+
+int kvc_score_attn(const void* q_win, const void* k, int dtype, int U, int Hq, int Hkv,
+                   int T, int W, int d, float scale, const float* head_scale, int causal,
+                   float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+  return kvc_score_attn_agg(q_win, k, dtype, U, Hq, Hkv, T, W, d, scale, head_scale, causal,
+                            KVC_AGG_SUM, scores, workspace, workspace_bytes, stream);
 }
 
 int kvc_score_linear(const void* hidden, const void* weight, const float* bias, int dtype,

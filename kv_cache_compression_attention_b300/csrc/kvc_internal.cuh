@@ -86,15 +86,15 @@ inline int prefer_max_shared(K* kernel, int device) {
 
 // Launchers (one per translation unit).  Arguments are already validated.
 int score_attn_simt(const void* q, const void* k, int dtype, int U, int Hq, int Hkv, int T,
-                    int W, int d, float scale, const float* head_scale, int causal,
+                    int W, int d, float scale, const float* head_scale, int causal, int agg,
                     float* scores, float* lse_ws, const Dev& dev, cudaStream_t s);
 size_t score_attn_simt_ws(int U, int Hq, int W);
 
 bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d);
 size_t score_attn_tc_ws(int Hq, int Hkv, int W);
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
-                  float scale, const float* head_scale, int causal, float* scores, void* ws,
-                  const Dev& dev, cudaStream_t s);
+                  float scale, const float* head_scale, int causal, int agg, float* scores,
+                  void* ws, const Dev& dev, cudaStream_t s);
 
 int score_linear_launch(const void* hidden, const void* weight, const float* bias, int dtype,
                         int U, int T, int Dh, int Hkv, float* scores, const Dev& dev,

@@ -105,7 +105,7 @@ template <typename Tin, int D>
 __global__ void __launch_bounds__(kColThreads)
 col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int Hq, int Hkv,
                 int T, int W, float scale, const float* __restrict__ head_scale, int causal,
-                const float* __restrict__ lse, float* __restrict__ scores) {
+                int agg_max, const float* __restrict__ lse, float* __restrict__ scores) {
   __shared__ float4 qs[kRowChunk][D / 4];
   __shared__ float cs[kRowChunk], ls[kRowChunk];
   const int ug = blockIdx.y;                 // u*Hkv + g
@@ -144,7 +144,8 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
           acc = fmaf(qv.z, kr[4 * x4 + 2], acc);
           acc = fmaf(qv.w, kr[4 * x4 + 3], acc);
         }
-        sum += expf(cs[rr] * acc - ls[rr]);
+        const float e = expf(cs[rr] * acc - ls[rr]);
+        sum = agg_max ? fmaxf(sum, e) : sum + e;
       }
     }
   }
@@ -153,7 +154,8 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
 
 template <typename Tin, int D>
 int run(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W, float scale,
-        const float* hs, int causal, float* scores, float* lse, int* status, cudaStream_t s) {
+        const float* hs, int causal, int agg, float* scores, float* lse, int* status,
+        cudaStream_t s) {
   const int64_t rows = (int64_t)U * Hq * W;
   dim3 g1((unsigned)((rows + kRowWarps - 1) / kRowWarps));
   row_lse_kernel<Tin, D><<<g1, kRowWarps * 32, 0, s>>>(
@@ -162,7 +164,7 @@ int run(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W, floa
   dim3 g2((unsigned)((T + kColThreads - 1) / kColThreads), (unsigned)(U * Hkv));
   col_mass_kernel<Tin, D><<<g2, kColThreads, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), U, Hq, Hkv, T, W, scale, hs,
-      causal, lse, scores);
+      causal, agg == KVC_AGG_MAX ? 1 : 0, lse, scores);
   return launch_status();
 }
 
@@ -173,14 +175,14 @@ size_t score_attn_simt_ws(int U, int Hq, int W) {
 }
 
 int score_attn_simt(const void* q, const void* k, int dtype, int U, int Hq, int Hkv, int T,
-                    int W, int d, float scale, const float* head_scale, int causal,
+                    int W, int d, float scale, const float* head_scale, int causal, int agg,
                     float* scores, float* lse_ws, const Dev& dev, cudaStream_t s) {
   if (dtype == KVC_F32) {
-    return d == 64 ? run<float, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s)
-                   : run<float, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s);
+    return d == 64 ? run<float, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, agg, scores, lse_ws, dev.status, s)
+                   : run<float, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, agg, scores, lse_ws, dev.status, s);
   }
-  return d == 64 ? run<uint16_t, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s)
-                 : run<uint16_t, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, scores, lse_ws, dev.status, s);
+  return d == 64 ? run<uint16_t, 64>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, agg, scores, lse_ws, dev.status, s)
+                 : run<uint16_t, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, agg, scores, lse_ws, dev.status, s);
 }
 
 }  // namespace kvc

@@ -124,6 +124,28 @@ __device__ __forceinline__ void merge_ms(float& M, float& L, float m, float l) {
   else       { L += l * tc::ex2(m - M); }
 }
 
+// Pass-2 accumulation of the window rows' weights of a token: their sum (the
+// attention mass) or, with kMax, their maximum.  Two lanes per 64-bit word.
+template <bool kMax>
+__device__ __forceinline__ uint64_t acc2(uint64_t s, float e0, float e1) {
+  if constexpr (kMax) {
+    const float2 a = tc::upk2(s);
+    return tc::pk2(fmaxf(a.x, e0), fmaxf(a.y, e1));
+  } else {
+    return tc::fadd2(s, tc::pk2(e0, e1));
+  }
+}
+template <bool kMax>
+__device__ __forceinline__ uint64_t comb2(uint64_t a, uint64_t b) {
+  const float2 y = tc::upk2(b);
+  return acc2<kMax>(a, y.x, y.y);
+}
+template <bool kMax>
+__device__ __forceinline__ float comb(float a, float b) {
+  return kMax ? fmaxf(a, b) : a + b;
+}
+
+template <bool kMax>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 Params p) {
@@ -432,7 +454,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const float4 q = cp[j];
               const float2 x = tc::upk2(tc::ffma2(tc::pk2(v[2 * j], v[2 * j + 1]),
                                                   tc::pk2(q.x, q.y), tc::pk2(q.z, q.w)));
-              s2[j & 3] = tc::fadd2(s2[j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+              s2[j & 3] = acc2<kMax>(s2[j & 3], tc::ex2(x.x), tc::ex2(x.y));
             }
           } else {
 #pragma unroll
@@ -441,26 +463,28 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const float4 q = cp[j];
               const float e0 = (r % W >= wmin) ? tc::ex2(fmaf(v[2 * j], q.x, q.z)) : 0.0f;
               const float e1 = ((r + 1) % W >= wmin) ? tc::ex2(fmaf(v[2 * j + 1], q.y, q.w)) : 0.0f;
-              s2[j & 3] = tc::fadd2(s2[j & 3], tc::pk2(e0, e1));
+              s2[j & 3] = acc2<kMax>(s2[j & 3], e0, e1);
             }
           }
         }
         tc::fence_before_sync();
         mbar_arrive(&sm.tmem_empty[b]);
-        const float2 a = tc::upk2(tc::fadd2(tc::fadd2(s2[0], s2[1]), tc::fadd2(s2[2], s2[3])));
+        const float2 a = tc::upk2(comb2<kMax>(comb2<kMax>(s2[0], s2[1]), comb2<kMax>(s2[2], s2[3])));
+        const float part = comb<kMax>(a.x, a.y);
         // quarters 1-3 hand their sums to quarter 0 through a double-buffered
         // slot; only the two quarters involved wait, never the whole epilogue
         const int pb = p2 & 1, use = p2 >> 1;
         if (wq != 0) {
           if (use > 0) mbar_wait(&sm.psum_empty[pb], (use - 1) & 1, p.status, abort_flag);
-          sm.psum[pb][wq][tl] = a.x + a.y;
+          sm.psum[pb][wq][tl] = part;
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.psum_full[pb]);
         } else {
           mbar_wait(&sm.psum_full[pb], use & 1, p.status, abort_flag);
           const float* ps = &sm.psum[pb][0][tl];
           if (tok < T)
-            p.scores[(int64_t)head * T + tok] = (a.x + a.y + ps[kTile]) + (ps[2 * kTile] + ps[3 * kTile]);
+            p.scores[(int64_t)head * T + tok] =
+                comb<kMax>(comb<kMax>(part, ps[kTile]), comb<kMax>(ps[2 * kTile], ps[3 * kTile]));
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.psum_empty[pb]);
         }
@@ -519,8 +543,8 @@ size_t score_attn_tc_ws(int Hq, int Hkv, int W) {
 }
 
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
-                  float scale, const float* head_scale, int causal, float* scores, void* ws,
-                  const Dev& dev, cudaStream_t s) {
+                  float scale, const float* head_scale, int causal, int agg, float* scores,
+                  void* ws, const Dev& dev, cudaStream_t s) {
   int rc = get_encoder();
   if (rc) return rc;
   const int G = Hq / Hkv, R = G * W;
@@ -562,9 +586,10 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
       // the attribute is the kernel's, shared by both row counts: the larger
       const size_t smax = smem_bytes(256);
       if ((int)smax > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
-      KVC_CUDA_TRY(cudaFuncSetAttribute(score_tc_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smax));
-      KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel,
+      for (auto fn : {score_tc_kernel<false>, score_tc_kernel<true>})
+        KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smax));
+      KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel<false>,
                                                                  kThreads, smem));
       if (per_sm < 1) per_sm = -1;
     }
@@ -601,8 +626,9 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (int rc2 = prefer_max_shared(score_tc_kernel, dev.device)) return rc2;
-  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, score_tc_kernel, tm_q, tm_k, p));
+  auto kern = agg == KVC_AGG_MAX ? score_tc_kernel<true> : score_tc_kernel<false>;
+  if (int rc2 = prefer_max_shared(kern, dev.device)) return rc2;
+  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, tm_q, tm_k, p));
   return launch_status();
 }
 

@@ -83,6 +83,22 @@ def test_score_attn_rejects_bad_arguments(lib):
     assert call(d=96) == -2
 
 
+def test_score_attn_agg_rejects_bad_arguments(lib):
+    f = lib.kvc_score_attn_agg
+
+    def call(agg, **kw):
+        a = dict(q=P, k=P, dt=1, U=1, Hq=8, Hkv=4, T=64, W=8, d=128, scale=0.1, scores=P)
+        a.update(kw)
+        return f(a["q"], a["k"], a["dt"], a["U"], a["Hq"], a["Hkv"], a["T"], a["W"], a["d"],
+                 a["scale"], None, 1, agg, a["scores"], None, 0, None)
+
+    assert call(2) == -1                 # aggregation outside the enum
+    assert call(-1) == -1
+    assert call(1, q=None) == -1
+    assert call(1, W=65) == -1
+    assert call(1, d=96) == -2
+
+
 def test_select_rejects_bad_arguments(lib):
     f = lib.kvc_select
 

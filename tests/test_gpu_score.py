@@ -29,10 +29,10 @@ def B():
     return binding
 
 
-def gpu_scores(B, q, k, scale, hs=None, causal=True):
+def gpu_scores(B, q, k, scale, hs=None, causal=True, aggregation="sum"):
     U, Hkv, T = k.shape[0], k.shape[1], k.shape[2]
     out = torch.full((U, Hkv, T), float("nan"), device="cuda", dtype=torch.float32)
-    B.kvc_score_attn(q, k, out, scale, head_scale=hs, causal=causal)
+    B.kvc_score_attn(q, k, out, scale, head_scale=hs, causal=causal, aggregation=aggregation)
     torch.cuda.synchronize()
     assert B.kvc_device_status() == 0
     return out
@@ -43,14 +43,17 @@ def rand(shape, dtype, seed, scale=1.0):
     return (scale * torch.randn(shape, generator=g, device="cuda")).to(dtype)
 
 
-@pytest.mark.parametrize("dtype,d,G,W,T", [
+SHAPES = [
     (torch.float32, 64, 2, 32, 1024),     # the tiny fp32 workload's shape
     (torch.float32, 128, 4, 16, 777),
     (torch.bfloat16, 128, 4, 64, 1000),   # tcgen05, R = 256, ragged tail
     (torch.bfloat16, 128, 2, 64, 1300),   # tcgen05, R = 128
     (torch.bfloat16, 128, 4, 64, 300),    # tcgen05, fewer tiles than cluster ranks
     (torch.bfloat16, 64, 4, 16, 500),     # SIMT bf16
-])
+]
+
+
+@pytest.mark.parametrize("dtype,d,G,W,T", SHAPES)
 @pytest.mark.parametrize("causal", [True, False])
 def test_score_attn_small(B, dtype, d, G, W, T, causal):
     U, Hkv = 2, 2
@@ -64,6 +67,31 @@ def test_score_attn_small(B, dtype, d, G, W, T, causal):
     assert mass_rel_err(got, ref) <= TOL[dtype]
     # every window row is a softmax: each kv head collects G*W
     np.testing.assert_allclose(got.sum(-1), G * W, rtol=TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype,d,G,W,T", SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_score_attn_max_small(B, dtype, d, G, W, T, causal):
+    """Largest attention weight per token (KVzip's aggregation), both paths."""
+    U, Hkv = 2, 2
+    q = rand((U, Hkv * G, W, d), dtype, 11)
+    k = rand((U, Hkv, T, d), dtype, 12)
+    hs = (0.5 + 1.5 * torch.rand((U, Hkv * G), generator=torch.Generator(device="cuda").manual_seed(13),
+                                 device="cuda")).float()
+    scale = d ** -0.5
+    got = np64(gpu_scores(B, q, k, scale, hs, causal, aggregation="max"))
+    ref = O.score_attn(np64(q), np64(k), scale, np64(hs), causal, aggregation="max")
+    assert mass_rel_err(got, ref) <= TOL[dtype]
+    assert (got > 0).all() and (got <= 1 + TOL[dtype]).all()
+
+
+def test_score_attn_max_llama32k_full(B):
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    got = np64(gpu_scores(B, q, k, w.scale, aggregation="max"))
+    ref = O.score_attn(np64(q), np64(k), w.scale, aggregation="max")
+    assert mass_rel_err(got, ref) <= 2e-2
 
 
 def test_score_attn_tiny_workload(B):
