@@ -172,12 +172,13 @@ size_t kvc_select_workspace(int U, int Hkv, int T, int mode);
  * counts      [U*Hkv] int32 (written)
  * offsets     [U*Hkv + 1] int64 (written): exclusive prefix sum of counts.
  * Requires 0 <= keep_ratio <= 1 (GLOBAL_TOPK), n_sink, n_recent >= 0,
- * Hkv*T <= 2^20 per selection pool (GLOBAL_TOPK pools a unit's heads), else
- * KVC_ERR_UNSUPPORTED.  A pool is selected by one thread-block cluster of
- * up to 16 CTAs that keep its keys and candidate lists in shared memory
- * (8 bytes per key): pools beyond about 370 K keys on a B300 (e.g. 8 heads
- * x 46 K tokens under GLOBAL_TOPK; one head under PER_HEAD / THRESHOLD)
- * also return KVC_ERR_UNSUPPORTED, before any kernel runs.
+ * Hkv*T <= 2^24 per selection pool (GLOBAL_TOPK pools a unit's heads;
+ * pooling several layers of a sequence is a matter of passing them as its
+ * heads) and U*Hkv <= 2^24, else KVC_ERR_UNSUPPORTED; at most 512 heads per
+ * GLOBAL_TOPK pool.  A pool is selected by one thread-block cluster of up
+ * to 16 CTAs; pools of up to 8 heads whose keys fit the cluster's shared
+ * memory (about 370 K keys on a B300) keep them on chip, larger ones re-read
+ * the scores from global memory in each pass.
  * Selection decisions are taken on the fp32 bits of the scores, so the
  * result is exact and deterministic.
  */

@@ -149,7 +149,8 @@ int kvc_select(const float* scores, int U, int Hkv, int T, int mode, double keep
     return KVC_ERR_INVALID;
   if (mode == KVC_SEL_PER_HEAD && !head_budget) return KVC_ERR_INVALID;
   int64_t pool = (mode == KVC_SEL_GLOBAL_TOPK) ? (int64_t)Hkv * T : (int64_t)T;
-  if (pool > (1ll << 20) || (int64_t)U * Hkv > (1ll << 24)) return KVC_ERR_UNSUPPORTED;
+  if (pool > (1ll << 24) || (int64_t)U * Hkv > (1ll << 24)) return KVC_ERR_UNSUPPORTED;
+  if (mode == KVC_SEL_GLOBAL_TOPK && Hkv > 512) return KVC_ERR_UNSUPPORTED;   // heads per pool
   // protected set size |P| (the two ranges may overlap when T is small)
   int64_t ns = n_sink < T ? n_sink : T;
   int64_t rs = T - (int64_t)n_recent;           // first recent token

@@ -105,6 +105,12 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
                   int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
                   cudaStream_t s);
 
+int select_stream_launch(const float* scores, int U, int Hkv, int T, int mode,
+                         int64_t need_global, float tau, const int32_t* head_budget, int n_sink,
+                         int n_recent, int nP, int32_t* kept_idx, int32_t* counts,
+                         int64_t* offsets, bool offsets_in_kernel, const Dev& dev,
+                         cudaStream_t s);
+
 int compact_launch(const void* k, const void* v, int row_bytes, int U, int Hkv, int T,
                    const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
                    int slack, void* kc, void* vc, int64_t capacity_rows, int64_t* start,

@@ -590,9 +590,30 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
                   int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
                   cudaStream_t s) {
   const int hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1;
-  if (hps > kMaxHps) return KVC_ERR_UNSUPPORTED;
   const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
   const int64_t pool = (int64_t)hps * T;
+  int nP = 0;
+  {
+    int rs = T - n_recent;
+    nP = n_sink + (T - rs) - (rs < n_sink ? n_sink - rs : 0);
+  }
+  // pools with more heads than the registers hold, or whose keys and lists
+  // do not fit a cluster's shared memory, take the streaming kernel
+  // several pools: one more single-block kernel scans the counts into offsets
+  auto launch_offsets = [&]() -> int {
+    if (nseg == 1) return KVC_OK;
+    if (int rc = prefer_max_shared(offsets_kernel, dev.device)) return rc;
+    return launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)counts,
+                      U * Hkv, offsets);
+  };
+  auto stream = [&]() -> int {
+    if (int rc = select_stream_launch(scores, U, Hkv, T, mode, need_global, tau, head_budget,
+                                      n_sink, n_recent, nP, kept_idx, counts, offsets,
+                                      nseg == 1, dev, s))
+      return rc;
+    return launch_offsets();
+  };
+  if (hps > kMaxHps) return stream();
   const size_t smem_max = (size_t)dev.max_smem_optin;
   const bool aligned = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
   // four keys per thread and step when every CTA's range is a multiple of 4
@@ -602,15 +623,11 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   int C = 1;
   while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
   while (C < 16 && smem_for(C) > smem_max) C *= 2;
-  if (smem_for(C) > smem_max) return KVC_ERR_UNSUPPORTED;
+  if (smem_for(C) > smem_max) return stream();
   Args a;
   a.scores = scores; a.T = T; a.hps = hps; a.mode = mode; a.need_global = need_global;
   a.tau = tau; a.head_budget = head_budget; a.n_sink = n_sink; a.n_recent = n_recent;
-  a.nP = 0;
-  {
-    int rs = T - n_recent;
-    a.nP = n_sink + (T - rs) - (rs < n_sink ? n_sink - rs : 0);
-  }
+  a.nP = nP;
   a.kept = kept_idx; a.counts = counts;
   a.offsets = (nseg == 1) ? offsets : nullptr;
   a.status = dev.status;
@@ -655,18 +672,14 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
       active_memo[key] = active;
     }
     if (active > 0) break;
-    if (C == 1 || smem_for(C / 2) > smem_max) return KVC_ERR_UNSUPPORTED;
+    if (C == 1 || smem_for(C / 2) > smem_max) return stream();
     C /= 2;
   }
   attr[1] = pdl_attr();
   cfg.numAttrs = 2;
   if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
   else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
-  if (nseg > 1) {
-    if (int rc = prefer_max_shared(offsets_kernel, dev.device)) return rc;
-    return launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)counts,
-                      U * Hkv, offsets);
-  }
+  if (int rc = launch_offsets()) return rc;
   return launch_status();
 }
 

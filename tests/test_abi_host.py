@@ -112,7 +112,9 @@ def test_select_rejects_bad_arguments(lib):
     assert call(ratio=float("nan")) == -1
     assert call(ns=-1) == -1
     assert call(mode=2, hb=None) == -1
-    assert call(T=1 << 21, mode=1) == -2   # pool larger than supported
+    assert call(T=(1 << 24) + 1, mode=1) == -2    # pool larger than supported
+    assert call(Hkv=1025, T=1 << 14) == -2         # more than 2^24 keys pooled across heads
+    assert call(Hkv=600, T=16) == -2               # more than 512 heads in one pool
 
 
 def test_compact_and_decode_reject_bad_arguments(lib):

@@ -81,17 +81,45 @@ def test_select_all_equal_scores_ties_by_token_then_head(B):
     check_same(got, O.select(s.numpy(), "global", keep_ratio=0.3, n_sink=1, n_recent=1))
 
 
-def test_select_largest_pools(B):
-    """A pool is one cluster's shared memory: 8 heads x 40 960 tokens (327 680
-    keys) is selected exactly; 8 x 65 536 (524 288 keys) is refused before
-    any kernel runs, and the context stays usable."""
-    s = inputs.random_scores((1, 8, 40960), seed=77)
-    got = gpu_select(B, s.cuda(), "global", keep_ratio=0.1, n_sink=4, n_recent=64)
-    check_same(got, O.select(s.numpy(), "global", keep_ratio=0.1, n_sink=4, n_recent=64))
-    with pytest.raises(B.KvcError) as e:
-        gpu_select(B, torch.zeros((1, 8, 65536), device="cuda"), "global", keep_ratio=0.1)
-    assert e.value.status == -2
-    assert B.kvc_device_status() == 0
+@pytest.mark.parametrize("shape,mode", [
+    ((1, 8, 40960), "global"),      # the largest shared-memory pools
+    ((1, 8, 65536), "global"),      # 524 288 keys: the streaming kernel
+    ((2, 32, 3000), "global"),      # more heads per pool than the registers hold
+    ((1, 2, 400000), "per_head"),   # one head of 400 000 tokens
+    ((1, 2, 400000), "threshold"),
+])
+def test_select_large_pools(B, shape, mode):
+    """Pools whose keys do not fit one cluster's shared memory, or with more
+    than 8 heads, take the streaming kernel: same result, bit for bit."""
+    s = inputs.random_scores(shape, seed=sum(shape), ties=True, specials=True)
+    sc = s.numpy()
+    kw = dict(n_sink=4, n_recent=64)
+    if mode == "global":
+        kw["keep_ratio"] = 0.1
+    elif mode == "per_head":
+        kw["head_budget"] = np.array([1000, 250000] * shape[0])
+    else:
+        kw["tau"] = 1.0
+    got = gpu_select(B, s.cuda(), mode, **kw)
+    check_same(got, O.select(sc, mode, **kw))
+
+
+def test_select_cross_layer_pool(B):
+    """One global budget over every layer and kv head of a sequence (32
+    layers x 8 kv heads = 256 heads of 16 384 tokens, 4.2 M keys per pool,
+    after KVSculpt's layer-and-head allocation), two sequences; the oracle
+    checks one, the other is checked for the invariants."""
+    U, H, T = 2, 256, 16384
+    s = inputs.random_scores((U, H, T), seed=2026)
+    got = gpu_select(B, s.cuda(), "global", keep_ratio=0.2, n_sink=4, n_recent=64)
+    ref = O.select(s[:1].numpy(), "global", keep_ratio=0.2, n_sink=4, n_recent=64)
+    kept, counts, offs = got
+    check_same((kept[:H], counts[:H], offs[:H + 1]), ref)
+    assert offs[-1] == U * math.floor(0.2 * H * T)
+    assert len(set(counts[:H].tolist())) > 1          # heads keep different counts
+    for i in range(H, 2 * H, 37):
+        k = kept[i, : counts[i]]
+        assert (np.diff(k) > 0).all() and k[:4].tolist() == [0, 1, 2, 3]
 
 
 def test_select_llama32k_full(B):
