@@ -372,7 +372,11 @@ def bench_c4(B, steps, warmup, device):
                score_linear_gbs=score_bytes / (t_score * 1e-6) / 1e9,
                score_linear_bytes=score_bytes,
                compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
-               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
+               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6),
+               cross_layer_select_us=t_cross,
+               cross_layer_keys_per_pool=w.layers * w.Hkv * w.T,
+               cross_layer_per_layer_kept_min=int(per_layer.min()),
+               cross_layer_per_layer_kept_max=int(per_layer.max()))
     del hidden, k, v, kc, vc, kept, flush
     torch.cuda.empty_cache()
     return out
@@ -424,12 +428,35 @@ def bench_c3(B, steps, warmup, device):
     per_head = counts.view(w.U, w.Hkv).float()
     score_bytes = k.numel() * 2 + q.numel() * 2 + scores.numel() * 4
     comp_bytes = compact_bytes(rows, w.d, 2)
+    # one budget over every layer and kv head of a sequence (units are
+    # batch-major, u = b * layers + layer, so the scores of a sequence are
+    # one contiguous [layers * Hkv, T] pool): the streaming select
+    nb = w.U // w.layers
+    pooled = scores.view(nb, w.layers * w.Hkv, w.T)
+
+    def cross():
+        B.kvc_select(pooled, "global", kept, counts, offs, keep_ratio=w.keep_ratio,
+                     n_sink=w.n_sink, n_recent=w.n_recent)
+    for _ in range(warmup):
+        cross()
+    torch.cuda.synchronize()
+    xe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in xe:
+        e0.record(s); cross(); e1.record(s)
+    torch.cuda.synchronize()
+    t_cross = statistics.mean(e0.elapsed_time(e1) for e0, e1 in xe) * 1e3
+    per_layer = counts.view(nb, w.layers, w.Hkv).sum(-1).float()
     out = dict(workload="c3_32layer", score_us=t_score, select_us=t_sel, compact_us=t_comp,
                kept_rows=rows,
                per_head_count_min=int(per_head.min()), per_head_count_max=int(per_head.max()),
                score_gbs=score_bytes / (t_score * 1e-6) / 1e9, score_bytes=score_bytes,
                compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
-               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
+               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6),
+               cross_layer_select_us=t_cross,
+               cross_layer_keys_per_pool=w.layers * w.Hkv * w.T,
+               cross_layer_per_layer_kept_min=int(per_layer.min()),
+               cross_layer_per_layer_kept_max=int(per_layer.max()))
     del q, k, v, kc, vc, kept, scores, ws
     torch.cuda.empty_cache()
     return out

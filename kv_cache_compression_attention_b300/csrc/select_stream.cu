@@ -156,22 +156,34 @@ select_stream_kernel(Args a) {
   uint32_t* wh = sh.whist[warp];
   const float* base = a.scores + (int64_t)head0 * T + t0;
 
-  // key of (head hh, local token j): 0 for a protected token
+  // key of (head hh, local token j) from its score: 0 for a protected token
+  auto key_of = [&](float x, int j) -> uint32_t {
+    return prot(t0 + j, T, a.n_sink, a.n_recent) ? 0u : score_key(x);
+  };
   auto key_at = [&](int hh, int j) -> uint32_t {
-    const int t = t0 + j;
-    if (prot(t, T, a.n_sink, a.n_recent)) return 0u;
-    return score_key(__ldg(base + (int64_t)hh * T + j));
+    return key_of(__ldg(base + (int64_t)hh * T + j), j);
   };
   // sweep over every (head, token) of the range, 32 consecutive tokens of
-  // one head per warp step (coalesced loads); f(hh, j, valid) is called by
-  // every lane of the warp (warp-uniform trip count)
+  // one head per warp group (coalesced), kU groups' loads in flight per
+  // lane; f(hh, j, valid, key) is called by every lane of the warp
   auto sweep = [&](auto&& f) {
+    constexpr int kU = 8;
     const int per_head = (nt + 31) >> 5;               // 32-token groups per head
     const int groups = per_head * hps;
-    for (int q0 = warp; q0 < groups; q0 += kWarps) {
-      const int hh = q0 / per_head;
-      const int j = (q0 - hh * per_head) * 32 + lane;
-      f(hh, j, j < nt);
+    for (int q0 = warp; q0 < groups; q0 += kWarps * kU) {
+      float x[kU];
+      int hv[kU], jv[kU];
+      bool ok[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int q = q0 + u * kWarps;
+        hv[u] = q / per_head;
+        jv[u] = (q - hv[u] * per_head) * 32 + lane;
+        ok[u] = q < groups && jv[u] < nt;
+        x[u] = ok[u] ? __ldg(base + (int64_t)hv[u] * T + jv[u]) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) f(hv[u], jv[u], ok[u], ok[u] ? key_of(x[u], jv[u]) : 0u);
     }
   };
 
@@ -188,8 +200,7 @@ select_stream_kernel(Args a) {
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      sweep([&](int hh, int j, bool ok) {
-        const uint32_t key = ok ? key_at(hh, j) : 0u;
+      sweep([&](int, int, bool, uint32_t key) {
         const bool cand = key != 0u && (key & pmask) == prefix;
         hist_add(wh, cand, (key >> shift) & 255u);
       });
@@ -251,7 +262,7 @@ select_stream_kernel(Args a) {
     // ---- ties: keep the first krem elements with key == thr in (t, g) order
     if (!whole_bin && krem < last_count) {
       uint32_t mine = 0;
-      sweep([&](int hh, int j, bool ok) { mine += (ok && key_at(hh, j) == thr); });
+      sweep([&](int, int, bool ok, uint32_t key) { mine += (ok && key == thr); });
       mine = __reduce_add_sync(0xffffffffu, mine);
       if (lane == 0) sh.warp_tmp[0][warp] = mine;
       __syncthreads();
@@ -308,14 +319,29 @@ select_stream_kernel(Args a) {
   };
   const int per_w = (nt + kWarps - 1) / kWarps;
   const int j_lo = min(nt, warp * per_w), j_hi = min(nt, j_lo + per_w);
-  for (int hh = 0; hh < hps; ++hh) {
-    uint32_t n = 0;
+  // (eight heads per step, so that eight loads per lane are in flight)
+  constexpr int kH = 8;
+  for (int hh0 = 0; hh0 < hps; hh0 += kH) {
+    uint32_t n[kH];
+#pragma unroll
+    for (int x = 0; x < kH; ++x) n[x] = 0u;
     for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
       const int j = j0 + lane;
-      const bool f = j < j_hi && keep(key_at(hh, j), j, hh);
-      n += __popc(__ballot_sync(0xffffffffu, f));
+      float v[kH];
+#pragma unroll
+      for (int x = 0; x < kH; ++x)
+        v[x] = (hh0 + x < hps && j < j_hi) ? __ldg(base + (int64_t)(hh0 + x) * T + j) : 0.0f;
+#pragma unroll
+      for (int x = 0; x < kH; ++x) {
+        const bool f = hh0 + x < hps && j < j_hi && keep(key_of(v[x], j), j, hh0 + x);
+        n[x] += __popc(__ballot_sync(0xffffffffu, f));
+      }
     }
-    if (lane == 0) wcnt[hh * kWarps + warp] = n;
+    if (lane == 0) {
+#pragma unroll
+      for (int x = 0; x < kH; ++x)
+        if (hh0 + x < hps) wcnt[(hh0 + x) * kWarps + warp] = n[x];
+    }
   }
   __syncthreads();
   // per head: exclusive prefix over the warps (in place), CTA total
@@ -353,15 +379,26 @@ select_stream_kernel(Args a) {
     }
   }
   // ---- emission, sweep 2: every warp writes its slice's kept tokens
-  for (int hh = 0; hh < hps; ++hh) {
-    int32_t* dst = a.kept + (int64_t)(head0 + hh) * T + hbase[hh] + wcnt[hh * kWarps + warp];
-    uint32_t n = 0;
+  for (int hh0 = 0; hh0 < hps; hh0 += kH) {
+    uint32_t n[kH];
+#pragma unroll
+    for (int x = 0; x < kH; ++x) n[x] = 0u;
     for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
       const int j = j0 + lane;
-      const bool f = j < j_hi && keep(key_at(hh, j), j, hh);
-      const uint32_t bm = __ballot_sync(0xffffffffu, f);
-      if (f) dst[n + __popc(bm & lt_mask)] = t0 + j;
-      n += __popc(bm);
+      float v[kH];
+#pragma unroll
+      for (int x = 0; x < kH; ++x)
+        v[x] = (hh0 + x < hps && j < j_hi) ? __ldg(base + (int64_t)(hh0 + x) * T + j) : 0.0f;
+#pragma unroll
+      for (int x = 0; x < kH; ++x) {
+        const int hh = hh0 + x;
+        const bool f = hh < hps && j < j_hi && keep(key_of(v[x], j), j, hh);
+        const uint32_t bm = __ballot_sync(0xffffffffu, f);
+        if (f)
+          a.kept[(int64_t)(head0 + hh) * T + hbase[hh] + wcnt[hh * kWarps + warp] + n[x] +
+                 __popc(bm & lt_mask)] = t0 + j;
+        n[x] += __popc(bm);
+      }
     }
   }
   // no CTA may leave while a peer can still read its shared memory
