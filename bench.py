@@ -372,11 +372,7 @@ def bench_c4(B, steps, warmup, device):
                score_linear_gbs=score_bytes / (t_score * 1e-6) / 1e9,
                score_linear_bytes=score_bytes,
                compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
-               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6),
-               cross_layer_select_us=t_cross,
-               cross_layer_keys_per_pool=w.layers * w.Hkv * w.T,
-               cross_layer_per_layer_kept_min=int(per_layer.min()),
-               cross_layer_per_layer_kept_max=int(per_layer.max()))
+               tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
     del hidden, k, v, kc, vc, kept, flush
     torch.cuda.empty_cache()
     return out
