@@ -273,6 +273,47 @@ def decode_attn(q, kc, vc, start, length, k_new=None, v_new=None, scale=1.0):
     return out, lse, kc, vc, length.astype(np.int32)
 
 
+QGROUP = 32     # elements per quantisation group (one row, consecutive along d)
+
+
+def quantize_rows(x):
+    """Group quantisation of cache rows ([KVTC] §2B: coefficients are
+    quantised in groups that share a scale and an offset, after the
+    Microscaling formats; here applied to the cached K/V rows themselves).
+
+    x [rows, d] with float32-representable values inside the float16 range,
+    d a multiple of 32.  For every row and group of 32 consecutive elements,
+    in float32 arithmetic (the integer codes are decided in the precision the
+    kernel decides them in):
+        lo    = fp16(min(group))                      round to nearest even
+        scale = fp16((max(group) - lo) / 255)         difference and quotient in fp32
+        code  = clamp(rint((x - lo) / scale), 0, 255)  0 for the whole group if scale == 0
+    Returns (codes uint8 [rows, d], params float16 [rows, d/32, 2] = (scale, lo)).
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    rows, d = xf.shape
+    g = xf.reshape(rows, d // QGROUP, QGROUP)
+    lo = g.min(axis=-1).astype(np.float16)
+    lo32 = lo.astype(np.float32)
+    scale = ((g.max(axis=-1) - lo32) / np.float32(255.0)).astype(np.float16)
+    sc32 = scale.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = (g - lo32[..., None]) / sc32[..., None]
+    codes = np.clip(np.rint(v), 0, 255)
+    codes = np.where(sc32[..., None] == 0, 0, codes).astype(np.uint8)
+    params = np.stack([scale, lo], axis=-1)
+    return codes.reshape(rows, d), params
+
+
+def dequantize_rows(codes, params):
+    """x' = code * scale + lo per group (float64; the product of an 8-bit
+    code and a float16 is exact).  Returns float64 [rows, d]."""
+    c = np.asarray(codes, dtype=F64)
+    rows, d = c.shape
+    p = np.asarray(params, dtype=F64)
+    return (c.reshape(rows, d // QGROUP, QGROUP) * p[..., 0:1] + p[..., 1:2]).reshape(rows, d)
+
+
 def fidelity(out_comp, out_full, lse_comp, lse_full):
     """Fidelity probe of a compressed cache against the full one.
 

@@ -205,6 +205,82 @@ def test_planted_max_mistake_is_caught():
     assert not np.allclose(O.score_attn(q, k, 0.7, None, True), ref, rtol=1e-6)
 
 
+# ------------------------------------------ group quantisation ([KVTC] §2B)
+def brute_quantize(x):
+    """Element by element with float32 / float16 scalars."""
+    rows, d = x.shape
+    codes = np.zeros((rows, d), dtype=np.uint8)
+    params = np.zeros((rows, d // 32, 2), dtype=np.float16)
+    for r in range(rows):
+        for gi in range(d // 32):
+            grp = [np.float32(v) for v in x[r, gi * 32:(gi + 1) * 32]]
+            lo = np.float16(min(grp))
+            lo32 = np.float32(lo)
+            sc = np.float16(np.float32(max(grp) - lo32) / np.float32(255.0))
+            sc32 = np.float32(sc)
+            params[r, gi] = (sc, lo)
+            for e, v in enumerate(grp):
+                if sc32 == 0:
+                    c = 0
+                else:
+                    c = int(min(255.0, max(0.0, float(np.rint(np.float32(v - lo32) / sc32)))))
+                codes[r, gi * 32 + e] = c
+    return codes, params
+
+
+def test_quantize_matches_brute_force_and_bound():
+    x = (np.random.default_rng(21).standard_normal((6, 128)) *
+         np.array([1.0, 8.0, 0.01, 1.0] * 32)).astype(np.float32)
+    codes, params = O.quantize_rows(x)
+    bc, bp = brute_quantize(x)
+    np.testing.assert_array_equal(codes, bc)
+    np.testing.assert_array_equal(params.view(np.uint16), bp.view(np.uint16))
+    # rounding error of a code is at most half a step, plus the offset's own
+    # rounding at the clamped ends
+    xr = O.dequantize_rows(codes, params).reshape(6, 4, 32)
+    g = x.reshape(6, 4, 32).astype(np.float64)
+    sc = params[..., 0].astype(np.float64)[..., None]
+    lo_err = np.abs(params[..., 1].astype(np.float64) - g.min(-1))[..., None]
+    assert (np.abs(xr - g) <= 0.5 * sc + lo_err + sc * 1e-3 + 1e-12).all()
+
+
+def test_quantize_closed_forms():
+    # integers 0..255 with both ends present: lo = 0, scale = 1, codes = values
+    rng = np.random.default_rng(22)
+    ints = rng.integers(0, 256, (3, 64)).astype(np.float32)
+    ints[:, 0] = 0; ints[:, 31] = 255; ints[:, 32] = 0; ints[:, 63] = 255
+    codes, params = O.quantize_rows(ints)
+    np.testing.assert_array_equal(codes, ints.astype(np.uint8))
+    np.testing.assert_array_equal(O.dequantize_rows(codes, params), ints)
+    # half steps round to even: 3.5 -> 4, 2.5 -> 2
+    h = ints.copy(); h[0, 5] = 3.5; h[0, 6] = 2.5
+    c2, _ = O.quantize_rows(h)
+    assert c2[0, 5] == 4 and c2[0, 6] == 2
+    # a constant group: scale 0, codes 0, the value back exactly (fp16-representable)
+    const = np.full((1, 32), 0.75, dtype=np.float32)
+    c3, p3 = O.quantize_rows(const)
+    assert (c3 == 0).all() and p3[0, 0, 0] == 0 and O.dequantize_rows(c3, p3)[0, 0] == 0.75
+
+
+def test_planted_quantize_mistakes_are_caught():
+    x = np.random.default_rng(23).standard_normal((2, 64)).astype(np.float32)
+    ref, _ = brute_quantize(x)
+
+    def floor_codes(xx):                   # truncation instead of rounding
+        xf = xx.reshape(2, 2, 32)
+        lo = xf.min(-1).astype(np.float16).astype(np.float32)
+        sc = ((xf.max(-1) - lo) / np.float32(255)).astype(np.float16).astype(np.float32)
+        return np.clip(np.floor((xf - lo[..., None]) / sc[..., None]), 0, 255).astype(np.uint8).reshape(2, 64)
+
+    def wide_groups(xx):                   # one group of 64
+        lo = np.float32(np.float16(xx.min(-1, keepdims=True)))
+        sc = np.float32(np.float16((xx.max(-1, keepdims=True) - lo) / np.float32(255)))
+        return np.clip(np.rint((xx - lo) / sc), 0, 255).astype(np.uint8)
+
+    assert not np.array_equal(floor_codes(x), ref)
+    assert not np.array_equal(wide_groups(x), ref)
+
+
 def test_score_linear_matches_loops_and_torch():
     h, w, b = rng_arrays(7, (2, 11, 13), (13, 3), (3,))
     got = O.score_linear(h, w, b)
