@@ -310,11 +310,40 @@ def bench_decode(B, steps, warmup, device):
     mean_rows = rows_before + n * (steps - 1) / 2.0
     row_bytes = w.d * 2
     bytes_step = 2 * mean_rows * row_bytes            # K and V rows streamed once
+    out_d = dict(workload=DECODE_WORKLOAD, us_per_step=ms * 1e3,
+                 kv_rows_per_step=mean_rows + n, bytes_per_step=bytes_step,
+                 kv_tokens_per_s=(mean_rows + n) / (ms * 1e-3),
+                 gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2, rows_at_start=rows0)
+    # the same steps over the group-quantised pool ([KVTC] §2B groups of 32 with a
+    # scale and an offset): the pool as compacted, quantised once before timing
+    kc2, vc2, start2, length2 = inputs.compressed_pool(w, lens, device)
     del kc, vc
-    return dict(workload=DECODE_WORKLOAD, us_per_step=ms * 1e3,
-                kv_rows_per_step=mean_rows + n, bytes_per_step=bytes_step,
-                kv_tokens_per_s=(mean_rows + n) / (ms * 1e-3),
-                gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2, rows_at_start=rows0)
+    rows_pool = kc2.shape[0]
+    kq = torch.empty((rows_pool, w.d), dtype=torch.uint8, device=device)
+    vq = torch.empty_like(kq)
+    kp = torch.empty((rows_pool, w.d // 32, 2), dtype=torch.float16, device=device)
+    vp = torch.empty_like(kp)
+    B.kvc_quantize_rows(kc2, kq, kp)
+    B.kvc_quantize_rows(vc2, vq, vp)
+    del kc2, vc2
+    for i in range(warmup):
+        q, kn, vn = steps_in[i]
+        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start2, length2, out, lse, k_new=kn, v_new=vn,
+                             max_len=max_len, scale=w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for i in range(warmup, warmup + steps):
+        q, kn, vn = steps_in[i]
+        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start2, length2, out, lse, k_new=kn, v_new=vn,
+                             max_len=max_len, scale=w.scale, workspace=ws)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms8 = e0.elapsed_time(e1) / steps
+    bytes8 = 2 * mean_rows * (w.d + (w.d // 32) * 4)  # codes + (scale, offset) pairs
+    out_d["q8"] = dict(us_per_step=ms8 * 1e3, bytes_per_step=bytes8,
+                       kv_tokens_per_s=(mean_rows + n) / (ms8 * 1e-3),
+                       gbs=bytes8 / (ms8 * 1e-3) / 1e9, launches_per_step=2)
+    return out_d
 
 
 def compact_bytes(rows, d, elt):
@@ -710,7 +739,10 @@ def main():
             {"kernel": "compact_kernel", "workload": "c3_32layer", "bound": "hbm",
              "achieved_gbs": c3["compact_gbs"], "frac": c3["compact_gbs"] / hbm},
             {"kernel": "decode_partial_kernel+decode_combine_kernel", "workload": DECODE_WORKLOAD,
-             "bound": "hbm", "achieved_gbs": dec["gbs"], "frac": dec["gbs"] / hbm}],
+             "bound": "hbm", "achieved_gbs": dec["gbs"], "frac": dec["gbs"] / hbm},
+            {"kernel": "decode_partial_mma_kernel<q8>+decode_combine_kernel (group-quantised pool)",
+             "workload": DECODE_WORKLOAD, "bound": "hbm", "time_us": dec["q8"]["us_per_step"],
+             "achieved_gbs": dec["q8"]["gbs"], "frac": dec["q8"]["gbs"] / hbm}],
         "fidelity": fid,
         "e2e": {"value": job_tokens_per_s(world, w.U * w.T, e2e_ms), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

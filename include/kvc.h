@@ -248,6 +248,40 @@ int kvc_decode_attn(const void* q, void* kc, void* vc, const int64_t* start, int
                     void* stream);
 
 /*
+ * Group-quantised copy of cache rows ([KVTC] §2B: coefficients quantised in
+ * groups that share a scale and an offset, after the Microscaling formats;
+ * applied here to the compacted K / V rows themselves).  For every row and
+ * group of 32 consecutive elements, in IEEE fp32:
+ *   lo    = fp16(min(group))                        (round to nearest even)
+ *   scale = fp16((max(group) - lo) / 255)
+ *   code  = clamp(rint((x - lo) / scale), 0, 255)    (0 for the group if scale == 0)
+ * x      [rows, d] dtype (KVC_BF16, d in {64, 128}; values inside the fp16
+ *        range; rows past the heads' lengths may hold anything)
+ * codes  [rows, d] uint8 (written), params [rows, d / 32] pairs of fp16
+ *        (scale, lo) (written).
+ */
+int kvc_quantize_rows(const void* x, int dtype, int64_t rows, int d,
+                      uint8_t* codes, void* params, void* stream);
+
+/*
+ * kvc_decode_attn over a group-quantised pool: kq / vq are the codes and
+ * kp / vp the (scale, lo) pairs of K and V as kvc_quantize_rows writes them
+ * (same row indexing as kc / vc, 16-byte aligned).  Every cached row is
+ * dequantised in the kernel (code * scale + lo in fp32, then bf16), which
+ * streams 144 instead of 256 bytes per row and tensor; k_new / v_new are
+ * attended exactly and appended quantised (codes and pair of row
+ * start[i] + len[i]).  dtype KVC_BF16, d = 128, Hq / Hkv <= 8; same
+ * workspace (kvc_decode_workspace), start / len semantics and status word as
+ * kvc_decode_attn.
+ */
+int kvc_decode_attn_q8(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* vp,
+                       const int64_t* start, int32_t* len,
+                       const void* k_new, const void* v_new,
+                       int dtype, int U, int Hq, int Hkv, int d, int max_len,
+                       float scale, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kvc_decode_attn without a workspace, for callers that cannot allocate
  * device memory (a plug-in inside a host engine that owns every allocation
  * and offers no workspace; a caller whose device-memory budget is fixed at

@@ -47,6 +47,9 @@ SIGNATURES = {
     "kvc_decode_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvc_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                              _P, _SZ, _P]),
+    "kvc_quantize_rows": (_I, [_P, _I, _I64, _I, _P, _P, _P]),
+    "kvc_decode_attn_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                                _P, _P, _P, _SZ, _P]),
     "kvc_decode_noalloc_scratch_bytes": (_SZ, []),
     "kvc_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                      _P, _P]),
@@ -192,6 +195,36 @@ def kvc_decode_attn(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=N
                                float(scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                _stream(stream))
     _check("kvc_decode_attn", rc)
+
+
+def kvc_quantize_rows(x, codes, params, stream=None):
+    """x [rows, d] bf16 -> codes [rows, d] uint8, params [rows, d / 32, 2] float16 (scale, lo)."""
+    rows, d = x.shape
+    rc = lib().kvc_quantize_rows(_ptr(x), _dtype(x), int(rows), int(d), _ptr(codes),
+                                 _ptr(params), _stream(stream))
+    _check("kvc_quantize_rows", rc)
+
+
+def kvc_decode_attn_q8(q, kq, kp, vq, vp, start, length, out, lse=None, k_new=None, v_new=None,
+                       max_len=None, scale=None, workspace=None, stream=None):
+    """kvc_decode_attn over a group-quantised pool (codes kq / vq [rows, d] uint8,
+    pairs kp / vp [rows, d / 32, 2] float16)."""
+    U, Hq, d = q.shape
+    Hkv = start.numel() // U
+    if max_len is None:
+        raise ValueError("max_len is required (upper bound of any head's length)")
+    if scale is None:
+        scale = d ** -0.5
+    dt = _dtype(q)
+    need = lib().kvc_decode_workspace(U, Hq, Hkv, d, int(max_len), dt)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_decode_attn_q8(_ptr(q), _ptr(kq), _ptr(kp), _ptr(vq), _ptr(vp), _ptr(start),
+                                  _ptr(length), _ptr(k_new), _ptr(v_new), dt, U, Hq, Hkv, d,
+                                  int(max_len), float(scale), _ptr(out), _ptr(lse),
+                                  _ptr(workspace), ws_bytes, _stream(stream))
+    _check("kvc_decode_attn_q8", rc)
 
 
 def kvc_decode_attn_noalloc(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,

@@ -222,6 +222,42 @@ int kvc_decode_attn(const void* q, void* kc, void* vc, const int64_t* start, int
                             kvc::as_stream(stream));
 }
 
+int kvc_quantize_rows(const void* x, int dtype, int64_t rows, int d, uint8_t* codes,
+                      void* params, void* stream) {
+  if (!x || !codes || !params) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (rows < 0) return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || (d != 64 && d != 128)) return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::quantize_rows_launch(x, rows, d, codes, params, dev, kvc::as_stream(stream));
+}
+
+int kvc_decode_attn_q8(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* vp,
+                       const int64_t* start, int32_t* len, const void* k_new, const void* v_new,
+                       int dtype, int U, int Hq, int Hkv, int d, int max_len, float scale,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (!q || !kq || !kp || !vq || !vp || !start || !len || !out) return KVC_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_len < 0 || !isfinite(scale))
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || d != 128) return KVC_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8 || (int64_t)U * Hkv > 65535) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(kq) || !aligned16(vq) || !aligned16(kp) || !aligned16(vp) || !aligned16(q))
+    return KVC_ERR_UNSUPPORTED;
+  size_t need = kvc::decode_ws_bytes(U, Hq, Hkv, d, max_len);
+  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::decode_q8_launch(q, kq, kp, vq, vp, start, len, k_new, v_new, U, Hq, Hkv, max_len,
+                               scale, out, lse, static_cast<float*>(workspace), dev,
+                               kvc::as_stream(stream));
+}
+
 int kvc_fidelity(const void* out_comp, const void* out_full, const float* lse_comp,
                  const float* lse_full, int dtype, int n, int d, float* rel_err, float* kl,
                  void* stream) {

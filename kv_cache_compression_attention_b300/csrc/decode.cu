@@ -21,6 +21,8 @@
 //            no CTA of this step reads a row another one writes), writes out
 //            and lse, then appends k_new / v_new at row start_i + L and
 //            bumps len.
+#include <cuda_fp16.h>
+
 #include <atomic>
 
 #include "kvc_internal.cuh"
@@ -309,13 +311,57 @@ decode_partial_kernel(const Tin* __restrict__ q, const Tin* __restrict__ kc,
   }
 }
 
+// Group quantisation of one element per lane of a warp that holds one group
+// of 32 ([KVTC] §2B: groups share a scale and an offset): lo = fp16(min),
+// scale = fp16((max - lo) / 255), code = clamp(rint((x - lo) / scale), 0, 255)
+// (0 when scale is 0), all in IEEE fp32.  Lane 0 writes (scale, lo) as an
+// fp16 pair.
+__device__ __forceinline__ void quantize_elem(float v, int lane, uint8_t* code, uint32_t* param) {
+  float mn = v, mx = v;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const __half lo16 = __float2half_rn(mn);
+  const float lo = __half2float(lo16);
+  const __half sc16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, lo), 255.0f));
+  const float sc = __half2float(sc16);
+  float c = 0.0f;
+  if (sc != 0.0f) c = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, lo), sc)), 0.0f), 255.0f);
+  *code = (uint8_t)c;
+  if (lane == 0)
+    *param = (uint32_t)__half_as_ushort(sc16) | ((uint32_t)__half_as_ushort(lo16) << 16);
+}
+
+// Group-quantised copy of bf16 rows of D elements: one warp per row, lane l
+// holds element l of every group.
+template <int D>
+__global__ void __launch_bounds__(256)
+quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, uint8_t* __restrict__ codes,
+                     uint32_t* __restrict__ params) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows;
+       row += (int64_t)gridDim.x * 8) {
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+      const float v = bf16lo((uint32_t)x[row * D + g * 32 + lane]);
+      quantize_elem(v, lane, codes + row * D + g * 32 + lane, params + row * (D / 32) + g);
+    }
+  }
+}
+
 template <typename Tin, int D, int G>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __restrict__ vc,
                       const int64_t* __restrict__ start, int32_t* __restrict__ len,
                       const Tin* __restrict__ k_new, const Tin* __restrict__ v_new, int n_heads,
                       int Hkv, int max_chunks, float scale_log2, const float* __restrict__ ws,
-                      Tin* __restrict__ out, float* __restrict__ lse, int* status) {
+                      Tin* __restrict__ out, float* __restrict__ lse, int* status,
+                      uint8_t* __restrict__ kq, uint32_t* __restrict__ kp,
+                      uint8_t* __restrict__ vq, uint32_t* __restrict__ vp) {
   __shared__ float red[D / 32][G];
   pdl_wait();
   pdl_trigger();
@@ -426,7 +472,14 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
     }
   }
   __syncthreads();                      // every thread has read len[i] and the pool
-  if (room) {
+  if (room && kq) {
+    // group-quantised pool: the new row's codes and (scale, offset) per
+    // group of 32 (warp w holds group w)
+    const int64_t row = start[i] + L;
+    quantize_elem(kn, lane, kq + row * D + x, kp + row * (D / 32) + warp);
+    quantize_elem(vn, lane, vq + row * D + x, vp + row * (D / 32) + warp);
+    if (x == 0) len[i] = L + 1;
+  } else if (room) {
     const int64_t row = start[i] + L;
     if (sizeof(Tin) == 2) {
       reinterpret_cast<uint16_t*>(kc)[row * D + x] = reinterpret_cast<const uint16_t*>(k_new)[nrow * D + x];
@@ -494,15 +547,64 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 constexpr int kRows = 64;      // rows per stage (16 per warp)
 constexpr int kStg = 3;
 
+// bf16 path: kStg stages of (K tile, V tile), kRows x (D + 8) bf16 each.
+// Group-quantised path: one (K, V) bf16 tile pair that the stage being
+// consumed is dequantised into, then the raw stages of (K codes, V codes,
+// K params, V params): kRows x D bytes and kRows x 16 bytes each; two raw
+// stages, so that three CTAs fit an SM.
+template <int D, bool kQ8>
+constexpr size_t tile_bytes() { return kQ8 ? (size_t)2 * kRows * (D + 8) * 2 : 0; }
 template <int D>
-constexpr size_t smem_bytes() { return (size_t)kStg * 2 * kRows * (D + 8) * 2; }
+constexpr size_t raw_stage_bytes() { return (size_t)2 * kRows * D + 2 * kRows * 16; }
+template <int D, bool kQ8 = false>
+constexpr size_t smem_bytes() {
+  return kQ8 ? tile_bytes<D, true>() + (size_t)2 * raw_stage_bytes<D>()
+             : (size_t)kStg * 2 * kRows * (D + 8) * 2;
+}
+
+// Packed fp32 pairs (one issue slot for two lanes of arithmetic).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// 16 codes (4 words) -> 16 bf16 (8 words): x = code * scale + lo.  A code
+// becomes the float 2^23 + code by placing it under the exponent byte 0x4B
+// (exact), and 2^23 is subtracted exactly before the scale-and-offset FMA.
+__device__ __forceinline__ void dequant16(const uint32_t (&w)[4], float sc, float lo,
+                                          uint32_t (&o)[8]) {
+  const uint64_t big = pk2(-8388608.0f, -8388608.0f), sc2 = pk2(sc, sc), lo2 = pk2(lo, lo);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const uint32_t e0 = __byte_perm(w[k], 0x4B000000u, 0x7540u + 2 * p);       // byte 2p
+      const uint32_t e1 = __byte_perm(w[k], 0x4B000000u, 0x7540u + 2 * p + 1);   // byte 2p+1
+      const uint64_t f = ffma2(fadd2(((uint64_t)e1 << 32) | e0, big), sc2, lo2);
+      o[2 * k + p] = pack_bf16(__uint_as_float((uint32_t)f), __uint_as_float((uint32_t)(f >> 32)));
+    }
+  }
+}
 
 }  // namespace mma
 
-template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32, 2)
-decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc,
-                          const uint16_t* __restrict__ vc, const int64_t* __restrict__ start,
+// kQ8: the pool holds group-quantised rows (codes [rows, D] uint8 in kc / vc,
+// (scale, offset) fp16 pairs [rows, D / 32] in kp / vp); every stage is
+// dequantised into one bf16 tile pair before the same MMAs.
+template <int D, int G, bool kQ8>
+__global__ void __launch_bounds__(kWarps * 32, kQ8 ? 3 : 2)
+decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kc,
+                          const void* __restrict__ vc, const uint32_t* __restrict__ kp,
+                          const uint32_t* __restrict__ vp, const int64_t* __restrict__ start,
                           const int32_t* __restrict__ len, int Hkv, int max_chunks,
                           float scale_log2, float* __restrict__ ws) {
   static_assert(G <= 8, "query heads per kv head");
@@ -511,7 +613,9 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   constexpr int NT = D / 8;                  // 8-wide output tiles
   extern __shared__ __align__(128) uint16_t smem_m[];
   __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
-  __shared__ float acc_sm[kWarps][G][D];
+  // the quantised variant merges its warps in the (then idle) tile area
+  __shared__ float acc_static[kQ8 ? 1 : kWarps * G * D];
+  constexpr int STG = kQ8 ? 2 : mma::kStg;   // stages in flight
   pdl_wait();
   pdl_trigger();
 
@@ -523,26 +627,52 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   const int nst = (nrows + mma::kRows - 1) / mma::kRows;
   const int u = i / Hkv, g = i - u * Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint16_t* kb = kc + (start[i] + rb) * D;
-  const uint16_t* vb = vc + (start[i] + rb) * D;
+  const int64_t row0 = start[i] + rb;
   const uint32_t sbase = smem_u32(smem_m);
+  constexpr uint32_t kTileBytes = (uint32_t)mma::tile_bytes<D, kQ8>();
+  constexpr uint32_t kRawBytes = (uint32_t)mma::raw_stage_bytes<D>();
 
-  // stage st -> slot: K rows then V rows, each kRows x RS elements
+  // stage st -> slot: K rows then V rows, each kRows x RS elements (bf16), or
+  // the raw codes and (scale, offset) pairs of the quantised pool
   auto issue = [&](int st) {
-    const int slot = st % mma::kStg;
-    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    const int slot = st % STG;
     const int r0 = st * mma::kRows;
-    for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
-      const int r = x / CPR, ch = x - r * CPR;
-      const bool ok = r0 + r < nrows;
-      const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
-      const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
-      mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
-      mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+    if constexpr (kQ8) {
+      constexpr int CB = D / 16;                  // 16-byte code chunks per row
+      const uint32_t raw = sbase + kTileBytes + (uint32_t)slot * kRawBytes;
+      const uint8_t* kb = static_cast<const uint8_t*>(kc) + row0 * D;
+      const uint8_t* vb = static_cast<const uint8_t*>(vc) + row0 * D;
+      for (int x = tid; x < mma::kRows * CB; x += kWarps * 32) {
+        const int r = x / CB, ch = x - r * CB;
+        const bool ok = r0 + r < nrows;
+        const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 16;
+        const uint32_t so = (uint32_t)(r * D + ch * 16);
+        mma::cp_async16(raw + so, kb + off, ok ? 16u : 0u);
+        mma::cp_async16(raw + (uint32_t)(mma::kRows * D) + so, vb + off, ok ? 16u : 0u);
+      }
+      for (int r = tid; r < mma::kRows; r += kWarps * 32) {
+        const bool ok = r0 + r < nrows;
+        const size_t off = (size_t)(row0 + (ok ? r0 + r : 0)) * (D / 32);
+        const uint32_t so = (uint32_t)(2 * mma::kRows * D + r * 16);
+        mma::cp_async16(raw + so, kp + off, ok ? 16u : 0u);
+        mma::cp_async16(raw + so + (uint32_t)(mma::kRows * 16), vp + off, ok ? 16u : 0u);
+      }
+    } else {
+      const uint16_t* kb = static_cast<const uint16_t*>(kc) + row0 * D;
+      const uint16_t* vb = static_cast<const uint16_t*>(vc) + row0 * D;
+      const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+      const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+      for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
+        const int r = x / CPR, ch = x - r * CPR;
+        const bool ok = r0 + r < nrows;
+        const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
+        const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
+        mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
+        mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+      }
     }
   };
-  for (int st = 0; st < mma::kStg - 1; ++st) {
+  for (int st = 0; st < STG - 1; ++st) {
     if (st < nst) issue(st);
     mma::cp_commit();
   }
@@ -569,13 +699,48 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   float m = -INFINITY, l = 0.0f;                  // for head lane / 4 (lanes of a quad agree)
 
   for (int st = 0; st < nst; ++st) {
-    mma::cp_wait<mma::kStg - 2>();
+    mma::cp_wait<STG - 2>();
     __syncthreads();                              // stage st landed; slot st-1 is free
-    if (st + mma::kStg - 1 < nst) issue(st + mma::kStg - 1);
+    if (st + STG - 1 < nst) issue(st + STG - 1);
     mma::cp_commit();
-    const int slot = st % mma::kStg;
-    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    const int slot = st % STG;
+    uint32_t ks, vs;
+    if constexpr (kQ8) {
+      // dequantise the raw stage into the tile pair (every thread 8 chunks of
+      // 16 codes), then every warp reads it
+      constexpr int CB = D / 16;
+      const uint32_t raw = sbase + kTileBytes + (uint32_t)slot * kRawBytes;
+      static_assert((2 * mma::kRows * CB) % (kWarps * 32) == 0, "whole chunks per thread");
+#pragma unroll
+      for (int it = 0; it < 2 * mma::kRows * CB / (kWarps * 32); ++it) {
+        const int x = tid + it * kWarps * 32;
+        const int t = x / (mma::kRows * CB), rem = x - t * (mma::kRows * CB);
+        const int r = rem / CB, ch = rem - r * CB;
+        uint32_t w[4], o[8];
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(raw + (uint32_t)(t * mma::kRows * D + r * D + ch * 16)));
+        uint32_t pr;
+        asm volatile("ld.shared.u32 %0, [%1];"
+                     : "=r"(pr)
+                     : "r"(raw + (uint32_t)(2 * mma::kRows * D + t * mma::kRows * 16 + r * 16 +
+                                            (ch >> 1) * 4)));
+        const float sc = __half2float(__ushort_as_half((unsigned short)(pr & 0xffffu)));
+        const float lo = __half2float(__ushort_as_half((unsigned short)(pr >> 16)));
+        mma::dequant16(w, sc, lo, o);
+        const uint32_t dst = sbase + (uint32_t)(t * mma::kRows * RS + r * RS + ch * 16) * 2u;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                     "r"(o[2]), "r"(o[3]) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16u), "r"(o[4]),
+                     "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+      }
+      __syncthreads();
+      ks = sbase;
+      vs = sbase + (uint32_t)(mma::kRows * RS) * 2u;
+    } else {
+      ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+      vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    }
     const int wr = warp * 16;                     // this warp's 16 rows of the stage
     // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -630,6 +795,9 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
   const int h = lane >> 2;
+  float (*acc_sm)[G][D] = reinterpret_cast<float (*)[G][D]>(
+      kQ8 ? reinterpret_cast<float*>(smem_m) : acc_static);
+  if constexpr (kQ8) __syncthreads();         // every warp is done with the tile
   if (h < G) {
     if ((lane & 3) == 0) { m_sm[warp][h] = m; l_sm[warp][h] = l; }
 #pragma unroll
@@ -657,31 +825,61 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __rest
   }
 }
 
+// A group-quantised pool (codes and fp16 (scale, offset) pairs per group of
+// 32); all null for a bf16 / fp32 pool.
+struct QPool {
+  uint8_t* kq = nullptr;
+  uint32_t* kp = nullptr;
+  uint8_t* vq = nullptr;
+  uint32_t* vp = nullptr;
+};
+
 template <typename Tin, int D, int G>
-int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, const void* k_new,
-        const void* v_new, int U, int Hkv, int max_len, float scale, void* out, float* lse,
-        float* ws, const Dev& dev, cudaStream_t s) {
+int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start, int32_t* len,
+        const void* k_new, const void* v_new, int U, int Hkv, int max_len, float scale, void* out,
+        float* lse, float* ws, const Dev& dev, cudaStream_t s) {
   const int n = U * Hkv;
   const int max_chunks = (max_len + kChunk - 1) / kChunk;
   const float sl2 = scale * kLog2e;
   if (max_chunks > 0) {
     dim3 grid((unsigned)max_chunks, (unsigned)n);
-    static std::atomic<uint64_t> attr_done{0};          // one bit per device
-    const uint64_t bit = 1ull << (dev.device & 63);
+    static std::atomic<uint64_t> attr_done{0};          // one bit per device and variant
+    const uint64_t bit = 1ull << (dev.device & 31);
     if constexpr (sizeof(Tin) == 2 && G <= 8) {
-      const size_t smem = mma::smem_bytes<D>();
-      auto kern = decode_partial_mma_kernel<D, G>;
-      if (!(attr_done.load() & bit)) {
-        KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        attr_done.fetch_or(bit);
+      if (qz.kq) {
+        if constexpr (D == 128) {
+          const size_t smem = mma::smem_bytes<D, true>();
+          auto kern = decode_partial_mma_kernel<D, G, true>;
+          if (!(attr_done.load() & (bit << 32))) {
+            KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            attr_done.fetch_or(bit << 32);
+          }
+          if (int rc = prefer_max_shared(kern, dev.device)) return rc;
+          if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
+                                  static_cast<const uint16_t*>(q), (const void*)qz.kq,
+                                  (const void*)qz.vq, (const uint32_t*)qz.kp,
+                                  (const uint32_t*)qz.vp, start, (const int32_t*)len, Hkv,
+                                  max_chunks, sl2, ws))
+            return rc;
+        } else {
+          return KVC_ERR_UNSUPPORTED;
+        }
+      } else {
+        const size_t smem = mma::smem_bytes<D>();
+        auto kern = decode_partial_mma_kernel<D, G, false>;
+        if (!(attr_done.load() & bit)) {
+          KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+          attr_done.fetch_or(bit);
+        }
+        if (int rc = prefer_max_shared(kern, dev.device)) return rc;
+        if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
+                                static_cast<const uint16_t*>(q), (const void*)kc, (const void*)vc,
+                                (const uint32_t*)nullptr, (const uint32_t*)nullptr, start,
+                                (const int32_t*)len, Hkv, max_chunks, sl2, ws))
+          return rc;
       }
-      if (int rc = prefer_max_shared(kern, dev.device)) return rc;
-      if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
-                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kc),
-                              static_cast<const uint16_t*>(vc), start, (const int32_t*)len, Hkv,
-                              max_chunks, sl2, ws))
-        return rc;
     } else {
+      if (qz.kq) return KVC_ERR_UNSUPPORTED;
       const size_t smem = partial_smem_bytes<Tin, D>();
       auto kern = decode_partial_kernel<Tin, D, G>;
       if (!(attr_done.load() & bit)) {
@@ -701,16 +899,16 @@ int run(const void* q, void* kc, void* vc, const int64_t* start, int32_t* len, c
                     static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc),
                     start, len, static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new),
                     n, Hkv, max_chunks, sl2, (const float*)ws, static_cast<Tin*>(out), lse,
-                    dev.status);
+                    dev.status, qz.kq, qz.kp, qz.vq, qz.vp);
 }
 
 template <typename Tin, int D>
-int dispatch_g(int G, const void* q, void* kc, void* vc, const int64_t* start, int32_t* len,
-               const void* kn, const void* vn, int U, int Hkv, int max_len, float scale,
-               void* out, float* lse, float* ws, const Dev& dev, cudaStream_t s) {
+int dispatch_g(int G, const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start,
+               int32_t* len, const void* kn, const void* vn, int U, int Hkv, int max_len,
+               float scale, void* out, float* lse, float* ws, const Dev& dev, cudaStream_t s) {
   switch (G) {
 #define KVC_G(GG) \
-    case GG: return run<Tin, D, GG>(q, kc, vc, start, len, kn, vn, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+    case GG: return run<Tin, D, GG>(q, kc, vc, qz, start, len, kn, vn, U, Hkv, max_len, scale, out, lse, ws, dev, s);
     KVC_G(1) KVC_G(2) KVC_G(3) KVC_G(4) KVC_G(5) KVC_G(6) KVC_G(7) KVC_G(8)
 #undef KVC_G
   }
@@ -729,11 +927,33 @@ int decode_launch(const void* q, void* kc, void* vc, const int64_t* start, int32
                   int d, int max_len, float scale, void* out, float* lse, float* ws,
                   const Dev& dev, cudaStream_t s) {
   const int G = Hq / Hkv;
+  const QPool none;
   if (dtype == KVC_F32)
-    return d == 64 ? dispatch_g<float, 64>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
-                   : dispatch_g<float, 128>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
-  return d == 64 ? dispatch_g<uint16_t, 64>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
-                 : dispatch_g<uint16_t, 128>(G, q, kc, vc, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+    return d == 64 ? dispatch_g<float, 64>(G, q, kc, vc, none, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
+                   : dispatch_g<float, 128>(G, q, kc, vc, none, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+  return d == 64 ? dispatch_g<uint16_t, 64>(G, q, kc, vc, none, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s)
+                 : dispatch_g<uint16_t, 128>(G, q, kc, vc, none, start, len, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+}
+
+int decode_q8_launch(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* vp,
+                     const int64_t* start, int32_t* len, const void* k_new, const void* v_new,
+                     int U, int Hq, int Hkv, int max_len, float scale, void* out, float* lse,
+                     float* ws, const Dev& dev, cudaStream_t s) {
+  QPool qz;
+  qz.kq = kq; qz.kp = static_cast<uint32_t*>(kp);
+  qz.vq = vq; qz.vp = static_cast<uint32_t*>(vp);
+  return dispatch_g<uint16_t, 128>(Hq / Hkv, q, nullptr, nullptr, qz, start, len, k_new, v_new,
+                                   U, Hkv, max_len, scale, out, lse, ws, dev, s);
+}
+
+int quantize_rows_launch(const void* x, int64_t rows, int d, uint8_t* codes, void* params,
+                         const Dev& dev, cudaStream_t s) {
+  if (rows <= 0) return KVC_OK;
+  const int64_t want = (rows + 7) / 8;
+  const unsigned blocks = (unsigned)(want < (int64_t)dev.sms * 8 ? want : (int64_t)dev.sms * 8);
+  auto kern = d == 64 ? quantize_rows_kernel<64> : quantize_rows_kernel<128>;
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, static_cast<const uint16_t*>(x), rows,
+                    codes, static_cast<uint32_t*>(params));
 }
 
 }  // namespace kvc

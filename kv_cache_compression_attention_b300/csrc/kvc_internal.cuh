@@ -122,6 +122,13 @@ int decode_launch(const void* q, void* kc, void* vc, const int64_t* start, int32
                   int d, int max_len, float scale, void* out, float* lse, float* ws,
                   const Dev& dev, cudaStream_t s);
 
+int decode_q8_launch(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* vp,
+                     const int64_t* start, int32_t* len, const void* k_new, const void* v_new,
+                     int U, int Hq, int Hkv, int max_len, float scale, void* out, float* lse,
+                     float* ws, const Dev& dev, cudaStream_t s);
+int quantize_rows_launch(const void* x, int64_t rows, int d, uint8_t* codes, void* params,
+                         const Dev& dev, cudaStream_t s);
+
 int fidelity_launch(const void* oc, const void* of, const float* lc, const float* lf,
                     int dtype, int n, int d, float* rel, float* kl, const Dev& dev,
                     cudaStream_t s);

@@ -148,3 +148,28 @@ def test_workspace_queries_are_pure_host(lib):
     assert lib.kvc_score_attn_workspace(1, 32, 8, 32768, 64, 128, 1) == tc
     assert lib.kvc_score_attn_workspace(128, 32, 8, 16384, 64, 128, 1) == tc
     assert lib.kvc_score_attn_workspace(1, 8, 4, 1024, 32, 64, 0) == 8 * 32 * 4
+
+
+def test_quantize_and_q8_decode_reject_bad_arguments(lib):
+    qz = lib.kvc_quantize_rows
+    assert qz(None, 1, 4, 128, P, P, None) == -1
+    assert qz(P, 7, 4, 128, P, P, None) == -1                 # unknown dtype
+    assert qz(P, 1, -1, 128, P, P, None) == -1                # negative row count
+    assert qz(P, 1, 4, 96, P, P, None) == -2                  # d outside {64, 128}
+    assert qz(P, 0, 4, 128, P, P, None) == -2                 # f32 rows
+    dq = lib.kvc_decode_attn_q8
+    args = [P, P, P, P, P, P, P, None, None, 1, 1, 8, 2, 128, 64, 0.1, P, P, P, 1 << 20, None]
+    bad = list(args); bad[1] = None                           # no K codes
+    assert dq(*bad) == -1
+    bad = list(args); bad[7] = P                              # k_new without v_new
+    assert dq(*bad) == -1
+    bad = list(args); bad[12] = 3                             # Hq % Hkv
+    assert dq(*bad) == -1
+    bad = list(args); bad[13] = 64                            # d
+    assert dq(*bad) == -2
+    bad = list(args); bad[11] = 32; bad[12] = 2               # 16 query heads per kv head
+    assert dq(*bad) == -2
+    bad = list(args); bad[2] = ctypes.c_void_p(24)            # unaligned scale/offset pairs
+    assert dq(*bad) == -2
+    bad = list(args); bad[19] = 0                             # workspace too small
+    assert dq(*bad) == -3
