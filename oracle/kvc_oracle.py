@@ -273,6 +273,63 @@ def decode_attn(q, kc, vc, start, length, k_new=None, v_new=None, scale=1.0):
     return out, lse, kc, vc, length.astype(np.int32)
 
 
+# ---------------------------------------------------- decode-time pruning
+def gather_scores(scores, kept_idx, counts, start, rows):
+    """Per-row scores of a compacted cache: the score of the token each row
+    holds, rscore[start_i + j] = scores[u, g, kept_idx[i, j]] for j < counts_i
+    (i = u*Hkv + g).  Rows outside the heads' kept ranges are NaN.
+    Returns float32 [rows]."""
+    sc = np.asarray(scores, dtype=np.float32)
+    U, Hkv, T = sc.shape
+    rscore = np.full(int(rows), np.nan, dtype=np.float32)
+    for i in range(U * Hkv):
+        u, g = divmod(i, Hkv)
+        for j in range(int(counts[i])):
+            rscore[int(start[i]) + j] = sc[u, g, kept_idx[i, j]]
+    return rscore
+
+
+def decode_prune(pools, rscore, start, length, s_new, tau, window, n_sink=0):
+    """Decode-time threshold pruning ([KVzap] §2.3: the `window` most recent
+    tokens are always kept, a token whose score is below tau is dropped, and
+    the pruning runs after attention, in decoding as in prefilling).
+
+    Runs after a decode step appended one token per head (its row is
+    start_i + length_i - 1, length_i already counting it).  Rows of a head
+    are in token order; rows [0, length_i - window) have been judged, the
+    last `window` rows are the window.  Per head i:
+      1. rscore[start_i + length_i - 1] = s_new[i]   (the new token's score);
+      2. e = length_i - window - 1 is the row of the token that just left the
+         window; if e >= n_sink (sinks are never dropped) and the token's
+         score is not >= tau (compared in float32; NaN is dropped), the rows
+         e+1 .. length_i-1 of every pool and of rscore move down by one and
+         length_i shrinks by one.
+    pools: list of arrays indexed by pool row (K and V rows, or their codes
+    and group parameters).  Works on copies; rows at or beyond the new
+    length are unspecified.  Returns (pools, rscore, length int32, dropped
+    bool [n])."""
+    pools = [np.array(p, copy=True) for p in pools]
+    rs = np.array(rscore, dtype=np.float32, copy=True)
+    length = np.array(length, dtype=np.int64, copy=True)
+    n = length.size
+    dropped = np.zeros(n, dtype=bool)
+    tau32 = np.float32(tau)
+    for i in range(n):
+        s0, L = int(start[i]), int(length[i])
+        if L < 1:
+            continue
+        rs[s0 + L - 1] = np.float32(s_new[i])
+        e = L - window - 1
+        if e < n_sink or rs[s0 + e] >= tau32:
+            continue
+        for p in pools:
+            p[s0 + e: s0 + L - 1] = p[s0 + e + 1: s0 + L].copy()
+        rs[s0 + e: s0 + L - 1] = rs[s0 + e + 1: s0 + L].copy()
+        length[i] = L - 1
+        dropped[i] = True
+    return pools, rs, length.astype(np.int32), dropped
+
+
 QGROUP = 32     # elements per quantisation group (one row, consecutive along d)
 
 

@@ -540,3 +540,137 @@ def test_planted_tie_break_mistake_is_caught():
     chosen = {(g, t) for _, g, t in cand[:6]}
     wrong = [[t for t in range(T) if (g, t) in chosen] for g in range(Hkv)]
     assert wrong != c["cases"][1]["kept"]
+
+
+# ------------------------------------- decode-time pruning ([KVzap] §2.3)
+def _prune_stream_matches(prune, tau, seed, steps=40, w=6, n_sink=2, T=40, heads=3, slack=48,
+                          nan_frac=0.05, tie_frac=0.1):
+    """Prefill compaction followed by `steps` decode steps of append + prune.
+    After every step each head's rows must be, in token order, the set the
+    rule defines without reference to rows: the prefill-kept tokens older
+    than the prefill window, the tokens that have left the window since then
+    with score >= tau, and the last w tokens.  The pools carry token ids, so
+    any misplaced row shows; the per-row scores must follow their rows."""
+    rng = np.random.default_rng(seed)
+    S = rng.standard_normal((heads, T + steps)).astype(np.float32)
+    if np.isfinite(tau):
+        S[rng.random(S.shape) < tie_frac] = np.float32(tau)
+    S[rng.random(S.shape) < nan_frac] = np.nan
+    kept = []
+    for i in range(heads):
+        mid = [t for t in range(n_sink, T - w) if rng.random() < 0.4]
+        kept.append(list(range(n_sink)) + mid + list(range(T - w, T)))
+    counts = np.array([len(k) for k in kept])
+    start = np.concatenate([[0], np.cumsum(counts + slack)[:-1]]).astype(np.int64)
+    rows = int((counts + slack).sum())
+    kpool = np.full((rows, 2), -1, dtype=np.int64)      # (token, head)
+    vpool = np.full(rows, -1.0)                         # token + 0.5
+    rscore = np.full(rows, np.nan, dtype=np.float32)
+    for i in range(heads):
+        for j, t in enumerate(kept[i]):
+            kpool[start[i] + j] = (t, i)
+            vpool[start[i] + j] = t + 0.5
+            rscore[start[i] + j] = S[i, t]
+    length = counts.astype(np.int32)
+    for step in range(steps):
+        pos = T + step
+        for i in range(heads):           # the decode step's append
+            kpool[start[i] + length[i]] = (pos, i)
+            vpool[start[i] + length[i]] = pos + 0.5
+        length = length + 1
+        (kpool, vpool), rscore, length, _ = prune([kpool, vpool], rscore, start, length,
+                                                  S[:, pos], tau, w, n_sink)
+        cur = pos + 1
+        for i in range(heads):
+            expect = ([t for t in kept[i] if t < T - w] +
+                      [t for t in range(T - w, cur - w) if S[i, t] >= np.float32(tau)] +
+                      list(range(cur - w, cur)))
+            s0, L = int(start[i]), int(length[i])
+            got = kpool[s0: s0 + L]
+            if L != len(expect) or list(got[:, 0]) != expect or np.any(got[:, 1] != i):
+                return False
+            if np.any(vpool[s0: s0 + L] != got[:, 0] + 0.5):
+                return False
+            if rscore[s0: s0 + L].tobytes() != S[i, got[:, 0]].tobytes():
+                return False
+    return True
+
+
+@pytest.mark.parametrize("tau", [0.0, 0.7, -1.3])
+@pytest.mark.parametrize("seed", [41, 42])
+def test_prune_matches_the_set_definition(tau, seed):
+    assert _prune_stream_matches(O.decode_prune, tau, seed)
+
+
+def test_prune_closed_forms():
+    # tau = -inf, no NaN: nothing is ever dropped; the cache only grows
+    assert _prune_stream_matches(O.decode_prune, -np.inf, 43, nan_frac=0.0)
+    # tau = +inf, finite scores: every token leaving the window goes, so the
+    # length stays at the prefill count after every step
+    pools = [np.arange(30, dtype=np.int64)]
+    length = np.array([12], dtype=np.int32)
+    rs = np.zeros(30, dtype=np.float32)
+    for step in range(10):
+        length = length + 1
+        pools, rs, length, dropped = O.decode_prune(pools, rs, [0], length, [1.0], np.inf, 5, 2)
+        assert length[0] == 12 and dropped[0]
+    # sinks are never dropped: 4 sinks, a window of 2, 3 rows before the append
+    pools, rs2, L2, dropped = O.decode_prune([np.arange(8)], np.full(8, -5.0, np.float32), [0],
+                                             np.array([4], np.int32), [2.5], np.inf, 2, 4)
+    assert L2[0] == 4 and not dropped[0] and rs2[3] == np.float32(2.5)
+    # no row at all: nothing written, nothing dropped
+    _, rs3, L3, d3 = O.decode_prune([np.arange(4)], np.zeros(4, np.float32), [0],
+                                    np.array([0], np.int32), [9.0], 0.0, 2, 0)
+    assert L3[0] == 0 and not d3[0] and not np.any(rs3)
+
+
+def test_gather_scores_brute_force():
+    rng = np.random.default_rng(44)
+    scores = rng.standard_normal((2, 3, 20)).astype(np.float32)
+    kept, counts, offsets = O.select(scores, "per_head", head_budget=np.full(6, 7), n_sink=2,
+                                     n_recent=3)
+    _, _, start, length = O.compact(np.zeros((2, 3, 20, 1)), np.zeros((2, 3, 20, 1)), kept, counts,
+                                    offsets, slack=4)
+    rs = O.gather_scores(scores, kept, counts, start, int(offsets[-1]) + 6 * 4)
+    for u in range(2):
+        for g in range(3):
+            i = u * 3 + g
+            picked = sorted(scores[u, g, t] for t in range(20)
+                            if t < 2 or t >= 17 or t in set(kept[i, :counts[i]].tolist()))
+            assert sorted(rs[start[i]: start[i] + length[i]].tolist()) == picked
+            assert np.all(np.isnan(rs[start[i] + length[i]: start[i] + length[i] + 4]))
+
+
+def _prune_planted(kind):
+    """Planted mistakes in decode-time pruning, each a copy of the rule with
+    one thing wrong."""
+    def prune(pools, rscore, start, length, s_new, tau, window, n_sink=0):
+        pools = [np.array(p, copy=True) for p in pools]
+        rs = np.array(rscore, dtype=np.float32, copy=True)
+        length = np.array(length, dtype=np.int64, copy=True)
+        for i in range(length.size):
+            s0, L = int(start[i]), int(length[i])
+            rs[s0 + L - (0 if kind == "score_row" else 1)] = np.float32(s_new[i])
+            e = L - window - (0 if kind == "exit_row" else 1)
+            s = rs[s0 + e]
+            if kind == "strict":
+                keep = s > np.float32(tau)
+            elif kind == "nan_kept":
+                keep = not (s < np.float32(tau))
+            else:
+                keep = s >= np.float32(tau)
+            if e < n_sink or keep:
+                continue
+            for p in pools:
+                p[s0 + e: s0 + L - 1] = p[s0 + e + 1: s0 + L].copy()
+            if kind != "scores_stay":
+                rs[s0 + e: s0 + L - 1] = rs[s0 + e + 1: s0 + L].copy()
+            length[i] = L - 1
+        return pools, rs, length.astype(np.int32), None
+    return prune
+
+
+@pytest.mark.parametrize("kind", ["score_row", "exit_row", "strict", "nan_kept", "scores_stay"])
+def test_planted_prune_mistakes_are_caught(kind):
+    assert not all(_prune_stream_matches(_prune_planted(kind), tau, seed)
+                   for tau in (0.0, 0.7) for seed in (41, 42))
