@@ -282,7 +282,7 @@ def bench_decode(B, steps, warmup, device):
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
     lens = inputs.head_budgets(w, "cpu")
     kc, vc, start, length = inputs.compressed_pool(w, lens, device)
-    max_len = int(lens.max()) + steps + warmup + 1
+    max_len = int(lens.max()) + steps + warmup + 5    # + 4 steps of the pruned stage split
     ws = torch.empty(B.kvc_decode_workspace(w.U, w.Hq, w.Hkv, w.d, max_len), dtype=torch.uint8,
                      device=device)
     steps_in = [inputs.decode_step_inputs(w, i, device) for i in range(steps + warmup)]
@@ -343,6 +343,62 @@ def bench_decode(B, steps, warmup, device):
     out_d["q8"] = dict(us_per_step=ms8 * 1e3, bytes_per_step=bytes8,
                        kv_tokens_per_s=(mean_rows + n) / (ms8 * 1e-3),
                        gbs=bytes8 / (ms8 * 1e-3) / 1e9, launches_per_step=2)
+    del kq, vq, kp, vp
+    # the same steps with decode-time threshold pruning ([KVzap] §2.3): the new
+    # token is scored by the linear surrogate, attended and appended, then the
+    # token leaving the 128-token window stays iff its score >= tau
+    window, n_sink, tau, Dh = 128, 4, 0.5, 4096
+    kc3, vc3, start3, length3 = inputs.compressed_pool(w, lens, device)
+    rscore = inputs.row_scores(kc3.shape[0], device, seed=61)
+    weight, bias = inputs.decode_surrogate(w, Dh, device)
+    hid = [inputs.decode_hidden(w, Dh, i, device) for i in range(steps + warmup)]
+    s_new = torch.empty((w.U, w.Hkv, 1), device=device)
+
+    def pruned_step(i):
+        q, kn, vn = steps_in[i]
+        B.kvc_score_linear(hid[i], weight, bias, s_new)
+        B.kvc_decode_attn(q, kc3, vc3, start3, length3, out, lse, k_new=kn, v_new=vn,
+                          max_len=max_len, scale=w.scale, workspace=ws)
+        B.kvc_decode_prune([kc3, vc3], rscore, start3, length3, s_new.view(-1), tau, window,
+                           n_sink)
+
+    for i in range(warmup):
+        pruned_step(i)
+    torch.cuda.synchronize()
+    rows_p0 = int(length3.sum().item())
+    e0.record(s)
+    for i in range(warmup, warmup + steps):
+        pruned_step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    msp = e0.elapsed_time(e1) / steps
+    rows_p1 = int(length3.sum().item())
+    # stage times from extra steps with events between the kernels (serialised)
+    hid_x = [inputs.decode_hidden(w, Dh, 10000 + i, device) for i in range(4)]
+    in_x = [inputs.decode_step_inputs(w, 10000 + i, device) for i in range(4)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(4)]
+    for i in range(4):
+        q, kn, vn = in_x[i]
+        ev[i][0].record(s)
+        B.kvc_score_linear(hid_x[i], weight, bias, s_new)
+        ev[i][1].record(s)
+        B.kvc_decode_attn(q, kc3, vc3, start3, length3, out, lse, k_new=kn, v_new=vn,
+                          max_len=max_len, scale=w.scale, workspace=ws)
+        ev[i][2].record(s)
+        B.kvc_decode_prune([kc3, vc3], rscore, start3, length3, s_new.view(-1), tau, window,
+                           n_sink)
+        ev[i][3].record(s)
+    torch.cuda.synchronize()
+    t_lin = statistics.mean(e[0].elapsed_time(e[1]) for e in ev[1:]) * 1e3
+    t_prune = statistics.mean(e[2].elapsed_time(e[3]) for e in ev[1:]) * 1e3
+    mean_rows_p = (rows_p0 + rows_p1) / 2.0
+    out_d["pruned"] = dict(us_per_step=msp * 1e3, window=window, n_sink=n_sink, tau=tau,
+                           surrogate_hidden=Dh, rows_at_timed_start=rows_p0,
+                           rows_at_timed_end=rows_p1,
+                           dropped_fraction=1.0 - (rows_p1 - rows_p0) / (n * steps),
+                           kv_tokens_per_s=(mean_rows_p + n) / (msp * 1e-3),
+                           overhead_us=(msp - ms) * 1e3, launches_per_step=4,
+                           stage_linear_us=t_lin, stage_prune_us=t_prune)
     return out_d
 
 

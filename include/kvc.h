@@ -138,8 +138,11 @@ int kvc_score_attn_agg(const void* q_win, const void* k, int dtype,
  * h_t in R^{Dh} to one score per kv head):
  *   scores[u,g,t] = bias[g] + sum_j hidden[u,t,j] * weight[j,g]
  * hidden [U, T, Dh] dtype; weight [Dh, Hkv] dtype; bias [Hkv] fp32 or NULL;
- * scores [U, Hkv, T] fp32.  Accumulates in fp32.  Requires Dh % 8 == 0 and
- * 1 <= Hkv <= 8.
+ * scores [U, Hkv, T] fp32.  Accumulates in fp32.  Requires Dh % 8 == 0,
+ * 1 <= Hkv <= 8 and a 16-byte aligned hidden.  Many rows stream through a
+ * persistent grid with the weight in shared memory; up to 1024 rows (e.g. the
+ * new token of each sequence in a decode step), or a weight too large for
+ * shared memory, take one CTA per row with the weight read from L2.
  */
 int kvc_score_linear(const void* hidden, const void* weight, const float* bias,
                      int dtype, int U, int T, int Dh, int Hkv,
@@ -280,6 +283,59 @@ int kvc_decode_attn_q8(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* 
                        int dtype, int U, int Hq, int Hkv, int d, int max_len,
                        float scale, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------- decode-time pruning */
+
+/* Most pools one kvc_decode_prune call moves (K and V rows, or the codes and
+ * (scale, lo) pairs of a quantised K and V). */
+#define KVC_PRUNE_MAX_POOLS 4
+
+/*
+ * Per-row scores of a compacted cache, the array kvc_decode_prune reads:
+ * rscore[start[i] + j] = scores[u, g, kept_idx[i, j]] for j < counts[i],
+ * i = u*Hkv + g ([KVzap] §2.3: a token's score decides whether it stays).
+ * scores [U, Hkv, T] fp32 (as kvc_score_attn / kvc_score_linear write them);
+ * kept_idx, counts as kvc_select writes them; start as kvc_compact writes it;
+ * rscore [capacity_rows] fp32 (written at the kept rows only).  An index
+ * outside [0, T) or a row at or beyond capacity_rows is skipped and reported
+ * as KVC_ERR_RANGE in the status word.
+ */
+int kvc_gather_scores(const float* scores, int U, int Hkv, int T, const int32_t* kept_idx,
+                      const int32_t* counts, const int64_t* start, float* rscore,
+                      int64_t capacity_rows, void* stream);
+
+/*
+ * Decode-time threshold pruning ([KVzap] §2.3: the `window` most recent
+ * tokens are always kept, a token whose score is below tau is dropped, and
+ * the pruning runs after attention, in decoding as in prefilling).
+ *
+ * Call it after a decode step that appended one token per head (so len[i]
+ * counts the new row, start[i] + len[i] - 1).  A head's rows are in token
+ * order; rows [0, len - window) have been judged, the last `window` rows are
+ * the window.  Per head i:
+ *   1. rscore[start[i] + len[i] - 1] = s_new[i]  (the new token's score);
+ *   2. e = len[i] - window - 1 is the row of the token that just left the
+ *      window; if e >= n_sink and !(rscore[start[i] + e] >= tau) (fp32; a NaN
+ *      score is dropped), rows e+1 .. len[i]-1 of every pool and of rscore
+ *      move down by one row and len[i] shrinks by one.
+ * Rows at or beyond the new len[i] are left unspecified.
+ *
+ * pools     HOST array of n_pools (1 .. KVC_PRUNE_MAX_POOLS) device pointers,
+ *           16-byte aligned, each indexed by pool row; row_bytes HOST array of
+ *           their row sizes (multiples of 16 bytes): e.g. {kc, vc} with
+ *           {2d, 2d} for bf16 pools, {kq, kp, vq, vp} with {d, d/8, d, d/8}
+ *           for quantised ones
+ * rscore    [capacity_rows] fp32 per-row scores (kvc_gather_scores)
+ * start     [n_heads] int64; len [n_heads] int32 (read, decremented on a drop)
+ * s_new     [n_heads] fp32 scores of the appended tokens (e.g. kvc_score_linear
+ *           on the new hidden states with T = 1)
+ * window >= 1, n_sink >= 0, tau not NaN, capacity_rows = rows of every pool.
+ * A head with start[i] + len[i] > capacity_rows is skipped and reported as
+ * KVC_ERR_RANGE.  No workspace; one CTA per head.
+ */
+int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, float* rscore,
+                     const int64_t* start, int32_t* len, const float* s_new, int n_heads,
+                     int window, int n_sink, float tau, int64_t capacity_rows, void* stream);
 
 /*
  * kvc_decode_attn without a workspace, for callers that cannot allocate

@@ -50,6 +50,9 @@ SIGNATURES = {
     "kvc_quantize_rows": (_I, [_P, _I, _I64, _I, _P, _P, _P]),
     "kvc_decode_attn_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                 _P, _P, _P, _SZ, _P]),
+    "kvc_gather_scores": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P]),
+    "kvc_decode_prune": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_I), _I, _P, _P, _P, _P, _I, _I,
+                              _I, _F, _I64, _P]),
     "kvc_decode_noalloc_scratch_bytes": (_SZ, []),
     "kvc_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                      _P, _P]),
@@ -225,6 +228,31 @@ def kvc_decode_attn_q8(q, kq, kp, vq, vp, start, length, out, lse=None, k_new=No
                                   int(max_len), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(workspace), ws_bytes, _stream(stream))
     _check("kvc_decode_attn_q8", rc)
+
+
+def kvc_gather_scores(scores, kept_idx, counts, start, rscore, stream=None):
+    """scores [U, Hkv, T] fp32 -> rscore[start_i + j] = scores of the kept rows."""
+    U, Hkv, T = scores.shape
+    rc = lib().kvc_gather_scores(_ptr(scores), U, Hkv, T, _ptr(kept_idx), _ptr(counts),
+                                 _ptr(start), _ptr(rscore), int(rscore.numel()), _stream(stream))
+    _check("kvc_gather_scores", rc)
+
+
+def kvc_decode_prune(pools, rscore, start, length, s_new, tau, window, n_sink=0, stream=None):
+    """Decode-time pruning after an appending decode step.  pools: the row-indexed
+    device tensors to move together (e.g. [kc, vc] or [kq, kp, vq, vp]), all with
+    rscore.numel() rows."""
+    n = len(pools)
+    ptrs = (_P * n)(*[_ptr(p) for p in pools])
+    rb = (_I * n)(*[int(p.stride(0) * p.element_size()) for p in pools])
+    rows = int(rscore.numel())
+    for p in pools:
+        if p.shape[0] != rows or not p.is_contiguous():
+            raise ValueError("every pool needs rscore.numel() contiguous rows")
+    rc = lib().kvc_decode_prune(ptrs, rb, n, _ptr(rscore), _ptr(start), _ptr(length),
+                                _ptr(s_new), int(length.numel()), int(window), int(n_sink),
+                                float(tau), rows, _stream(stream))
+    _check("kvc_decode_prune", rc)
 
 
 def kvc_decode_attn_noalloc(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,

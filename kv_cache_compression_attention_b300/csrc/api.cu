@@ -126,7 +126,6 @@ int kvc_score_linear(const void* hidden, const void* weight, const float* bias, 
   if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
   if (U <= 0 || T <= 0 || Dh <= 0 || Hkv <= 0) return KVC_ERR_INVALID;
   if (Dh % 8 || Hkv > 8 || !aligned16(hidden)) return KVC_ERR_UNSUPPORTED;
-  if ((int64_t)Dh * Hkv * 4 > 96 * 1024) return KVC_ERR_UNSUPPORTED;
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
@@ -256,6 +255,39 @@ int kvc_decode_attn_q8(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* 
   return kvc::decode_q8_launch(q, kq, kp, vq, vp, start, len, k_new, v_new, U, Hq, Hkv, max_len,
                                scale, out, lse, static_cast<float*>(workspace), dev,
                                kvc::as_stream(stream));
+}
+
+int kvc_gather_scores(const float* scores, int U, int Hkv, int T, const int32_t* kept_idx,
+                      const int32_t* counts, const int64_t* start, float* rscore,
+                      int64_t capacity_rows, void* stream) {
+  if (!scores || !kept_idx || !counts || !start || !rscore) return KVC_ERR_INVALID;
+  if (U < 0 || Hkv < 0 || T < 0 || capacity_rows < 0) return KVC_ERR_INVALID;
+  if ((int64_t)U * Hkv > 65535) return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::gather_scores_launch(scores, U, Hkv, T, kept_idx, counts, start, rscore,
+                                   capacity_rows, dev, kvc::as_stream(stream));
+}
+
+int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, float* rscore,
+                     const int64_t* start, int32_t* len, const float* s_new, int n_heads,
+                     int window, int n_sink, float tau, int64_t capacity_rows, void* stream) {
+  if (!pools || !row_bytes || !rscore || !start || !len || !s_new) return KVC_ERR_INVALID;
+  if (n_pools < 1 || n_pools > KVC_PRUNE_MAX_POOLS) return KVC_ERR_INVALID;
+  if (n_heads < 0 || window < 1 || n_sink < 0 || capacity_rows < 0 || isnan(tau))
+    return KVC_ERR_INVALID;
+  for (int p = 0; p < n_pools; ++p) {
+    if (!pools[p] || row_bytes[p] <= 0) return KVC_ERR_INVALID;
+    if (row_bytes[p] % 16 || row_bytes[p] > 65536 || !aligned16(pools[p]))
+      return KVC_ERR_UNSUPPORTED;
+  }
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::decode_prune_launch(pools, row_bytes, n_pools, rscore, start, len, s_new, n_heads,
+                                  window, n_sink, tau, capacity_rows, dev,
+                                  kvc::as_stream(stream));
 }
 
 int kvc_fidelity(const void* out_comp, const void* out_full, const float* lse_comp,

@@ -129,6 +129,14 @@ int decode_q8_launch(const void* q, uint8_t* kq, void* kp, uint8_t* vq, void* vp
 int quantize_rows_launch(const void* x, int64_t rows, int d, uint8_t* codes, void* params,
                          const Dev& dev, cudaStream_t s);
 
+int decode_prune_launch(void* const* pools, const int* row_bytes, int n_pools, float* rscore,
+                        const int64_t* start, int32_t* len, const float* s_new, int n_heads,
+                        int window, int n_sink, float tau, int64_t capacity_rows, const Dev& dev,
+                        cudaStream_t s);
+int gather_scores_launch(const float* scores, int U, int Hkv, int T, const int32_t* kept_idx,
+                         const int32_t* counts, const int64_t* start, float* rscore,
+                         int64_t capacity_rows, const Dev& dev, cudaStream_t s);
+
 int fidelity_launch(const void* oc, const void* of, const float* lc, const float* lf,
                     int dtype, int n, int d, float* rel, float* kl, const Dev& dev,
                     cudaStream_t s);

@@ -178,6 +178,69 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Few rows (a decode step scores one new token per sequence), or a weight
+// too large for shared memory: one CTA per hidden row, the weight read from
+// L2 (every CTA reads the same Dh x HK values).  Thread x takes the 16-byte
+// chunks x, x + 128, ... of the row; partial sums are reduced by shuffles
+// and across the four warps in shared memory.
+constexpr int kRowThreads = 128;
+constexpr int64_t kFewRows = 1024;   // up to this many rows: one CTA per row
+
+template <typename Tin, int HK, bool kVecW>
+__global__ void __launch_bounds__(kRowThreads, 4)
+linear_row_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
+                  const float* __restrict__ bias, int T, int Dh, float* __restrict__ scores) {
+  constexpr int E = Vec<Tin>::E;
+  __shared__ float part[kRowThreads / 32][HK];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t row = blockIdx.x;
+  const int NC = Dh / E;
+  const uint4* hrow = reinterpret_cast<const uint4*>(hidden + row * (int64_t)Dh);
+  float acc[HK];
+#pragma unroll
+  for (int g = 0; g < HK; ++g) acc[g] = 0.0f;
+  // chunk c's weights (E rows of HK values) are HK 16-byte words at
+  // weight + c * E * HK, loaded as vectors when the weight is 16-byte aligned
+  const uint4* wvec = reinterpret_cast<const uint4*>(weight);
+  for (int c = threadIdx.x; c < NC; c += kRowThreads) {
+    float x[E];
+    unpack(__ldg(hrow + c), x, Tin());
+    if (kVecW) {
+      float wv[E * HK];
+#pragma unroll
+      for (int k = 0; k < HK; ++k) unpack(__ldg(wvec + (int64_t)c * HK + k), wv + k * E, Tin());
+#pragma unroll
+      for (int jj = 0; jj < E; ++jj)
+#pragma unroll
+        for (int g = 0; g < HK; ++g) acc[g] = fmaf(x[jj], wv[jj * HK + g], acc[g]);
+    } else {
+      const Tin* wrow = weight + (int64_t)c * E * HK;
+#pragma unroll
+      for (int jj = 0; jj < E; ++jj)
+#pragma unroll
+        for (int g = 0; g < HK; ++g) acc[g] = fmaf(x[jj], to_f(__ldg(wrow + jj * HK + g)), acc[g]);
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int g = 0; g < HK; ++g) {
+    float v = acc[g];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) part[warp][g] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < HK) {
+    const int g = threadIdx.x;
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRowThreads / 32; ++w) v += part[w][g];
+    const int64_t u = row / T, t = row - u * T;
+    scores[(u * HK + g) * (int64_t)T + t] = v + (bias ? bias[g] : 0.0f);
+  }
+}
+
 template <typename Tin, int HK>
 size_t smem_bytes(int Dh) {
   const int NC = Dh / Vec<Tin>::E;
@@ -189,7 +252,15 @@ template <typename Tin, int HK>
 int run(const void* hidden, const void* weight, const float* bias, int U, int T, int Dh,
         float* scores, const Dev& dev, cudaStream_t s) {
   const size_t smem = smem_bytes<Tin, HK>(Dh);
-  if ((int)smem > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)U * T;
+  if (rows <= kFewRows || smem > (size_t)dev.max_smem_optin) {
+    if (rows > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+    auto rk = (reinterpret_cast<uintptr_t>(weight) & 15u) ? linear_row_kernel<Tin, HK, false>
+                                                          : linear_row_kernel<Tin, HK, true>;
+    return launch_pdl(rk, dim3((unsigned)rows), dim3(kRowThreads), 0, s,
+                      static_cast<const Tin*>(hidden), static_cast<const Tin*>(weight), bias, T,
+                      Dh, scores);
+  }
   auto kern = linear_kernel<Tin, HK>;
   // raise the kernel's dynamic shared-memory limit when a call needs more
   // than any earlier one on this device
@@ -198,7 +269,6 @@ int run(const void* hidden, const void* weight, const float* bias, int U, int T,
     KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     attr_bytes[dev.device & 63].store((int)smem);
   }
-  const int64_t rows = (int64_t)U * T;
   const int64_t tasks = (rows + kRows - 1) / kRows;
   int64_t blocks = dev.sms;
   const int64_t need = (tasks + kWarps - 1) / kWarps;

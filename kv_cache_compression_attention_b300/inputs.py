@@ -262,6 +262,25 @@ def decode_step_inputs(w: Workload, step: int, device="cpu"):
     return q, kn, vn
 
 
+def decode_surrogate(w: Workload, Dh: int, device="cpu"):
+    """weight [Dh, Hkv] ~ N(0, 1/Dh), bias zeros [Hkv]: the linear surrogate that
+    scores each decode step's new token (outputs ~ N(0, 1), as in linear_scorer)."""
+    g = _gen(device, _seed(w, 15))
+    weight = (_randn((Dh, w.Hkv), g, device) / math.sqrt(Dh)).to(w.torch_dtype)
+    return weight, torch.zeros(w.Hkv, dtype=torch.float32, device=device)
+
+
+def decode_hidden(w: Workload, Dh: int, step: int, device="cpu") -> torch.Tensor:
+    """hidden [U, 1, Dh] ~ N(0,1) of one decode step's new token."""
+    g = _gen(device, _seed(w, 16, extra=step + 1))
+    return _randn((w.U, 1, Dh), g, device).to(w.torch_dtype)
+
+
+def row_scores(rows: int, device="cpu", seed: int = 0) -> torch.Tensor:
+    """Per-row scores ~ N(0,1) float32 [rows] for a ready-made compressed pool."""
+    return _randn((rows,), _gen(device, seed), device)
+
+
 def random_scores(shape, device="cpu", seed: int = 0, ties: bool = False,
                   specials: bool = False) -> torch.Tensor:
     """fp32 score tensors for selection tests.

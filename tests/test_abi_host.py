@@ -173,3 +173,27 @@ def test_quantize_and_q8_decode_reject_bad_arguments(lib):
     assert dq(*bad) == -2
     bad = list(args); bad[19] = 0                             # workspace too small
     assert dq(*bad) == -3
+
+
+def test_prune_and_gather_reject_bad_arguments(lib):
+    def arr(t, *v):
+        return (t * len(v))(*v)
+    pools = arr(ctypes.c_void_p, 16, 32)
+    rb = arr(ctypes.c_int, 256, 256)
+    pr = lib.kvc_decode_prune
+    ok = [pools, rb, 2, P, P, P, P, 8, 16, 4, 0.5, 1000, None]
+    for k, v, want in [(0, None, -1), (2, 0, -1), (2, 5, -1), (3, None, -1), (8, 0, -1),
+                       (9, -1, -1), (10, float("nan"), -1), (11, -1, -1), (7, -1, -1)]:
+        bad = list(ok); bad[k] = v
+        assert pr(*bad) == want, (k, v)
+    bad = list(ok); bad[0] = arr(ctypes.c_void_p, 16, None)
+    assert pr(*bad) == -1                                     # a null pool
+    bad = list(ok); bad[1] = arr(ctypes.c_int, 256, 24)
+    assert pr(*bad) == -2                                     # rows not whole 16-byte vectors
+    bad = list(ok); bad[0] = arr(ctypes.c_void_p, 16, 40)
+    assert pr(*bad) == -2                                     # unaligned pool
+    ga = lib.kvc_gather_scores
+    assert ga(None, 1, 8, 64, P, P, P, P, 100, None) == -1
+    assert ga(P, -1, 8, 64, P, P, P, P, 100, None) == -1
+    assert ga(P, 1, 8, 64, P, P, P, P, -1, None) == -1
+    assert ga(P, 9000, 8, 64, P, P, P, P, 100, None) == -2    # more heads than grid rows

@@ -127,9 +127,13 @@ def test_score_attn_32layer_sampled_units(B):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("Hkv,Dh,T", [(4, 256, 1000), (3, 64, 37), (8, 128, 129)])
-def test_score_linear_small(B, dtype, Hkv, Dh, T):
-    U = 2
+@pytest.mark.parametrize("U,Hkv,Dh,T", [
+    (2, 4, 256, 1000), (2, 8, 128, 1100),     # streaming kernel (weights in shared memory)
+    (2, 3, 64, 37), (2, 8, 128, 129),         # few rows: one CTA per row
+    (64, 8, 4096, 1),                         # a decode step's new tokens, Llama-3-8B hidden size
+    (1, 8, 8192, 1500),                       # weights too large for shared memory, many rows
+])
+def test_score_linear_small(B, dtype, U, Hkv, Dh, T):
     h = rand((U, T, Dh), dtype, 5)
     wt = rand((Dh, Hkv), dtype, 6, scale=Dh ** -0.5)
     bias = rand((Hkv,), torch.float32, 7)
