@@ -31,7 +31,7 @@ struct PrunePools {
   int n;
 };
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 decode_prune_kernel(PrunePools pools, float* __restrict__ rscore,
                     const int64_t* __restrict__ start, int32_t* __restrict__ len,
                     const float* __restrict__ s_new, int window, int n_sink, float tau,
@@ -69,31 +69,36 @@ decode_prune_kernel(PrunePools pools, float* __restrict__ rscore,
   const int64_t total = first[KVC_PRUNE_MAX_POOLS];
   const int nscore = window - 1;
   for (int64_t c0 = 0, f0 = 0; c0 < total || f0 < nscore; c0 += kChunk, f0 += kThreads) {
+    // vector q of the index space -> its address in row e+1+ of its pool
+    auto src_of = [&](int64_t q, int& vpr) {
+      uint4* base = pools.base[0];
+      int64_t q0 = 0;
+      vpr = pools.vpr[0];
+#pragma unroll
+      for (int k = 1; k < KVC_PRUNE_MAX_POOLS; ++k)
+        if (q >= first[k]) { base = pools.base[k]; vpr = pools.vpr[k]; q0 = first[k]; }
+      return base + (s0 + e + 1) * vpr + (q - q0);
+    };
     uint4 r[kVec];
-    uint4* dst[kVec];
 #pragma unroll
     for (int x = 0; x < kVec; ++x) {
       const int64_t q = c0 + x * kThreads + threadIdx.x;
-      dst[x] = nullptr;
-      if (q < total) {
-        uint4* base = pools.base[0];
-        int vpr = pools.vpr[0];
-        int64_t q0 = 0;
-#pragma unroll
-        for (int k = 1; k < KVC_PRUNE_MAX_POOLS; ++k)
-          if (q >= first[k]) { base = pools.base[k]; vpr = pools.vpr[k]; q0 = first[k]; }
-        uint4* src = base + (s0 + e + 1) * vpr + (q - q0);
-        r[x] = *src;
-        dst[x] = src - vpr;
-      }
+      int vpr;
+      if (q < total) r[x] = *src_of(q, vpr);
     }
     const int64_t f = f0 + threadIdx.x;
     float sf = 0.f;
     if (f < nscore) sf = rscore[s0 + e + 1 + f];
     __syncthreads();
 #pragma unroll
-    for (int x = 0; x < kVec; ++x)
-      if (dst[x]) *dst[x] = r[x];
+    for (int x = 0; x < kVec; ++x) {
+      const int64_t q = c0 + x * kThreads + threadIdx.x;
+      int vpr;
+      if (q < total) {
+        uint4* src = src_of(q, vpr);
+        *(src - vpr) = r[x];
+      }
+    }
     if (f < nscore) rscore[s0 + e + f] = sf;
   }
   if (threadIdx.x == 0) {

@@ -181,13 +181,14 @@ linear_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
 // Few rows (a decode step scores one new token per sequence), or a weight
 // too large for shared memory: one CTA per hidden row, the weight read from
 // L2 (every CTA reads the same Dh x HK values).  Thread x takes the 16-byte
-// chunks x, x + 128, ... of the row; partial sums are reduced by shuffles
-// and across the four warps in shared memory.
-constexpr int kRowThreads = 128;
+// chunks x, x + 512, ... of the row (one chunk per thread up to Dh = 4096
+// bf16, so each thread's loads are all in flight at once); partial sums are
+// reduced by shuffles and across the sixteen warps in shared memory.
+constexpr int kRowThreads = 512;
 constexpr int64_t kFewRows = 1024;   // up to this many rows: one CTA per row
 
 template <typename Tin, int HK, bool kVecW>
-__global__ void __launch_bounds__(kRowThreads, 4)
+__global__ void __launch_bounds__(kRowThreads, 1)
 linear_row_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight,
                   const float* __restrict__ bias, int T, int Dh, float* __restrict__ scores) {
   constexpr int E = Vec<Tin>::E;
