@@ -371,6 +371,175 @@ def dequantize_rows(codes, params):
     return (c.reshape(rows, d // QGROUP, QGROUP) * p[..., 0:1] + p[..., 1:2]).reshape(rows, d)
 
 
+# ------------------------------------------- VECTOR three-way routing
+# [VECTOR] "Méthodologie : VECTOR": keys are kept exactly for every token of
+# the candidate pool; values are retained, approximated (dropped and rebuilt
+# as W_OLS k from the stored key) or evicted.  Step 1 widens the base
+# eviction's pool to 1 - p_c + p_a; step 2 scores each pool token by its
+# reconstruction error eps = ||v - W_OLS k||^2; step 3 drops the values of
+# the 2 p_a lowest-error tokens and keeps K and V of the rest.  Synthetic
+# caches carry no rotary encoding, so the inverse rotation before the
+# reconstruction is the identity here.
+
+def fit_ols(k_cal, v_cal):
+    """Offline OLS calibration of the K -> V predictor, one matrix per kv
+    head: W = argmin_W sum_t ||v_t - W k_t||^2 = (sum_t v_t k_t^T)
+    (sum_t k_t k_t^T)^-1 (normal equations).  k_cal, v_cal [Hkv, N, d] with
+    N >= d.  Returns float64 [Hkv, d, d] (row = output dimension)."""
+    kc = np.asarray(k_cal, dtype=F64)
+    vc = np.asarray(v_cal, dtype=F64)
+    Hkv, N, d = kc.shape
+    W = np.zeros((Hkv, d, d), dtype=F64)
+    for g in range(Hkv):
+        gram = kc[g].T @ kc[g]             # sum_t k_t k_t^T
+        cross = vc[g].T @ kc[g]            # sum_t v_t k_t^T
+        W[g] = np.linalg.solve(gram.T, cross.T).T
+    return W
+
+
+def vector_budgets(p_c, p_a, Hkv, T, n_sink, n_recent):
+    """Integer budgets of one unit: the pool B_pool = floor((1 - p_c + p_a)
+    Hkv T) (raised to the protected set, as in global selection) and the
+    approximated count A = floor(2 p_a Hkv T), capped at the pool's
+    non-protected tokens (protected tokens keep exact values).  Returns
+    (pool keep ratio, B_pool_eff, A)."""
+    nP = int(protected_mask(T, n_sink, n_recent).sum())
+    ratio = (1.0 - float(p_c)) + float(p_a)
+    B = global_budget(ratio, Hkv, T)
+    B_eff = min(max(B, Hkv * nP), Hkv * T)
+    A = min(global_budget(2.0 * float(p_a), Hkv, T), B_eff - Hkv * nP)
+    return ratio, B_eff, A
+
+
+def vector_residual(k, v, W, kept_idx, counts, n_sink, n_recent):
+    """Step 2: reconstruction error of every pool token, as a selection key
+    per pool position.  For head i = u*Hkv + g and pool position j < counts_i
+    holding token t = kept_idx[i, j]:
+        eps = sum_x (v[u,g,t,x] - sum_y W[g,x,y] k[u,g,t,y])^2
+    key[u, g, j] = -eps (float32) for tokens that may be approximated; NaN for
+    protected tokens (sinks, recent window: their values stay exact) and for
+    positions j >= counts_i.  Returns float32 [U, Hkv, T]."""
+    kk = np.asarray(k, dtype=F64)
+    vv = np.asarray(v, dtype=F64)
+    Wm = np.asarray(W, dtype=F64)
+    U, Hkv, T, d = kk.shape
+    P = protected_mask(T, n_sink, n_recent)
+    key = np.full((U, Hkv, T), np.nan, dtype=np.float32)
+    for u in range(U):
+        for g in range(Hkv):
+            i = u * Hkv + g
+            for j in range(int(counts[i])):
+                t = int(kept_idx[i, j])
+                if P[t]:
+                    continue
+                r = vv[u, g, t] - Wm[g] @ kk[u, g, t]
+                key[u, g, j] = np.float32(-(r @ r))
+    return key
+
+
+def vector_approx(key, A):
+    """Step 3's choice, per unit: the A pool positions with the lowest
+    error, i.e. the highest key, ranked across the unit's heads by (key desc,
+    position asc, head asc); NaN keys are never chosen.  Returns (approx_pos
+    int32 [U*Hkv, T] padded with -1, ascending per head; counts int32)."""
+    kf = np.asarray(key, dtype=np.float32)
+    U, Hkv, T = kf.shape
+    pos = np.full((U * Hkv, T), -1, dtype=np.int32)
+    cnt = np.zeros(U * Hkv, dtype=np.int32)
+    for u in range(U):
+        cand = [(-float(kf[u, g, j]), j, g) for g in range(Hkv) for j in range(T)
+                if not np.isnan(kf[u, g, j])]
+        cand.sort()
+        chosen = [[] for _ in range(Hkv)]
+        for _, j, g in cand[:A]:
+            chosen[g].append(j)
+        for g in range(Hkv):
+            js = sorted(chosen[g])
+            pos[u * Hkv + g, :len(js)] = js
+            cnt[u * Hkv + g] = len(js)
+    return pos, cnt
+
+
+def vector_compact(k, v, kept_idx, counts, approx_pos, approx_counts, slack=0):
+    """Step 3's asymmetric truncation as a cache layout.  Head i keeps the K
+    rows of all counts_i pool tokens, the approximated ones first:
+      kc rows [kstart_i, kstart_i + counts_i + slack): the napprox_i tokens
+        at the chosen pool positions (ascending), then the exact tokens
+        (ascending);
+      vc rows [vstart_i, vstart_i + nexact_i + slack): the exact tokens' V.
+    kstart_i = sum_{h<i} (counts_h + slack), vstart_i = sum_{h<i} (nexact_h +
+    slack).  Byte-exact copies.  Returns (kc, vc, kstart int64, klen int32,
+    vstart int64, napprox int32)."""
+    k = np.asarray(k)
+    v = np.asarray(v)
+    U, Hkv, T, d = k.shape
+    n = U * Hkv
+    napprox = np.asarray(approx_counts, dtype=np.int32).copy()
+    nexact = np.asarray(counts, dtype=np.int64) - napprox
+    kstart = np.zeros(n, dtype=np.int64)
+    vstart = np.zeros(n, dtype=np.int64)
+    for i in range(1, n):
+        kstart[i] = kstart[i - 1] + int(counts[i - 1]) + slack
+        vstart[i] = vstart[i - 1] + int(nexact[i - 1]) + slack
+    kc = np.zeros((int(kstart[-1] + counts[n - 1] + slack) if n else 0, d), dtype=k.dtype)
+    vc = np.zeros((int(vstart[-1] + nexact[n - 1] + slack) if n else 0, d), dtype=v.dtype)
+    for i in range(n):
+        u, g = divmod(i, Hkv)
+        apos = set(int(j) for j in approx_pos[i, :napprox[i]])
+        approx_t = [int(kept_idx[i, j]) for j in range(int(counts[i])) if j in apos]
+        exact_t = [int(kept_idx[i, j]) for j in range(int(counts[i])) if j not in apos]
+        for r, t in enumerate(approx_t + exact_t):
+            kc[kstart[i] + r] = k[u, g, t]
+        for r, t in enumerate(exact_t):
+            vc[vstart[i] + r] = v[u, g, t]
+    return kc, vc, kstart, np.asarray(counts, dtype=np.int32).copy(), vstart, napprox
+
+
+def decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox, W, k_new=None, v_new=None,
+                       scale=1.0):
+    """One decode step over a VECTOR cache.  Head i = u*Hkv + g holds klen_i
+    keys at kc[kstart_i:]; the value of row j is the reconstruction
+    W[g] @ kc[kstart_i + j] for j < napprox_i and vc[vstart_i + j - napprox_i]
+    otherwise.  k_new / v_new [U, Hkv, d], if given, are appended as an exact
+    row (kc row kstart_i + klen_i, vc row vstart_i + klen_i - napprox_i) and
+    klen_i grows by one.  Then, as in decode_attn, lse = log sum_j exp(s_j),
+    o = sum_j softmax_j * value_j with s_j = scale <q, k_j>.  Works on copies;
+    returns (out float64 [U, Hq, d], lse float64 [U, Hq], kc, vc, klen)."""
+    qq = np.asarray(q, dtype=F64)
+    Wm = np.asarray(W, dtype=F64)
+    kc = np.array(kc, copy=True)
+    vc = np.array(vc, copy=True)
+    klen = np.array(klen, dtype=np.int64, copy=True)
+    U, Hq, d = qq.shape
+    Hkv = klen.size // U
+    G = Hq // Hkv
+    out = np.zeros((U, Hq, d), dtype=F64)
+    lse = np.zeros((U, Hq), dtype=F64)
+    for u in range(U):
+        for g in range(Hkv):
+            i = u * Hkv + g
+            ks, vs, na = int(kstart[i]), int(vstart[i]), int(napprox[i])
+            if k_new is not None:
+                kc[ks + klen[i]] = np.asarray(k_new)[u, g]
+                vc[vs + klen[i] - na] = np.asarray(v_new)[u, g]
+                klen[i] += 1
+            L = int(klen[i])
+            K = kc[ks: ks + L].astype(F64)
+            V = np.concatenate([K[:na] @ Wm[g].T, vc[vs: vs + L - na].astype(F64)])
+            for j in range(G):
+                h = g * G + j
+                if L == 0:
+                    lse[u, h] = -np.inf
+                    continue
+                logits = scale * (K @ qq[u, h])
+                m = logits.max()
+                e = np.exp(logits - m)
+                l = e.sum()
+                lse[u, h] = m + math.log(l)
+                out[u, h] = (e / l) @ V
+    return out, lse, kc, vc, klen.astype(np.int32)
+
+
 def fidelity(out_comp, out_full, lse_comp, lse_full):
     """Fidelity probe of a compressed cache against the full one.
 

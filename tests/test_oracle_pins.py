@@ -674,3 +674,164 @@ def _prune_planted(kind):
 def test_planted_prune_mistakes_are_caught(kind):
     assert not all(_prune_stream_matches(_prune_planted(kind), tau, seed)
                    for tau in (0.0, 0.7) for seed in (41, 42))
+
+
+# --------------------------------------------- VECTOR three-way routing
+def _lowrank_kv(rng, Hkv, N, d, r, noise):
+    """K and V as linear maps of one shared low-rank state plus noise."""
+    h = rng.standard_normal((Hkv, N, r))
+    Ak = rng.standard_normal((Hkv, d, r))
+    Av = rng.standard_normal((Hkv, d, r))
+    k = np.einsum("gnr,gdr->gnd", h, Ak) + noise * rng.standard_normal((Hkv, N, d))
+    v = np.einsum("gnr,gdr->gnd", h, Av) + noise * rng.standard_normal((Hkv, N, d))
+    return k, v
+
+
+def test_fit_ols_closed_form_and_lstsq():
+    rng = np.random.default_rng(71)
+    # exact linear relation v = A k: the fit returns A
+    k = rng.standard_normal((2, 40, 6))
+    A = rng.standard_normal((2, 6, 6))
+    v = np.einsum("gxy,gny->gnx", A, k)
+    np.testing.assert_allclose(O.fit_ols(k, v), A, rtol=0, atol=1e-9)
+    # noisy: residuals orthogonal to the keys, and equal to an SVD least squares
+    k, v = _lowrank_kv(rng, 2, 200, 8, 3, 0.3)
+    W = O.fit_ols(k, v)
+    for g in range(2):
+        res = v[g] - k[g] @ W[g].T
+        np.testing.assert_allclose(res.T @ k[g], 0.0, atol=1e-8)
+        sol = np.linalg.lstsq(k[g], v[g], rcond=None)[0]      # k @ sol ~ v
+        np.testing.assert_allclose(W[g], sol.T, rtol=1e-9, atol=1e-9)
+
+
+def test_vector_budgets_memory_accounting():
+    # K rows for the pool plus V rows for the exact tokens = 2 (1 - p_c) pairs
+    for p_c, p_a, Hkv, T in [(0.9, 0.05, 8, 32768), (0.75, 0.1, 4, 1000), (0.5, 0.2, 2, 777)]:
+        _, B, A = O.vector_budgets(p_c, p_a, Hkv, T, 4, 64)
+        assert abs((B + (B - A)) - 2 * (1 - p_c) * Hkv * T) <= 2
+    # the approximated count never reaches into the protected set
+    _, B, A = O.vector_budgets(0.5, 0.45, 2, 100, 4, 16)
+    assert B - A == 2 * 20
+
+
+def _vector_case(seed, U=2, Hkv=3, T=40, d=6):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((U, Hkv, T, d))
+    v = rng.standard_normal((U, Hkv, T, d))
+    W = rng.standard_normal((Hkv, d, d))                      # not symmetric
+    scores = rng.standard_normal((U, Hkv, T)).astype(np.float32)
+    kept, counts, offsets = O.select(scores, "global", keep_ratio=0.5, n_sink=2, n_recent=3)
+    return k, v, W, kept, counts
+
+
+def test_vector_residual_brute_force():
+    k, v, W, kept, counts = _vector_case(72)
+    key = O.vector_residual(k, v, W, kept, counts, 2, 3)
+    U, Hkv, T, d = k.shape
+    for u in range(U):
+        for g in range(Hkv):
+            i = u * Hkv + g
+            for j in range(T):
+                if j >= counts[i]:
+                    assert np.isnan(key[u, g, j])
+                    continue
+                t = kept[i, j]
+                if t < 2 or t >= T - 3:
+                    assert np.isnan(key[u, g, j])
+                    continue
+                eps = 0.0
+                for x in range(d):
+                    rec = sum(W[g, x, y] * k[u, g, t, y] for y in range(d))
+                    eps += (v[u, g, t, x] - rec) ** 2
+                assert key[u, g, j] == np.float32(-eps)
+    # v = W k exactly: every error is zero
+    v2 = np.einsum("gxy,ugty->ugtx", W, k)
+    key2 = O.vector_residual(k, v2, W, kept, counts, 2, 3)
+    ok = ~np.isnan(key2)
+    assert ok.sum() > 0 and np.all(np.abs(key2[ok]) < 1e-9)
+
+
+def test_vector_approx_and_compact_invariants():
+    k, v, W, kept, counts = _vector_case(73)
+    key = O.vector_residual(k, v, W, kept, counts, 2, 3)
+    U, Hkv, T, d = k.shape
+    A = 15
+    pos, cnt = O.vector_approx(key, A)
+    for u in range(U):
+        heads = range(u * Hkv, (u + 1) * Hkv)
+        assert sum(cnt[i] for i in heads) == A
+        # every chosen error is <= every eligible unchosen error of the unit
+        chosen = [float(-key[u, i - u * Hkv, j]) for i in heads for j in pos[i, :cnt[i]]]
+        rest = [float(-key[u, g, j]) for g in range(Hkv) for j in range(T)
+                if not np.isnan(key[u, g, j]) and j not in set(pos[u * Hkv + g, :cnt[u * Hkv + g]])]
+        assert max(chosen) <= min(rest)
+    kc, vc, kstart, klen, vstart, napprox = O.vector_compact(k, v, kept, counts, pos, cnt, slack=2)
+    for i in range(U * Hkv):
+        u, g = divmod(i, Hkv)
+        pool = [int(t) for t in kept[i, :counts[i]]]
+        approx_t = [pool[j] for j in pos[i, :cnt[i]]]
+        exact_t = [t for t in pool if t not in approx_t]
+        assert klen[i] == len(pool) and napprox[i] == len(approx_t)
+        np.testing.assert_array_equal(kc[kstart[i]: kstart[i] + napprox[i]], k[u, g, approx_t])
+        np.testing.assert_array_equal(kc[kstart[i] + napprox[i]: kstart[i] + klen[i]], k[u, g, exact_t])
+        np.testing.assert_array_equal(vc[vstart[i]: vstart[i] + len(exact_t)], v[u, g, exact_t])
+        # protected tokens keep exact values
+        assert all(t >= 2 and t < T - 3 for t in approx_t)
+
+
+def test_decode_attn_vector_against_sdpa_and_special_cases():
+    k, v, W, kept, counts = _vector_case(74)
+    U, Hkv, T, d = k.shape
+    key = O.vector_residual(k, v, W, kept, counts, 2, 3)
+    pos, cnt = O.vector_approx(key, 12)
+    kc, vc, kstart, klen, vstart, napprox = O.vector_compact(k, v, kept, counts, pos, cnt, slack=1)
+    rng = np.random.default_rng(75)
+    G = 2
+    q = rng.standard_normal((U, Hkv * G, d))
+    kn = rng.standard_normal((U, Hkv, d))
+    vn = rng.standard_normal((U, Hkv, d))
+    out, lse, _, _, klen2 = O.decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox, W,
+                                                 kn, vn, 0.4)
+    np.testing.assert_array_equal(klen2, klen + 1)
+    for i in range(U * Hkv):
+        u, g = divmod(i, Hkv)
+        pool = [int(t) for t in kept[i, :counts[i]]]
+        approx_t = set(pool[j] for j in pos[i, :cnt[i]])
+        K = np.concatenate([k[u, g, pool], kn[u, g][None]])
+        V = np.concatenate([np.stack([W[g] @ k[u, g, t] if t in approx_t else v[u, g, t]
+                                      for t in pool]), vn[u, g][None]])
+        for j in range(G):
+            h = g * G + j
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q[u, h][None, None, None]), torch.from_numpy(K[None, None]),
+                torch.from_numpy(V[None, None]), scale=0.4)[0, 0, 0].numpy()
+            np.testing.assert_allclose(out[u, h], ref, rtol=1e-10, atol=1e-12)
+            logits = 0.4 * (K @ q[u, h])
+            assert abs(lse[u, h] - (logits.max() + np.log(np.exp(logits - logits.max()).sum()))) < 1e-12
+    # no approximated rows: the plain decode over the same rows
+    z = np.zeros_like(napprox)
+    kc0, vc0, ks0, kl0, vs0, _ = O.vector_compact(k, v, kept, counts, pos, z, slack=1)
+    o1, l1, _, _, _ = O.decode_attn_vector(q, kc0, vc0, ks0, kl0, vs0, z, W, None, None, 0.4)
+    o2, l2, _, _, _ = O.decode_attn(q, kc0, vc0, ks0, kl0, None, None, 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-12)
+
+
+def test_planted_vector_mistakes_are_caught():
+    k, v, W, kept, counts = _vector_case(76)
+    key = O.vector_residual(k, v, W, kept, counts, 2, 3)
+    # transposed predictor: the errors change
+    keyT = O.vector_residual(k, v, np.transpose(W, (0, 2, 1)), kept, counts, 2, 3)
+    ok = ~np.isnan(key)
+    assert not np.allclose(key[ok], keyT[ok])
+    # approximating the highest-error tokens instead of the lowest picks others
+    pos, cnt = O.vector_approx(key, 10)
+    pos_bad, cnt_bad = O.vector_approx(-key, 10)
+    assert any(set(pos[i, :cnt[i]]) != set(pos_bad[i, :cnt_bad[i]]) for i in range(len(cnt)))
+    # reconstructing with W^T in the decode changes the outputs
+    kc, vc, kstart, klen, vstart, napprox = O.vector_compact(k, v, kept, counts, pos, cnt)
+    q = np.random.default_rng(77).standard_normal((2, 3, 6))
+    o1, _, _, _, _ = O.decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox, W)
+    o2, _, _, _, _ = O.decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox,
+                                          np.transpose(W, (0, 2, 1)))
+    assert not np.allclose(o1, o2)
