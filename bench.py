@@ -402,6 +402,123 @@ def bench_decode(B, steps, warmup, device):
     return out_d
 
 
+def bench_vector(B, w, steps, warmup, device):
+    """VECTOR three-way routing on the 32k layer (p_c = 0.9, p_a = 0.05): score ->
+    pool select (1 - p_c + p_a, global top-k) -> reconstruction-error keys ->
+    select of the 2 p_a lowest-error tokens -> K-for-all / V-for-exact
+    compaction, timed as one step (L2 flushed before each) and stage by stage;
+    then decode steps over batch-64 VECTOR caches (two thirds of every pool
+    approximated) against the plain decode of the same pool lengths."""
+    p_c, p_a = 0.9, 0.05
+    L = LayerWorkload(B, w, device)
+    W = inputs.vector_predictor(w, device)
+    v = inputs.vector_values(w, L.k, W, device)
+    n = L.n
+    nP = w.n_sink + w.n_recent
+    ratio = (1.0 - p_c) + p_a
+    Bpool = max(math.floor(ratio * w.Hkv * w.T), w.Hkv * nP)
+    A = min(math.floor(2.0 * p_a * w.Hkv * w.T), Bpool - w.Hkv * nP)
+    key = torch.empty((w.U, w.Hkv, w.T), device=device)
+    apos = torch.empty((n, w.T), dtype=torch.int32, device=device)
+    acnt = torch.empty(n, dtype=torch.int32, device=device)
+    aoff = torch.empty(n + 1, dtype=torch.int64, device=device)
+    kc = torch.empty((Bpool * w.U + n * w.slack, w.d), dtype=L.k.dtype, device=device)
+    vc = torch.empty(((Bpool - A) * w.U + n * w.slack, w.d), dtype=L.k.dtype, device=device)
+    ks = torch.empty(n, dtype=torch.int64, device=device)
+    kl = torch.empty(n, dtype=torch.int32, device=device)
+    vs = torch.empty(n, dtype=torch.int64, device=device)
+    na = torch.empty(n, dtype=torch.int32, device=device)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream()
+
+    def stages():
+        yield lambda: L.score()
+        yield lambda: B.kvc_select(L.scores, "global", L.kept, L.counts, L.offs, keep_ratio=ratio,
+                                   n_sink=w.n_sink, n_recent=w.n_recent)
+        yield lambda: B.kvc_vector_residual(L.k, v, W, L.kept, L.counts, key, w.n_sink,
+                                            w.n_recent)
+        yield lambda: B.kvc_select(key, "global", apos, acnt, aoff,
+                                   keep_ratio=(A + 0.5) / (w.Hkv * w.T))
+        yield lambda: B.kvc_vector_compact(L.k, v, L.kept, L.counts, L.offs, apos, acnt, aoff,
+                                           kc, vc, ks, kl, vs, na, slack=w.slack)
+
+    for _ in range(warmup):
+        flush_l2(flush)
+        for f in stages():
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush)
+        ev[i][0].record(s)
+        for f in stages():
+            f()
+        ev[i][1].record(s)
+    torch.cuda.synchronize()
+    t_step = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush)
+        evs[i][0].record(s)
+        for x, f in enumerate(stages()):
+            f()
+            evs[i][x + 1].record(s)
+    torch.cuda.synchronize()
+    st = [statistics.mean(e[x].elapsed_time(e[x + 1]) for e in evs) * 1e3 for x in range(5)]
+    pool_rows = int(L.offs[-1].item())
+    eligible = pool_rows - n * nP
+    res_bytes = eligible * 2 * w.d * 2 + n * w.T * 4            # K and V rows read, keys written
+    res_flops = eligible * 2.0 * w.d * w.d
+    comp_bytes = pool_rows * (2 * w.d * 2 + 4) + (pool_rows - w.U * A) * 2 * w.d * 2
+    out = dict(workload=w.name, p_c=p_c, p_a=p_a, pool_rows=pool_rows, approximated=w.U * A,
+               step_us=t_step, kv_tokens_per_s=w.U * w.T / (t_step * 1e-6),
+               stages_us=dict(score=st[0], select_pool=st[1], residual=st[2],
+                              select_approx=st[3], compact=st[4]),
+               residual_gbs=res_bytes / (st[2] * 1e-6) / 1e9,
+               residual_tflops=res_flops / (st[2] * 1e-6) / 1e12,
+               compact_gbs=comp_bytes / (st[4] * 1e-6) / 1e9,
+               cache_rows_k=int(kl.sum()), cache_rows_v=int((kl - na).sum()))
+    del L, v, kc, vc
+    torch.cuda.empty_cache()
+    # decode over batch-64 VECTOR caches
+    wd = inputs.WORKLOADS[DECODE_WORKLOAD]
+    lens = inputs.head_budgets(wd, "cpu")
+    nap = (lens.to(torch.int64) * 2 // 3).to(torch.int32)
+    dkc, dvc, dks, dkl, dvs, dna = inputs.vector_pool(wd, lens, nap, device)
+    Wd = inputs.vector_predictor(wd, device)
+    dsteps = max(16, steps)
+    max_len = int(lens.max()) + dsteps + warmup + 1
+    ws = torch.empty(B.kvc_decode_vector_workspace(wd.U, wd.Hq, wd.Hkv, wd.d, max_len),
+                     dtype=torch.uint8, device=device)
+    steps_in = [inputs.decode_step_inputs(wd, i, device) for i in range(dsteps + warmup)]
+    o = torch.empty((wd.U, wd.Hq, wd.d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((wd.U, wd.Hq), device=device)
+    for i in range(warmup):
+        q, kn, vn = steps_in[i]
+        B.kvc_decode_attn_vector(q, dkc, dvc, dks, dkl, dvs, dna, Wd, o, lse, k_new=kn,
+                                 v_new=vn, max_len=max_len, scale=wd.scale, workspace=ws)
+    torch.cuda.synchronize()
+    rows_k0 = int(dkl.sum())
+    rows_a = int(dna.sum())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(warmup, warmup + dsteps):
+        q, kn, vn = steps_in[i]
+        B.kvc_decode_attn_vector(q, dkc, dvc, dks, dkl, dvs, dna, Wd, o, lse, k_new=kn,
+                                 v_new=vn, max_len=max_len, scale=wd.scale, workspace=ws)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / dsteps
+    nh = wd.U * wd.Hkv
+    mean_k = rows_k0 + nh * (dsteps - 1) / 2.0
+    bytes_step = (mean_k + (mean_k - rows_a)) * wd.d * 2          # K rows + exact V rows
+    out["decode"] = dict(workload=DECODE_WORKLOAD, approximated_fraction=rows_a / rows_k0,
+                         us_per_step=ms * 1e3, bytes_per_step=bytes_step,
+                         kv_tokens_per_s=(mean_k + nh) / (ms * 1e-3),
+                         gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2)
+    return out
+
+
 def compact_bytes(rows, d, elt):
     """Algorithmic bytes of one compaction: every kept K and V row read once
     and written once, plus its int32 source index."""
@@ -663,7 +780,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "decode", "c4", "c3"], default=None,
+    ap.add_argument("--only", choices=["layer", "decode", "c4", "c3", "vector"], default=None,
                     help="profiling runs: time only one workload")
     args = ap.parse_args()
     world, rank, local = dist_setup(args.gpus)
@@ -713,6 +830,12 @@ def main():
         return
     if args.only == "c3":
         print(json.dumps(bench_c3(B, args.steps, args.warmup, device)))
+        return
+    if args.only == "vector":
+        vec = bench_vector(B, w, args.steps, args.warmup, device)
+        vec["residual_frac"] = vec["residual_gbs"] / hbm
+        vec["decode"]["frac"] = vec["decode"]["gbs"] / hbm
+        print(json.dumps(vec))
         return
 
     # ---- timed region: exactly K steps of the layer pass

@@ -337,6 +337,79 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                      const int64_t* start, int32_t* len, const float* s_new, int n_heads,
                      int window, int n_sink, float tau, int64_t capacity_rows, void* stream);
 
+/* ------------------------------------------------ VECTOR three-way routing */
+
+/*
+ * VECTOR ("A Simple Plug-in for Improving Eviction-Based KV Cache
+ * Compression", Méthodologie : VECTOR): the base eviction selects a widened
+ * pool of 1 - p_c + p_a of the tokens (kvc_select, e.g. global top-k); every
+ * pool token keeps its key; the 2 p_a pool tokens whose values an offline OLS
+ * predictor W rebuilds best from their keys (v ~ W k) drop their values; the
+ * rest keep K and V.  W is [Hkv, d, d] bf16, row = output dimension.  The
+ * pages rotate keys back before the reconstruction (RoPE); caches without a
+ * rotary encoding need no rotation, which is what these calls assume.
+ *
+ * Step 2, the reconstruction error as a selection key: for pool position
+ * j < counts[i] of head i = u*Hkv + g holding token t = kept_idx[i, j],
+ *   key[u, g, j] = -sum_x (v[u,g,t,x] - sum_y W[g,x,y] k[u,g,t,y])^2
+ * (fp32 accumulation of bf16 products), and key = NaN for protected tokens
+ * (t < n_sink or t >= T - n_recent: their values stay exact) and for
+ * positions j >= counts[i].  A global top-k of `key` (kvc_select, mode
+ * KVC_SEL_GLOBAL_TOPK, no protection, a budget of at most the non-protected
+ * pool tokens) then picks the lowest-error positions of each unit, in
+ * (error asc, position asc, head asc) order.
+ * k, v [U, Hkv, T, d] bf16, d = 128, 16-byte aligned; W as above; key
+ * [U, Hkv, T] fp32 (written in full).
+ */
+int kvc_vector_residual(const void* k, const void* v, const void* W, int dtype, int U, int Hkv,
+                        int T, int d, const int32_t* kept_idx, const int32_t* counts,
+                        int n_sink, int n_recent, float* key, void* stream);
+
+/*
+ * Step 3 as a cache layout.  Head i keeps the K rows of all counts[i] pool
+ * tokens and the V rows of the exact ones:
+ *   kc rows [kstart_i, kstart_i + counts_i + slack): the approximated tokens
+ *     (pool positions approx_pos[i, 0..approx_counts[i]), ascending) first,
+ *     then the exact tokens in pool order;
+ *   vc rows [vstart_i, vstart_i + counts_i - approx_counts_i + slack): the
+ *     exact tokens' values;
+ *   kstart_i = offsets[i] + i*slack, vstart_i = offsets[i] - approx_offsets[i]
+ *   + i*slack; klen[i] = counts[i]; napprox[i] = approx_counts[i].
+ * kept_idx / counts / offsets: the pool (kvc_select); approx_pos /
+ * approx_counts / approx_offsets: the global top-k of the residual keys
+ * (kvc_select on kvc_vector_residual's output).  Byte copies; a row beyond
+ * kc_rows / vc_rows or an index out of range is skipped and reported as
+ * KVC_ERR_RANGE.  bf16, d = 128, 16-byte aligned pools.
+ */
+int kvc_vector_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, int d,
+                       const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
+                       const int32_t* approx_pos, const int32_t* approx_counts,
+                       const int64_t* approx_offsets, int slack_per_head, void* kc,
+                       int64_t kc_rows, void* vc, int64_t vc_rows, int64_t* kstart,
+                       int32_t* klen, int64_t* vstart, int32_t* napprox, void* stream);
+
+/* Bytes of workspace kvc_decode_attn_vector needs when no head holds more
+ * than max_len keys (counting the appended one). */
+size_t kvc_decode_vector_workspace(int U, int Hq, int Hkv, int d, int max_len);
+
+/*
+ * One decode step over a VECTOR cache.  Head i holds klen[i] keys at
+ * kc[kstart[i]..]; the value of key row j is W[g] kc[kstart[i] + j] for
+ * j < napprox[i] (rebuilt) and vc[vstart[i] + j - napprox[i]] otherwise.  If
+ * k_new / v_new are given they are appended as an exact row (kc row
+ * kstart[i] + klen[i], vc row vstart[i] + klen[i] - napprox[i]) and klen[i]
+ * grows by one.  Output and log-sum-exp as kvc_decode_attn.  The rebuilt
+ * values are never formed row by row: the approximated rows' attention
+ * weights are applied to their keys, and W[g] once per query head to that
+ * sum (the same result up to rounding order).  bf16, d = 128,
+ * Hq / Hkv <= 8, 16-byte aligned q, kc, vc and W.
+ */
+int kvc_decode_attn_vector(const void* q, void* kc, void* vc, const int64_t* kstart,
+                           int32_t* klen, const int64_t* vstart, const int32_t* napprox,
+                           const void* W, const void* k_new, const void* v_new, int dtype, int U,
+                           int Hq, int Hkv, int d, int max_len, float scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * kvc_decode_attn without a workspace, for callers that cannot allocate
  * device memory (a plug-in inside a host engine that owns every allocation

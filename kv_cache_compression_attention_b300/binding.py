@@ -50,6 +50,12 @@ SIGNATURES = {
     "kvc_quantize_rows": (_I, [_P, _I, _I64, _I, _P, _P, _P]),
     "kvc_decode_attn_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                 _P, _P, _P, _SZ, _P]),
+    "kvc_vector_residual": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "kvc_vector_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I64,
+                                _P, _I64, _P, _P, _P, _P, _P]),
+    "kvc_decode_vector_workspace": (_SZ, [_I, _I, _I, _I, _I]),
+    "kvc_decode_attn_vector": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                    _I, _F, _P, _P, _P, _SZ, _P]),
     "kvc_gather_scores": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P]),
     "kvc_decode_prune": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_I), _I, _P, _P, _P, _P, _I, _I,
                               _I, _F, _I64, _P]),
@@ -180,6 +186,10 @@ def kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype=KVC_BF16) -> int:
     return lib().kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype)
 
 
+def kvc_decode_vector_workspace(U, Hq, Hkv, d, max_len) -> int:
+    return lib().kvc_decode_vector_workspace(U, Hq, Hkv, d, max_len)
+
+
 def kvc_decode_attn(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,
                     max_len=None, scale=None, workspace=None, stream=None):
     U, Hq, d = q.shape
@@ -228,6 +238,54 @@ def kvc_decode_attn_q8(q, kq, kp, vq, vp, start, length, out, lse=None, k_new=No
                                   int(max_len), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(workspace), ws_bytes, _stream(stream))
     _check("kvc_decode_attn_q8", rc)
+
+
+def kvc_vector_residual(k, v, W, kept_idx, counts, key, n_sink=0, n_recent=0, stream=None):
+    """VECTOR step 2: key[u, g, j] = -||v - W k||^2 of pool position j (NaN if
+    protected or empty).  k, v [U, Hkv, T, d] bf16; W [Hkv, d, d] bf16."""
+    U, Hkv, T, d = k.shape
+    rc = lib().kvc_vector_residual(_ptr(k), _ptr(v), _ptr(W), _dtype(k), U, Hkv, T, d,
+                                   _ptr(kept_idx), _ptr(counts), int(n_sink), int(n_recent),
+                                   _ptr(key), _stream(stream))
+    _check("kvc_vector_residual", rc)
+
+
+def kvc_vector_compact(k, v, kept_idx, counts, offsets, approx_pos, approx_counts,
+                       approx_offsets, kc, vc, kstart, klen, vstart, napprox, slack=0,
+                       stream=None):
+    """VECTOR step 3: K rows of every pool token (approximated first), V rows of
+    the exact ones."""
+    U, Hkv, T, d = k.shape
+    rc = lib().kvc_vector_compact(_ptr(k), _ptr(v), _dtype(k), U, Hkv, T, d, _ptr(kept_idx),
+                                  _ptr(counts), _ptr(offsets), _ptr(approx_pos),
+                                  _ptr(approx_counts), _ptr(approx_offsets), int(slack),
+                                  _ptr(kc), int(kc.shape[0]), _ptr(vc), int(vc.shape[0]),
+                                  _ptr(kstart), _ptr(klen), _ptr(vstart), _ptr(napprox),
+                                  _stream(stream))
+    _check("kvc_vector_compact", rc)
+
+
+def kvc_decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox, W, out, lse=None,
+                           k_new=None, v_new=None, max_len=None, scale=None, workspace=None,
+                           stream=None):
+    """One decode step over a VECTOR cache (values of the first napprox rows of
+    each head rebuilt as W k)."""
+    U, Hq, d = q.shape
+    Hkv = kstart.numel() // U
+    if max_len is None:
+        raise ValueError("max_len is required (upper bound of any head's length)")
+    if scale is None:
+        scale = d ** -0.5
+    need = lib().kvc_decode_vector_workspace(U, Hq, Hkv, d, int(max_len))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_decode_attn_vector(_ptr(q), _ptr(kc), _ptr(vc), _ptr(kstart), _ptr(klen),
+                                      _ptr(vstart), _ptr(napprox), _ptr(W), _ptr(k_new),
+                                      _ptr(v_new), _dtype(q), U, Hq, Hkv, d, int(max_len),
+                                      float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                      ws_bytes, _stream(stream))
+    _check("kvc_decode_attn_vector", rc)
 
 
 def kvc_gather_scores(scores, kept_idx, counts, start, rscore, stream=None):

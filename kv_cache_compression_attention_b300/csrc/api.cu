@@ -290,6 +290,77 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                                   kvc::as_stream(stream));
 }
 
+int kvc_vector_residual(const void* k, const void* v, const void* W, int dtype, int U, int Hkv,
+                        int T, int d, const int32_t* kept_idx, const int32_t* counts,
+                        int n_sink, int n_recent, float* key, void* stream) {
+  if (!k || !v || !W || !kept_idx || !counts || !key) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U < 0 || Hkv <= 0 || T < 0 || d <= 0 || n_sink < 0 || n_recent < 0) return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || d != 128) return KVC_ERR_UNSUPPORTED;
+  if ((int64_t)U * Hkv > 65535 || !aligned16(k) || !aligned16(v) || !aligned16(W))
+    return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::vector_residual_launch(k, v, W, U, Hkv, T, kept_idx, counts, n_sink, n_recent, key,
+                                     dev, kvc::as_stream(stream));
+}
+
+int kvc_vector_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, int d,
+                       const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
+                       const int32_t* approx_pos, const int32_t* approx_counts,
+                       const int64_t* approx_offsets, int slack_per_head, void* kc,
+                       int64_t kc_rows, void* vc, int64_t vc_rows, int64_t* kstart,
+                       int32_t* klen, int64_t* vstart, int32_t* napprox, void* stream) {
+  if (!k || !v || !kept_idx || !counts || !offsets || !approx_pos || !approx_counts ||
+      !approx_offsets || !kc || !vc || !kstart || !klen || !vstart || !napprox)
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U < 0 || Hkv <= 0 || T < 0 || d <= 0 || slack_per_head < 0 || kc_rows < 0 || vc_rows < 0)
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || d != 128) return KVC_ERR_UNSUPPORTED;
+  if ((int64_t)U * Hkv > 65535 || !aligned16(k) || !aligned16(v) || !aligned16(kc) ||
+      !aligned16(vc))
+    return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::vector_compact_launch(k, v, U, Hkv, T, kept_idx, counts, offsets, approx_pos,
+                                    approx_counts, approx_offsets, slack_per_head, kc, kc_rows,
+                                    vc, vc_rows, kstart, klen, vstart, napprox, dev,
+                                    kvc::as_stream(stream));
+}
+
+size_t kvc_decode_vector_workspace(int U, int Hq, int Hkv, int d, int max_len) {
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || max_len < 0) return 0;
+  return kvc::decode_vector_ws_bytes(U, Hq, Hkv, d, max_len);
+}
+
+int kvc_decode_attn_vector(const void* q, void* kc, void* vc, const int64_t* kstart,
+                           int32_t* klen, const int64_t* vstart, const int32_t* napprox,
+                           const void* W, const void* k_new, const void* v_new, int dtype, int U,
+                           int Hq, int Hkv, int d, int max_len, float scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !kc || !vc || !kstart || !klen || !vstart || !napprox || !W || !out)
+    return KVC_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_len < 0 || !isfinite(scale))
+    return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || d != 128) return KVC_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8 || (int64_t)U * Hkv > 65535) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(W))
+    return KVC_ERR_UNSUPPORTED;
+  size_t need = kvc::decode_vector_ws_bytes(U, Hq, Hkv, d, max_len);
+  if (workspace_bytes < need || (need && !workspace)) return KVC_ERR_WORKSPACE;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::decode_vector_launch(q, kc, vc, kstart, klen, vstart, napprox, W, k_new, v_new, U,
+                                   Hq, Hkv, max_len, scale, out, lse,
+                                   static_cast<float*>(workspace), dev, kvc::as_stream(stream));
+}
+
 int kvc_fidelity(const void* out_comp, const void* out_full, const float* lse_comp,
                  const float* lse_full, int dtype, int n, int d, float* rel_err, float* kl,
                  void* stream) {

@@ -26,6 +26,7 @@
 #include <atomic>
 
 #include "kvc_internal.cuh"
+#include "mma_sync.cuh"
 
 namespace kvc {
 namespace {
@@ -492,6 +493,116 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
   }
 }
 
+// Merge for a VECTOR cache: the chunks of the approximated rows hold
+// sum_j p_j k_j (their K tile stood in for V), the others sum_j p_j v_j.  With
+// both under one maximum and one normaliser, the output is
+//   o = (sum_exact p_j v_j + W_g (sum_approx p_j k_j)) / l,
+// i.e. every approximated value W_g k_j is rebuilt by one d x d product per
+// query head instead of one per row (the reconstruction is linear).  The new
+// token is appended as an exact row.
+template <int D, int G>
+__global__ void __launch_bounds__(D)
+decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restrict__ kc,
+                             uint16_t* __restrict__ vc, const int64_t* __restrict__ kstart,
+                             int32_t* __restrict__ klen, const int64_t* __restrict__ vstart,
+                             const int32_t* __restrict__ napprox, const uint16_t* __restrict__ W,
+                             const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+                             int n_heads, int Hkv, int max_chunks, float scale_log2,
+                             const float* __restrict__ ws, uint16_t* __restrict__ out,
+                             float* __restrict__ lse, int* status) {
+  __shared__ float red[D / 32][G];
+  __shared__ float ak_sm[G][D];
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int u = i / Hkv, g = i - u * Hkv;
+  const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
+  const int L = klen[i];
+  int na = napprox[i];
+  if (na < 0 || na > L) { if (x == 0) report(status, KVC_ERR_RANGE); na = na < 0 ? 0 : L; }
+  const int ne = L - na;
+  const int cha = (na + kChunk - 1) / kChunk;
+  int nch = cha + (ne + kChunk - 1) / kChunk;
+  if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
+  const bool append = k_new != nullptr;
+  bool room = append;
+  if (append && i + 1 < n_heads &&
+      (kstart[i] + L >= kstart[i + 1] || vstart[i] + ne >= vstart[i + 1])) {
+    if (x == 0) report(status, KVC_ERR_RANGE);
+    room = false;
+  }
+  const int64_t nrow = (int64_t)u * Hkv + g;
+  const float kn = append ? Elt<uint16_t>::get(k_new + nrow * D, x) : 0.0f;
+  const float vn = append ? Elt<uint16_t>::get(v_new + nrow * D, x) : 0.0f;
+  float snew[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float a = append ? Elt<uint16_t>::get(q + (nrow * G + h) * D, x) * kn : 0.0f;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (lane == 0) red[warp][h] = a;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) a += red[w][h];
+    snew[h] = a * scale_log2;
+  }
+  const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
+  float av[G], M[G], lsum[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float m = append ? snew[h] : -INFINITY;
+    for (int c = 0; c < nch; ++c) m = fmaxf(m, base[(int64_t)(c * G + h) * (D + 2) + D]);
+    float a = 0.0f, ak = 0.0f, ls = 0.0f;
+    for (int c = 0; c < nch; ++c) {
+      const float* pc = base + (int64_t)(c * G + h) * (D + 2);
+      const float mc = pc[D];
+      const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - m);
+      if (c < cha) ak += pc[x] * f; else a += pc[x] * f;
+      ls += pc[D + 1] * f;
+    }
+    if (append) {
+      const float f = exp2f(snew[h] - m);
+      a += vn * f;
+      ls += f;
+    }
+    ak_sm[h][x] = ak;
+    av[h] = a;
+    M[h] = m;
+    lsum[h] = ls;
+  }
+  __syncthreads();
+  // out dimension x: sum_y W[g][x][y] * ak[h][y], the row read as 16-byte words
+  float rec[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) rec[h] = 0.0f;
+  const uint4* wrow = reinterpret_cast<const uint4*>(W + ((int64_t)g * D + x) * D);
+  for (int ch = 0; ch < D / 8; ++ch) {
+    const uint4 w4 = __ldg(wrow + ch);
+    const float wf[8] = {bf16lo(w4.x), bf16hi(w4.x), bf16lo(w4.y), bf16hi(w4.y),
+                         bf16lo(w4.z), bf16hi(w4.z), bf16lo(w4.w), bf16hi(w4.w)};
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rec[h] = fmaf(wf[e], ak_sm[h][ch * 8 + e], rec[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int64_t orow = nrow * G + h;
+    Elt<uint16_t>::put(out + orow * D, x, lsum[h] > 0.0f ? (av[h] + rec[h]) / lsum[h] : 0.0f);
+    if (lse && x == 0) lse[orow] = lsum[h] > 0.0f ? (M[h] + log2f(lsum[h])) * kLn2 : -INFINITY;
+  }
+  __syncthreads();                      // every thread has read klen[i] and the pool
+  if (room) {
+    kc[(kstart[i] + L) * D + x] = k_new[nrow * D + x];
+    vc[(vstart[i] + ne) * D + x] = v_new[nrow * D + x];
+    if (x == 0) klen[i] = L + 1;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // bf16 partial kernel on the tensor cores.  Per row of the cache the G query
 // heads need G * d multiply-adds for q.k and again for p.v; done on the SIMT
@@ -505,44 +616,7 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
 // ldmatrix conflict-free.
 namespace mma {
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// D = A (16x16 bf16, row) . B (16x8 bf16, col) + C, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
+using namespace ::kvc::mmasync;
 
 constexpr int kRows = 64;      // rows per stage (16 per warp)
 constexpr int kStg = 3;
@@ -606,7 +680,8 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
                           const void* __restrict__ vc, const uint32_t* __restrict__ kp,
                           const uint32_t* __restrict__ vp, const int64_t* __restrict__ start,
                           const int32_t* __restrict__ len, int Hkv, int max_chunks,
-                          float scale_log2, float* __restrict__ ws) {
+                          float scale_log2, float* __restrict__ ws,
+                          const int64_t* __restrict__ vstart, const int32_t* __restrict__ napprox) {
   static_assert(G <= 8, "query heads per kv head");
   constexpr int RS = D + 8;                  // padded row stride (elements)
   constexpr int CPR = D * 2 / 16;            // 16-byte chunks per row
@@ -621,13 +696,31 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
 
   const int i = blockIdx.y, c = blockIdx.x;
   const int L = len[i];
-  const int rb = c * kChunk;
-  if (rb >= L) return;
-  const int nrows = min(L, rb + kChunk) - rb;
+  // the chunk's rows: c * kChunk.. of the head, or (a VECTOR cache, napprox
+  // set) the chunks of the napprox approximated rows first, whose values are
+  // rebuilt from their keys later (the K tile stands in for the V tile), then
+  // the chunks of the exact rows, whose values start at vstart[i]
+  int rb = c * kChunk, seg = L;
+  int64_t row0 = start[i] + rb, vrow0 = row0;
+  bool k_as_v = false;
+  if (napprox != nullptr) {
+    const int na = napprox[i];
+    const int cha = (na + kChunk - 1) / kChunk;
+    if (c < cha) {
+      seg = na;
+      k_as_v = true;
+    } else {
+      rb = (c - cha) * kChunk;
+      seg = L - na;
+      row0 = start[i] + na + rb;
+      vrow0 = vstart[i] + rb;
+    }
+  }
+  if (rb >= seg) return;
+  const int nrows = min(seg, rb + kChunk) - rb;
   const int nst = (nrows + mma::kRows - 1) / mma::kRows;
   const int u = i / Hkv, g = i - u * Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t row0 = start[i] + rb;
   const uint32_t sbase = smem_u32(smem_m);
   constexpr uint32_t kTileBytes = (uint32_t)mma::tile_bytes<D, kQ8>();
   constexpr uint32_t kRawBytes = (uint32_t)mma::raw_stage_bytes<D>();
@@ -659,7 +752,7 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
       }
     } else {
       const uint16_t* kb = static_cast<const uint16_t*>(kc) + row0 * D;
-      const uint16_t* vb = static_cast<const uint16_t*>(vc) + row0 * D;
+      const uint16_t* vb = static_cast<const uint16_t*>(vc) + vrow0 * D;
       const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
       const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
       for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
@@ -668,7 +761,7 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
         const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
         const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
         mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
-        mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+        if (!k_as_v) mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
       }
     }
   };
@@ -739,7 +832,7 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
       vs = sbase + (uint32_t)(mma::kRows * RS) * 2u;
     } else {
       ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-      vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+      vs = k_as_v ? ks : ks + (uint32_t)(mma::kRows * RS) * 2u;
     }
     const int wr = warp * 16;                     // this warp's 16 rows of the stage
     // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
@@ -859,7 +952,8 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
                                   static_cast<const uint16_t*>(q), (const void*)qz.kq,
                                   (const void*)qz.vq, (const uint32_t*)qz.kp,
                                   (const uint32_t*)qz.vp, start, (const int32_t*)len, Hkv,
-                                  max_chunks, sl2, ws))
+                                  max_chunks, sl2, ws, (const int64_t*)nullptr,
+                                  (const int32_t*)nullptr))
             return rc;
         } else {
           return KVC_ERR_UNSUPPORTED;
@@ -875,7 +969,8 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
         if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
                                 static_cast<const uint16_t*>(q), (const void*)kc, (const void*)vc,
                                 (const uint32_t*)nullptr, (const uint32_t*)nullptr, start,
-                                (const int32_t*)len, Hkv, max_chunks, sl2, ws))
+                                (const int32_t*)len, Hkv, max_chunks, sl2, ws,
+                                (const int64_t*)nullptr, (const int32_t*)nullptr))
           return rc;
       }
     } else {
@@ -915,7 +1010,60 @@ int dispatch_g(int G, const void* q, void* kc, void* vc, const QPool& qz, const 
   return KVC_ERR_UNSUPPORTED;
 }
 
+template <int G>
+int run_vector(const void* q, void* kc, void* vc, const int64_t* kstart, int32_t* klen,
+               const int64_t* vstart, const int32_t* napprox, const void* W, const void* k_new,
+               const void* v_new, int U, int Hkv, int max_len, float scale, void* out,
+               float* lse, float* ws, const Dev& dev, cudaStream_t s) {
+  constexpr int D = 128;
+  const int n = U * Hkv;
+  // approximated and exact rows are chunked apart: one chunk more at most
+  const int max_chunks = (max_len + kChunk - 1) / kChunk + 1;
+  const float sl2 = scale * kLog2e;
+  const size_t smem = mma::smem_bytes<D>();
+  auto kern = decode_partial_mma_kernel<D, G, false>;
+  static std::atomic<uint32_t> attr_done{0};            // one bit per device
+  const uint32_t bit = 1u << (dev.device & 31);
+  if (!(attr_done.load() & bit)) {
+    KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr_done.fetch_or(bit);
+  }
+  if (int rc = prefer_max_shared(kern, dev.device)) return rc;
+  if (int rc = launch_pdl(kern, dim3((unsigned)max_chunks, (unsigned)n), dim3(kWarps * 32), smem,
+                          s, static_cast<const uint16_t*>(q), (const void*)kc, (const void*)vc,
+                          (const uint32_t*)nullptr, (const uint32_t*)nullptr, kstart,
+                          (const int32_t*)klen, Hkv, max_chunks, sl2, ws, vstart, napprox))
+    return rc;
+  auto comb = decode_combine_vector_kernel<D, G>;
+  if (int rc = prefer_max_shared(comb, dev.device)) return rc;
+  return launch_pdl(comb, dim3((unsigned)n), dim3(D), 0, s, static_cast<const uint16_t*>(q),
+                    static_cast<uint16_t*>(kc), static_cast<uint16_t*>(vc), kstart, klen, vstart,
+                    napprox, static_cast<const uint16_t*>(W),
+                    static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new), n,
+                    Hkv, max_chunks, sl2, (const float*)ws, static_cast<uint16_t*>(out), lse,
+                    dev.status);
+}
+
 }  // namespace
+
+size_t decode_vector_ws_bytes(int U, int Hq, int Hkv, int d, int max_len) {
+  const int64_t chunks = (max_len + kChunk - 1) / kChunk + 1;
+  return (size_t)U * Hkv * chunks * (Hq / Hkv) * (d + 2) * sizeof(float);
+}
+
+int decode_vector_launch(const void* q, void* kc, void* vc, const int64_t* kstart,
+                         int32_t* klen, const int64_t* vstart, const int32_t* napprox,
+                         const void* W, const void* k_new, const void* v_new, int U, int Hq,
+                         int Hkv, int max_len, float scale, void* out, float* lse, float* ws,
+                         const Dev& dev, cudaStream_t s) {
+  switch (Hq / Hkv) {
+#define KVC_G(GG) \
+    case GG: return run_vector<GG>(q, kc, vc, kstart, klen, vstart, napprox, W, k_new, v_new, U, Hkv, max_len, scale, out, lse, ws, dev, s);
+    KVC_G(1) KVC_G(2) KVC_G(3) KVC_G(4) KVC_G(5) KVC_G(6) KVC_G(7) KVC_G(8)
+#undef KVC_G
+  }
+  return KVC_ERR_UNSUPPORTED;
+}
 
 size_t decode_ws_bytes(int U, int Hq, int Hkv, int d, int max_len) {
   const int64_t chunks = (max_len + kChunk - 1) / kChunk;

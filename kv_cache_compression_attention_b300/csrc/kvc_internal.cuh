@@ -137,6 +137,23 @@ int gather_scores_launch(const float* scores, int U, int Hkv, int T, const int32
                          const int32_t* counts, const int64_t* start, float* rscore,
                          int64_t capacity_rows, const Dev& dev, cudaStream_t s);
 
+int vector_residual_launch(const void* k, const void* v, const void* W, int U, int Hkv, int T,
+                           const int32_t* kept_idx, const int32_t* counts, int n_sink,
+                           int n_recent, float* key, const Dev& dev, cudaStream_t s);
+int vector_compact_launch(const void* k, const void* v, int U, int Hkv, int T,
+                          const int32_t* kept_idx, const int32_t* counts,
+                          const int64_t* offsets, const int32_t* approx_pos,
+                          const int32_t* approx_counts, const int64_t* approx_offsets, int slack,
+                          void* kc, int64_t kc_rows, void* vc, int64_t vc_rows, int64_t* kstart,
+                          int32_t* klen, int64_t* vstart, int32_t* napprox, const Dev& dev,
+                          cudaStream_t s);
+size_t decode_vector_ws_bytes(int U, int Hq, int Hkv, int d, int max_len);
+int decode_vector_launch(const void* q, void* kc, void* vc, const int64_t* kstart,
+                         int32_t* klen, const int64_t* vstart, const int32_t* napprox,
+                         const void* W, const void* k_new, const void* v_new, int U, int Hq,
+                         int Hkv, int max_len, float scale, void* out, float* lse, float* ws,
+                         const Dev& dev, cudaStream_t s);
+
 int fidelity_launch(const void* oc, const void* of, const float* lc, const float* lf,
                     int dtype, int n, int d, float* rel, float* kl, const Dev& dev,
                     cudaStream_t s);

@@ -281,6 +281,51 @@ def row_scores(rows: int, device="cpu", seed: int = 0) -> torch.Tensor:
     return _randn((rows,), _gen(device, seed), device)
 
 
+def vector_predictor(w: Workload, device="cpu") -> torch.Tensor:
+    """The K -> V predictor of the VECTOR workloads, W [Hkv, d, d] bf16 with
+    entries ~ N(0, 1/d) (row = output dimension), so W k has the scale of k."""
+    g = _gen(device, _seed(w, 17))
+    return (_randn((w.Hkv, w.d, w.d), g, device) / math.sqrt(w.d)).to(torch.bfloat16)
+
+
+def vector_values(w: Workload, k: torch.Tensor, W: torch.Tensor, device="cpu") -> torch.Tensor:
+    """Values that K predicts linearly, as when K and V are two projections of
+    one hidden state: v_t = W_g k_t + sigma_t * N(0, I) with sigma_t ~ U[0, 1]
+    per (unit, kv head, token), so tokens differ in how well v is rebuilt from
+    k.  Returns bf16 [U, Hkv, T, d]."""
+    gs = _gen(device, _seed(w, 18))
+    gn = _gen(device, _seed(w, 19))
+    sigma = torch.rand((w.U, w.Hkv, w.T, 1), generator=gs, device=device)
+    out = torch.empty((w.U, w.Hkv, w.T, w.d), dtype=torch.bfloat16, device=device)
+    for u in range(w.U):
+        pred = torch.einsum("gty,gxy->gtx", k[u].float(), W.float())
+        noise = _randn((w.Hkv, w.T, w.d), gn, device)
+        out[u] = (pred + sigma[u] * noise).to(torch.bfloat16)
+    return out
+
+
+def vector_pool(w: Workload, lengths: torch.Tensor, napprox: torch.Tensor, device="cpu"):
+    """A ready-made VECTOR cache: head i holds lengths_i key rows (the first
+    napprox_i of them approximated) and lengths_i - napprox_i value rows, rows
+    ~ N(0,1), w.slack free rows per head in each pool for appends.
+    Returns (kc, vc, kstart int64, klen int32, vstart int64, napprox int32)."""
+    lens = lengths.to(torch.int64).cpu()
+    na = napprox.to(torch.int64).cpu()
+    n = lens.numel()
+    kcap, vcap = lens + w.slack, lens - na + w.slack
+    kstart = torch.zeros(n, dtype=torch.int64)
+    vstart = torch.zeros(n, dtype=torch.int64)
+    if n > 1:
+        kstart[1:] = torch.cumsum(kcap, 0)[:-1]
+        vstart[1:] = torch.cumsum(vcap, 0)[:-1]
+    gk = _gen(device, _seed(w, 20))
+    gv = _gen(device, _seed(w, 21))
+    kc = _randn((int(kcap.sum()), w.d), gk, device).to(w.torch_dtype)
+    vc = _randn((int(vcap.sum()), w.d), gv, device).to(w.torch_dtype)
+    return (kc, vc, kstart.to(device), lens.to(torch.int32).to(device), vstart.to(device),
+            na.to(torch.int32).to(device))
+
+
 def random_scores(shape, device="cpu", seed: int = 0, ties: bool = False,
                   specials: bool = False) -> torch.Tensor:
     """fp32 score tensors for selection tests.

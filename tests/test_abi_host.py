@@ -197,3 +197,36 @@ def test_prune_and_gather_reject_bad_arguments(lib):
     assert ga(P, -1, 8, 64, P, P, P, P, 100, None) == -1
     assert ga(P, 1, 8, 64, P, P, P, P, -1, None) == -1
     assert ga(P, 9000, 8, 64, P, P, P, P, 100, None) == -2    # more heads than grid rows
+
+
+def test_vector_entry_points_reject_bad_arguments(lib):
+    r = lib.kvc_vector_residual
+    ok = [P, P, P, 1, 1, 8, 64, 128, P, P, 4, 16, P, None]
+    assert r(*ok[:0], None, *ok[1:]) == -1                      # no K
+    for k, v, want in [(3, 7, -1), (5, 0, -1), (10, -1, -1), (7, 64, -2), (3, 0, -2)]:
+        bad = list(ok); bad[k] = v
+        assert r(*bad) == want, (k, v)
+    bad = list(ok); bad[2] = ctypes.c_void_p(24)
+    assert r(*bad) == -2                                        # unaligned W
+    c = lib.kvc_vector_compact
+    okc = [P, P, 1, 1, 8, 64, 128, P, P, P, P, P, P, 0, P, 100, P, 100, P, P, P, P, None]
+    bad = list(okc); bad[9] = None
+    assert c(*bad) == -1                                        # no approximated positions
+    bad = list(okc); bad[13] = -1
+    assert c(*bad) == -1                                        # negative slack
+    bad = list(okc); bad[6] = 64
+    assert c(*bad) == -2                                        # d
+    d = lib.kvc_decode_attn_vector
+    okd = [P, P, P, P, P, P, P, P, None, None, 1, 1, 8, 2, 128, 64, 0.1, P, P, P, 1 << 20, None]
+    bad = list(okd); bad[7] = None
+    assert d(*bad) == -1                                        # no predictor
+    bad = list(okd); bad[8] = P
+    assert d(*bad) == -1                                        # k_new without v_new
+    bad = list(okd); bad[14] = 64
+    assert d(*bad) == -2
+    bad = list(okd); bad[20] = 0
+    assert d(*bad) == -3                                        # workspace too small
+    # one more split-K chunk than the plain decode: approximated and exact rows
+    # are chunked apart
+    assert lib.kvc_decode_vector_workspace(64, 32, 8, 128, 10086) == \
+        64 * 8 * (20 + 1) * 4 * 130 * 4
