@@ -521,7 +521,7 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
   int na = napprox[i];
   if (na < 0 || na > L) { if (x == 0) report(status, KVC_ERR_RANGE); na = na < 0 ? 0 : L; }
   const int ne = L - na;
-  const int cha = (na + kChunk - 1) / kChunk;
+  const int cha = (na + 2 * kChunk - 1) / (2 * kChunk);    // chunks of 1024 approximated rows
   int nch = cha + (ne + kChunk - 1) / kChunk;
   if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
   const bool append = k_new != nullptr;
@@ -704,9 +704,14 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
   int64_t row0 = start[i] + rb, vrow0 = row0;
   bool k_as_v = false;
   if (napprox != nullptr) {
+    // approximated rows stream K only: twice the rows per chunk and per stage
+    // (the stage's V tile holds the next 64 keys), the same bytes as a chunk
+    // of exact rows
     const int na = napprox[i];
-    const int cha = (na + kChunk - 1) / kChunk;
+    const int cha = (na + 2 * kChunk - 1) / (2 * kChunk);
     if (c < cha) {
+      rb = c * 2 * kChunk;
+      row0 = start[i] + rb;
       seg = na;
       k_as_v = true;
     } else {
@@ -717,8 +722,9 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
     }
   }
   if (rb >= seg) return;
-  const int nrows = min(seg, rb + kChunk) - rb;
-  const int nst = (nrows + mma::kRows - 1) / mma::kRows;
+  const int SR = k_as_v ? 2 * mma::kRows : mma::kRows;      // rows per stage
+  const int nrows = min(seg, rb + (k_as_v ? 2 * kChunk : kChunk)) - rb;
+  const int nst = (nrows + SR - 1) / SR;
   const int u = i / Hkv, g = i - u * Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sbase = smem_u32(smem_m);
@@ -755,13 +761,24 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
       const uint16_t* vb = static_cast<const uint16_t*>(vc) + vrow0 * D;
       const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
       const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
-      for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
-        const int r = x / CPR, ch = x - r * CPR;
-        const bool ok = r0 + r < nrows;
-        const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
-        const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
-        mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
-        if (!k_as_v) mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+      if (k_as_v) {
+        // 128 keys: rows 64..127 land in the V tile, which follows the K tile
+        const int r0k = st * 2 * mma::kRows;
+        for (int x = tid; x < 2 * mma::kRows * CPR; x += kWarps * 32) {
+          const int r = x / CPR, ch = x - r * CPR;
+          const bool ok = r0k + r < nrows;
+          const size_t off = (size_t)(ok ? r0k + r : 0) * D + ch * 8;
+          mma::cp_async16(ks + (uint32_t)(r * RS + ch * 8) * 2u, kb + off, ok ? 16u : 0u);
+        }
+      } else {
+        for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
+          const int r = x / CPR, ch = x - r * CPR;
+          const bool ok = r0 + r < nrows;
+          const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
+          const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
+          mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
+          mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
+        }
       }
     }
   };
@@ -832,55 +849,64 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
       vs = sbase + (uint32_t)(mma::kRows * RS) * 2u;
     } else {
       ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-      vs = k_as_v ? ks : ks + (uint32_t)(mma::kRows * RS) * 2u;
+      vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
     }
-    const int wr = warp * 16;                     // this warp's 16 rows of the stage
-    // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
-    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const int j = lane >> 3, r = lane & 7;
-      const uint32_t rowaddr = ks + (uint32_t)((wr + (j >> 1) * 8 + r) * RS + (j & 1) * 8) * 2u;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t b[4];
-        mma::ldsm_x4(rowaddr + kk * 32u, b);
-        mma::mma_bf16(s0, qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
-        mma::mma_bf16(s1, qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+    auto tile_step = [&](uint32_t ks, uint32_t vs, int base) {
+      const int wr = warp * 16;                     // this warp's 16 rows of the stage
+      // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int j = lane >> 3, r = lane & 7;
+        const uint32_t rowaddr = ks + (uint32_t)((wr + (j >> 1) * 8 + r) * RS + (j & 1) * 8) * 2u;
+  #pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t b[4];
+          mma::ldsm_x4(rowaddr + kk * 32u, b);
+          mma::mma_bf16(s0, qa[kk][0], 0u, qa[kk][1], 0u, b[0], b[1]);
+          mma::mma_bf16(s1, qa[kk][0], 0u, qa[kk][1], 0u, b[2], b[3]);
+        }
       }
-    }
-    // ---- online softmax in base 2 over the 16 tokens (row = head lane / 4)
-    const int tcol = (lane & 3) * 2;
-    const int base_row = st * mma::kRows + wr;
-    float x0 = (base_row + tcol < nrows) ? s0[0] * scale_log2 : -INFINITY;
-    float x1 = (base_row + tcol + 1 < nrows) ? s0[1] * scale_log2 : -INFINITY;
-    float x2 = (base_row + 8 + tcol < nrows) ? s1[0] * scale_log2 : -INFINITY;
-    float x3 = (base_row + 8 + tcol + 1 < nrows) ? s1[1] * scale_log2 : -INFINITY;
-    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float mn = fmaxf(m, mx);
-    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-    if (mn != -INFINITY) {
-      const float alpha = mma::ex2(m - mn);        // m = -inf -> 0
-      l *= alpha;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) { o[nt][0] *= alpha; o[nt][1] *= alpha; }
-      p0 = mma::ex2(x0 - mn); p1 = mma::ex2(x1 - mn); p2 = mma::ex2(x2 - mn); p3 = mma::ex2(x3 - mn);
-      l += (p0 + p1) + (p2 + p3);
-      m = mn;
-    }
-    // ---- O += P . V: P (heads x 16 tokens) is the A operand
-    const uint32_t pa0 = mma::pack_bf16(p0, p1), pa2 = mma::pack_bf16(p2, p3);
-    {
-      const int j = lane >> 3, r = lane & 7;
-      const uint32_t rowaddr = vs + (uint32_t)((wr + (j & 1) * 8 + r) * RS + (j >> 1) * 8) * 2u;
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        uint32_t b[4];
-        mma::ldsm_x4_t(rowaddr + dn * 32u, b);
-        mma::mma_bf16(o[2 * dn], pa0, 0u, pa2, 0u, b[0], b[1]);
-        mma::mma_bf16(o[2 * dn + 1], pa0, 0u, pa2, 0u, b[2], b[3]);
+      // ---- online softmax in base 2 over the 16 tokens (row = head lane / 4)
+      const int tcol = (lane & 3) * 2;
+      const int base_row = base + wr;
+      float x0 = (base_row + tcol < nrows) ? s0[0] * scale_log2 : -INFINITY;
+      float x1 = (base_row + tcol + 1 < nrows) ? s0[1] * scale_log2 : -INFINITY;
+      float x2 = (base_row + 8 + tcol < nrows) ? s1[0] * scale_log2 : -INFINITY;
+      float x3 = (base_row + 8 + tcol + 1 < nrows) ? s1[1] * scale_log2 : -INFINITY;
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m, mx);
+      float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+      if (mn != -INFINITY) {
+        const float alpha = mma::ex2(m - mn);        // m = -inf -> 0
+        l *= alpha;
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt) { o[nt][0] *= alpha; o[nt][1] *= alpha; }
+        p0 = mma::ex2(x0 - mn); p1 = mma::ex2(x1 - mn); p2 = mma::ex2(x2 - mn); p3 = mma::ex2(x3 - mn);
+        l += (p0 + p1) + (p2 + p3);
+        m = mn;
       }
+      // ---- O += P . V: P (heads x 16 tokens) is the A operand
+      const uint32_t pa0 = mma::pack_bf16(p0, p1), pa2 = mma::pack_bf16(p2, p3);
+      {
+        const int j = lane >> 3, r = lane & 7;
+        const uint32_t rowaddr = vs + (uint32_t)((wr + (j & 1) * 8 + r) * RS + (j >> 1) * 8) * 2u;
+  #pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          uint32_t b[4];
+          mma::ldsm_x4_t(rowaddr + dn * 32u, b);
+          mma::mma_bf16(o[2 * dn], pa0, 0u, pa2, 0u, b[0], b[1]);
+          mma::mma_bf16(o[2 * dn + 1], pa0, 0u, pa2, 0u, b[2], b[3]);
+        }
+      }
+    };
+    if (k_as_v) {
+      tile_step(ks, ks, st * 2 * mma::kRows);
+      tile_step(ks + (uint32_t)(mma::kRows * RS) * 2u, ks + (uint32_t)(mma::kRows * RS) * 2u,
+                st * 2 * mma::kRows + mma::kRows);
+    } else {
+      tile_step(ks, vs, st * mma::kRows);
     }
   }
   mma::cp_wait<0>();
