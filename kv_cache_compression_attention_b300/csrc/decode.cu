@@ -500,6 +500,8 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
 // i.e. every approximated value W_g k_j is rebuilt by one d x d product per
 // query head instead of one per row (the reconstruction is linear).  The new
 // token is appended as an exact row.
+constexpr int kVecStaged = 64;   // chunks staged by the VECTOR merge (W takes most of its smem)
+
 template <int D, int G>
 __global__ void __launch_bounds__(D)
 decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restrict__ kc,
@@ -510,13 +512,21 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
                              int n_heads, int Hkv, int max_chunks, float scale_log2,
                              const float* __restrict__ ws, uint16_t* __restrict__ out,
                              float* __restrict__ lse, int* status) {
+  constexpr int WS = D + 8;                // padded W row: 16-byte row reads spread over banks
   __shared__ float red[D / 32][G];
   __shared__ float ak_sm[G][D];
-  pdl_wait();
-  pdl_trigger();
+  __shared__ __align__(16) uint16_t w_sm[D * WS];
   const int i = blockIdx.x;
   const int u = i / Hkv, g = i - u * Hkv;
   const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
+  // W_g does not depend on the partial kernel: fetch it while that kernel drains
+  for (int e = x; e < D * (D / 8); e += D) {
+    const int r = e / (D / 8), ch = e - r * (D / 8);
+    mmasync::cp_async16(smem_u32(w_sm + r * WS + ch * 8), W + ((int64_t)g * D + r) * D + ch * 8, 16u);
+  }
+  mmasync::cp_commit();
+  pdl_wait();
+  pdl_trigger();
   const int L = klen[i];
   int na = napprox[i];
   if (na < 0 || na > L) { if (x == 0) report(status, KVC_ERR_RANGE); na = na < 0 ? 0 : L; }
@@ -552,36 +562,89 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
   }
   const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
   float av[G], M[G], lsum[G];
+  if (nch <= kVecStaged) {
+    // as in decode_combine_kernel: every chunk's (max, sum) staged in shared
+    // memory, one warp per head for the maxima and normalisers
+    __shared__ float s_w[kVecStaged * G], s_l[kVecStaged * G];
+    __shared__ float s_M[G], s_L[G];
+    for (int e = x; e < nch * G; e += D) {
+      const float* pc = base + (int64_t)e * (D + 2);
+      s_w[e] = pc[D];
+      s_l[e] = pc[D + 1];
+    }
+    __syncthreads();
+    for (int h = warp; h < G; h += D / 32) {
+      float m = append ? snew[h] : -INFINITY;
+      for (int c = lane; c < nch; c += 32) m = fmaxf(m, s_w[c * G + h]);
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float m = append ? snew[h] : -INFINITY;
-    for (int c = 0; c < nch; ++c) m = fmaxf(m, base[(int64_t)(c * G + h) * (D + 2) + D]);
-    float a = 0.0f, ak = 0.0f, ls = 0.0f;
-    for (int c = 0; c < nch; ++c) {
-      const float* pc = base + (int64_t)(c * G + h) * (D + 2);
-      const float mc = pc[D];
-      const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - m);
-      if (c < cha) ak += pc[x] * f; else a += pc[x] * f;
-      ls += pc[D + 1] * f;
+      for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) s_M[h] = m;
     }
-    if (append) {
-      const float f = exp2f(snew[h] - m);
-      a += vn * f;
-      ls += f;
+    __syncthreads();
+    for (int e = x; e < nch * G; e += D) {
+      const float mc = s_w[e];
+      s_w[e] = (mc == -INFINITY) ? 0.0f : exp2f(mc - s_M[e % G]);
     }
-    ak_sm[h][x] = ak;
-    av[h] = a;
-    M[h] = m;
-    lsum[h] = ls;
+    __syncthreads();
+    for (int h = warp; h < G; h += D / 32) {
+      float ls = 0.0f;
+      for (int c = lane; c < nch; c += 32) ls += s_w[c * G + h] * s_l[c * G + h];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      if (lane == 0) s_L[h] = ls;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float a = 0.0f, ak = 0.0f;
+#pragma unroll 4
+      for (int c = 0; c < cha; ++c) ak += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
+#pragma unroll 4
+      for (int c = cha; c < nch; ++c) a += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
+      M[h] = s_M[h];
+      lsum[h] = s_L[h];
+      if (append) {
+        const float f = exp2f(snew[h] - M[h]);
+        a += vn * f;
+        lsum[h] += f;
+      }
+      ak_sm[h][x] = ak;
+      av[h] = a;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float m = append ? snew[h] : -INFINITY;
+      for (int c = 0; c < nch; ++c) m = fmaxf(m, base[(int64_t)(c * G + h) * (D + 2) + D]);
+      float a = 0.0f, ak = 0.0f, ls = 0.0f;
+      for (int c = 0; c < nch; ++c) {
+        const float* pc = base + (int64_t)(c * G + h) * (D + 2);
+        const float mc = pc[D];
+        const float f = (mc == -INFINITY) ? 0.0f : exp2f(mc - m);
+        if (c < cha) ak += pc[x] * f; else a += pc[x] * f;
+        ls += pc[D + 1] * f;
+      }
+      if (append) {
+        const float f = exp2f(snew[h] - m);
+        a += vn * f;
+        ls += f;
+      }
+      ak_sm[h][x] = ak;
+      av[h] = a;
+      M[h] = m;
+      lsum[h] = ls;
+    }
   }
+  mmasync::cp_wait<0>();
   __syncthreads();
   // out dimension x: sum_y W[g][x][y] * ak[h][y], the row read as 16-byte words
   float rec[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) rec[h] = 0.0f;
-  const uint4* wrow = reinterpret_cast<const uint4*>(W + ((int64_t)g * D + x) * D);
+  const uint4* wrow = reinterpret_cast<const uint4*>(w_sm + x * WS);
+#pragma unroll 4
   for (int ch = 0; ch < D / 8; ++ch) {
-    const uint4 w4 = __ldg(wrow + ch);
+    const uint4 w4 = wrow[ch];
     const float wf[8] = {bf16lo(w4.x), bf16hi(w4.x), bf16lo(w4.y), bf16hi(w4.y),
                          bf16lo(w4.z), bf16hi(w4.z), bf16lo(w4.w), bf16hi(w4.w)};
 #pragma unroll

@@ -41,15 +41,11 @@ vector_residual_kernel(const uint16_t* __restrict__ k, const uint16_t* __restric
                        int n_sink, int n_recent, float* __restrict__ key, int* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   ResidualSmem& sm = *reinterpret_cast<ResidualSmem*>(smem_raw);
-  pdl_wait();
-  pdl_trigger();
   const int i = blockIdx.y;
   const int g = i % Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int cnt = counts[i];
-  const int ntiles = (T + kTile - 1) / kTile;
-  const int64_t head_row0 = (int64_t)i * T;     // row of token 0 of head i in k / v
-  // stage W_g once (16-byte chunks, row-padded)
+  // stage W_g once (16-byte chunks, row-padded); W does not depend on the
+  // previous kernel, so the copy overlaps its tail
   {
     const uint16_t* wg = W + (int64_t)g * D * D;
     const uint32_t wb = smem_u32(sm.w);
@@ -58,9 +54,14 @@ vector_residual_kernel(const uint16_t* __restrict__ k, const uint16_t* __restric
       cp_async16(wb + (uint32_t)(r * RS + ch * 8) * 2u, wg + r * D + ch * 8, 16u);
     }
     cp_commit();
-    cp_wait<0>();
-    __syncthreads();
   }
+  pdl_wait();
+  pdl_trigger();
+  const int cnt = counts[i];
+  const int ntiles = (T + kTile - 1) / kTile;
+  const int64_t head_row0 = (int64_t)i * T;     // row of token 0 of head i in k / v
+  cp_wait<0>();
+  __syncthreads();
   const uint32_t kb = smem_u32(sm.kt[warp]), vb = smem_u32(sm.vt[warp]);
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int j0 = tile * kTile + warp * 16;           // this warp's first pool position

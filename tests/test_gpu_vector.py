@@ -277,3 +277,32 @@ def test_decode_vector_batch64_sampled(B):
     torch.cuda.synchronize()
     assert B.kvc_device_status() == 0
     np.testing.assert_array_equal(kl.cpu().numpy(), kl0 + 4)
+
+
+def test_decode_vector_many_chunks(B):
+    """A head with more split-K chunks than the merge stages in shared memory
+    (36 000 approximated + 36 000 exact rows: 36 + 71 chunks)."""
+    d, G, na, ne = 128, 2, 36000, 36000
+    g = torch.Generator().manual_seed(95)
+    kc = torch.randn((na + ne + 1, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((ne + 1, d), generator=g).to(torch.bfloat16)
+    W = (torch.randn((1, d, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    q = torch.randn((1, G, d), generator=g).to(torch.bfloat16)
+    kn = torch.randn((1, 1, d), generator=g).to(torch.bfloat16)
+    vn = torch.randn((1, 1, d), generator=g).to(torch.bfloat16)
+    ks, vs = np.zeros(1, np.int64), np.zeros(1, np.int64)
+    kl, nap = np.array([na + ne], np.int32), np.array([na], np.int32)
+    kc_t, vc_t, kl_t = kc.cuda(), vc.cuda(), torch.from_numpy(kl).cuda()
+    out = torch.empty((1, G, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, G), device="cuda")
+    B.kvc_decode_attn_vector(q.cuda(), kc_t, vc_t, torch.from_numpy(ks).cuda(), kl_t,
+                             torch.from_numpy(vs).cuda(), torch.from_numpy(nap).cuda(), W.cuda(),
+                             out, lse, k_new=kn.cuda(), v_new=vn.cuda(), max_len=na + ne + 1)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    ro, rl, _, _, rkl = O.decode_attn_vector(np64(q), kc.float().numpy(), vc.float().numpy(), ks,
+                                             kl, vs, nap, W.float().numpy(), np64(kn), np64(vn),
+                                             d ** -0.5)
+    assert row_rel_err(np64(out).reshape(-1, d), ro.reshape(-1, d)) <= 2e-2
+    assert lse_err(np64(lse), rl) <= 2e-2
+    np.testing.assert_array_equal(kl_t.cpu().numpy(), rkl)
