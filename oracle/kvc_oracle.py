@@ -15,7 +15,9 @@ Sources (web pages on KV-cache compression; cited by title and section):
             §2D (budgets that differ per layer and per KV head).
 * [VECTOR]  "A Simple Plug-in for Improving Eviction-Based KV Cache
             Compression", "Énoncé du Problème" (importance eviction: score
-            tokens, drop the low-score entries).
+            tokens, drop the low-score entries) and "Méthodologie : VECTOR"
+            (three-way routing: keys kept, values kept / rebuilt by an OLS
+            predictor from the key / evicted).
 * [KVTC]    "KV Cache Transform Coding for Compact Storage in LLM Inference" §2A
             (attention sinks and the recent sliding window are kept as is).
 * [KVzap]   "KVzap: Fast, Adaptive, and Faithful KV Cache Pruning"

@@ -835,3 +835,17 @@ def test_planted_vector_mistakes_are_caught():
     o2, _, _, _, _ = O.decode_attn_vector(q, kc, vc, kstart, klen, vstart, napprox,
                                           np.transpose(W, (0, 2, 1)))
     assert not np.allclose(o1, o2)
+
+
+def test_fit_ols_recovers_the_synthetic_predictor():
+    """The VECTOR workloads draw the predictor W and values v = W k + noise;
+    the oracle's offline OLS fit on such calibration pairs recovers W."""
+    from kv_cache_compression_attention_b300 import inputs
+    w = inputs.WORKLOADS["c1_tiny"].with_(T=32768)     # sampling error ~ 0.026 relative
+    k = torch.randn((w.U, w.Hkv, w.T, w.d), generator=torch.Generator().manual_seed(78))
+    W = inputs.vector_predictor(w, "cpu")
+    v = inputs.vector_values(w, k, W, "cpu")
+    fit = O.fit_ols(k[0].numpy(), v[0].float().numpy())
+    Wf = W.float().numpy()
+    rel = np.linalg.norm(fit - Wf) / np.linalg.norm(Wf)
+    assert rel < 0.05, rel
