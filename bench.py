@@ -869,6 +869,7 @@ def main():
     dec["peak_gbs"] = hbm
     c4 = bench_c4(B, max(3, args.steps // 4), 3, device)
     c3 = bench_c3(B, 3, 3, device)
+    vec = bench_vector(B, w, max(5, args.steps // 2), 3, device)
     comp_c2 = compact_bytes(r["kept_rows"], w.d, 2)
     comp_c2_us = statistics.mean(r["compact_ms"]) * 1e3
 
@@ -899,6 +900,7 @@ def main():
         "decode": dec,
         "c4_qwen128k": c4,
         "c3_32layer": c3,
+        "vector": vec,
         "rooflines": [
             {"kernel": "score_tc_kernel", "workload": WORKLOAD, "bound": "hbm",
              "achieved_gbs": achieved, "frac": achieved / hbm},
@@ -921,7 +923,17 @@ def main():
              "bound": "hbm", "achieved_gbs": dec["gbs"], "frac": dec["gbs"] / hbm},
             {"kernel": "decode_partial_mma_kernel<q8>+decode_combine_kernel (group-quantised pool)",
              "workload": DECODE_WORKLOAD, "bound": "hbm", "time_us": dec["q8"]["us_per_step"],
-             "achieved_gbs": dec["q8"]["gbs"], "frac": dec["q8"]["gbs"] / hbm}],
+             "achieved_gbs": dec["q8"]["gbs"], "frac": dec["q8"]["gbs"] / hbm},
+            {"kernel": "vector_residual_kernel", "workload": WORKLOAD + " (VECTOR p_c 0.9, p_a 0.05)",
+             "bound": "hbm", "time_us": vec["stages_us"]["residual"],
+             "achieved_gbs": vec["residual_gbs"], "frac": vec["residual_gbs"] / hbm,
+             "tensor_tflops": vec["residual_tflops"]},
+            {"kernel": "vector_compact_kernel", "workload": WORKLOAD + " (VECTOR)", "bound": "hbm",
+             "time_us": vec["stages_us"]["compact"], "achieved_gbs": vec["compact_gbs"],
+             "frac": vec["compact_gbs"] / hbm},
+            {"kernel": "decode_partial_mma_kernel+decode_combine_vector_kernel (VECTOR cache)",
+             "workload": DECODE_WORKLOAD, "bound": "hbm", "time_us": vec["decode"]["us_per_step"],
+             "achieved_gbs": vec["decode"]["gbs"], "frac": vec["decode"]["gbs"] / hbm}],
         "fidelity": fid,
         "e2e": {"value": job_tokens_per_s(world, w.U * w.T, e2e_ms), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -432,12 +432,23 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
       if (lane == 0) s_L[h] = Ls;
     }
     __syncthreads();
+    // column x of every chunk and head: chunks outer, heads inner, so that
+    // 4 x G loads are in flight per thread
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+#pragma unroll 4
+    for (int c = 0; c < nch; ++c) {
+      float pv[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) pv[h] = base[(int64_t)(c * G + h) * (D + 2) + x];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(s_w[c * G + h], pv[h], acc[h]);
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float M = s_M[h];
-      float a = 0.0f, lsum = s_L[h];
-#pragma unroll 4
-      for (int c = 0; c < nch; ++c) a += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
+      float a = acc[h], lsum = s_L[h];
       if (append) {
         const float f = exp2f(snew[h] - M);
         a += vn * f;
@@ -594,13 +605,29 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
       if (lane == 0) s_L[h] = ls;
     }
     __syncthreads();
+    // chunks outer, heads inner: 4 x G loads in flight per thread
+    float acc_k[G], acc_v[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc_k[h] = acc_v[h] = 0.0f;
+#pragma unroll 4
+    for (int c = 0; c < cha; ++c) {
+      float pv[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) pv[h] = base[(int64_t)(c * G + h) * (D + 2) + x];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc_k[h] = fmaf(s_w[c * G + h], pv[h], acc_k[h]);
+    }
+#pragma unroll 4
+    for (int c = cha; c < nch; ++c) {
+      float pv[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) pv[h] = base[(int64_t)(c * G + h) * (D + 2) + x];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc_v[h] = fmaf(s_w[c * G + h], pv[h], acc_v[h]);
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float a = 0.0f, ak = 0.0f;
-#pragma unroll 4
-      for (int c = 0; c < cha; ++c) ak += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
-#pragma unroll 4
-      for (int c = cha; c < nch; ++c) a += s_w[c * G + h] * base[(int64_t)(c * G + h) * (D + 2) + x];
+      float a = acc_v[h], ak = acc_k[h];
       M[h] = s_M[h];
       lsum[h] = s_L[h];
       if (append) {
