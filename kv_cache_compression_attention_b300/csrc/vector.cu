@@ -25,7 +25,7 @@ using namespace ::kvc::mmasync;
 
 constexpr int D = 128;              // head dimension of the VECTOR path
 constexpr int RS = D + 8;           // padded smem row (bf16 elements): conflict-free ldmatrix
-constexpr int kResWarps = 4;        // 16 pool positions per warp and tile
+constexpr int kResWarps = 8;        // 16 pool positions per warp and tile
 constexpr int kTile = kResWarps * 16;
 
 struct ResidualSmem {
