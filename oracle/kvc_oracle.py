@@ -117,6 +117,31 @@ def score_linear(hidden, weight, bias=None):
     return out
 
 
+def gelu(z):
+    """GELU(z) = z * Phi(z) = z (1 + erf(z / sqrt 2)) / 2 (the exact form)."""
+    from scipy.special import erf
+    z = np.asarray(z, dtype=F64)
+    return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def score_mlp(hidden, w1, b1, w2, b2=None):
+    """Two-layer surrogate score ([KVzap] §2.2, the MLP variant: hidden width
+    D_h / 8 with a GELU): for every token t of unit u and kv head g
+        z_m = b1_m + sum_j hidden[u,t,j] * w1[j,m]
+        score[u,g,t] = b2_g + sum_m GELU(z_m) * w2[m,g]
+    hidden [U, T, Dh], w1 [Dh, Dm], b1 [Dm] or None, w2 [Dm, Hkv], b2 [Hkv] or
+    None.  As for the linear surrogate, the raw output is compared with tau.
+    Returns float64 [U, Hkv, T]."""
+    h = np.asarray(hidden, dtype=F64)
+    z = np.einsum("utj,jm->utm", h, np.asarray(w1, dtype=F64))
+    if b1 is not None:
+        z = z + np.asarray(b1, dtype=F64)
+    out = np.einsum("utm,mg->ugt", gelu(z), np.asarray(w2, dtype=F64))
+    if b2 is not None:
+        out = out + np.asarray(b2, dtype=F64)[None, :, None]
+    return out
+
+
 # -------------------------------------------------------------- selection
 def protected_mask(T, n_sink, n_recent):
     """Tokens that are always kept: the first n_sink (attention sinks,

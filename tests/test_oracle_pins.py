@@ -849,3 +849,60 @@ def test_fit_ols_recovers_the_synthetic_predictor():
     Wf = W.float().numpy()
     rel = np.linalg.norm(fit - Wf) / np.linalg.norm(Wf)
     assert rel < 0.05, rel
+
+
+# ------------------------------------------ MLP surrogate ([KVzap] §2.2)
+def test_gelu_special_cases_and_torch():
+    z = np.array([0.0, 1.0, -1.0, 8.0, -8.0, 0.5, -3.0])
+    g = O.gelu(z)
+    assert g[0] == 0.0
+    assert abs(g[1] - 0.8413447460685429) < 1e-15          # Phi(1) = 0.841344746...
+    assert abs(g[1] - g[2] - 1.0) < 1e-15                  # GELU(z) - GELU(-z) = z
+    assert abs(g[3] - 8.0) < 1e-14 and abs(g[4]) < 1e-14
+    ref = torch.nn.functional.gelu(torch.from_numpy(z)).numpy()
+    np.testing.assert_allclose(g, ref, rtol=1e-15, atol=1e-16)
+
+
+def test_score_mlp_brute_force():
+    rng = np.random.default_rng(79)
+    U, T, Dh, Dm, Hkv = 2, 3, 5, 4, 3
+    h = rng.standard_normal((U, T, Dh))
+    w1, b1 = rng.standard_normal((Dh, Dm)), rng.standard_normal(Dm)
+    w2, b2 = rng.standard_normal((Dm, Hkv)), rng.standard_normal(Hkv)
+    got = O.score_mlp(h, w1, b1, w2, b2)
+    for u in range(U):
+        for t in range(T):
+            act = []
+            for m in range(Dm):
+                z = b1[m] + sum(h[u, t, j] * w1[j, m] for j in range(Dh))
+                act.append(0.5 * z * (1.0 + math.erf(z / math.sqrt(2.0))))
+            for g in range(Hkv):
+                ref = b2[g] + sum(act[m] * w2[m, g] for m in range(Dm))
+                assert abs(got[u, g, t] - ref) < 1e-12
+
+
+def test_score_mlp_reduces_to_linear_when_gelu_is_identity():
+    # pre-activations far above 0: GELU(z) = z to double precision, so the MLP
+    # is the linear surrogate with weight w1 w2 and bias b1 w2 + b2
+    rng = np.random.default_rng(80)
+    h = rng.standard_normal((1, 6, 4)) * 0.1
+    w1, b1 = rng.standard_normal((4, 3)) * 0.1, np.full(3, 40.0)
+    w2, b2 = rng.standard_normal((3, 2)), rng.standard_normal(2)
+    got = O.score_mlp(h, w1, b1, w2, b2)
+    ref = O.score_linear(h, w1 @ w2, b1 @ w2 + b2)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_planted_mlp_mistakes_are_caught():
+    rng = np.random.default_rng(81)
+    h = rng.standard_normal((1, 8, 6))
+    w1, b1 = rng.standard_normal((6, 5)), rng.standard_normal(5)
+    w2 = rng.standard_normal((5, 2))
+    ref = O.score_mlp(h, w1, b1, w2)
+    z = np.einsum("utj,jm->utm", h, w1) + b1
+    tanh_gelu = 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+    relu = np.maximum(z, 0)
+    no_bias = O.gelu(np.einsum("utj,jm->utm", h, w1))
+    for bad in (tanh_gelu, relu, no_bias):
+        out = np.einsum("utm,mg->ugt", bad, w2)
+        assert np.abs(out - ref).max() > 1e-5
