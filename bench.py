@@ -575,7 +575,25 @@ def bench_c4(B, steps, warmup, device):
                score_linear_bytes=score_bytes,
                compact_gbs=comp_bytes / (t_comp * 1e-6) / 1e9, compact_bytes=comp_bytes,
                tokens_per_s=w.U * w.T / ((t_score + t_sel + t_comp) * 1e-6))
-    del hidden, k, v, kc, vc, kept, flush
+    # the two-layer surrogate ([KVzap] §2.2, width Dh / 8) on the same hidden states
+    w1, b1, w2, b2 = inputs.mlp_scorer(w, device)
+    mws = torch.empty(B.lib().kvc_score_mlp_workspace(w.U, w.T, w1.shape[1]), dtype=torch.uint8,
+                      device=device)
+    for _ in range(2):
+        B.kvc_score_mlp(hidden, w1, b1, w2, b2, scores, workspace=mws)
+    torch.cuda.synchronize()
+    mev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in mev:
+        flush_l2(flush)
+        e[0].record(s)
+        B.kvc_score_mlp(hidden, w1, b1, w2, b2, scores, workspace=mws)
+        e[1].record(s)
+    torch.cuda.synchronize()
+    t_mlp = statistics.mean(e[0].elapsed_time(e[1]) for e in mev) * 1e3
+    mlp_flops = 2.0 * w.U * w.T * w.Dh * w1.shape[1] + 2.0 * w.U * w.T * w1.shape[1] * w.Hkv
+    out.update(score_mlp_us=t_mlp, score_mlp_tflops=mlp_flops / (t_mlp * 1e-6) / 1e12,
+               score_mlp_width=int(w1.shape[1]))
+    del hidden, k, v, kc, vc, kept, flush, mws
     torch.cuda.empty_cache()
     return out
 
@@ -915,6 +933,9 @@ def main():
              "achieved_gbs": c4["score_linear_gbs"], "frac": c4["score_linear_gbs"] / hbm},
             {"kernel": "compact_kernel", "workload": "c4_qwen128k", "bound": "hbm",
              "achieved_gbs": c4["compact_gbs"], "frac": c4["compact_gbs"] / hbm},
+            {"kernel": "cuBLAS bf16 GEMM + mlp_out_kernel (two-layer surrogate)",
+             "workload": "c4_qwen128k", "bound": "tensor", "time_us": c4["score_mlp_us"],
+             "achieved_tflops": c4["score_mlp_tflops"], "frac": c4["score_mlp_tflops"] / bf16},
             {"kernel": "score_tc_kernel", "workload": "c3_32layer", "bound": "hbm",
              "achieved_gbs": c3["score_gbs"], "frac": c3["score_gbs"] / hbm},
             {"kernel": "compact_kernel", "workload": "c3_32layer", "bound": "hbm",

@@ -148,6 +148,29 @@ int kvc_score_linear(const void* hidden, const void* weight, const float* bias,
                      int dtype, int U, int T, int Dh, int Hkv,
                      float* scores, void* stream);
 
+/* Bytes of workspace kvc_score_mlp needs: the bf16 first-layer output
+ * [U*T, Dm] (rounded up to 256 bytes) plus 32 MiB of GEMM scratch. */
+size_t kvc_score_mlp_workspace(int U, int T, int Dm);
+
+/*
+ * Two-layer surrogate score ([KVzap] §2.2, the MLP variant: hidden width
+ * Dh / 8 with a GELU):
+ *   z[u,t,m]     = b1[m] + sum_j hidden[u,t,j] * w1[j,m]
+ *   scores[u,g,t] = b2[g] + sum_m GELU(z[u,t,m]) * w2[m,g],
+ *   GELU(z) = z (1 + erf(z / sqrt 2)) / 2.
+ * hidden [U, T, Dh], w1 [Dh, Dm], w2 [Dm, Hkv] dtype (KVC_BF16); b1 [Dm],
+ * b2 [Hkv] fp32 or NULL; scores [U, Hkv, T] fp32.  The first layer is a
+ * cuBLAS bf16 GEMM with fp32 accumulation whose output is rounded to bf16
+ * in the workspace; bias, GELU and the second layer accumulate in fp32.
+ * Requires Dh % 8 == 0, Dm % 8 == 0, Dm <= 1024, 1 <= Hkv <= 8, 16-byte
+ * aligned hidden and w1, a 256-byte aligned workspace of
+ * kvc_score_mlp_workspace bytes.  The first call on a device creates a
+ * cuBLAS handle there (cuBLAS allocates its own small state once).
+ */
+int kvc_score_mlp(const void* hidden, const void* w1, const float* b1, const void* w2,
+                  const float* b2, int dtype, int U, int T, int Dh, int Dm, int Hkv,
+                  float* scores, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ----------------------------------------------------------------- select */
 
 /* Bytes of workspace kvc_select needs (currently 0 for every mode). */

@@ -50,6 +50,8 @@ SIGNATURES = {
     "kvc_quantize_rows": (_I, [_P, _I, _I64, _I, _P, _P, _P]),
     "kvc_decode_attn_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                 _P, _P, _P, _SZ, _P]),
+    "kvc_score_mlp_workspace": (_SZ, [_I, _I, _I]),
+    "kvc_score_mlp": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_vector_residual": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "kvc_vector_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I64,
                                 _P, _I64, _P, _P, _P, _P, _P]),
@@ -161,6 +163,22 @@ def kvc_score_linear(hidden, weight, bias, scores, stream=None):
     rc = lib().kvc_score_linear(_ptr(hidden), _ptr(weight), _ptr(bias), _dtype(hidden), U, T, Dh,
                                 Hkv, _ptr(scores), _stream(stream))
     _check("kvc_score_linear", rc)
+    return scores
+
+
+def kvc_score_mlp(hidden, w1, b1, w2, b2, scores, workspace=None, stream=None):
+    """Two-layer surrogate: hidden [U, T, Dh] bf16, w1 [Dh, Dm] bf16, b1 [Dm] fp32,
+    w2 [Dm, Hkv] bf16, b2 [Hkv] fp32 -> scores [U, Hkv, T] fp32."""
+    U, T, Dh = hidden.shape
+    Dm, Hkv = w2.shape
+    need = lib().kvc_score_mlp_workspace(U, T, Dm)
+    if workspace is None:
+        workspace = _workspace(need, hidden.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_score_mlp(_ptr(hidden), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2),
+                             _dtype(hidden), U, T, Dh, Dm, Hkv, _ptr(scores), _ptr(workspace),
+                             ws_bytes, _stream(stream))
+    _check("kvc_score_mlp", rc)
     return scores
 
 

@@ -290,6 +290,28 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                                   kvc::as_stream(stream));
 }
 
+size_t kvc_score_mlp_workspace(int U, int T, int Dm) {
+  if (U < 0 || T < 0 || Dm <= 0) return 0;
+  return kvc::score_mlp_ws_bytes(U, T, Dm);
+}
+
+int kvc_score_mlp(const void* hidden, const void* w1, const float* b1, const void* w2,
+                  const float* b2, int dtype, int U, int T, int Dh, int Dm, int Hkv,
+                  float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!hidden || !w1 || !w2 || !scores) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || T <= 0 || Dh <= 0 || Dm <= 0 || Hkv <= 0) return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || Dh % 8 || Dm % 8 || Dm > 1024 || Hkv > 8) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(hidden) || !aligned16(w1)) return KVC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVC_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < kvc::score_mlp_ws_bytes(U, T, Dm)) return KVC_ERR_WORKSPACE;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::score_mlp_launch(hidden, w1, b1, w2, b2, U, T, Dh, Dm, Hkv, scores, workspace, dev,
+                               kvc::as_stream(stream));
+}
+
 int kvc_vector_residual(const void* k, const void* v, const void* W, int dtype, int U, int Hkv,
                         int T, int d, const int32_t* kept_idx, const int32_t* counts,
                         int n_sink, int n_recent, float* key, void* stream) {

@@ -137,6 +137,10 @@ int gather_scores_launch(const float* scores, int U, int Hkv, int T, const int32
                          const int32_t* counts, const int64_t* start, float* rscore,
                          int64_t capacity_rows, const Dev& dev, cudaStream_t s);
 
+size_t score_mlp_ws_bytes(int U, int T, int Dm);
+int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const void* w2,
+                     const float* b2, int U, int T, int Dh, int Dm, int Hkv, float* scores,
+                     void* workspace, const Dev& dev, cudaStream_t s);
 int vector_residual_launch(const void* k, const void* v, const void* W, int U, int Hkv, int T,
                            const int32_t* kept_idx, const int32_t* counts, int n_sink,
                            int n_recent, float* key, const Dev& dev, cudaStream_t s);

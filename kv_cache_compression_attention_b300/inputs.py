@@ -217,6 +217,18 @@ def linear_scorer(w: Workload, device="cpu"):
     return hidden, weight, bias
 
 
+def mlp_scorer(w: Workload, device="cpu"):
+    """Weights of the two-layer surrogate for workload w (hidden width Dh / 8):
+    w1 [Dh, Dh/8] ~ N(0, 1/Dh), w2 [Dh/8, Hkv] ~ N(0, 8/Dh) in the workload
+    dtype, biases b1 ~ N(0, 0.1^2) [Dh/8] and b2 zeros [Hkv] in fp32."""
+    dm = w.Dh // 8
+    g1, g2, g3 = _gen(device, _seed(w, 22)), _gen(device, _seed(w, 23)), _gen(device, _seed(w, 24))
+    w1 = (_randn((w.Dh, dm), g1, device) / math.sqrt(w.Dh)).to(w.torch_dtype)
+    w2 = (_randn((dm, w.Hkv), g2, device) / math.sqrt(dm)).to(w.torch_dtype)
+    b1 = 0.1 * _randn((dm,), g3, device)
+    return w1, b1, w2, torch.zeros(w.Hkv, dtype=torch.float32, device=device)
+
+
 def head_budgets(w: Workload, device="cpu") -> torch.Tensor:
     """Per-(unit, kv head) kept-token budgets floor(U[lo, hi] * T), int32 [U*Hkv]."""
     lo, hi = w.len_frac

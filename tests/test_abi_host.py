@@ -230,3 +230,22 @@ def test_vector_entry_points_reject_bad_arguments(lib):
     # are chunked apart
     assert lib.kvc_decode_vector_workspace(64, 32, 8, 128, 10086) == \
         64 * 8 * (20 + 1) * 4 * 130 * 4
+
+
+def test_score_mlp_rejects_bad_arguments(lib):
+    f = lib.kvc_score_mlp
+    ws = ctypes.c_void_p(256)
+    ok = [P, P, P, P, P, 1, 1, 128, 3584, 448, 4, P, ws, 1 << 40, None]
+    bad = list(ok); bad[0] = None
+    assert f(*bad) == -1
+    bad = list(ok); bad[10] = 9
+    assert f(*bad) == -2                                        # more than 8 kv heads
+    bad = list(ok); bad[9] = 452
+    assert f(*bad) == -2                                        # Dm not a multiple of 8
+    bad = list(ok); bad[9] = 2048
+    assert f(*bad) == -2                                        # Dm beyond 1024
+    bad = list(ok); bad[12] = P
+    assert f(*bad) == -2                                        # workspace not 256-byte aligned
+    bad = list(ok); bad[13] = 1000
+    assert f(*bad) == -3
+    assert lib.kvc_score_mlp_workspace(1, 131072, 448) == 131072 * 448 * 2 + (32 << 20)

@@ -168,3 +168,34 @@ def test_score_attn_rejects_non_positive_temperature_on_device(B, dtype, d, G, W
     B.kvc_score_attn(q, k, out, d ** -0.5, head_scale=hs)
     assert B.kvc_device_status() == -1            # KVC_ERR_INVALID, recorded on the device
     assert B.kvc_device_status() == 0
+
+
+@pytest.mark.parametrize("Hkv,Dh,Dm,T", [(4, 256, 32, 300), (1, 512, 64, 77), (8, 128, 16, 1000)])
+def test_score_mlp_small(B, Hkv, Dh, Dm, T):
+    U = 2
+    g = torch.Generator().manual_seed(97 + Hkv)
+    h = torch.randn((U, T, Dh), generator=g).to(torch.bfloat16)
+    w1 = (torch.randn((Dh, Dm), generator=g) / Dh ** 0.5).to(torch.bfloat16)
+    b1 = 0.1 * torch.randn(Dm, generator=g)
+    w2 = (torch.randn((Dm, Hkv), generator=g) / Dm ** 0.5).to(torch.bfloat16)
+    b2 = torch.randn(Hkv, generator=g)
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda")
+    B.kvc_score_mlp(h.cuda(), w1.cuda(), b1.cuda(), w2.cuda(), b2.cuda(), out)
+    torch.cuda.synchronize()
+    ref = O.score_mlp(np64(h), np64(w1), np64(b1), np64(w2), np64(b2))
+    assert row_rel_err(np64(out), ref) <= 2e-2
+
+
+def test_score_mlp_qwen128k_sampled_rows(B):
+    """The 128k Qwen-shaped layer (hidden 3584, MLP width 448, 4 kv heads)."""
+    w = inputs.WORKLOADS["c4_qwen128k"]
+    hid, _, _ = inputs.linear_scorer(w, "cuda")
+    w1, b1, w2, b2 = inputs.mlp_scorer(w, "cuda")
+    out = torch.empty((w.U, w.Hkv, w.T), device="cuda")
+    B.kvc_score_mlp(hid, w1, b1, w2, b2, out)
+    torch.cuda.synchronize()
+    rows = torch.cat([torch.arange(0, 256), torch.arange(70000, 70256),
+                      torch.arange(w.T - 256, w.T)]).cuda()
+    ref = O.score_mlp(np64(hid[:, rows]), np64(w1), np64(b1), np64(w2), np64(b2))
+    assert row_rel_err(np64(out[:, :, rows]), ref) <= 2e-2
+    assert torch.isfinite(out).all()
