@@ -101,6 +101,58 @@ def score_attn(q_win, k, scale, head_scale=None, causal=True, aggregation="sum")
     return out
 
 
+def value_norms(v, gram, G):
+    """||W_O^h v_t|| for every query head h and token t, from the Gram
+    matrices gram[h] = W_O^h^T W_O^h (d x d) of the output projection's
+    per-head slices: sqrt(v^T gram[h] v).  v [U, Hkv, T, d], gram [Hq, d, d],
+    query head h reads kv head h // G.  Returns float64 [U, Hq, T]."""
+    vv = np.asarray(v, dtype=F64)
+    M = np.asarray(gram, dtype=F64)
+    U, Hkv, T, d = vv.shape
+    out = np.zeros((U, Hkv * G, T), dtype=F64)
+    for u in range(U):
+        for h in range(Hkv * G):
+            x = vv[u, h // G]                                   # [T, d]
+            out[u, h] = np.sqrt(np.maximum(np.einsum("td,de,te->t", x, M[h], x), 0.0))
+    return out
+
+
+def score_kvzip_plus(q_win, k, v, gram, hnorm, scale, head_scale=None, causal=True):
+    """KVzip+ score ([KVzap] §2.1): the largest attention weight a token
+    receives from the window rows, each weighted by the size of the token's
+    value contribution to the residual stream relative to the row's hidden
+    state.  The printed formula divides a_ji by ||W_O v_i|| / ||h_j||; the
+    text (and the normalisation it cites) weights by the contribution, so
+    this reads it as
+        s+[u,g,t] = max_{h in g, w} p[(h,w), t] * ||W_O^h v_t|| / ||h_w||
+    with p the row softmax of score_attn, ||W_O^h v_t|| from value_norms and
+    hnorm [U, W] the hidden-state norms of the window positions.
+    Returns float64 [U, Hkv, T]."""
+    q = np.asarray(q_win, dtype=F64)
+    kk = np.asarray(k, dtype=F64)
+    U, Hq, W, d = q.shape
+    _, Hkv, T, _ = kk.shape
+    G = Hq // Hkv
+    vn = value_norms(v, gram, G)
+    hn = np.asarray(hnorm, dtype=F64)
+    hs = None if head_scale is None else np.asarray(head_scale, dtype=F64)
+    out = np.zeros((U, Hkv, T), dtype=F64)
+    for u in range(U):
+        for g in range(Hkv):
+            for i in range(G):
+                h = g * G + i
+                c = scale * (1.0 if hs is None else hs[u, h])
+                logits = c * (q[u, h] @ kk[u, g].T)             # [W, T]
+                if causal:
+                    for w in range(W):
+                        logits[w, T - W + w + 1:] = -np.inf
+                m = logits.max(axis=1, keepdims=True)
+                lse = m + np.log(np.exp(logits - m).sum(axis=1, keepdims=True))
+                p = np.exp(logits - lse) / hn[u][:, None]        # a_wt / ||h_w||
+                out[u, g] = np.maximum(out[u, g], p.max(axis=0) * vn[u, h])
+    return out
+
+
 def score_linear(hidden, weight, bias=None):
     """Linear surrogate score ([KVzap] §2.2): score[u,g,t] = b_g + h[u,t,:] . W[:,g].
 

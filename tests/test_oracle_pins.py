@@ -906,3 +906,67 @@ def test_planted_mlp_mistakes_are_caught():
     for bad in (tanh_gelu, relu, no_bias):
         out = np.einsum("utm,mg->ugt", bad, w2)
         assert np.abs(out - ref).max() > 1e-5
+
+
+# -------------------------------------------------- KVzip+ ([KVzap] §2.1)
+def test_value_norms_against_an_explicit_projection():
+    rng = np.random.default_rng(82)
+    U, Hkv, G, T, d, Dm = 1, 2, 2, 7, 4, 6
+    v = rng.standard_normal((U, Hkv, T, d))
+    WO = rng.standard_normal((Hkv * G, Dm, d))                 # per-head slices of W_O
+    gram = np.einsum("hmd,hme->hde", WO, WO)
+    got = O.value_norms(v, gram, G)
+    for h in range(Hkv * G):
+        for t in range(T):
+            assert abs(got[0, h, t] - np.linalg.norm(WO[h] @ v[0, h // G, t])) < 1e-12
+
+
+def test_kvzip_plus_brute_force_and_reductions():
+    q, k = rng_arrays(83, (1, 4, 3, 5), (1, 2, 9, 5))
+    v = np.random.default_rng(84).standard_normal((1, 2, 9, 5))
+    WO = np.random.default_rng(85).standard_normal((4, 7, 5))
+    gram = np.einsum("hmd,hme->hde", WO, WO)
+    hn = np.array([[2.0, 0.5, 3.0]])
+    got = O.score_kvzip_plus(q, k, v, gram, hn, 0.6)
+    G, W, T = 2, 3, 9
+    for g in range(2):
+        for t in range(T):
+            best = 0.0
+            for i in range(G):
+                h = g * G + i
+                for w in range(W):
+                    if t > T - W + w:
+                        continue
+                    logits = [0.6 * float(q[0, h, w] @ k[0, g, tt]) for tt in range(T - W + w + 1)]
+                    mx = max(logits)
+                    den = sum(math.exp(x - mx) for x in logits)
+                    a = math.exp(logits[t] - mx) / den
+                    best = max(best, a * np.linalg.norm(WO[h] @ v[0, g, t]) / hn[0, w])
+            assert abs(got[0, g, t] - best) < 1e-12
+    # unit hidden norms and identity Grams on unit-norm values: the KVzip score
+    vu = v / np.linalg.norm(v, axis=-1, keepdims=True)
+    eye = np.broadcast_to(np.eye(5), (4, 5, 5))
+    np.testing.assert_allclose(O.score_kvzip_plus(q, k, vu, eye, np.ones((1, 3)), 0.6),
+                               O.score_attn(q, k, 0.6, aggregation="max"), rtol=1e-12)
+
+
+def test_planted_kvzip_plus_mistakes_are_caught():
+    q, k = rng_arrays(86, (1, 4, 3, 5), (1, 2, 9, 5))
+    v = np.random.default_rng(87).standard_normal((1, 2, 9, 5))
+    WO = np.random.default_rng(88).standard_normal((4, 7, 5))
+    gram = np.einsum("hmd,hme->hde", WO, WO)
+    hn = np.array([[2.0, 0.5, 3.0]])
+    ref = O.score_kvzip_plus(q, k, v, gram, hn, 0.6)
+    # the printed division (contribution in the denominator) ranks differently
+    vn = O.value_norms(v, gram, 2)
+    div = np.zeros_like(ref)
+    for g in range(2):
+        for i in range(2):
+            h = g * 2 + i
+            p = O.score_attn(q[:, h:h + 1], k[:, g:g + 1], 0.6, aggregation="max")
+            div[0, g] = np.maximum(div[0, g], p[0, 0] / vn[0, h])
+    assert not np.allclose(div, ref)
+    # one head's Gram for the whole group
+    gram_bad = gram.copy()
+    gram_bad[1] = gram[0]
+    assert not np.allclose(O.score_kvzip_plus(q, k, v, gram_bad, hn, 0.6), ref)
