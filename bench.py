@@ -49,6 +49,8 @@ from kv_cache_compression_attention_b300 import inputs  # noqa: E402
 
 METRIC = "KV tokens/s scored+selected+compacted"
 WORKLOAD = "c2_llama32k"
+# fp32 FMA peak of the SIMT cores: 148 SMs x 128 FMA/clk x 2 FLOP x 2.032 GHz
+ALU_FP32_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 DECODE_WORKLOAD = "c5_decode"
 
 
@@ -218,6 +220,30 @@ def bench_score_max(L, steps, warmup):
         flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s); L.score("max"); e1.record(s)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+
+def bench_kvzip_plus(B, L, steps, warmup):
+    """The KVzip+ score ([KVzap] §2.1) on the same layer: value norms on warp
+    MMAs, then the SIMT column pass; mean CUDA-event time per call, L2 flushed
+    before each."""
+    w = L.w
+    gram, hnorm = inputs.kvzip_plus_weights(w, L.k.device)
+    ws = torch.empty(B.lib().kvc_score_kvzip_plus_workspace(w.U, w.Hq, w.Hkv, w.T, w.W),
+                     dtype=torch.uint8, device=L.k.device)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=L.k.device)
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        B.kvc_score_kvzip_plus(L.q, L.k, L.v, gram, hnorm, L.scores, w.scale, workspace=ws)
+    ts = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        B.kvc_score_kvzip_plus(L.q, L.k, L.v, gram, hnorm, L.scores, w.scale, workspace=ws)
+        e1.record(s)
         ts.append((e0, e1))
     torch.cuda.synchronize()
     return statistics.mean(a.elapsed_time(b) for a, b in ts)
@@ -879,6 +905,7 @@ def main():
     # ---- sub-measurements (outside the headline timed region)
     e2e_ms, h2d, d2h = bench_e2e(B, L, max(6, args.steps // 2), 2)
     score_max_ms = bench_score_max(L, max(5, args.steps // 2), 3)
+    kvzip_ms = bench_kvzip_plus(B, L, 3, 1)
     fid = fidelity_probe(B, L)
     del L
     torch.cuda.empty_cache()
@@ -926,6 +953,11 @@ def main():
              "time_us": score_max_ms * 1e3,
              "achieved_gbs": score_bytes / (score_max_ms * 1e-3) / 1e9,
              "frac": score_bytes / (score_max_ms * 1e-3) / 1e9 / hbm},
+            {"kernel": "value_norm_kernel + row_lse_kernel + col_mass_kernel (KVzip+)",
+             "workload": WORKLOAD, "bound": "alu", "time_us": kvzip_ms * 1e3,
+             "achieved_tflops": 2 * score_flops / (kvzip_ms * 1e-3) / 1e12,
+             "peak_tflops": ALU_FP32_TFLOPS,
+             "frac": 2 * score_flops / (kvzip_ms * 1e-3) / 1e12 / ALU_FP32_TFLOPS},
             {"kernel": "compact_kernel", "workload": WORKLOAD, "bound": "hbm",
              "achieved_gbs": comp_c2 / (comp_c2_us * 1e-6) / 1e9,
              "frac": comp_c2 / (comp_c2_us * 1e-6) / 1e9 / hbm},

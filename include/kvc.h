@@ -148,6 +148,34 @@ int kvc_score_linear(const void* hidden, const void* weight, const float* bias,
                      int dtype, int U, int T, int Dh, int Hkv,
                      float* scores, void* stream);
 
+/* Bytes of workspace kvc_score_kvzip_plus needs: the value norms
+ * [U, Hq, T] fp32 (rounded up to 256 bytes), then the scoring pass's own
+ * workspace (as kvc_score_attn_workspace). */
+size_t kvc_score_kvzip_plus_workspace(int U, int Hq, int Hkv, int T, int W);
+
+/*
+ * KVzip+ score ([KVzap] §2.1): the largest attention weight a token receives
+ * from the window rows, each weighted by the token's value contribution to
+ * the residual stream over the row's hidden-state norm.  The printed formula
+ * divides a_ji by ||W_O v_i|| / ||h_j||; the text and the normalisation it
+ * cites weight by the contribution, which is what this computes:
+ *   scores[u,g,t] = max_{h in g, w} p[(h,w), t] * ||W_O^h v_t|| / hnorm[u,w]
+ * with p the row softmax of kvc_score_attn (same scale, head_scale and
+ * causal mask) and ||W_O^h v_t|| = sqrt(v_t^T gram[h] v_t), gram[h] =
+ * W_O^h^T W_O^h the d x d Gram matrix of the output projection's slice for
+ * query head h (model weights, formed offline).
+ * q_win [U, Hq, W, d], k, v [U, Hkv, T, d], gram [Hq, d, d] dtype (KVC_BF16,
+ * d = 128, 16-byte aligned); hnorm [U, W] fp32 (> 0); scores [U, Hkv, T]
+ * fp32.  The value norms run on warp-level bf16 MMAs; the scoring pass is
+ * the tensor-core scorer of kvc_score_attn in a KVzip+ mode when G*W is 128
+ * or 256 and W is a multiple of G*W / 4 (a quarter of the rows lies inside
+ * one query head), else the SIMT pass (fp32).
+ */
+int kvc_score_kvzip_plus(const void* q_win, const void* k, const void* v, const void* gram,
+                         const float* hnorm, int dtype, int U, int Hq, int Hkv, int T, int W,
+                         int d, float scale, const float* head_scale, int causal, float* scores,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace kvc_score_mlp needs: the bf16 first-layer output
  * [U*T, Dm] (rounded up to 256 bytes) plus 32 MiB of GEMM scratch. */
 size_t kvc_score_mlp_workspace(int U, int T, int Dm);

@@ -50,6 +50,9 @@ SIGNATURES = {
     "kvc_quantize_rows": (_I, [_P, _I, _I64, _I, _P, _P, _P]),
     "kvc_decode_attn_q8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                 _P, _P, _P, _SZ, _P]),
+    "kvc_score_kvzip_plus_workspace": (_SZ, [_I, _I, _I, _I, _I]),
+    "kvc_score_kvzip_plus": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P,
+                                  _P, _SZ, _P]),
     "kvc_score_mlp_workspace": (_SZ, [_I, _I, _I]),
     "kvc_score_mlp": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_vector_residual": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
@@ -163,6 +166,23 @@ def kvc_score_linear(hidden, weight, bias, scores, stream=None):
     rc = lib().kvc_score_linear(_ptr(hidden), _ptr(weight), _ptr(bias), _dtype(hidden), U, T, Dh,
                                 Hkv, _ptr(scores), _stream(stream))
     _check("kvc_score_linear", rc)
+    return scores
+
+
+def kvc_score_kvzip_plus(q_win, k, v, gram, hnorm, scores, scale, head_scale=None, causal=True,
+                         workspace=None, stream=None):
+    """KVzip+ scores [U, Hkv, T] fp32 (q_win, k, v, gram bf16; hnorm [U, W] fp32)."""
+    U, Hq, W, d = q_win.shape
+    _, Hkv, T, _ = k.shape
+    need = lib().kvc_score_kvzip_plus_workspace(U, Hq, Hkv, T, W)
+    if workspace is None:
+        workspace = _workspace(need, k.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_score_kvzip_plus(_ptr(q_win), _ptr(k), _ptr(v), _ptr(gram), _ptr(hnorm),
+                                    _dtype(k), U, Hq, Hkv, T, W, d, float(scale),
+                                    _ptr(head_scale), int(bool(causal)), _ptr(scores),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    _check("kvc_score_kvzip_plus", rc)
     return scores
 
 

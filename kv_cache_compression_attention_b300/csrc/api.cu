@@ -290,6 +290,33 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                                   kvc::as_stream(stream));
 }
 
+size_t kvc_score_kvzip_plus_workspace(int U, int Hq, int Hkv, int T, int W) {
+  if (U < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T < 0 || W <= 0) return 0;
+  return kvc::score_kvzip_plus_ws_bytes(U, Hq, Hkv, T, W);
+}
+
+int kvc_score_kvzip_plus(const void* q_win, const void* k, const void* v, const void* gram,
+                         const float* hnorm, int dtype, int U, int Hq, int Hkv, int T, int W,
+                         int d, float scale, const float* head_scale, int causal, float* scores,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q_win || !k || !v || !gram || !hnorm || !scores) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (U <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T <= 0 || W <= 0 || W > T || d <= 0)
+    return KVC_ERR_INVALID;
+  if (!(scale > 0.0f) || !isfinite(scale)) return KVC_ERR_INVALID;
+  if (dtype != KVC_BF16 || d != 128) return KVC_ERR_UNSUPPORTED;
+  if ((int64_t)U * Hkv > 65535 || !aligned16(v) || !aligned16(gram)) return KVC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVC_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < kvc::score_kvzip_plus_ws_bytes(U, Hq, Hkv, T, W))
+    return KVC_ERR_WORKSPACE;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::score_kvzip_plus_launch(q_win, k, v, gram, hnorm, U, Hq, Hkv, T, W, scale,
+                                      head_scale, causal ? 1 : 0, scores, workspace, dev,
+                                      kvc::as_stream(stream));
+}
+
 size_t kvc_score_mlp_workspace(int U, int T, int Dm) {
   if (U < 0 || T < 0 || Dm <= 0) return 0;
   return kvc::score_mlp_ws_bytes(U, T, Dm);

@@ -92,9 +92,12 @@ size_t score_attn_simt_ws(int U, int Hq, int W);
 
 bool score_attn_tc_supported(int dtype, int Hq, int Hkv, int W, int d);
 size_t score_attn_tc_ws(int Hq, int Hkv, int W);
+// Aggregation code of the KVzip+ score inside the library (not an ABI value).
+constexpr int kAggKvzipPlus = 2;
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
                   float scale, const float* head_scale, int causal, int agg, float* scores,
-                  void* ws, const Dev& dev, cudaStream_t s);
+                  void* ws, const Dev& dev, cudaStream_t s, const float* hnorm = nullptr,
+                  const float* vnorm = nullptr);
 
 int score_linear_launch(const void* hidden, const void* weight, const float* bias, int dtype,
                         int U, int T, int Dh, int Hkv, float* scores, const Dev& dev,
@@ -137,6 +140,15 @@ int gather_scores_launch(const float* scores, int U, int Hkv, int T, const int32
                          const int32_t* counts, const int64_t* start, float* rscore,
                          int64_t capacity_rows, const Dev& dev, cudaStream_t s);
 
+int score_kvzip_plus_simt(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
+                          float scale, const float* head_scale, int causal, const float* hnorm,
+                          const float* vnorm, float* scores, float* lse_ws, const Dev& dev,
+                          cudaStream_t s);
+size_t score_kvzip_plus_ws_bytes(int U, int Hq, int Hkv, int T, int W);
+int score_kvzip_plus_launch(const void* q, const void* k, const void* v, const void* gram,
+                            const float* hnorm, int U, int Hq, int Hkv, int T, int W,
+                            float scale, const float* head_scale, int causal, float* scores,
+                            void* workspace, const Dev& dev, cudaStream_t s);
 size_t score_mlp_ws_bytes(int U, int T, int Dm);
 int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const void* w2,
                      const float* b2, int U, int T, int Dh, int Dm, int Hkv, float* scores,

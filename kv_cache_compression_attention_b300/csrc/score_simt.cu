@@ -105,7 +105,8 @@ template <typename Tin, int D>
 __global__ void __launch_bounds__(kColThreads)
 col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int Hq, int Hkv,
                 int T, int W, float scale, const float* __restrict__ head_scale, int causal,
-                int agg_max, const float* __restrict__ lse, float* __restrict__ scores) {
+                int agg_max, const float* __restrict__ lse, float* __restrict__ scores,
+                const float* __restrict__ hnorm, const float* __restrict__ vnorm) {
   __shared__ float4 qs[kRowChunk][D / 4];
   __shared__ float cs[kRowChunk], ls[kRowChunk];
   const int ug = blockIdx.y;                 // u*Hkv + g
@@ -117,6 +118,12 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
   if (valid) load_row<Tin>(k + ((int64_t)ug * T + t) * D, D, kr);
   float sum = 0.0f;
   const int64_t row0 = ((int64_t)u * Hq + (int64_t)g * G) * W;   // first row of the group
+  // KVzip+ (vnorm set): a head's largest weight over its rows, each divided
+  // by the row's hidden-state norm (folded into the row's normaliser), times
+  // the token's value contribution ||W_O^h v_t||; the maximum over heads
+  const bool plus = vnorm != nullptr;
+  int cur_h = 0;
+  float hmax = 0.0f;
   for (int r0 = 0; r0 < R; r0 += kRowChunk) {
     const int nr = min(kRowChunk, R - r0);
     __syncthreads();
@@ -128,12 +135,17 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
       const int r = r0 + threadIdx.x;
       const int h = g * G + r / W;
       cs[threadIdx.x] = scale * (head_scale ? head_scale[(int64_t)u * Hq + h] : 1.0f);
-      ls[threadIdx.x] = lse[row0 + r];
+      ls[threadIdx.x] = lse[row0 + r] + (plus ? logf(hnorm[(int64_t)u * W + r % W]) : 0.0f);
     }
     __syncthreads();
     if (valid) {
       for (int rr = 0; rr < nr; ++rr) {
         const int w = (r0 + rr) % W;
+        if (plus && (r0 + rr) / W != cur_h) {
+          sum = fmaxf(sum, hmax * vnorm[((int64_t)u * Hq + g * G + cur_h) * T + t]);
+          hmax = 0.0f;
+          cur_h = (r0 + rr) / W;
+        }
         if (causal && t > T - W + w) continue;
         float acc = 0.0f;
 #pragma unroll
@@ -145,17 +157,19 @@ col_mass_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, int U, int
           acc = fmaf(qv.w, kr[4 * x4 + 3], acc);
         }
         const float e = expf(cs[rr] * acc - ls[rr]);
-        sum = agg_max ? fmaxf(sum, e) : sum + e;
+        if (plus) hmax = fmaxf(hmax, e);
+        else sum = agg_max ? fmaxf(sum, e) : sum + e;
       }
     }
   }
+  if (valid && plus) sum = fmaxf(sum, hmax * vnorm[((int64_t)u * Hq + g * G + cur_h) * T + t]);
   if (valid) scores[(int64_t)ug * T + t] = sum;
 }
 
 template <typename Tin, int D>
 int run(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W, float scale,
         const float* hs, int causal, int agg, float* scores, float* lse, int* status,
-        cudaStream_t s) {
+        cudaStream_t s, const float* hnorm = nullptr, const float* vnorm = nullptr) {
   const int64_t rows = (int64_t)U * Hq * W;
   dim3 g1((unsigned)((rows + kRowWarps - 1) / kRowWarps));
   row_lse_kernel<Tin, D><<<g1, kRowWarps * 32, 0, s>>>(
@@ -164,11 +178,19 @@ int run(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W, floa
   dim3 g2((unsigned)((T + kColThreads - 1) / kColThreads), (unsigned)(U * Hkv));
   col_mass_kernel<Tin, D><<<g2, kColThreads, 0, s>>>(
       static_cast<const Tin*>(q), static_cast<const Tin*>(k), U, Hq, Hkv, T, W, scale, hs,
-      causal, agg == KVC_AGG_MAX ? 1 : 0, lse, scores);
+      causal, agg == KVC_AGG_MAX ? 1 : 0, lse, scores, hnorm, vnorm);
   return launch_status();
 }
 
 }  // namespace
+
+int score_kvzip_plus_simt(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
+                          float scale, const float* head_scale, int causal, const float* hnorm,
+                          const float* vnorm, float* scores, float* lse_ws, const Dev& dev,
+                          cudaStream_t s) {
+  return run<uint16_t, 128>(q, k, U, Hq, Hkv, T, W, scale, head_scale, causal, KVC_AGG_MAX,
+                            scores, lse_ws, dev.status, s, hnorm, vnorm);
+}
 
 size_t score_attn_simt_ws(int U, int Hq, int W) {
   return (size_t)U * Hq * W * sizeof(float);

@@ -84,6 +84,8 @@ struct Params {
   ulonglong2* parts; // [2][grid][R] per-CTA row partials: (max2 | tag, sum | tag)
   uint64_t tag0;     // this launch's tag base (unique per launch)
   int* status;
+  const float* hnorm;  // KVzip+ only: hidden-state norm per (unit, window row)
+  const float* vnorm;  // KVzip+ only: ||W_O^h v_t|| per (unit, query head, token)
 };
 
 struct SmemSmall {
@@ -145,7 +147,10 @@ __device__ __forceinline__ float comb(float a, float b) {
   return kMax ? fmaxf(a, b) : a + b;
 }
 
-template <bool kMax>
+// kPlus (with kMax): the KVzip+ score -- each row's weights divided by the
+// row's hidden-state norm (folded into its normaliser), each quarter's
+// maximum (one query head's rows) times the token's value norm for that head
+template <bool kMax, bool kPlus = false>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 Params p) {
@@ -425,7 +430,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (et < R) {
         float M = sm.mpart[0][et], L = sm.lpart[0][et];
         merge_ms(M, L, sm.mpart[1][et], sm.lpart[1][et]);
-        sm.nlse[et] = -(M + __log2f(L));   // -lse2 of row et
+        float nl = -(M + __log2f(L));      // -lse2 of row et
+        if constexpr (kPlus) nl -= __log2f(p.hnorm[(int64_t)u * W + et % W]);
+        sm.nlse[et] = nl;
       }
       tc::named_sync(1, kEpiThreads);
       if (et < R / 2)
@@ -470,7 +477,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc::fence_before_sync();
         mbar_arrive(&sm.tmem_empty[b]);
         const float2 a = tc::upk2(comb2<kMax>(comb2<kMax>(s2[0], s2[1]), comb2<kMax>(s2[2], s2[3])));
-        const float part = comb<kMax>(a.x, a.y);
+        float part = comb<kMax>(a.x, a.y);
+        if constexpr (kPlus)
+          part *= (tok < T) ? p.vnorm[((int64_t)u * p.Hq + g * p.G + rc0 / W) * T + tok] : 0.0f;
         // quarters 1-3 hand their sums to quarter 0 through a double-buffered
         // slot; only the two quarters involved wait, never the whole epilogue
         const int pb = p2 & 1, use = p2 >> 1;
@@ -544,7 +553,8 @@ size_t score_attn_tc_ws(int Hq, int Hkv, int W) {
 
 int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, int W,
                   float scale, const float* head_scale, int causal, int agg, float* scores,
-                  void* ws, const Dev& dev, cudaStream_t s) {
+                  void* ws, const Dev& dev, cudaStream_t s, const float* hnorm,
+                  const float* vnorm) {
   int rc = get_encoder();
   if (rc) return rc;
   const int G = Hq / Hkv, R = G * W;
@@ -572,6 +582,7 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   Params p;
   p.T = T; p.W = W; p.R = R; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.scale = scale;
   p.head_scale = head_scale; p.causal = causal; p.scores = scores;
+  p.hnorm = hnorm; p.vnorm = vnorm;
   p.n_tiles = (T + kTile - 1) / kTile; p.status = dev.status;
   p.heads = U * Hkv;
   const size_t smem = smem_bytes(R);
@@ -586,7 +597,7 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
       // the attribute is the kernel's, shared by both row counts: the larger
       const size_t smax = smem_bytes(256);
       if ((int)smax > dev.max_smem_optin) return KVC_ERR_UNSUPPORTED;
-      for (auto fn : {score_tc_kernel<false>, score_tc_kernel<true>})
+      for (auto fn : {score_tc_kernel<false>, score_tc_kernel<true>, score_tc_kernel<true, true>})
         KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smax));
       KVC_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_tc_kernel<false>,
@@ -626,7 +637,9 @@ int score_attn_tc(const void* q, const void* k, int U, int Hq, int Hkv, int T, i
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kern = agg == KVC_AGG_MAX ? score_tc_kernel<true> : score_tc_kernel<false>;
+  auto kern = agg == kAggKvzipPlus ? score_tc_kernel<true, true>
+              : agg == KVC_AGG_MAX  ? score_tc_kernel<true>
+                                    : score_tc_kernel<false>;
   if (int rc2 = prefer_max_shared(kern, dev.device)) return rc2;
   KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, tm_q, tm_k, p));
   return launch_status();

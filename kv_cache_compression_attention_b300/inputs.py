@@ -217,6 +217,21 @@ def linear_scorer(w: Workload, device="cpu"):
     return hidden, weight, bias
 
 
+def kvzip_plus_weights(w: Workload, device="cpu"):
+    """Synthetic model weights for the KVzip+ score: the Gram matrices
+    gram[h] = W_O^h^T W_O^h of a random output projection W_O [Hq*d, Hq*d] ~
+    N(0, 1/(Hq*d)) split by query head (bf16 [Hq, d, d]), and the norms of
+    the window positions' hidden states h ~ N(0, I_{Hq*d}) (fp32 [U, W])."""
+    dm = w.Hq * w.d
+    g1, g2 = _gen(device, _seed(w, 25)), _gen(device, _seed(w, 26))
+    gram = torch.empty((w.Hq, w.d, w.d), dtype=torch.bfloat16, device=device)
+    for h in range(w.Hq):
+        wo = _randn((dm, w.d), g1, device) / math.sqrt(dm)
+        gram[h] = (wo.T @ wo).to(torch.bfloat16)
+    hnorm = _randn((w.U, w.W, dm), g2, device).norm(dim=-1)
+    return gram, hnorm
+
+
 def mlp_scorer(w: Workload, device="cpu"):
     """Weights of the two-layer surrogate for workload w (hidden width Dh / 8):
     w1 [Dh, Dh/8] ~ N(0, 1/Dh), w2 [Dh/8, Hkv] ~ N(0, 8/Dh) in the workload

@@ -249,3 +249,20 @@ def test_score_mlp_rejects_bad_arguments(lib):
     bad = list(ok); bad[13] = 1000
     assert f(*bad) == -3
     assert lib.kvc_score_mlp_workspace(1, 131072, 448) == 131072 * 448 * 2 + (32 << 20)
+
+
+def test_score_kvzip_plus_rejects_bad_arguments(lib):
+    f = lib.kvc_score_kvzip_plus
+    ws = ctypes.c_void_p(256)
+    ok = [P, P, P, P, P, 1, 1, 32, 8, 4096, 64, 128, 0.09, None, 1, P, ws, 1 << 40, None]
+    for k, v, want in [(4, None, -1), (9, 3, -1), (10, 5000, -1), (12, 0.0, -1), (11, 64, -2),
+                       (5, 0, -2), (17, 100, -3)]:
+        bad = list(ok); bad[k] = v
+        assert f(*bad) == want, (k, v)
+    bad = list(ok); bad[16] = P
+    assert f(*bad) == -2                                        # workspace not 256-byte aligned
+    # value norms, then the tensor-core scorer's row partials (G*W = 256, W = 64)
+    assert lib.kvc_score_kvzip_plus_workspace(1, 32, 8, 32768, 64) == \
+        32 * 32768 * 4 + 2 * 1024 * 256 * 16
+    # G*W = 256 with W = 32: quarters span two heads, the SIMT pass (one lse per row)
+    assert lib.kvc_score_kvzip_plus_workspace(1, 32, 4, 1024, 32) == 32 * 1024 * 4 + 32 * 32 * 4

@@ -199,3 +199,47 @@ def test_score_mlp_qwen128k_sampled_rows(B):
     ref = O.score_mlp(np64(hid[:, rows]), np64(w1), np64(b1), np64(w2), np64(b2))
     assert row_rel_err(np64(out[:, :, rows]), ref) <= 2e-2
     assert torch.isfinite(out).all()
+
+
+def kvzip_case(seed, U, Hq, Hkv, W, T, d=128):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((U, Hq, W, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((U, Hkv, T, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((U, Hkv, T, d), generator=g).to(torch.bfloat16)
+    wo = torch.randn((Hq, 3 * d, d), generator=g) / (3 * d) ** 0.5
+    gram = torch.einsum("hmd,hme->hde", wo, wo).to(torch.bfloat16).contiguous()
+    hnorm = 0.5 + torch.rand((U, W), generator=g) * 2
+    return q, k, v, gram, hnorm
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("Hq,Hkv,W,T", [
+    (8, 2, 16, 300), (4, 4, 8, 77), (16, 2, 32, 513),    # SIMT scoring pass
+    (8, 2, 64, 700), (4, 2, 64, 300),                     # tensor-core pass (G*W = 256, 128)
+])
+def test_score_kvzip_plus_small(B, causal, Hq, Hkv, W, T):
+    U = 2
+    q, k, v, gram, hnorm = kvzip_case(101 + Hq + T, U, Hq, Hkv, W, T)
+    hs = 0.5 + torch.rand((U, Hq), generator=torch.Generator().manual_seed(5))
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda")
+    B.kvc_score_kvzip_plus(q.cuda(), k.cuda(), v.cuda(), gram.cuda(), hnorm.cuda(), out, 0.09,
+                           head_scale=hs.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    ref = O.score_kvzip_plus(np64(q), np64(k), np64(v), np64(gram), np64(hnorm), 0.09,
+                             head_scale=np64(hs), causal=causal)
+    assert mass_rel_err(np64(out), ref) <= 2e-2
+
+
+def test_score_kvzip_plus_llama32k_full(B):
+    """The 32k Llama-3-8B-shaped layer with a synthetic output projection."""
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, v = inputs.keys_values(w, q, "cuda")
+    gram, hnorm = inputs.kvzip_plus_weights(w, "cuda")
+    out = torch.empty((w.U, w.Hkv, w.T), device="cuda")
+    B.kvc_score_kvzip_plus(q, k, v, gram, hnorm, out, w.scale)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    ref = O.score_kvzip_plus(np64(q), np64(k), np64(v), np64(gram), np64(hnorm), w.scale)
+    assert mass_rel_err(np64(out), ref) <= 2e-2
