@@ -73,11 +73,16 @@ mlp_out_kernel(const uint16_t* __restrict__ pre, const float* __restrict__ b1,
   }
 }
 
-// One cuBLAS handle per device, created on first use and kept for the process.
-cublasHandle_t handle_for(int device) {
+// One cuBLAS handle per device, created on first use and kept for the
+// process.  Setting its stream and workspace and enqueuing the GEMM happen
+// under the same lock, so host threads sharing a device do not race on them.
+std::mutex& handle_mutex() {
   static std::mutex mu;
+  return mu;
+}
+
+cublasHandle_t handle_for(int device) {
   static cublasHandle_t handles[64] = {};
-  std::lock_guard<std::mutex> lock(mu);
   cublasHandle_t& h = handles[device & 63];
   if (!h && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
   return h;
@@ -106,21 +111,24 @@ int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const 
   const int64_t rows = (int64_t)U * T;
   if (rows == 0) return KVC_OK;
   if (Dm > kMaxDm) return KVC_ERR_UNSUPPORTED;
-  cublasHandle_t h = handle_for(dev.device);
-  if (!h) return KVC_ERR_CUDA;
+  if (rows > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint16_t* pre = reinterpret_cast<uint16_t*>(ws);
   void* cws = ws + (score_mlp_ws_bytes(U, T, Dm) - kCublasWs);
-  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return KVC_ERR_CUDA;
-  if (cublasSetWorkspace(h, cws, kCublasWs) != CUBLAS_STATUS_SUCCESS) return KVC_ERR_CUDA;
-  // row-major pre [rows, Dm] = hidden [rows, Dh] . W1 [Dh, Dm], i.e. in the
-  // column-major terms of cuBLAS pre^T (Dm x rows) = W1^T (Dm x Dh) . hidden^T
-  const float one = 1.0f, zero = 0.0f;
-  if (rows > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
-  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, Dm, (int)rows, Dh, &one, w1, CUDA_R_16BF, Dm,
-                   hidden, CUDA_R_16BF, Dh, &zero, pre, CUDA_R_16BF, Dm, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return KVC_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(handle_mutex());
+    cublasHandle_t h = handle_for(dev.device);
+    if (!h) return KVC_ERR_CUDA;
+    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return KVC_ERR_CUDA;
+    if (cublasSetWorkspace(h, cws, kCublasWs) != CUBLAS_STATUS_SUCCESS) return KVC_ERR_CUDA;
+    // row-major pre [rows, Dm] = hidden [rows, Dh] . W1 [Dh, Dm], i.e. in the
+    // column-major terms of cuBLAS pre^T (Dm x rows) = W1^T (Dm x Dh) . hidden^T
+    const float one = 1.0f, zero = 0.0f;
+    if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, Dm, (int)rows, Dh, &one, w1, CUDA_R_16BF, Dm,
+                     hidden, CUDA_R_16BF, Dh, &zero, pre, CUDA_R_16BF, Dm, CUBLAS_COMPUTE_32F,
+                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return KVC_ERR_CUDA;
+  }
   const uint16_t* w2b = static_cast<const uint16_t*>(w2);
   switch (Hkv) {
     case 1: return launch_out<1>(pre, b1, w2b, b2, rows, T, Dm, scores, dev, s);

@@ -204,7 +204,8 @@ vector_compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, 
       vd = vs + r;
     }
     const int t = (j >= 0 && j < cnt) ? kept_idx[(int64_t)i * T + j] : -1;
-    if (t < 0 || t >= T || ks + o >= kc_rows || vd >= vc_rows) {
+    const bool v_bad = o >= na && (vd < 0 || vd >= vc_rows);   // exact rows need a V row
+    if (t < 0 || t >= T || ks + o < 0 || ks + o >= kc_rows || v_bad) {
       report(status, KVC_ERR_RANGE);
     } else {
       src = (int64_t)i * T + t;
