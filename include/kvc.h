@@ -2,12 +2,17 @@
  * kvc.h -- C ABI of the B300 (sm_103a) KV-cache compression hot path.
  *
  * One transformer layer's KV cache goes through four steps:
- *   score   -> a per-(unit, kv head, token) importance score,
+ *   score   -> a per-(unit, kv head, token) importance score (attention mass
+ *              or maximum, KVzip+, linear or two-layer surrogate),
  *   select  -> a budget (global top-k across heads, per-head top-k, or a
  *              fixed threshold) that always keeps the sink and recent tokens,
  *   compact -> a gather of the kept K/V rows into one variable-length cache,
  *   decode  -> varlen decode attention over that cache (the consumer), plus a
  *              fidelity probe against full-cache attention.
+ * Variants of the cache: group-quantised rows (kvc_quantize_rows,
+ * kvc_decode_attn_q8), VECTOR's keys-for-all / values-for-some routing
+ * (kvc_vector_*, kvc_decode_attn_vector), and decode-time threshold pruning
+ * (kvc_gather_scores, kvc_decode_prune).
  *
  * Sources, cited by page title and section:
  *   [Sculpt] "KVSculpt: KV Cache Compression as Distillation"
@@ -19,6 +24,8 @@
  *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
  *    library never allocates or frees device memory; steps that need scratch
  *    take a caller-provided workspace whose size a *_workspace() query gives.
+ *    (One exception: the first kvc_score_mlp call on a device creates the
+ *    cuBLAS handle its GEMM runs on, and cuBLAS allocates its own state.)
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream).  Nothing synchronises except
  *    kvc_device_status().
