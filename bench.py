@@ -50,6 +50,8 @@ from kv_cache_compression_attention_b300 import inputs  # noqa: E402
 METRIC = "KV tokens/s scored+selected+compacted"
 WORKLOAD = "c2_llama32k"
 DECODE_WORKLOAD = "c5_decode"
+# passes of the window-against-keys contraction the attention-mass scorer issues
+SCORE_PASSES = 2
 
 
 def profiled_traffic(kernel_src, summary):
@@ -302,64 +304,159 @@ def bench_e2e(B, L, steps, warmup):
     return ms, h2d, d2h
 
 
+def build_decode_caches(B, w, device):
+    """The batch-64 decode workload's caches: full 32k caches (K, V with the
+    sinks and needles of the generator) and the compressed caches cut from
+    them by this library's own path -- window scores (W = 64), a per-head
+    top-k at budgets floor(U[0.1, 0.3] * T) that keeps 4 sinks and the 64
+    most recent tokens, and a compaction with 256 slack rows per head for the
+    appends.  Also a second compressed cache at the same budgets whose kept
+    tokens are chosen by random scores (random eviction), and the full cache
+    laid out as a pool with the same slack (every token kept)."""
+    q_win = inputs.window_queries(w, device)
+    k, v = inputs.keys_values(w, q_win, device)
+    n = w.U * w.Hkv
+    budgets = inputs.head_budgets(w, device)
+    scores = torch.empty((w.U, w.Hkv, w.T), device=device)
+    B.kvc_score_attn(q_win, k, scores, w.scale)
+    del q_win
+    kept = torch.empty((n, w.T), dtype=torch.int32, device=device)
+    counts = torch.empty(n, dtype=torch.int32, device=device)
+    offs = torch.empty(n + 1, dtype=torch.int64, device=device)
+
+    def cut(sc):
+        B.kvc_select(sc, "per_head", kept, counts, offs, head_budget=budgets, n_sink=w.n_sink,
+                     n_recent=w.n_recent)
+        rows = int(offs[-1].item()) + n * w.slack
+        kc = torch.empty((rows, w.d), dtype=k.dtype, device=device)
+        vc = torch.empty_like(kc)
+        st = torch.empty(n, dtype=torch.int64, device=device)
+        ln = torch.empty(n, dtype=torch.int32, device=device)
+        B.kvc_compact(k, v, kept, counts, offs, kc, vc, st, ln, slack=w.slack)
+        return kc, vc, st, ln
+
+    comp = cut(scores)
+    rand = cut(inputs.random_scores((w.U, w.Hkv, w.T), device, seed=505))
+    allk = torch.arange(w.T, dtype=torch.int32, device=device).repeat(n, 1)
+    allc = torch.full((n,), w.T, dtype=torch.int32, device=device)
+    allo = torch.arange(n + 1, device=device, dtype=torch.int64) * w.T
+    kf = torch.empty((n * (w.T + w.slack), w.d), dtype=k.dtype, device=device)
+    vf = torch.empty_like(kf)
+    sf = torch.empty(n, dtype=torch.int64, device=device)
+    lf = torch.empty(n, dtype=torch.int32, device=device)
+    B.kvc_compact(k, v, allk, allc, allo, kf, vf, sf, lf, slack=w.slack)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    del k, v, kept, scores, allk
+    torch.cuda.empty_cache()
+    return comp, rand, (kf, vf, sf, lf)
+
+
+def _quantiles(x):
+    x = x.flatten().float()
+    q = torch.quantile(x, torch.tensor([0.5, 0.99], device=x.device))
+    return {"mean": float(x.mean()), "p50": float(q[0]), "p99": float(q[1]),
+            "max": float(x.max())}
+
+
 def bench_decode(B, steps, warmup, device):
+    """Decode over the compressed caches of the batch-64 workload: `steps`
+    timed steps (256, the workload's count), each appending one token per
+    head, then the same steps over the full caches for the fidelity of every
+    step (rel-L2 output error and KL against full-cache attention)."""
     w = inputs.WORKLOADS[DECODE_WORKLOAD]
-    lens = inputs.head_budgets(w, "cpu")
-    kc, vc, start, length = inputs.compressed_pool(w, lens, device)
-    max_len = int(lens.max()) + steps + warmup + 5    # + 4 steps of the pruned stage split
-    ws = torch.empty(B.kvc_decode_workspace(w.U, w.Hq, w.Hkv, w.d, max_len), dtype=torch.uint8,
-                     device=device)
-    steps_in = [inputs.decode_step_inputs(w, i, device) for i in range(steps + warmup)]
+    assert steps <= w.slack, "every step appends one row per head into the slack"
+    (kc, vc, start, length), rnd, full = build_decode_caches(B, w, device)
+    n = w.U * w.Hkv
+    len0 = length.clone()
+    lens = len0.cpu()
+    # the split-K grid is sized by max_len: the compressed caches' own bound,
+    # and the full length for the full caches
+    max_len = int(lens.max()) + max(steps, warmup) + 1
+    max_len_full = w.T + max(steps, warmup) + 1
+    ws = torch.empty(B.kvc_decode_workspace(w.U, w.Hq, w.Hkv, w.d, max_len_full),
+                     dtype=torch.uint8, device=device)
+    steps_in = [inputs.decode_step_inputs(w, i, device) for i in range(max(steps, warmup))]
     out = torch.empty((w.U, w.Hq, w.d), dtype=torch.bfloat16, device=device)
     lse = torch.empty((w.U, w.Hq), device=device)
     s = torch.cuda.current_stream()
     rows0 = int(lens.sum())
-    for i in range(warmup):
+
+    def run(kc_, vc_, st_, ln_, i, o=out, l=lse, ml=max_len):
         q, kn, vn = steps_in[i]
-        B.kvc_decode_attn(q, kc, vc, start, length, out, lse, k_new=kn, v_new=vn,
-                          max_len=max_len, scale=w.scale, workspace=ws)
+        B.kvc_decode_attn(q, kc_, vc_, st_, ln_, o, l, k_new=kn, v_new=vn, max_len=ml,
+                          scale=w.scale, workspace=ws)
+
+    for i in range(warmup):
+        run(kc, vc, start, length, i)
+    length.copy_(len0)                      # the timed steps append into the same slack rows
     torch.cuda.synchronize()
-    rows_before = int(length.sum().item())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
-    for i in range(warmup, warmup + steps):
-        q, kn, vn = steps_in[i]
-        B.kvc_decode_attn(q, kc, vc, start, length, out, lse, k_new=kn, v_new=vn,
-                          max_len=max_len, scale=w.scale, workspace=ws)
+    for i in range(steps):
+        run(kc, vc, start, length, i)
     e1.record(s)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    n = w.U * w.Hkv
     # rows attended per step: the cached rows (read from HBM) + the appended one
-    mean_rows = rows_before + n * (steps - 1) / 2.0
+    mean_rows = rows0 + n * (steps - 1) / 2.0
     row_bytes = w.d * 2
     bytes_step = 2 * mean_rows * row_bytes            # K and V rows streamed once
-    out_d = dict(workload=DECODE_WORKLOAD, us_per_step=ms * 1e3,
+    out_d = dict(workload=DECODE_WORKLOAD, steps=steps, us_per_step=ms * 1e3,
                  kv_rows_per_step=mean_rows + n, bytes_per_step=bytes_step,
                  kv_tokens_per_s=(mean_rows + n) / (ms * 1e-3),
-                 gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2, rows_at_start=rows0)
+                 gbs=bytes_step / (ms * 1e-3) / 1e9, launches_per_step=2, rows_at_start=rows0,
+                 cache="cut from full 32k caches: window scores, per-head top-k at "
+                       "floor(U[0.1,0.3]*T) with 4 sinks + 64 recent kept")
+    # fidelity of every step against full-cache attention ([Sculpt] §4: KL);
+    # the random-eviction cache at the same budgets is the comparison point
+    kf, vf, sf, lf = full
+    lf0 = lf.clone()
+    rk, rv, rs, rl = rnd
+    rl0 = rl.clone()
+    of = torch.empty_like(out); lfu = torch.empty_like(lse)
+    orr = torch.empty_like(out); lrr = torch.empty_like(lse)
+    rel = torch.empty((steps, w.U * w.Hq), device=device); kl = torch.empty_like(rel)
+    rrel = torch.empty_like(rel); rkl = torch.empty_like(rel)
+    length.copy_(len0); lf.copy_(lf0); rl.copy_(rl0)
+    for i in range(steps):
+        run(kc, vc, start, length, i)
+        run(kf, vf, sf, lf, i, of, lfu, max_len_full)
+        run(rk, rv, rs, rl, i, orr, lrr)
+        B.kvc_fidelity(out, of, lse, lfu, rel[i], kl[i])
+        B.kvc_fidelity(orr, of, lrr, lfu, rrel[i], rkl[i])
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    out_d["fidelity"] = {
+        "steps": steps, "pairs_per_step": w.U * w.Hq,
+        "rel_err": _quantiles(rel), "kl": _quantiles(kl),
+        "random_eviction": {"rel_err": _quantiles(rrel), "kl": _quantiles(rkl)},
+        "kl_step0_mean": float(kl[0].mean()), "kl_last_step_mean": float(kl[-1].mean())}
+    del kf, vf, rk, rv, full, rnd
+    torch.cuda.empty_cache()
     # the same steps over the group-quantised pool ([KVTC] §2B groups of 32 with a
-    # scale and an offset): the pool as compacted, quantised once before timing
-    kc2, vc2, start2, length2 = inputs.compressed_pool(w, lens, device)
-    del kc, vc
-    rows_pool = kc2.shape[0]
+    # scale and an offset): the compressed pool quantised once before timing
+    rows_pool = kc.shape[0]
     kq = torch.empty((rows_pool, w.d), dtype=torch.uint8, device=device)
     vq = torch.empty_like(kq)
     kp = torch.empty((rows_pool, w.d // 32, 2), dtype=torch.float16, device=device)
     vp = torch.empty_like(kp)
-    B.kvc_quantize_rows(kc2, kq, kp)
-    B.kvc_quantize_rows(vc2, vq, vp)
-    del kc2, vc2
-    for i in range(warmup):
+    B.kvc_quantize_rows(kc, kq, kp)
+    B.kvc_quantize_rows(vc, vq, vp)
+
+    def run8(i):
         q, kn, vn = steps_in[i]
-        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start2, length2, out, lse, k_new=kn, v_new=vn,
+        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start, length, out, lse, k_new=kn, v_new=vn,
                              max_len=max_len, scale=w.scale, workspace=ws)
+
+    length.copy_(len0)
+    for i in range(warmup):
+        run8(i)
+    length.copy_(len0)
     torch.cuda.synchronize()
     e0.record(s)
-    for i in range(warmup, warmup + steps):
-        q, kn, vn = steps_in[i]
-        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start2, length2, out, lse, k_new=kn, v_new=vn,
-                             max_len=max_len, scale=w.scale, workspace=ws)
+    for i in range(steps):
+        run8(i)
     e1.record(s)
     torch.cuda.synchronize()
     ms8 = e0.elapsed_time(e1) / steps
@@ -370,12 +467,16 @@ def bench_decode(B, steps, warmup, device):
     del kq, vq, kp, vp
     # the same steps with decode-time threshold pruning ([KVzap] §2.3): the new
     # token is scored by the linear surrogate, attended and appended, then the
-    # token leaving the 128-token window stays iff its score >= tau
+    # token leaving the 128-token window stays iff its score >= tau.  The
+    # surrogate's synthetic scores of the cached rows are ~ N(0, 1).
     window, n_sink, tau, Dh = 128, 4, 0.5, 4096
-    kc3, vc3, start3, length3 = inputs.compressed_pool(w, lens, device)
+    # pruning moves rows: the warm-up runs on a copy, the timed steps on the
+    # pool as compacted (warm-up + timed appends together could exceed the slack)
+    kc3, vc3, start3 = kc.clone(), vc.clone(), start
+    length3 = len0.clone()
     rscore = inputs.row_scores(kc3.shape[0], device, seed=61)
     weight, bias = inputs.decode_surrogate(w, Dh, device)
-    hid = [inputs.decode_hidden(w, Dh, i, device) for i in range(steps + warmup)]
+    hid = [inputs.decode_hidden(w, Dh, i, device) for i in range(max(steps, warmup))]
     s_new = torch.empty((w.U, w.Hkv, 1), device=device)
 
     def pruned_step(i):
@@ -388,19 +489,12 @@ def bench_decode(B, steps, warmup, device):
 
     for i in range(warmup):
         pruned_step(i)
-    torch.cuda.synchronize()
-    rows_p0 = int(length3.sum().item())
-    e0.record(s)
-    for i in range(warmup, warmup + steps):
-        pruned_step(i)
-    e1.record(s)
-    torch.cuda.synchronize()
-    msp = e0.elapsed_time(e1) / steps
-    rows_p1 = int(length3.sum().item())
-    # stage times from extra steps with events between the kernels (serialised)
+    # stage times from 4 extra warm-up steps with events between the kernels
+    # (serialised), still on the copy
     hid_x = [inputs.decode_hidden(w, Dh, 10000 + i, device) for i in range(4)]
     in_x = [inputs.decode_step_inputs(w, 10000 + i, device) for i in range(4)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(4)]
+    assert warmup + 4 <= w.slack
     for i in range(4):
         q, kn, vn = in_x[i]
         ev[i][0].record(s)
@@ -413,6 +507,18 @@ def bench_decode(B, steps, warmup, device):
                            n_sink)
         ev[i][3].record(s)
     torch.cuda.synchronize()
+    kc3, vc3 = kc, vc
+    length3.copy_(len0)
+    rscore = inputs.row_scores(kc3.shape[0], device, seed=61)
+    torch.cuda.synchronize()
+    rows_p0 = int(length3.sum().item())
+    e0.record(s)
+    for i in range(steps):
+        pruned_step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    msp = e0.elapsed_time(e1) / steps
+    rows_p1 = int(length3.sum().item())
     t_lin = statistics.mean(e[0].elapsed_time(e[1]) for e in ev[1:]) * 1e3
     t_prune = statistics.mean(e[2].elapsed_time(e[3]) for e in ev[1:]) * 1e3
     mean_rows_p = (rows_p0 + rows_p1) / 2.0
@@ -423,6 +529,8 @@ def bench_decode(B, steps, warmup, device):
                            kv_tokens_per_s=(mean_rows_p + n) / (msp * 1e-3),
                            overhead_us=(msp - ms) * 1e3, launches_per_step=4,
                            stage_linear_us=t_lin, stage_prune_us=t_prune)
+    del kc, vc, kc3, vc3, ws
+    torch.cuda.empty_cache()
     return out_d
 
 
@@ -703,7 +811,11 @@ def bench_c3(B, steps, warmup, device):
 
 
 def fidelity_probe(B, L):
-    """One decode step over the compacted cache and over the full cache."""
+    """One decode step over the compacted cache and over the full cache, and
+    the same step over a cache of the same size whose kept tokens are chosen
+    by random scores (random eviction at the same keep ratio, the comparison
+    point: a score that finds the attended tokens retains more of the probe's
+    attention mass, i.e. a lower KL)."""
     w = L.w
     n = L.n
     dev = L.k.device
@@ -712,27 +824,46 @@ def fidelity_probe(B, L):
     q = L.q[:, :, -1, :].contiguous()
     kn = torch.randn((w.U, w.Hkv, w.d), generator=g, device=dev).to(L.k.dtype)
     vn = torch.randn((w.U, w.Hkv, w.d), generator=g, device=dev).to(L.k.dtype)
-    L.score(); L.select(); L.compact()
     allk = torch.arange(w.T, dtype=torch.int32, device=dev).repeat(n, 1).contiguous()
     allc = torch.full((n,), w.T, dtype=torch.int32, device=dev)
     allo = (torch.arange(n + 1, device=dev) * w.T).to(torch.int64)
-    kf = torch.empty((n * (w.T + w.slack), w.d), dtype=L.k.dtype, device=dev)
+    kf = torch.empty((n * (w.T + w.slack + 1), w.d), dtype=L.k.dtype, device=dev)
     vf = torch.empty_like(kf)
     sf = torch.empty(n, dtype=torch.int64, device=dev)
     lf = torch.empty(n, dtype=torch.int32, device=dev)
-    B.kvc_compact(L.k, L.v, allk, allc, allo, kf, vf, sf, lf, slack=w.slack)
-    oc = torch.empty_like(q); of = torch.empty_like(q)
-    lc = torch.empty((w.U, w.Hq), device=dev); lfu = torch.empty_like(lc)
-    B.kvc_decode_attn(q, L.kc, L.vc, L.start, L.len, oc, lc, k_new=kn, v_new=vn,
-                      max_len=w.T + 1, scale=w.scale)
+    B.kvc_compact(L.k, L.v, allk, allc, allo, kf, vf, sf, lf, slack=w.slack + 1)
+    of = torch.empty_like(q)
+    lfu = torch.empty((w.U, w.Hq), device=dev)
     B.kvc_decode_attn(q, kf, vf, sf, lf, of, lfu, k_new=kn, v_new=vn, max_len=w.T + 1,
                       scale=w.scale)
-    rel = torch.empty(w.U * w.Hq, device=dev); kl = torch.empty_like(rel)
-    B.kvc_fidelity(oc, of, lc, lfu, rel, kl)
-    torch.cuda.synchronize()
-    return {"workload": WORKLOAD, "keep_ratio": w.keep_ratio,
-            "rel_err_mean": float(rel.mean()), "rel_err_max": float(rel.max()),
-            "kl_mean": float(kl.mean()), "kl_max": float(kl.max())}
+    res = {"workload": WORKLOAD, "keep_ratio": w.keep_ratio}
+    for name, scores in (("score", None),
+                         ("random_eviction", inputs.random_scores((w.U, w.Hkv, w.T), dev,
+                                                                  seed=404))):
+        if scores is None:
+            L.score()
+        else:
+            L.scores.copy_(scores)
+        L.select()
+        # one slack row per head for the probe's appended token
+        B.kvc_compact(L.k, L.v, L.kept, L.counts, L.offs, L.kc, L.vc, L.start, L.len, slack=1)
+        oc = torch.empty_like(q)
+        lc = torch.empty((w.U, w.Hq), device=dev)
+        B.kvc_decode_attn(q, L.kc, L.vc, L.start, L.len, oc, lc, k_new=kn, v_new=vn,
+                          max_len=w.T + 1, scale=w.scale)
+        rel = torch.empty(w.U * w.Hq, device=dev); kl = torch.empty_like(rel)
+        B.kvc_fidelity(oc, of, lc, lfu, rel, kl)
+        torch.cuda.synchronize()
+        d = {"rel_err_mean": float(rel.mean()), "rel_err_max": float(rel.max()),
+             "kl_mean": float(kl.mean()), "kl_max": float(kl.max()),
+             "retained_mass_mean": float(torch.exp(-kl).mean())}
+        if scores is None:
+            res.update(d)
+        else:
+            res[name] = d
+    assert B.kvc_device_status() == 0
+    del kf, vf
+    return res
 
 
 # ----------------------------------------------------------- CPU oracle
@@ -907,7 +1038,8 @@ def main():
     fid = fidelity_probe(B, L)
     del L
     torch.cuda.empty_cache()
-    dec = bench_decode(B, max(16, args.steps), max(3, args.warmup), device)
+    dec = bench_decode(B, inputs.WORKLOADS[DECODE_WORKLOAD].decode_steps, max(3, args.warmup),
+                       device)
     dec["frac"] = dec["gbs"] / hbm
     dec["peak_gbs"] = hbm
     c4 = bench_c4(B, max(3, args.steps // 4), 3, device)
@@ -941,8 +1073,14 @@ def main():
                      "traffic": profiled_traffic("score_tc.cu", "score_tc_c2_llama32k_traffic.json"),
                      "algorithmic_bytes": score_bytes,
                      "tensor_tflops": score_flops / (score_ms * 1e-3) / 1e12,
-                     "tensor_frac": score_flops / (score_ms * 1e-3) / 1e12 / bf16},
+                     "tensor_frac": score_flops / (score_ms * 1e-3) / 1e12 / bf16,
+                     # the contraction the kernel issues: both of its passes
+                     "tensor_tflops_issued": SCORE_PASSES * score_flops / (score_ms * 1e-3) / 1e12,
+                     "tensor_frac_issued": SCORE_PASSES * score_flops / (score_ms * 1e-3) / 1e12 / bf16},
         "decode": dec,
+        # the other workloads' whole-step throughput (score + select + compact)
+        "tokens_per_s_c3_32layer": c3["tokens_per_s"],
+        "tokens_per_s_c4_qwen128k": c4["tokens_per_s"],
         "c4_qwen128k": c4,
         "c3_32layer": c3,
         "vector": vec,

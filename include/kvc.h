@@ -265,6 +265,11 @@ int kvc_select(const float* scores, int U, int Hkv, int T, int mode,
  * kc, vc   [capacity_rows, d] dtype; capacity_rows must be at least
  *          offsets[U*Hkv] + U*Hkv*slack_per_head (the device checks every
  *          row and records KVC_ERR_RANGE instead of writing past it).
+ * The device also checks the offsets against counts and T before it reads
+ * an index: a row j of head i with j < 0, j >= counts[i] or j >= T (offsets
+ * that disagree with counts), or a kept index outside [0, T), is skipped
+ * and recorded as KVC_ERR_RANGE; an offsets total outside [0, U*Hkv*T]
+ * copies nothing and records KVC_ERR_RANGE.
  * start    [U*Hkv] int64 (written), len [U*Hkv] int32 (written = counts).
  * Requires d * element size to be a multiple of 16 bytes and 16-byte aligned
  * k, v, kc, vc.
@@ -476,16 +481,20 @@ int kvc_decode_attn_vector(const void* q, void* kc, void* vc, const int64_t* kst
  *
  * Same arguments, semantics and results as kvc_decode_attn, minus the
  * workspace.  The split-K scratch is a fixed array of
- * KVC_DECODE_NOALLOC_SCRATCH_BYTES in the library's device memory, reserved
- * on every GPU that loads the library until the process exits.  Nothing is
- * allocated or freed by the call.
+ * KVC_DECODE_NOALLOC_SCRATCH_BYTES in the library's device memory, held on
+ * every GPU where the library's device code has been loaded until the process
+ * exits.  The call itself allocates and frees nothing.
  *  - Limit: sizes with kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype) >
  *    KVC_DECODE_NOALLOC_SCRATCH_BYTES are refused with KVC_ERR_WORKSPACE
  *    before any CUDA call (e.g. 64 x 8 kv heads, G = 4, d = 128 fit up to
  *    max_len = 7680).
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make it before any
- *    stream capture.
+ *    (cudaGetSymbolAddress) with that device current.  With CUDA's lazy
+ *    module loading (the default) that lookup is also what loads the module
+ *    and so reserves the array on that device: the first call can fail with
+ *    KVC_ERR_CUDA when the device's memory is already committed.  Make the
+ *    first call on each device at start-up, before the caller commits its
+ *    device memory and before any stream capture.
  *  - All calls on a device share the array: calls whose kernels can overlap
  *    on the GPU race and must be serialised by the caller.  The array keeps
  *    the last call's contents; nothing in it needs clearing, since each step

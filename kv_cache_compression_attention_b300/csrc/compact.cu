@@ -59,7 +59,14 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int vpr
     start[i] = offs[i] + (int64_t)i * slack;
     len[i] = counts[i];
   }
+  // The offsets come from the caller.  A total outside [0, n_heads * T]
+  // cannot describe kept rows of this cache: report it and copy nothing
+  // (this also bounds the task loop below).
   const int64_t total = offs[n_heads];
+  if (total < 0 || total > (int64_t)n_heads * T) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(status, KVC_ERR_RANGE);
+    return;
+  }
   const int64_t tasks = (total + kBlockRows - 1) / kBlockRows;
   const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
@@ -78,14 +85,21 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int vpr
     if (lane < kBlockRows && r < total) {
       int i = lo;
       while (i + 1 < n_heads && offs[i + 1] <= r) ++i;
+      // row j of head i: checked against the head's count and T before its
+      // index is read (offsets that disagree with the counts are the
+      // caller's error and are reported, never followed)
       const int64_t j = r - offs[i];
-      const int32_t t = __ldg(kept_idx + (int64_t)i * T + j);
       const int64_t dst = r + (int64_t)i * slack;
-      if (t < 0 || t >= T || j >= __ldg(counts + i) || dst >= capacity_rows) {
+      if (j < 0 || j >= T || j >= __ldg(counts + i) || dst >= capacity_rows) {
         report(status, KVC_ERR_RANGE);
       } else {
-        src_row = (int64_t)i * T + t;
-        dst_row = dst;
+        const int32_t t = __ldg(kept_idx + (int64_t)i * T + j);
+        if (t < 0 || t >= T) {
+          report(status, KVC_ERR_RANGE);
+        } else {
+          src_row = (int64_t)i * T + t;
+          dst_row = dst;
+        }
       }
     }
     const int nrows = (int)((total - r0) < kBlockRows ? (total - r0) : kBlockRows);

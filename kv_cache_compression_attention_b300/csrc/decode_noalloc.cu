@@ -8,14 +8,18 @@
 // workspace, or a caller whose device-memory budget is fixed at start-up and
 // must not grow (or stall the device, which cudaMalloc may do) in the middle
 // of serving.  This entry point serves them: its scratch is a fixed array in
-// the library's own device memory, reserved when the library is loaded on a
-// GPU and held by every GPU that loads it until the process exits.
+// the library's own device memory, held on each GPU where the library's
+// device code is loaded until the process exits.
 //
 // Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
 // routine.  The first call on a device looks up the array's device address
 // with cudaGetSymbolAddress (in host code the array's name is only a host
-// stand-in, not a device address) and caches it; make that first call before
-// any stream capture.  Every call on a device shares the one array, so calls
+// stand-in, not a device address) and caches it.  Under CUDA's lazy module
+// loading (the default) that lookup is what loads the module on the device,
+// so the array is reserved inside the first call, which then fails with
+// KVC_ERR_CUDA if the device has no memory left: make that first call at
+// start-up, before the caller commits its device memory and before any
+// stream capture.  Every call on a device shares the one array, so calls
 // whose kernels overlap on the GPU (different streams, no ordering between
 // them) race on it; serialise them.  The array keeps the last call's
 // contents, and nothing in it has to start at zero: every record the step

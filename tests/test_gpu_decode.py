@@ -249,3 +249,83 @@ def test_decode_more_chunks_than_the_combine_stages(B):
                                np64(kn), np64(vn), 128 ** -0.5)
     assert row_rel_err(np64(out).reshape(-1, 128), ro.reshape(-1, 128)) <= 2e-2
     assert lse_err(np64(lse), rl) <= 2e-2
+
+
+def test_decode_fidelity_c5_sequence_against_oracle(B):
+    """The batch-64 decode workload as configured, on one sampled sequence:
+    its compressed cache is cut from its full 32k cache (window scores ->
+    per-head top-k at its budgets, 4 sinks + 64 recent -> compaction with 256
+    slack rows), then 256 decode steps run over the compressed and the full
+    cache.  The GPU selection is fed the oracle's scores (the bit-exact
+    contract), so both sides hold the same kept tokens; the fidelity of steps
+    0 and 255 (rel-L2 output error, KL = lse_full - lse_comp, [Sculpt] §4) is
+    compared with the oracle's, which follows every append on its own copies."""
+    w = inputs.WORKLOADS["c5_decode"]
+    u = 37
+    q_all = inputs.window_queries(w, "cuda")
+    k_all, v_all = inputs.keys_values(w, q_all, "cuda")
+    qw, k, v = q_all[u:u + 1].contiguous(), k_all[u:u + 1].contiguous(), v_all[u:u + 1].contiguous()
+    del q_all, k_all, v_all
+    torch.cuda.empty_cache()
+    n = w.Hkv
+    budgets = inputs.head_budgets(w, "cpu")[u * n:(u + 1) * n]
+    s_ref = O.score_attn(np64(qw), np64(k), w.scale).astype(np.float32)
+    r_kept, r_counts, r_offs = O.select(s_ref, "per_head", head_budget=budgets.numpy(),
+                                        n_sink=w.n_sink, n_recent=w.n_recent)
+    kept = torch.empty((n, w.T), dtype=torch.int32, device="cuda")
+    counts = torch.empty(n, dtype=torch.int32, device="cuda")
+    offs = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+    B.kvc_select(torch.from_numpy(s_ref).cuda(), "per_head", kept, counts, offs,
+                 head_budget=budgets.cuda(), n_sink=w.n_sink, n_recent=w.n_recent)
+    np.testing.assert_array_equal(counts.cpu().numpy(), r_counts)
+    np.testing.assert_array_equal(offs.cpu().numpy(), r_offs)
+
+    def gpu_pool(kept_, counts_, offs_):
+        rows = int(offs_[-1].item()) + n * w.slack
+        kc = torch.zeros((rows, w.d), dtype=k.dtype, device="cuda")
+        vc = torch.zeros_like(kc)
+        st = torch.empty(n, dtype=torch.int64, device="cuda")
+        ln = torch.empty(n, dtype=torch.int32, device="cuda")
+        B.kvc_compact(k, v, kept_, counts_, offs_, kc, vc, st, ln, slack=w.slack)
+        return kc, vc, st, ln
+
+    comp = gpu_pool(kept, counts, offs)
+    all_np = np.tile(np.arange(w.T, dtype=np.int32), (n, 1))
+    allc_np = np.full(n, w.T, dtype=np.int32)
+    allo_np = np.arange(n + 1, dtype=np.int64) * w.T
+    full = gpu_pool(torch.from_numpy(all_np).cuda(), torch.from_numpy(allc_np).cuda(),
+                    torch.from_numpy(allo_np).cuda())
+    # the oracle's own caches, from its own selection
+    kh, vh = np64(k), np64(v)
+    o_comp = list(O.compact(kh, vh, r_kept, r_counts, r_offs, w.slack))
+    o_full = list(O.compact(kh, vh, all_np, allc_np, allo_np, w.slack))
+    max_len = w.T + w.decode_steps
+    rel = torch.empty(w.Hq, device="cuda")
+    kl = torch.empty_like(rel)
+    for step in range(w.decode_steps):
+        q, kn, vn = inputs.decode_step_inputs(w, step, "cuda")
+        q, kn, vn = q[u:u + 1].contiguous(), kn[u:u + 1].contiguous(), vn[u:u + 1].contiguous()
+        oc = torch.empty_like(q); of = torch.empty_like(q)
+        lc = torch.empty((1, w.Hq), device="cuda"); lf = torch.empty_like(lc)
+        B.kvc_decode_attn(q, *comp, oc, lc, k_new=kn, v_new=vn, max_len=max_len, scale=w.scale)
+        B.kvc_decode_attn(q, *full, of, lf, k_new=kn, v_new=vn, max_len=max_len, scale=w.scale)
+        B.kvc_fidelity(oc, of, lc, lf, rel, kl)
+        qs, kns, vns = np64(q), np64(kn), np64(vn)
+        if step in (0, w.decode_steps - 1):
+            roc, rlc, o_comp[0], o_comp[1], o_comp[3] = O.decode_attn(
+                qs, o_comp[0], o_comp[1], o_comp[2], o_comp[3], kns, vns, w.scale)
+            rof, rlf, o_full[0], o_full[1], o_full[3] = O.decode_attn(
+                qs, o_full[0], o_full[1], o_full[2], o_full[3], kns, vns, w.scale)
+            r_rel, r_kl = O.fidelity(roc, rof, rlc, rlf)
+            torch.cuda.synchronize()
+            assert B.kvc_device_status() == 0
+            g_kl, g_rel = np64(kl), np64(rel)
+            tol = 2e-2 * np.maximum(1.0, np.abs(rlf.reshape(-1)))
+            assert (np.abs(g_kl - r_kl.reshape(-1)) <= tol).all(), step
+            assert (r_kl >= -1e-9).all()                     # a subset retains mass <= 1
+            assert (np.abs(g_rel - r_rel.reshape(-1)) <= 2e-2 * np.maximum(1.0, r_rel.reshape(-1))).all(), step
+        else:
+            for arrs in (o_comp, o_full):
+                _, _, arrs[0], arrs[1], arrs[3] = _append_only(qs, arrs[0], arrs[1], arrs[2],
+                                                               arrs[3], kns, vns)
+    np.testing.assert_array_equal(comp[3].cpu().numpy(), r_counts + w.decode_steps)

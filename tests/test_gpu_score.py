@@ -110,8 +110,33 @@ def test_score_attn_llama32k_full(B):
     got = np64(gpu_scores(B, q, k, w.scale))
     ref = O.score_attn(np64(q), np64(k), w.scale)
     assert mass_rel_err(got, ref) <= 2e-2
-    # the sinks dominate and every needle outranks the median token
-    assert (got[:, :, :4].min() > np.median(got))
+    # the sinks and every needle outrank the median token of their head
+    pos = inputs.needle_positions(w).numpy()[0]
+    med = np.median(got, axis=-1)                     # [U, Hkv]
+    assert (got[0, :, :4] > med[0, :, None]).all()
+    assert (got[0][:, pos] > med[0, :, None]).all()
+
+
+def test_score_attn_tiny_workload_keeps_every_needle(B):
+    """The GPU scores of the tiny workload, selected at keep 0.25 by the GPU
+    top-k, keep all 16 needles in every kv head (the oracle's pin of the same
+    structure is a CPU test)."""
+    w = inputs.WORKLOADS["c1_tiny"]
+    q = inputs.window_queries(w, "cuda")
+    k, _ = inputs.keys_values(w, q, "cuda")
+    s = gpu_scores(B, q, k, w.scale)
+    n = w.U * w.Hkv
+    kept = torch.empty((n, w.T), dtype=torch.int32, device="cuda")
+    counts = torch.empty(n, dtype=torch.int32, device="cuda")
+    offs = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+    B.kvc_select(s, "global", kept, counts, offs, keep_ratio=w.keep_ratio, n_sink=w.n_sink,
+                 n_recent=w.n_recent)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    pos = set(inputs.needle_positions(w).numpy()[0].tolist())
+    kept, counts = kept.cpu().numpy(), counts.cpu().numpy()
+    for g in range(n):
+        assert pos <= set(kept[g, : counts[g]].tolist()), g
 
 
 def test_score_attn_32layer_sampled_units(B):

@@ -233,3 +233,32 @@ def test_compact_reports_capacity_overflow_without_writing_past(B):
     assert B.kvc_device_status() == -6            # KVC_ERR_RANGE
     assert B.kvc_device_status() == 0             # cleared
     assert guard[T + 5:].abs().sum().item() == 0  # nothing written past the capacity
+
+
+@pytest.mark.parametrize("case", ["first_offset_not_zero", "step_beyond_T", "total_beyond_cache"])
+def test_compact_rejects_offsets_that_disagree_with_counts(B, case):
+    """Offsets are caller data: rows they place outside a head's count (or
+    outside T) are reported as KVC_ERR_RANGE before any index is read, and
+    nothing is written outside the stated capacity."""
+    U, Hkv, T, d = 1, 2, 64, 128
+    k = torch.randn((U, Hkv, T, d), device="cuda").to(torch.bfloat16)
+    v = torch.randn_like(k)
+    kept = np.tile(np.arange(T, dtype=np.int32), (2, 1))
+    counts = np.array([10, 12], dtype=np.int32)
+    if case == "first_offset_not_zero":
+        offs = np.array([5, 15, 27], dtype=np.int64)       # rows 0..4 belong to no head
+    elif case == "step_beyond_T":
+        offs = np.array([0, T + 7, T + 19], dtype=np.int64)  # head 0 spans more than T rows
+    else:
+        offs = np.array([0, 10, 3 * T], dtype=np.int64)      # total above U * Hkv * T
+    cap = 40
+    guard = torch.zeros((cap + 16, d), dtype=torch.bfloat16, device="cuda")
+    vguard = torch.zeros_like(guard)
+    start = torch.empty(2, dtype=torch.int64, device="cuda")
+    length = torch.empty(2, dtype=torch.int32, device="cuda")
+    B.kvc_compact(k, v, torch.as_tensor(kept).cuda(), torch.as_tensor(counts).cuda(),
+                  torch.as_tensor(offs).cuda(), guard[:cap], vguard[:cap], start, length)
+    assert B.kvc_device_status() == -6            # KVC_ERR_RANGE
+    assert B.kvc_device_status() == 0             # cleared
+    assert guard[cap:].abs().sum().item() == 0    # nothing written past the capacity
+    assert vguard[cap:].abs().sum().item() == 0

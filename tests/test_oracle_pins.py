@@ -304,6 +304,31 @@ def test_threshold_keep_fraction_matches_gaussian_tail():
     assert abs(frac - 0.30854) < 0.01
 
 
+
+def test_tiny_workload_keeps_every_needle():
+    """Statistical sanity of the sink / needle construction (keys aligned with
+    the group's mean window-query direction: 4 sqrt(d) u for the sinks, 3 sqrt(d)
+    u + noise for the needles): on the tiny workload at keep ratio 0.25 the
+    oracle's global top-k keeps all 16 needles in every kv head, and the
+    needles are the highest-scoring tokens after the four sinks.  If this
+    fails, the generator does not build the structure the fidelity probe
+    relies on ([KVTC] §2A sinks; [KVzap] §2.1 attention-based scores)."""
+    from kv_cache_compression_attention_b300 import inputs
+    w = inputs.WORKLOADS["c1_tiny"]
+    q = inputs.window_queries(w)
+    k, _ = inputs.keys_values(w, q)
+    s = O.score_attn(q.double().numpy(), k.double().numpy(), w.scale)
+    kept, counts, _ = O.select(s.astype(np.float32), "global", keep_ratio=w.keep_ratio,
+                               n_sink=w.n_sink, n_recent=w.n_recent)
+    pos = inputs.needle_positions(w).numpy()[0]
+    assert pos.size == 16
+    for g in range(w.Hkv):
+        kept_g = set(kept[g, : counts[g]].tolist())
+        assert all(int(p) in kept_g for p in pos), g
+        order = np.argsort(-s[0, g], kind="stable")
+        assert set(order[:4].tolist()) == set(range(4))             # the sinks first
+        assert set(order[4:4 + pos.size].tolist()) == set(pos.tolist())   # then the needles
+
 # ------------------------------------------------------------ selection
 @pytest.mark.parametrize("seed", range(4))
 @pytest.mark.parametrize("ties,specials", [(False, False), (True, False), (True, True)])

@@ -4,11 +4,13 @@ A plug-in inside a host engine that owns every device allocation, or a
 caller whose device-memory budget is fixed at start-up, cannot hand
 kvc_decode_attn a workspace.  kvc_decode_attn_noalloc takes its split-K
 scratch from a fixed array in the library's own device memory instead.  The
-GPU test calls both entry points through the C ABI on identical copies of one
-compressed cache, two decode steps in a row (each appending a token), and
-checks that outputs, lse, lengths and the appended rows agree within the
-tolerance of the other decode tests.  The host test checks the refusals that
-happen before any CUDA call.
+GPU test first leaves non-zero records of a larger call in that array, then
+calls both entry points through the C ABI on identical copies of one
+compressed cache, two decode steps in a row (each appending a token): both
+run the same kernels on the same split, so outputs, lse, lengths and the
+appended rows must agree bit for bit; the outputs are also checked against
+the CPU oracle's decode within the tolerance of the other decode tests.  The
+host test checks the refusals that happen before any CUDA call.
 
 This file is collected last on purpose: the shared scratch array keeps the
 previous call's contents, and the test must pass after every other test as
@@ -57,15 +59,31 @@ def test_noalloc_matches_workspace_entry_point_two_calls(dtype):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     from kv_cache_compression_attention_b300 import binding as B
+    from oracle import kvc_oracle as O
     B.lib()
     U, Hkv, G, d, slack = 2, 3, 4, 128, 2
+    g = torch.Generator().manual_seed(22)
+    # a larger call first, with other lengths, so that the shared array holds
+    # non-zero records at the offsets the checked calls use
+    dl = [3000, 7, 1500, 2999, 640, 1]
+    dk, dv, ds, dn = [t.cuda() for t in _pool(dl, 1, d, dtype, 23)]
+    dq = torch.randn((U, Hkv * G, d), generator=g).to(dtype).cuda()
+    dout = torch.empty_like(dq)
+    B.kvc_decode_attn_noalloc(dq, dk, dv, ds, dn, dout, None, max_len=max(dl) + 1,
+                              scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    del dk, dv, ds, dn, dq, dout
+
     lens = [0, 1, 511, 512, 513, 2000]
     kc, vc, start, length = _pool(lens, slack, d, dtype, 21)
     # two identical copies: one for each entry point
     a = [t.cuda() for t in (kc, vc, start, length)]
     b = [t.clone().cuda() for t in (kc, vc, start, length)]
+    # the oracle's own copy of the cache state (float64 arrays)
+    o_kc, o_vc = np64(kc), np64(vc)
+    o_start, o_len = start.numpy(), length.numpy()
     max_len = max(lens) + slack
-    g = torch.Generator().manual_seed(22)
     for step in range(2):
         q = torch.randn((U, Hkv * G, d), generator=g).to(dtype).cuda()
         kn = torch.randn((U, Hkv, d), generator=g).to(dtype).cuda()
@@ -80,9 +98,15 @@ def test_noalloc_matches_workspace_entry_point_two_calls(dtype):
                                   v_new=vn, max_len=max_len, scale=d ** -0.5)
         torch.cuda.synchronize()
         assert B.kvc_device_status() == 0
-        assert row_rel_err(np64(out_b).reshape(-1, d), np64(out_a).reshape(-1, d)) <= TOL[dtype]
-        assert lse_err(np64(lse_b), np64(lse_a)) <= TOL[dtype]
+        # same kernels, same split: identical bits
+        np.testing.assert_array_equal(out_b.cpu().float().numpy(), out_a.cpu().float().numpy())
+        np.testing.assert_array_equal(lse_b.cpu().numpy(), lse_a.cpu().numpy())
         np.testing.assert_array_equal(b[3].cpu().numpy(), a[3].cpu().numpy())
         np.testing.assert_array_equal(b[0].cpu().float().numpy(), a[0].cpu().float().numpy())
         np.testing.assert_array_equal(b[1].cpu().float().numpy(), a[1].cpu().float().numpy())
+        # and the oracle's decode of the same step
+        r_out, r_lse, o_kc, o_vc, o_len = O.decode_attn(np64(q), o_kc, o_vc, o_start, o_len,
+                                                        np64(kn), np64(vn), d ** -0.5)
+        assert row_rel_err(np64(out_b).reshape(-1, d), r_out.reshape(-1, d)) <= TOL[dtype]
+        assert lse_err(np64(lse_b), r_lse) <= TOL[dtype]
     np.testing.assert_array_equal(b[3].cpu().numpy(), np.asarray(lens) + 2)
