@@ -24,8 +24,6 @@
  *  - Pointers are DEVICE pointers owned by the caller unless stated.  The
  *    library never allocates or frees device memory; steps that need scratch
  *    take a caller-provided workspace whose size a *_workspace() query gives.
- *    (One exception: the first kvc_score_mlp call on a device creates the
- *    cuBLAS handle its GEMM runs on, and cuBLAS allocates its own state.)
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream).  Nothing synchronises except
  *    kvc_device_status().
@@ -183,9 +181,10 @@ int kvc_score_kvzip_plus(const void* q_win, const void* k, const void* v, const 
                          int d, float scale, const float* head_scale, int causal, float* scores,
                          void* workspace, size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace kvc_score_mlp needs: the bf16 first-layer output
- * [U*T, Dm] (rounded up to 256 bytes) plus 32 MiB of GEMM scratch. */
-size_t kvc_score_mlp_workspace(int U, int T, int Dm);
+/* Bytes of workspace kvc_score_mlp needs: the first-layer weight transposed
+ * to [Dm', Dh] bf16, Dm' = Dm rounded up to 32 (to 64 when Dm > 512), rounded
+ * up to 256 bytes.  0 for a non-positive Dh or Dm. */
+size_t kvc_score_mlp_workspace(int Dh, int Dm);
 
 /*
  * Two-layer surrogate score ([KVzap] §2.2, the MLP variant: hidden width
@@ -194,13 +193,15 @@ size_t kvc_score_mlp_workspace(int U, int T, int Dm);
  *   scores[u,g,t] = b2[g] + sum_m GELU(z[u,t,m]) * w2[m,g],
  *   GELU(z) = z (1 + erf(z / sqrt 2)) / 2.
  * hidden [U, T, Dh], w1 [Dh, Dm], w2 [Dm, Hkv] dtype (KVC_BF16); b1 [Dm],
- * b2 [Hkv] fp32 or NULL; scores [U, Hkv, T] fp32.  The first layer is a
- * cuBLAS bf16 GEMM with fp32 accumulation whose output is rounded to bf16
- * in the workspace; bias, GELU and the second layer accumulate in fp32.
+ * b2 [Hkv] fp32 or NULL; scores [U, Hkv, T] fp32.  The first layer runs on
+ * the tensor cores (bf16 products, fp32 accumulation in TMEM); each z is
+ * rounded to bf16 when the epilogue takes it out of TMEM, and bias, GELU and
+ * the second layer accumulate in fp32.  Two launches: w1 transposed into the
+ * workspace, then the fused kernel (up to 512 columns of z per pass over the
+ * hidden states; Dm > 512 takes two passes).
  * Requires Dh % 8 == 0, Dm % 8 == 0, Dm <= 1024, 1 <= Hkv <= 8, 16-byte
  * aligned hidden and w1, a 256-byte aligned workspace of
- * kvc_score_mlp_workspace bytes.  The first call on a device creates a
- * cuBLAS handle there (cuBLAS allocates its own small state once).
+ * kvc_score_mlp_workspace(Dh, Dm) bytes.
  */
 int kvc_score_mlp(const void* hidden, const void* w1, const float* b1, const void* w2,
                   const float* b2, int dtype, int U, int T, int Dh, int Dm, int Hkv,

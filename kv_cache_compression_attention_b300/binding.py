@@ -53,7 +53,7 @@ SIGNATURES = {
     "kvc_score_kvzip_plus_workspace": (_SZ, [_I, _I, _I, _I, _I]),
     "kvc_score_kvzip_plus": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P,
                                   _P, _SZ, _P]),
-    "kvc_score_mlp_workspace": (_SZ, [_I, _I, _I]),
+    "kvc_score_mlp_workspace": (_SZ, [_I, _I]),
     "kvc_score_mlp": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_vector_residual": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
     "kvc_vector_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I64,
@@ -191,7 +191,7 @@ def kvc_score_mlp(hidden, w1, b1, w2, b2, scores, workspace=None, stream=None):
     w2 [Dm, Hkv] bf16, b2 [Hkv] fp32 -> scores [U, Hkv, T] fp32."""
     U, T, Dh = hidden.shape
     Dm, Hkv = w2.shape
-    need = lib().kvc_score_mlp_workspace(U, T, Dm)
+    need = lib().kvc_score_mlp_workspace(Dh, Dm)
     if workspace is None:
         workspace = _workspace(need, hidden.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -77,7 +77,7 @@ def build(verbose: bool = False, ptxas_v: bool = False, jobs: int | None = None)
             if log:
                 print(log, file=sys.stderr)
     if _stale(LIB, objs):
-        cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcublas"]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

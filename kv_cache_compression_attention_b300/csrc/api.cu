@@ -317,9 +317,9 @@ int kvc_score_kvzip_plus(const void* q_win, const void* k, const void* v, const 
                                       kvc::as_stream(stream));
 }
 
-size_t kvc_score_mlp_workspace(int U, int T, int Dm) {
-  if (U < 0 || T < 0 || Dm <= 0) return 0;
-  return kvc::score_mlp_ws_bytes(U, T, Dm);
+size_t kvc_score_mlp_workspace(int Dh, int Dm) {
+  if (Dh <= 0 || Dm <= 0) return 0;
+  return kvc::score_mlp_ws_bytes(Dh, Dm);
 }
 
 int kvc_score_mlp(const void* hidden, const void* w1, const float* b1, const void* w2,
@@ -331,7 +331,7 @@ int kvc_score_mlp(const void* hidden, const void* w1, const float* b1, const voi
   if (dtype != KVC_BF16 || Dh % 8 || Dm % 8 || Dm > 1024 || Hkv > 8) return KVC_ERR_UNSUPPORTED;
   if (!aligned16(hidden) || !aligned16(w1)) return KVC_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVC_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < kvc::score_mlp_ws_bytes(U, T, Dm)) return KVC_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < kvc::score_mlp_ws_bytes(Dh, Dm)) return KVC_ERR_WORKSPACE;
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;

@@ -149,7 +149,7 @@ int score_kvzip_plus_launch(const void* q, const void* k, const void* v, const v
                             const float* hnorm, int U, int Hq, int Hkv, int T, int W,
                             float scale, const float* head_scale, int causal, float* scores,
                             void* workspace, const Dev& dev, cudaStream_t s);
-size_t score_mlp_ws_bytes(int U, int T, int Dm);
+size_t score_mlp_ws_bytes(int Dh, int Dm);
 int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const void* w2,
                      const float* b2, int U, int T, int Dh, int Dm, int Hkv, float* scores,
                      void* workspace, const Dev& dev, cudaStream_t s);

@@ -248,7 +248,10 @@ def test_score_mlp_rejects_bad_arguments(lib):
     assert f(*bad) == -2                                        # workspace not 256-byte aligned
     bad = list(ok); bad[13] = 1000
     assert f(*bad) == -3
-    assert lib.kvc_score_mlp_workspace(1, 131072, 448) == 131072 * 448 * 2 + (32 << 20)
+    assert lib.kvc_score_mlp_workspace(3584, 448) == 448 * 3584 * 2        # w1 transposed
+    assert lib.kvc_score_mlp_workspace(512, 16) == 32 * 512 * 2            # rows padded to 32
+    assert lib.kvc_score_mlp_workspace(4096, 1000) == 1024 * 4096 * 2      # two passes of 512
+    assert lib.kvc_score_mlp_workspace(0, 448) == 0
 
 
 def test_score_kvzip_plus_rejects_bad_arguments(lib):

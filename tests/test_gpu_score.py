@@ -195,7 +195,12 @@ def test_score_attn_rejects_non_positive_temperature_on_device(B, dtype, d, G, W
     assert B.kvc_device_status() == 0
 
 
-@pytest.mark.parametrize("Hkv,Dh,Dm,T", [(4, 256, 32, 300), (1, 512, 64, 77), (8, 128, 16, 1000)])
+@pytest.mark.parametrize("Hkv,Dh,Dm,T", [
+    (4, 256, 32, 300), (1, 512, 64, 77), (8, 128, 16, 1000),
+    (4, 3584, 448, 257),      # the 128k layer's widths: two MMAs of N = 224, ragged row tile
+    (3, 200, 520, 129),       # Dh not a multiple of the 64-wide k-block; two passes of 288
+    (8, 1024, 1000, 333),     # two passes of 512 columns, padded rows of W1t
+])
 def test_score_mlp_small(B, Hkv, Dh, Dm, T):
     U = 2
     g = torch.Generator().manual_seed(97 + Hkv)
