@@ -62,7 +62,8 @@ struct Params {
   int n_tiles;       // 128-row tiles
   int n_pass;        // 1 or 2
   int np;            // columns per pass (multiple of 32, <= 512)
-  int bn;            // columns per MMA / per B box (np or np / 2, <= 256)
+  int bn;            // columns per MMA (np or np / 2, <= 256)
+  int bw;            // rows per W1t box (a CTA's share of the slab, <= 256)
   int stages;
   const float* b1;
   const uint16_t* w2;   // bf16 [Dm, Hkv]
@@ -98,6 +99,27 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// The same load delivered to every CTA of the cluster in `mask` (same
+// shared-memory offset and mbarrier offset in each).
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask),
+      "l"(policy)
+      : "memory");
+}
+
+// Arrive on the mbarrier at the same offset in every CTA of `mask` once the
+// tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 
@@ -167,9 +189,17 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
   const uint32_t stage_bytes = kABytes + b_bytes;
   const int S = p.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // cluster of cl CTAs (1 or 2): each CTA streams its own hidden rows and 1/cl
+  // of every W1t slab, delivered to all of them; a slab is refilled only when
+  // every CTA of the cluster has finished with it
+  const int cl = (int)tc::cluster_nctarank();
+  const int rank = (int)tc::cluster_ctarank();
+  const uint16_t cmask = (uint16_t)((1u << cl) - 1u);
+  const int n_groups = (p.n_tiles + cl - 1) / cl;
+  const int group0 = blockIdx.x / cl, group_step = gridDim.x / cl;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], 1); }
+    for (int s = 0; s < S; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], cl); }
     mbar_init(&sm.tmem_full, 1);
     mbar_init(&sm.tmem_empty, kEpiWarps);
     sm.abort_flag = 0;
@@ -177,6 +207,9 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
   }
   if (warp == kMmaWarp) tc::tmem_alloc(&sm.tmem_base, kTmemCols);
   __syncthreads();
+  // the peers' barriers are initialised before any multicast reaches them
+  tc::cluster_arrive();
+  tc::cluster_wait();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
@@ -189,8 +222,11 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
       tc::prefetch_tmap(&tm_h);
       tc::prefetch_tmap(&tm_w);
       const uint64_t pol_h = policy_evict_first(), pol_w = policy_evict_last();
+      // this CTA's share of a slab: rows [rank * rpc, (rank + 1) * rpc) in boxes of bw
+      const int rpc = p.np / cl, bw = p.bw;
       int J = 0;
-      for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x)
+      for (int grp = group0; grp < n_groups; grp += group_step) {
+        const int tile = grp * cl + rank;      // past the last tile: zero rows, not stored
         for (int ps = 0; ps < p.n_pass; ++ps)
           for (int kb = 0; kb < p.n_kb; ++kb, ++J) {
             const int s = J % S;
@@ -198,14 +234,23 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             const uint32_t dst = st0 + (uint32_t)s * stage_bytes;
             mbar_arrive_expect_tx(&sm.full[s], stage_bytes);
             tma_load_2d_hint(dst, &tm_h, kb * kKBlock, tile * kTileRows, &sm.full[s], pol_h);
-            for (int j = 0; j < p.np / p.bn; ++j)
-              tma_load_2d_hint(dst + kABytes + (uint32_t)j * p.bn * 128u, &tm_w, kb * kKBlock,
-                               ps * p.np + j * p.bn, &sm.full[s], pol_w);
+            for (int r0 = rank * rpc; r0 < (rank + 1) * rpc; r0 += bw) {
+              const uint32_t bdst = dst + kABytes + (uint32_t)r0 * 128u;
+              if (cl > 1)
+                tma_load_2d_mc(bdst, &tm_w, kb * kKBlock, ps * p.np + r0, &sm.full[s], cmask,
+                               pol_w);
+              else
+                tma_load_2d_hint(bdst, &tm_w, kb * kKBlock, ps * p.np + r0, &sm.full[s], pol_w);
+            }
           }
-      // every load issued has landed before the CTA can exit (normally the
-      // MMA warp saw them all; after a timeout it may not have)
-      for (int j = (J > S ? J - S : 0); j < J; ++j)
+      }
+      // every load into this CTA has landed and every CTA of the cluster has
+      // released the last use of every stage before the CTA can exit
+      // (normally all of this is long done; after a timeout it may not be)
+      for (int j = (J > S ? J - S : 0); j < J; ++j) {
         mbar_wait(&sm.full[j % S], (j / S) & 1, p.status, nullptr);
+        mbar_wait(&sm.empty[j % S], (j / S) & 1, p.status, nullptr);
+      }
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
@@ -213,7 +258,7 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
       const uint32_t idesc = tc::idesc_bf16_f32(kTileRows, p.bn);
       const int nb = p.np / p.bn;
       int J = 0, item = 0;
-      for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x)
+      for (int grp = group0; grp < n_groups; grp += group_step)
         for (int ps = 0; ps < p.n_pass; ++ps, ++item) {
           // the epilogue has drained the previous item's accumulator
           if (item > 0) mbar_wait(&sm.tmem_empty, (item - 1) & 1, p.status, abort_flag);
@@ -232,7 +277,8 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 tc::mma_bf16(tmem + (uint32_t)(j * p.bn), ad, bd, idesc, (kb | kk) != 0);
               }
             }
-            tc::mma_commit(&sm.empty[s]);
+            if (cl > 1) mma_commit_mc(&sm.empty[s], cmask);
+            else tc::mma_commit(&sm.empty[s]);
           }
           tc::mma_commit(&sm.tmem_full);
         }
@@ -246,7 +292,8 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     const int c_lo = wq * cs, c_hi = min(p.np, c_lo + cs);
     const int ng = c_hi > c_lo ? (c_hi - c_lo) / 16 : 0;
     int item = 0;
-    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
+    for (int grp = group0; grp < n_groups; grp += group_step) {
+      const int tile = grp * cl + rank;
       float acc[HK];
 #pragma unroll
       for (int g = 0; g < HK; ++g) acc[g] = 0.0f;
@@ -313,6 +360,9 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     }
   }
   __syncthreads();
+  // no CTA leaves while a peer may still deliver into its shared memory
+  tc::cluster_arrive();
+  tc::cluster_wait();
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -346,6 +396,18 @@ void pass_split(int Dm, int* n_pass, int* np) {
 
 size_t head_bytes(int Hkv) { return sizeof(SmemHead) + 3 * 128 * (size_t)Hkv * 4 + 1024; }
 
+// CTAs per cluster.  The kernel can run as pairs that share every W1t slab
+// (each CTA loads half of it and multicasts it to both), which halves the L2
+// reads of the first-layer weight; on the 128k layer that measured 406 us
+// against 392 us for single CTAs: the kernel is held by the latency of each
+// stage's loads, not by L2 bandwidth (ncu: L2 29 %, DRAM 32 %, tensor pipe
+// 48 %), so single CTAs are launched.
+int cluster_size(int n_tiles, int sms) {
+  (void)n_tiles;
+  (void)sms;
+  return 1;
+}
+
 template <int HK>
 int launch_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p, size_t smem,
               const Dev& dev, cudaStream_t s) {
@@ -360,9 +422,24 @@ int launch_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p,
     }
   }
   if (int rc = prefer_max_shared(mlp_tc_kernel<HK>, dev.device)) return rc;
-  const int grid = p.n_tiles < dev.sms ? p.n_tiles : dev.sms;
-  return launch_pdl(mlp_tc_kernel<HK>, dim3((unsigned)grid), dim3(kThreads), smem, s, tm_h, tm_w,
-                    p);
+  const int cl = cluster_size(p.n_tiles, dev.sms);
+  const int groups = (p.n_tiles + cl - 1) / cl;
+  const int grid = cl * (groups < dev.sms / cl ? groups : dev.sms / cl);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0] = pdl_attr();
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, mlp_tc_kernel<HK>, tm_h, tm_w, p));
+  return KVC_OK;
 }
 
 }  // namespace
@@ -387,6 +464,10 @@ int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const 
   p.n_tiles = (int)((rows + kTileRows - 1) / kTileRows);
   pass_split(Dm, &p.n_pass, &p.np);
   p.bn = p.np <= 256 ? p.np : p.np / 2;
+  {
+    const int rpc = p.np / cluster_size(p.n_tiles, dev.sms);   // a CTA's rows of a slab
+    p.bw = rpc <= 256 ? rpc : rpc / 2;
+  }
   p.b1 = b1;
   p.w2 = static_cast<const uint16_t*>(w2);
   p.b2 = b2;
@@ -416,7 +497,7 @@ int score_mlp_launch(const void* hidden, const void* w1, const float* b1, const 
   {
     cuuint64_t dims[2] = {(cuuint64_t)Dh, (cuuint64_t)(p.n_pass * p.np)};
     cuuint64_t strides[1] = {(cuuint64_t)Dh * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)p.bn};
+    cuuint32_t box[2] = {(cuuint32_t)kKBlock, (cuuint32_t)p.bw};
     cuuint32_t es[2] = {1, 1};
     if (g_encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w1t, dims, strides, box, es,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

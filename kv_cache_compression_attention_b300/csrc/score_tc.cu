@@ -96,6 +96,7 @@ struct SmemSmall {
   uint32_t tmem_base;
   int abort_flag;
   float4 cl4[128];                     // column pairs (c, c', -lse2, -lse2') for pass 2
+  float4 nl4[64];                      // -lse2 of four consecutive columns (uniform c)
   float coef[256];                     // c_r = scale * f * log2(e) per window row
   float nlse[256];                     // -lse2 per window row
   float mpart[4][256], lpart[4][256];  // per column slice (max2, sum) of each row
@@ -337,23 +338,47 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = (tc0 + j <= tlim[mt]) ? v[j] : -INFINITY;
             }
-            const float cm = tc::max32(v);
-            if (cm > m[mt]) {
-              const float sc = (m[mt] == -INFINITY) ? 0.0f : tc::ex2(c_r[mt] * (m[mt] - cm));
-              const uint64_t sc2 = tc::pk2(sc, sc);
-#pragma unroll
-              for (int x = 0; x < 4; ++x) acc[mt][x] = tc::ffma2(acc[mt][x], sc2, 0ull);
-              m[mt] = cm;
-            }
-            if (m[mt] != -INFINITY) {
+            // The row's reference m only moves when a chunk's terms relative
+            // to it would reach 2^64: the chunk is summed against the current
+            // m, and only a first chunk, a chunk that large (or one holding
+            // inf / NaN) takes the maximum and rescales.  The running sum
+            // stays below 2^80, far from fp32's range.
+            uint64_t cs[4] = {0ull, 0ull, 0ull, 0ull};
+            bool redo = m[mt] == -INFINITY;
+            if (!redo) {
               const float nm = -c_r[mt] * m[mt];
               const uint64_t nm2 = tc::pk2(nm, nm);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float2 x = tc::upk2(tc::ffma2(tc::pk2(v[2 * j], v[2 * j + 1]), c2, nm2));
-                acc[mt][j & 3] = tc::fadd2(acc[mt][j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+                cs[j & 3] = tc::fadd2(cs[j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+              }
+              const float2 t = tc::upk2(tc::fadd2(tc::fadd2(cs[0], cs[1]), tc::fadd2(cs[2], cs[3])));
+              redo = !(t.x + t.y < 1.8e19f);
+            }
+            if (redo) {
+              const float cm = tc::max32(v);
+              if (cm > m[mt]) {
+                const float sc = (m[mt] == -INFINITY) ? 0.0f : tc::ex2(c_r[mt] * (m[mt] - cm));
+                const uint64_t sc2 = tc::pk2(sc, sc);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) acc[mt][x] = tc::ffma2(acc[mt][x], sc2, 0ull);
+                m[mt] = cm;
+              }
+#pragma unroll
+              for (int x = 0; x < 4; ++x) cs[x] = 0ull;
+              if (m[mt] != -INFINITY) {
+                const float nm = -c_r[mt] * m[mt];
+                const uint64_t nm2 = tc::pk2(nm, nm);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const float2 x = tc::upk2(tc::ffma2(tc::pk2(v[2 * j], v[2 * j + 1]), c2, nm2));
+                  cs[j & 3] = tc::fadd2(cs[j & 3], tc::pk2(tc::ex2(x.x), tc::ex2(x.y)));
+                }
               }
             }
+#pragma unroll
+            for (int x = 0; x < 4; ++x) acc[mt][x] = tc::fadd2(acc[mt][x], cs[x]);
           }
           tc::fence_before_sync();
           mbar_arrive(&sm.tmem_empty[b]);
@@ -438,7 +463,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (et < R / 2)
         sm.cl4[et] = make_float4(sm.coef[2 * et], sm.coef[2 * et + 1], sm.nlse[2 * et],
                                  sm.nlse[2 * et + 1]);
+      if (et < R / 4)
+        sm.nl4[et] = make_float4(sm.nlse[4 * et], sm.nlse[4 * et + 1], sm.nlse[4 * et + 2],
+                                 sm.nlse[4 * et + 3]);
       tc::named_sync(1, kEpiThreads);
+      // one softmax scale for this thread's quarter of the columns: no
+      // per-row temperature, or a quarter inside one query head's rows
+      const bool cuni = !p.head_scale || (rc0 / W == (rc0 + qcols - 1) / W);
+      const float cq = sm.coef[rc0];
+      const uint64_t cq2 = tc::pk2(cq, cq);
       // the next kernel of the stream may be scheduled once every CTA is here
       if (et == 0 && kr == 0) pdl_trigger();
       // ---- pass 2: this thread's token and quarter of the R columns
@@ -455,7 +488,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           float v[32];
           tc::tmem_ld32(tmem + lane_addr + (uint32_t)b * 256u + (uint32_t)(rc0 + c), v);
           const float4* cp = &sm.cl4[(rc0 + c) >> 1];
-          if (wmin <= 0) {
+          if (wmin <= 0 && cuni) {
+            const float4* np4 = &sm.nl4[(rc0 + c) >> 2];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 q = np4[j];
+              const float2 x0 = tc::upk2(tc::ffma2(tc::pk2(v[4 * j], v[4 * j + 1]), cq2,
+                                                   tc::pk2(q.x, q.y)));
+              const float2 x1 = tc::upk2(tc::ffma2(tc::pk2(v[4 * j + 2], v[4 * j + 3]), cq2,
+                                                   tc::pk2(q.z, q.w)));
+              s2[(2 * j) & 3] = acc2<kMax>(s2[(2 * j) & 3], tc::ex2(x0.x), tc::ex2(x0.y));
+              s2[(2 * j + 1) & 3] = acc2<kMax>(s2[(2 * j + 1) & 3], tc::ex2(x1.x), tc::ex2(x1.y));
+            }
+          } else if (wmin <= 0) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float4 q = cp[j];

@@ -110,8 +110,9 @@ def test_score_attn_llama32k_full(B):
     got = np64(gpu_scores(B, q, k, w.scale))
     ref = O.score_attn(np64(q), np64(k), w.scale)
     assert mass_rel_err(got, ref) <= 2e-2
-    # the sinks and every needle outrank the median token of their head
-    pos = inputs.needle_positions(w).numpy()[0]
+    # the sinks and every needle outrank the median token of their head (the
+    # positions are drawn on the device the keys were built on)
+    pos = inputs.needle_positions(w, "cuda").cpu().numpy()[0]
     med = np.median(got, axis=-1)                     # [U, Hkv]
     assert (got[0, :, :4] > med[0, :, None]).all()
     assert (got[0][:, pos] > med[0, :, None]).all()
@@ -133,7 +134,7 @@ def test_score_attn_tiny_workload_keeps_every_needle(B):
                  n_recent=w.n_recent)
     torch.cuda.synchronize()
     assert B.kvc_device_status() == 0
-    pos = set(inputs.needle_positions(w).numpy()[0].tolist())
+    pos = set(inputs.needle_positions(w, "cuda").cpu().numpy()[0].tolist())
     kept, counts = kept.cpu().numpy(), counts.cpu().numpy()
     for g in range(n):
         assert pos <= set(kept[g, : counts[g]].tolist()), g
