@@ -467,7 +467,8 @@ def bench_decode(B, steps, warmup, device):
     del kq, vq, kp, vp
     # the same steps with decode-time threshold pruning ([KVzap] §2.3): the new
     # token is scored by the linear surrogate, attended and appended, then the
-    # token leaving the 128-token window stays iff its score >= tau.  The
+    # token leaving the 128-token window stays iff its score >= tau (the
+    # window kept as a ring of row indices: a drop moves one row).  The
     # surrogate's synthetic scores of the cached rows are ~ N(0, 1).
     window, n_sink, tau, Dh = 128, 4, 0.5, 4096
     # pruning moves rows: the warm-up runs on a copy, the timed steps on the
@@ -479,13 +480,16 @@ def bench_decode(B, steps, warmup, device):
     hid = [inputs.decode_hidden(w, Dh, i, device) for i in range(max(steps, warmup))]
     s_new = torch.empty((w.U, w.Hkv, 1), device=device)
 
+    ring = torch.empty((n, window), dtype=torch.int32, device=device)
+    B.kvc_prune_ring_init(length3, window, w.T, ring)
+
     def pruned_step(i):
         q, kn, vn = steps_in[i]
         B.kvc_score_linear(hid[i], weight, bias, s_new)
         B.kvc_decode_attn(q, kc3, vc3, start3, length3, out, lse, k_new=kn, v_new=vn,
                           max_len=max_len, scale=w.scale, workspace=ws)
-        B.kvc_decode_prune([kc3, vc3], rscore, start3, length3, s_new.view(-1), tau, window,
-                           n_sink)
+        B.kvc_decode_prune_ring([kc3, vc3], rscore, start3, length3, ring, w.T + i,
+                                s_new.view(-1), tau, window, n_sink)
 
     for i in range(warmup):
         pruned_step(i)
@@ -503,13 +507,14 @@ def bench_decode(B, steps, warmup, device):
         B.kvc_decode_attn(q, kc3, vc3, start3, length3, out, lse, k_new=kn, v_new=vn,
                           max_len=max_len, scale=w.scale, workspace=ws)
         ev[i][2].record(s)
-        B.kvc_decode_prune([kc3, vc3], rscore, start3, length3, s_new.view(-1), tau, window,
-                           n_sink)
+        B.kvc_decode_prune_ring([kc3, vc3], rscore, start3, length3, ring, w.T + warmup + i,
+                                s_new.view(-1), tau, window, n_sink)
         ev[i][3].record(s)
     torch.cuda.synchronize()
     kc3, vc3 = kc, vc
     length3.copy_(len0)
     rscore = inputs.row_scores(kc3.shape[0], device, seed=61)
+    B.kvc_prune_ring_init(length3, window, w.T, ring)
     torch.cuda.synchronize()
     rows_p0 = int(length3.sum().item())
     e0.record(s)
@@ -528,6 +533,7 @@ def bench_decode(B, steps, warmup, device):
                            dropped_fraction=1.0 - (rows_p1 - rows_p0) / (n * steps),
                            kv_tokens_per_s=(mean_rows_p + n) / (msp * 1e-3),
                            overhead_us=(msp - ms) * 1e3, launches_per_step=4,
+                           window_layout="ring of row indices (one row moved per drop)",
                            stage_linear_us=t_lin, stage_prune_us=t_prune)
     del kc, vc, kc3, vc3, ws
     torch.cuda.empty_cache()

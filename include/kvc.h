@@ -401,6 +401,45 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                      const int64_t* start, int32_t* len, const float* s_new, int n_heads,
                      int window, int n_sink, float tau, int64_t capacity_rows, void* stream);
 
+/*
+ * The same pruning with the window kept as a ring ([KVzap] §2.3, as
+ * kvc_decode_prune): a head's rows are not kept in token order, so a drop
+ * moves one row instead of the window's.  The window (a head's last `window`
+ * appended rows) is a FIFO of row indices (relative to start[i]):
+ * ring[i*window + t % window] holds the entry appended at step counter t
+ * (-1: no row).  Call it after a decode step with counter t_new (any counter
+ * that grows by one per step, the same for every head) appended row
+ * len[i] - 1.  Per head i, with s = t_new % window and e = ring[i*window + s]
+ * the row that leaves the window:
+ *   - e < n_sink (no row, or a sink: the sinks are a head's first rows and
+ *     never move) or rscore[start[i] + e] >= tau (fp32; a NaN score goes):
+ *     the row stays; rscore[start[i] + len[i] - 1] = s_new[i] and
+ *     ring[i*window + s] = len[i] - 1;
+ *   - otherwise row len[i] - 1 of every pool moves into row e,
+ *     rscore[start[i] + e] = s_new[i], ring[i*window + s] = e and len[i]
+ *     shrinks by one.
+ * The rows a head holds and their scores are those kvc_decode_prune gives,
+ * in another order.  Arguments as kvc_decode_prune, plus ring [n_heads,
+ * window] int32 (read and written; set up by kvc_prune_ring_init) and
+ * t_new >= 0.  An e >= len[i] - 1 is reported as KVC_ERR_RANGE and the row
+ * stays.  No workspace; one warp per head.
+ */
+int kvc_decode_prune_ring(void* const* pools, const int* row_bytes, int n_pools, float* rscore,
+                          const int64_t* start, int32_t* len, int32_t* ring, int64_t t_new,
+                          const float* s_new, int n_heads, int window, int n_sink, float tau,
+                          int64_t capacity_rows, void* stream);
+
+/*
+ * The ring of kvc_decode_prune_ring for heads whose last `window` rows are
+ * their window in append order (a compaction, or kvc_decode_prune's layout):
+ * the entry of counter t_next - window + k is row len[i] - window + k
+ * (k < window; -1 where that row would be negative), t_next = the counter of
+ * the next decode step.  len [n_heads] int32; ring [n_heads, window] int32
+ * (written).
+ */
+int kvc_prune_ring_init(const int32_t* len, int n_heads, int window, int64_t t_next,
+                        int32_t* ring, void* stream);
+
 /* ------------------------------------------------ VECTOR three-way routing */
 
 /*

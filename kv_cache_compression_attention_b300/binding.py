@@ -64,6 +64,9 @@ SIGNATURES = {
     "kvc_gather_scores": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I64, _P]),
     "kvc_decode_prune": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_I), _I, _P, _P, _P, _P, _I, _I,
                               _I, _F, _I64, _P]),
+    "kvc_decode_prune_ring": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_I), _I, _P, _P, _P, _P,
+                                   _I64, _P, _I, _I, _I, _F, _I64, _P]),
+    "kvc_prune_ring_init": (_I, [_P, _I, _I, _I64, _P, _P]),
     "kvc_decode_noalloc_scratch_bytes": (_SZ, []),
     "kvc_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                      _P, _P]),
@@ -349,6 +352,30 @@ def kvc_decode_prune(pools, rscore, start, length, s_new, tau, window, n_sink=0,
                                 _ptr(s_new), int(length.numel()), int(window), int(n_sink),
                                 float(tau), rows, _stream(stream))
     _check("kvc_decode_prune", rc)
+
+
+def kvc_decode_prune_ring(pools, rscore, start, length, ring, t_new, s_new, tau, window,
+                          n_sink=0, stream=None):
+    """Decode-time pruning with the window kept as a ring of row indices:
+    ring [n_heads, window] int32 (kvc_prune_ring_init), t_new the position of
+    the token the step appended."""
+    n = len(pools)
+    ptrs = (_P * n)(*[_ptr(p) for p in pools])
+    rb = (_I * n)(*[int(p.stride(0) * p.element_size()) for p in pools])
+    rows = int(rscore.numel())
+    for p in pools:
+        if p.shape[0] != rows or not p.is_contiguous():
+            raise ValueError("every pool needs rscore.numel() contiguous rows")
+    rc = lib().kvc_decode_prune_ring(ptrs, rb, n, _ptr(rscore), _ptr(start), _ptr(length),
+                                     _ptr(ring), int(t_new), _ptr(s_new), int(length.numel()),
+                                     int(window), int(n_sink), float(tau), rows, _stream(stream))
+    _check("kvc_decode_prune_ring", rc)
+
+
+def kvc_prune_ring_init(length, window, t_next, ring, stream=None):
+    rc = lib().kvc_prune_ring_init(_ptr(length), int(length.numel()), int(window), int(t_next),
+                                   _ptr(ring), _stream(stream))
+    _check("kvc_prune_ring_init", rc)
 
 
 def kvc_decode_attn_noalloc(q, kc, vc, start, length, out, lse=None, k_new=None, v_new=None,

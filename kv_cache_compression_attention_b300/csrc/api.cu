@@ -290,6 +290,38 @@ int kvc_decode_prune(void* const* pools, const int* row_bytes, int n_pools, floa
                                   kvc::as_stream(stream));
 }
 
+int kvc_prune_ring_init(const int32_t* len, int n_heads, int window, int64_t t_next,
+                        int32_t* ring, void* stream) {
+  if (!len || !ring) return KVC_ERR_INVALID;
+  if (n_heads < 0 || window < 1 || t_next < 0) return KVC_ERR_INVALID;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::prune_ring_init_launch(len, n_heads, window, t_next, ring, dev,
+                                     kvc::as_stream(stream));
+}
+
+int kvc_decode_prune_ring(void* const* pools, const int* row_bytes, int n_pools, float* rscore,
+                          const int64_t* start, int32_t* len, int32_t* ring, int64_t t_new,
+                          const float* s_new, int n_heads, int window, int n_sink, float tau,
+                          int64_t capacity_rows, void* stream) {
+  if (!pools || !row_bytes || !rscore || !start || !len || !ring || !s_new) return KVC_ERR_INVALID;
+  if (n_pools < 1 || n_pools > KVC_PRUNE_MAX_POOLS) return KVC_ERR_INVALID;
+  if (n_heads < 0 || window < 1 || n_sink < 0 || capacity_rows < 0 || t_new < 0 || isnan(tau))
+    return KVC_ERR_INVALID;
+  for (int p = 0; p < n_pools; ++p) {
+    if (!pools[p] || row_bytes[p] <= 0) return KVC_ERR_INVALID;
+    if (row_bytes[p] % 16 || row_bytes[p] > 65536 || !aligned16(pools[p]))
+      return KVC_ERR_UNSUPPORTED;
+  }
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::decode_prune_ring_launch(pools, row_bytes, n_pools, rscore, start, len, ring, t_new,
+                                       s_new, n_heads, window, n_sink, tau, capacity_rows, dev,
+                                       kvc::as_stream(stream));
+}
+
 size_t kvc_score_kvzip_plus_workspace(int U, int Hq, int Hkv, int T, int W) {
   if (U < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || T < 0 || W <= 0) return 0;
   return kvc::score_kvzip_plus_ws_bytes(U, Hq, Hkv, T, W);

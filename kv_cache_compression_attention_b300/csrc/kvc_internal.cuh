@@ -136,6 +136,13 @@ int decode_prune_launch(void* const* pools, const int* row_bytes, int n_pools, f
                         const int64_t* start, int32_t* len, const float* s_new, int n_heads,
                         int window, int n_sink, float tau, int64_t capacity_rows, const Dev& dev,
                         cudaStream_t s);
+int decode_prune_ring_launch(void* const* pools, const int* row_bytes, int n_pools,
+                             float* rscore, const int64_t* start, int32_t* len, int32_t* ring,
+                             int64_t t_new, const float* s_new, int n_heads, int window,
+                             int n_sink, float tau, int64_t capacity_rows, const Dev& dev,
+                             cudaStream_t s);
+int prune_ring_init_launch(const int32_t* len, int n_heads, int window, int64_t t_next,
+                           int32_t* ring, const Dev& dev, cudaStream_t s);
 int gather_scores_launch(const float* scores, int U, int Hkv, int T, const int32_t* kept_idx,
                          const int32_t* counts, const int64_t* start, float* rscore,
                          int64_t capacity_rows, const Dev& dev, cudaStream_t s);

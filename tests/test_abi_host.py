@@ -269,3 +269,27 @@ def test_score_kvzip_plus_rejects_bad_arguments(lib):
         32 * 32768 * 4 + 2 * 1024 * 256 * 16
     # G*W = 256 with W = 32: quarters span two heads, the SIMT pass (one lse per row)
     assert lib.kvc_score_kvzip_plus_workspace(1, 32, 4, 1024, 32) == 32 * 1024 * 4 + 32 * 32 * 4
+
+
+def test_prune_ring_rejects_bad_arguments(lib):
+    def arr(t, *v):
+        return (t * len(v))(*v)
+    pools = arr(ctypes.c_void_p, 16, 32)
+    rb = arr(ctypes.c_int, 256, 256)
+    pr = lib.kvc_decode_prune_ring
+    ok = [pools, rb, 2, P, P, P, P, 1000, P, 8, 16, 4, 0.5, 1000, None]
+    for k, v, want in [(0, None, -1), (2, 0, -1), (2, 5, -1), (3, None, -1), (6, None, -1),
+                       (7, -1, -1), (8, None, -1), (10, 0, -1), (11, -1, -1),
+                       (12, float("nan"), -1), (13, -1, -1), (9, -1, -1)]:
+        bad = list(ok); bad[k] = v
+        assert pr(*bad) == want, (k, v)
+    bad = list(ok); bad[1] = arr(ctypes.c_int, 256, 24)
+    assert pr(*bad) == -2                                     # rows not whole 16-byte vectors
+    bad = list(ok); bad[0] = arr(ctypes.c_void_p, 16, 40)
+    assert pr(*bad) == -2                                     # unaligned pool
+    ri = lib.kvc_prune_ring_init
+    assert ri(None, 8, 16, 100, P, None) == -1
+    assert ri(P, 8, 16, 100, None, None) == -1
+    assert ri(P, -1, 16, 100, P, None) == -1
+    assert ri(P, 8, 0, 100, P, None) == -1
+    assert ri(P, 8, 16, -1, P, None) == -1

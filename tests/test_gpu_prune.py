@@ -220,3 +220,104 @@ def test_decode_prune_batch64(B):
             np.testing.assert_array_equal(bits(kc[r]), bits(torch.from_numpy(ok[:L]).to(torch.bfloat16)))
             np.testing.assert_array_equal(bits(vc[r]), bits(torch.from_numpy(ov[:L]).to(torch.bfloat16)))
             np.testing.assert_array_equal(bits(rs[r]), ors[:L].view(np.int32))
+
+
+def head_rows(pools, rscore, start, length, i):
+    """The rows head i holds as a sorted list of byte strings (every pool's
+    row bytes and the row's score bits): the content of the head as a set."""
+    r = slice(int(start[i]), int(start[i]) + int(length[i]))
+    parts = [np.ascontiguousarray(p[r]).reshape(int(length[i]), -1).view(np.uint8) for p in pools]
+    parts.append(np.ascontiguousarray(rscore[r]).reshape(-1, 1).view(np.uint8))
+    rows = np.concatenate(parts, axis=1)
+    return sorted(bytes(x) for x in rows)
+
+
+@pytest.mark.parametrize("quantised", [False, True])
+def test_decode_prune_ring_matches_the_ordered_rule(B, quantised):
+    """kvc_decode_prune_ring on a stream of decode steps: the rows every head
+    holds (pool rows and their scores, compared as a set) and the lengths
+    equal the oracle's token-ordered pruning at every step; a drop moves one
+    row, so the order differs."""
+    U, Hkv, G, T, d = 2, 4, 4, 900, 128
+    n_sink, window, slack, steps, tau = 4, 16, 48, 40, 0.25
+    scores, kept, counts, offsets, start, length, kc, vc = prefill(U, Hkv, T, d, n_sink, window,
+                                                                   slack, 62 + quantised)
+    rows = kc.shape[0]
+    n = U * Hkv
+    rs0 = O.gather_scores(scores, kept, counts, start, rows)
+    st = torch.from_numpy(start).cuda()
+    ln = torch.from_numpy(length).cuda()
+    rs = torch.from_numpy(rs0).cuda()
+    kc_t = torch.from_numpy(kc).to(torch.bfloat16).cuda()
+    vc_t = torch.from_numpy(vc).to(torch.bfloat16).cuda()
+    if quantised:
+        kq = torch.empty((rows, d), dtype=torch.uint8, device="cuda")
+        kp = torch.empty((rows, d // 32, 2), dtype=torch.float16, device="cuda")
+        vq, vp = torch.empty_like(kq), torch.empty_like(kp)
+        B.kvc_quantize_rows(kc_t, kq, kp)
+        B.kvc_quantize_rows(vc_t, vq, vp)
+        pools_gpu = [kq, kp, vq, vp]
+        rkq, rkp = O.quantize_rows(kc)
+        rvq, rvp = O.quantize_rows(vc)
+        pools_ref = [rkq, rkp, rvq, rvp]
+    else:
+        pools_gpu = [kc_t, vc_t]
+        pools_ref = [kc, vc]
+    ring = torch.full((n, window), -1, dtype=torch.int32, device="cuda")
+    B.kvc_prune_ring_init(ln, window, T, ring)
+    ref_len = length.copy()
+    rs_ref = rs0.copy()
+    rng = np.random.default_rng(64)
+    g = torch.Generator().manual_seed(65)
+    max_len = int(length.max()) + steps + 1
+    dropped_total = 0
+    for step in range(steps):
+        q = torch.randn((U, Hkv * G, d), generator=g).to(torch.bfloat16)
+        kn = torch.randn((U, Hkv, d), generator=g).to(torch.bfloat16)
+        vn = torch.randn((U, Hkv, d), generator=g).to(torch.bfloat16)
+        s_new = step_scores(rng, n, tau)
+        out = torch.empty((U, Hkv * G, d), dtype=torch.bfloat16, device="cuda")
+        if quantised:
+            B.kvc_decode_attn_q8(q.cuda(), kq, kp, vq, vp, st, ln, out, None, k_new=kn.cuda(),
+                                 v_new=vn.cuda(), max_len=max_len)
+        else:
+            B.kvc_decode_attn(q.cuda(), kc_t, vc_t, st, ln, out, None, k_new=kn.cuda(),
+                              v_new=vn.cuda(), max_len=max_len)
+        B.kvc_decode_prune_ring(pools_gpu, rs, st, ln, ring, T + step,
+                                torch.from_numpy(s_new).cuda(), tau, window, n_sink)
+        # oracle: append (quantised like the kernel when the pool is), prune in token order
+        if quantised:
+            akq, akp = O.quantize_rows(kn.float().numpy().reshape(-1, d))
+            avq, avp = O.quantize_rows(vn.float().numpy().reshape(-1, d))
+            for i in range(n):
+                r = int(start[i] + ref_len[i])
+                pools_ref[0][r], pools_ref[1][r] = akq[i], akp[i]
+                pools_ref[2][r], pools_ref[3][r] = avq[i], avp[i]
+        else:
+            kf, vf = kn.float().numpy(), vn.float().numpy()
+            for i in range(n):
+                u, gg = divmod(i, Hkv)
+                r = int(start[i] + ref_len[i])
+                pools_ref[0][r], pools_ref[1][r] = kf[u, gg], vf[u, gg]
+        ref_len = ref_len + 1
+        pools_ref, rs_ref, ref_len, dropped = O.decode_prune(pools_ref, rs_ref, start, ref_len,
+                                                             s_new, tau, window, n_sink)
+        dropped_total += int(dropped.sum())
+        torch.cuda.synchronize()
+        assert B.kvc_device_status() == 0
+        np.testing.assert_array_equal(ln.cpu().numpy(), ref_len, err_msg=f"step {step}")
+        got_pools = [bits(p) for p in pools_gpu]
+        ref_bits = []
+        for rp in pools_ref:
+            if rp.dtype == np.float16:
+                ref_bits.append(rp.view(np.int16))
+            elif rp.dtype == np.uint8:
+                ref_bits.append(rp)
+            else:   # bf16 values held in float32
+                ref_bits.append(torch.from_numpy(np.ascontiguousarray(rp)).to(torch.bfloat16)
+                                .view(torch.int16).numpy())
+        got_rs, ref_rs = bits(rs), rs_ref.view(np.int32)
+        for i in range(n):
+            assert head_rows(got_pools, got_rs, start, ref_len, i) == \
+                head_rows(ref_bits, ref_rs, start, ref_len, i), (step, i)
+    assert 0 < dropped_total < steps * n
