@@ -470,7 +470,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // one softmax scale for this thread's quarter of the columns: no
       // per-row temperature, or a quarter inside one query head's rows
       const bool cuni = !p.head_scale || (rc0 / W == (rc0 + qcols - 1) / W);
-      const float cq = sm.coef[rc0];
+      const float cq = sm.cl4[rc0 >> 1].x;   // (sm.coef belongs to the next round once
+                                             // a warp finishes this one)
       const uint64_t cq2 = tc::pk2(cq, cq);
       // the next kernel of the stream may be scheduled once every CTA is here
       if (et == 0 && kr == 0) pdl_trigger();

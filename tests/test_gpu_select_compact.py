@@ -104,6 +104,31 @@ def test_select_large_pools(B, shape, mode):
     check_same(got, O.select(sc, mode, **kw))
 
 
+@pytest.mark.parametrize("shape,kind", [
+    ((1, 8, 16384), "equal"),        # every key equal: ranked by (token, head) alone
+    ((1, 8, 32768), "levels"),       # six distinct values: large tie blocks
+    ((1, 3, 70001), "specials"),     # NaN, +-inf, -0 / +0, ragged per-CTA ranges
+    ((3, 8, 9000), "specials"),      # three pools in one launch
+    ((9, 8, 8192), "random"),        # nine pools in one launch
+])
+def test_select_global_pools_ties_and_specials(B, shape, kind):
+    """Global pools of 65 K - 262 K keys with tie blocks and special values,
+    at budgets from nothing to everything, bit-exact against the oracle."""
+    if kind == "equal":
+        s = torch.full(shape, 0.25)
+    elif kind == "levels":
+        g = torch.Generator().manual_seed(3)
+        s = torch.randint(0, 6, shape, generator=g).float() * 0.5
+    else:
+        s = inputs.random_scores(shape, seed=sum(shape), ties=kind != "random",
+                                 specials=kind == "specials")
+    sc = s.numpy()
+    for ratio, ns, nr in [(0.1, 4, 64), (0.37, 0, 0), (0.0, 2, 2), (1.0, 1, 1),
+                          (0.999, 3, 5)]:
+        kw = dict(keep_ratio=ratio, n_sink=ns, n_recent=nr)
+        check_same(gpu_select(B, s.cuda(), "global", **kw), O.select(sc, "global", **kw))
+
+
 def test_select_cross_layer_pool(B):
     """One global budget over every layer and kv head of a sequence (32
     layers x 8 kv heads = 256 heads of 16 384 tokens, 4.2 M keys per pool,
