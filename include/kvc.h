@@ -334,8 +334,10 @@ int kvc_quantize_rows(const void* x, int dtype, int64_t rows, int d,
  * kvc_decode_attn over a group-quantised pool: kq / vq are the codes and
  * kp / vp the (scale, lo) pairs of K and V as kvc_quantize_rows writes them
  * (same row indexing as kc / vc, 16-byte aligned).  Every cached row is
- * dequantised in the kernel (code * scale + lo in fp32, then bf16), which
- * streams 144 instead of 256 bytes per row and tensor; k_new / v_new are
+ * dequantised in the kernel (code * scale + lo, rounded once to fp16), which
+ * streams 144 instead of 256 bytes per row and tensor; the dot products take
+ * the queries and the softmax weights as fp16 (exact for bf16 queries of
+ * magnitude 2^-14 .. 65504) and accumulate in fp32; k_new / v_new are
  * attended exactly and appended quantised (codes and pair of row
  * start[i] + len[i]).  dtype KVC_BF16, d = 128, Hq / Hkv <= 8; same
  * workspace (kvc_decode_workspace), start / len semantics and status word as

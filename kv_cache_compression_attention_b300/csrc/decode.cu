@@ -32,6 +32,7 @@ namespace kvc {
 namespace {
 
 constexpr int kChunk = 512;     // rows per partial CTA
+constexpr int kQ8Chunk = 1024;  // rows per partial CTA over a quantised pool
 constexpr int kWarps = 4;       // compute warps per partial CTA
 constexpr int kStageRows = 32;  // rows per shared-memory stage (8 per compute warp)
 constexpr int kStages = 4;
@@ -362,7 +363,7 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
                       int Hkv, int max_chunks, float scale_log2, const float* __restrict__ ws,
                       Tin* __restrict__ out, float* __restrict__ lse, int* status,
                       uint8_t* __restrict__ kq, uint32_t* __restrict__ kp,
-                      uint8_t* __restrict__ vq, uint32_t* __restrict__ vp) {
+                      uint8_t* __restrict__ vq, uint32_t* __restrict__ vp, int chunk) {
   __shared__ float red[D / 32][G];
   pdl_wait();
   pdl_trigger();
@@ -370,7 +371,7 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
   const int u = i / Hkv, g = i - u * Hkv;
   const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
   const int L = len[i];
-  int nch = (L + kChunk - 1) / kChunk;
+  int nch = (L + chunk - 1) / chunk;
   if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
   const bool append = k_new != nullptr;
   bool room = append;
@@ -712,63 +713,67 @@ constexpr int kRows = 64;      // rows per stage (16 per warp)
 constexpr int kStg = 3;
 
 // bf16 path: kStg stages of (K tile, V tile), kRows x (D + 8) bf16 each.
-// Group-quantised path: one (K, V) bf16 tile pair that the stage being
-// consumed is dequantised into, then the raw stages of (K codes, V codes,
-// K params, V params): kRows x D bytes and kRows x 16 bytes each; two raw
-// stages, so that three CTAs fit an SM.
-template <int D, bool kQ8>
-constexpr size_t tile_bytes() { return kQ8 ? (size_t)2 * kRows * (D + 8) * 2 : 0; }
 template <int D>
-constexpr size_t raw_stage_bytes() { return (size_t)2 * kRows * D + 2 * kRows * 16; }
-template <int D, bool kQ8 = false>
-constexpr size_t smem_bytes() {
-  return kQ8 ? tile_bytes<D, true>() + (size_t)2 * raw_stage_bytes<D>()
-             : (size_t)kStg * 2 * kRows * (D + 8) * 2;
+constexpr size_t smem_bytes() { return (size_t)kStg * 2 * kRows * (D + 8) * 2; }
+// Quantised path: kQ8Stg stages of (K codes, V codes, K pairs, V pairs),
+// code rows padded to D + 16 bytes; three CTAs fit an SM.
+constexpr int kQ8Stg = 3;
+template <int D>
+constexpr int q8_row_bytes() { return D + 16; }
+template <int D>
+constexpr size_t q8_smem_bytes() {
+  return (size_t)kQ8Stg * (2 * kRows * q8_row_bytes<D>() + 2 * kRows * (D / 8));
 }
 
-// Packed fp32 pairs (one issue slot for two lanes of arithmetic).
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+// D = A (16x16 f16, row) . B (16x8 f16, col) + C, fp32 accumulators.
+__device__ __forceinline__ void mma_f16x4(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
+// The same with rows 8-15 of A zero.
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a2, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
-// 16 codes (4 words) -> 16 bf16 (8 words): x = code * scale + lo.  A code
-// becomes the float 2^23 + code by placing it under the exponent byte 0x4B
-// (exact), and 2^23 is subtracted exactly before the scale-and-offset FMA.
-__device__ __forceinline__ void dequant16(const uint32_t (&w)[4], float sc, float lo,
-                                          uint32_t (&o)[8]) {
-  const uint64_t big = pk2(-8388608.0f, -8388608.0f), sc2 = pk2(sc, sc), lo2 = pk2(lo, lo);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      const uint32_t e0 = __byte_perm(w[k], 0x4B000000u, 0x7540u + 2 * p);       // byte 2p
-      const uint32_t e1 = __byte_perm(w[k], 0x4B000000u, 0x7540u + 2 * p + 1);   // byte 2p+1
-      const uint64_t f = ffma2(fadd2(((uint64_t)e1 << 32) | e0, big), sc2, lo2);
-      o[2 * k + p] = pack_bf16(__uint_as_float((uint32_t)f), __uint_as_float((uint32_t)(f >> 32)));
-    }
-  }
+// Two codes of w (the bytes `sel` picks into the low byte of each half) ->
+// f16x2 code * scale + lo.  A code under the exponent byte 0x64 is the fp16
+// 1024 + code (exact); 1024 is subtracted exactly, then one fused
+// multiply-add rounds the value once to fp16.
+__device__ __forceinline__ uint32_t deq2(uint32_t w, uint32_t sel, uint32_t sc2, uint32_t lo2) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
+  uint32_t c, x;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(h), "r"(0x64006400u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(x) : "r"(c), "r"(sc2), "r"(lo2));
+  return x;
 }
 
 }  // namespace mma
 
-// kQ8: the pool holds group-quantised rows (codes [rows, D] uint8 in kc / vc,
-// (scale, offset) fp16 pairs [rows, D / 32] in kp / vp); every stage is
-// dequantised into one bf16 tile pair before the same MMAs.
-template <int D, int G, bool kQ8>
-__global__ void __launch_bounds__(kWarps * 32, kQ8 ? 3 : 2)
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32, 2)
 decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kc,
-                          const void* __restrict__ vc, const uint32_t* __restrict__ kp,
-                          const uint32_t* __restrict__ vp, const int64_t* __restrict__ start,
+                          const void* __restrict__ vc, const int64_t* __restrict__ start,
                           const int32_t* __restrict__ len, int Hkv, int max_chunks,
                           float scale_log2, float* __restrict__ ws,
                           const int64_t* __restrict__ vstart, const int32_t* __restrict__ napprox) {
@@ -778,9 +783,8 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
   constexpr int NT = D / 8;                  // 8-wide output tiles
   extern __shared__ __align__(128) uint16_t smem_m[];
   __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
-  // the quantised variant merges its warps in the (then idle) tile area
-  __shared__ float acc_static[kQ8 ? 1 : kWarps * G * D];
-  constexpr int STG = kQ8 ? 2 : mma::kStg;   // stages in flight
+  __shared__ float acc_sm[kWarps][G][D];
+  constexpr int STG = mma::kStg;             // stages in flight
   pdl_wait();
   pdl_trigger();
 
@@ -818,57 +822,32 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
   const int u = i / Hkv, g = i - u * Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t sbase = smem_u32(smem_m);
-  constexpr uint32_t kTileBytes = (uint32_t)mma::tile_bytes<D, kQ8>();
-  constexpr uint32_t kRawBytes = (uint32_t)mma::raw_stage_bytes<D>();
 
-  // stage st -> slot: K rows then V rows, each kRows x RS elements (bf16), or
-  // the raw codes and (scale, offset) pairs of the quantised pool
+  // stage st -> slot: K rows then V rows, each kRows x RS elements (bf16)
   auto issue = [&](int st) {
     const int slot = st % STG;
     const int r0 = st * mma::kRows;
-    if constexpr (kQ8) {
-      constexpr int CB = D / 16;                  // 16-byte code chunks per row
-      const uint32_t raw = sbase + kTileBytes + (uint32_t)slot * kRawBytes;
-      const uint8_t* kb = static_cast<const uint8_t*>(kc) + row0 * D;
-      const uint8_t* vb = static_cast<const uint8_t*>(vc) + row0 * D;
-      for (int x = tid; x < mma::kRows * CB; x += kWarps * 32) {
-        const int r = x / CB, ch = x - r * CB;
-        const bool ok = r0 + r < nrows;
-        const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 16;
-        const uint32_t so = (uint32_t)(r * D + ch * 16);
-        mma::cp_async16(raw + so, kb + off, ok ? 16u : 0u);
-        mma::cp_async16(raw + (uint32_t)(mma::kRows * D) + so, vb + off, ok ? 16u : 0u);
-      }
-      for (int r = tid; r < mma::kRows; r += kWarps * 32) {
-        const bool ok = r0 + r < nrows;
-        const size_t off = (size_t)(row0 + (ok ? r0 + r : 0)) * (D / 32);
-        const uint32_t so = (uint32_t)(2 * mma::kRows * D + r * 16);
-        mma::cp_async16(raw + so, kp + off, ok ? 16u : 0u);
-        mma::cp_async16(raw + so + (uint32_t)(mma::kRows * 16), vp + off, ok ? 16u : 0u);
+    const uint16_t* kb = static_cast<const uint16_t*>(kc) + row0 * D;
+    const uint16_t* vb = static_cast<const uint16_t*>(vc) + vrow0 * D;
+    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
+    if (k_as_v) {
+      // 128 keys: rows 64..127 land in the V tile, which follows the K tile
+      const int r0k = st * 2 * mma::kRows;
+      for (int x = tid; x < 2 * mma::kRows * CPR; x += kWarps * 32) {
+        const int r = x / CPR, ch = x - r * CPR;
+        const bool ok = r0k + r < nrows;
+        const size_t off = (size_t)(ok ? r0k + r : 0) * D + ch * 8;
+        mma::cp_async16(ks + (uint32_t)(r * RS + ch * 8) * 2u, kb + off, ok ? 16u : 0u);
       }
     } else {
-      const uint16_t* kb = static_cast<const uint16_t*>(kc) + row0 * D;
-      const uint16_t* vb = static_cast<const uint16_t*>(vc) + vrow0 * D;
-      const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-      const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
-      if (k_as_v) {
-        // 128 keys: rows 64..127 land in the V tile, which follows the K tile
-        const int r0k = st * 2 * mma::kRows;
-        for (int x = tid; x < 2 * mma::kRows * CPR; x += kWarps * 32) {
-          const int r = x / CPR, ch = x - r * CPR;
-          const bool ok = r0k + r < nrows;
-          const size_t off = (size_t)(ok ? r0k + r : 0) * D + ch * 8;
-          mma::cp_async16(ks + (uint32_t)(r * RS + ch * 8) * 2u, kb + off, ok ? 16u : 0u);
-        }
-      } else {
-        for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
-          const int r = x / CPR, ch = x - r * CPR;
-          const bool ok = r0 + r < nrows;
-          const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
-          const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
-          mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
-          mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
-        }
+      for (int x = tid; x < mma::kRows * CPR; x += kWarps * 32) {
+        const int r = x / CPR, ch = x - r * CPR;
+        const bool ok = r0 + r < nrows;
+        const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 8;
+        const uint32_t so = (uint32_t)(r * RS + ch * 8) * 2u;
+        mma::cp_async16(ks + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
+        mma::cp_async16(vs + so, vb + off, ok ? 16u : 0u);
       }
     }
   };
@@ -904,43 +883,8 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
     if (st + STG - 1 < nst) issue(st + STG - 1);
     mma::cp_commit();
     const int slot = st % STG;
-    uint32_t ks, vs;
-    if constexpr (kQ8) {
-      // dequantise the raw stage into the tile pair (every thread 8 chunks of
-      // 16 codes), then every warp reads it
-      constexpr int CB = D / 16;
-      const uint32_t raw = sbase + kTileBytes + (uint32_t)slot * kRawBytes;
-      static_assert((2 * mma::kRows * CB) % (kWarps * 32) == 0, "whole chunks per thread");
-#pragma unroll
-      for (int it = 0; it < 2 * mma::kRows * CB / (kWarps * 32); ++it) {
-        const int x = tid + it * kWarps * 32;
-        const int t = x / (mma::kRows * CB), rem = x - t * (mma::kRows * CB);
-        const int r = rem / CB, ch = rem - r * CB;
-        uint32_t w[4], o[8];
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(raw + (uint32_t)(t * mma::kRows * D + r * D + ch * 16)));
-        uint32_t pr;
-        asm volatile("ld.shared.u32 %0, [%1];"
-                     : "=r"(pr)
-                     : "r"(raw + (uint32_t)(2 * mma::kRows * D + t * mma::kRows * 16 + r * 16 +
-                                            (ch >> 1) * 4)));
-        const float sc = __half2float(__ushort_as_half((unsigned short)(pr & 0xffffu)));
-        const float lo = __half2float(__ushort_as_half((unsigned short)(pr >> 16)));
-        mma::dequant16(w, sc, lo, o);
-        const uint32_t dst = sbase + (uint32_t)(t * mma::kRows * RS + r * RS + ch * 16) * 2u;
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
-                     "r"(o[2]), "r"(o[3]) : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16u), "r"(o[4]),
-                     "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
-      }
-      __syncthreads();
-      ks = sbase;
-      vs = sbase + (uint32_t)(mma::kRows * RS) * 2u;
-    } else {
-      ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
-      vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
-    }
+    const uint32_t ks = sbase + (uint32_t)(slot * 2 * mma::kRows * RS) * 2u;
+    const uint32_t vs = ks + (uint32_t)(mma::kRows * RS) * 2u;
     auto tile_step = [&](uint32_t ks, uint32_t vs, int base) {
       const int wr = warp * 16;                     // this warp's 16 rows of the stage
       // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
@@ -1004,15 +948,240 @@ decode_partial_mma_kernel(const uint16_t* __restrict__ q, const void* __restrict
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
   const int h = lane >> 2;
-  float (*acc_sm)[G][D] = reinterpret_cast<float (*)[G][D]>(
-      kQ8 ? reinterpret_cast<float*>(smem_m) : acc_static);
-  if constexpr (kQ8) __syncthreads();         // every warp is done with the tile
   if (h < G) {
     if ((lane & 3) == 0) { m_sm[warp][h] = m; l_sm[warp][h] = l; }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       acc_sm[warp][h][nt * 8 + (lane & 3) * 2] = o[nt][0];
       acc_sm[warp][h][nt * 8 + (lane & 3) * 2 + 1] = o[nt][1];
+    }
+  }
+  __syncthreads();
+  float* out = ws + ((int64_t)i * max_chunks + c) * G * (D + 2);
+  for (int e = tid; e < G * D; e += kWarps * 32) {
+    const int hh = e / D, x = e - hh * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, m_sm[w][hh]);
+    float a = 0.0f, lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = (m_sm[w][hh] == -INFINITY) ? 0.0f : exp2f(m_sm[w][hh] - M);
+      a += acc_sm[w][hh][x] * f;
+      lsum += l_sm[w][hh] * f;
+    }
+    out[hh * (D + 2) + x] = a;
+    if (x == 0) { out[hh * (D + 2) + D] = M; out[hh * (D + 2) + D + 1] = lsum; }
+  }
+}
+
+// Partial kernel over a group-quantised pool (codes [rows, D] uint8, fp16
+// (scale, lo) pairs [rows, D / 32]).  The raw codes and pairs stream through
+// a cp.async ring (code rows padded to D + 16 bytes, so ldmatrix is
+// conflict-free; rows past the chunk zero-filled, so they read as 0) and
+// every warp dequantises its 16 rows of a stage straight into MMA operand
+// registers (no bf16 tile, one barrier per stage):
+//  * S = Q . K^T: ldmatrix hands a lane 4 consecutive codes (dims 16kk + 4t
+//    .. +3) of token lane / 4; the contraction takes a k-step's 16 dims in
+//    that order (the query fragment is loaded to match), so the 4 codes are
+//    the lane's two B registers.
+//  * O^T += V^T . P^T: ldmatrix.trans hands a lane the codes of tokens 2t,
+//    2t+1 at dims 2g, 2g+1 of a 16-dim chunk, which are exactly the A
+//    fragment of the chunk with its even dims as rows 0-7 and its odd dims as
+//    rows 8-15; P from the S accumulators is the B fragment as it stands.
+// Dequantisation is code * scale + lo rounded once to fp16 (three
+// instructions per two codes); queries and probabilities enter the MMAs as
+// fp16, products accumulate in fp32.  The accumulators are rescaled only when
+// a head's running maximum moves.
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+decode_partial_q8_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ kq,
+                         const uint8_t* __restrict__ vq, const uint32_t* __restrict__ kp,
+                         const uint32_t* __restrict__ vp, const int64_t* __restrict__ start,
+                         const int32_t* __restrict__ len, int Hkv, int max_chunks,
+                         float scale_log2, float* __restrict__ ws) {
+  static_assert(D == 128 && G <= 8, "shape");
+  constexpr int RSB = mma::q8_row_bytes<D>();
+  constexpr int PB = D / 8;                        // pair bytes per row (4 per 32 dims)
+  constexpr int STG = mma::kQ8Stg;
+  constexpr int MT = D / 16;                       // 16-dim output chunks
+  constexpr uint32_t kCodeB = (uint32_t)(mma::kRows * RSB);
+  constexpr uint32_t kParB = (uint32_t)(mma::kRows * PB);
+  constexpr uint32_t kStageB = 2 * kCodeB + 2 * kParB;
+  extern __shared__ __align__(128) uint8_t smem_q8[];
+  __shared__ float m_sm[kWarps][G], l_sm[kWarps][G];
+  pdl_wait();
+  pdl_trigger();
+
+  const int i = blockIdx.y, c = blockIdx.x;
+  const int L = len[i];
+  const int rb = c * kQ8Chunk;
+  if (rb >= L) return;
+  const int nrows = min(L, rb + kQ8Chunk) - rb;
+  const int nst = (nrows + mma::kRows - 1) / mma::kRows;
+  const int u = i / Hkv, g = i - u * Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t sbase = smem_u32(smem_q8);
+  const int64_t row0 = start[i] + rb;
+
+  // stage st -> slot: K codes, V codes, K pairs, V pairs
+  auto issue = [&](int st) {
+    const int slot = st % STG;
+    const int r0 = st * mma::kRows;
+    const uint32_t sk = sbase + (uint32_t)slot * kStageB, sv = sk + kCodeB;
+    const uint32_t spk = sv + kCodeB, spv = spk + kParB;
+    const uint8_t* kb = kq + row0 * D;
+    const uint8_t* vb = vq + row0 * D;
+    constexpr int CB = D / 16;                     // 16-byte code chunks per row
+    for (int x = tid; x < mma::kRows * CB; x += kWarps * 32) {
+      const int r = x / CB, ch = x - r * CB;
+      const bool ok = r0 + r < nrows;
+      const size_t off = (size_t)(ok ? r0 + r : 0) * D + ch * 16;
+      const uint32_t so = (uint32_t)(r * RSB + ch * 16);
+      mma::cp_async16(sk + so, kb + off, ok ? 16u : 0u);     // zero-fill past the end
+      mma::cp_async16(sv + so, vb + off, ok ? 16u : 0u);
+    }
+    for (int r = tid; r < mma::kRows; r += kWarps * 32) {
+      const bool ok = r0 + r < nrows;
+      const size_t off = (size_t)(row0 + (ok ? r0 + r : 0)) * (D / 32);
+      mma::cp_async16(spk + (uint32_t)(r * PB), kp + off, ok ? 16u : 0u);
+      mma::cp_async16(spv + (uint32_t)(r * PB), vp + off, ok ? 16u : 0u);
+    }
+  };
+  for (int st = 0; st < STG - 1; ++st) {
+    if (st < nst) issue(st);
+    mma::cp_commit();
+  }
+
+  // Q as the A operand (rows = query heads lane / 4), fp16, dims of k-step kk
+  // in the order the K codes arrive: 16kk + 4t, +1 | 16kk + 4t + 2, +3
+  const int t4 = lane & 3, gi = lane >> 2;
+  uint32_t qa[D / 16][2];
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    if (gi < G) {
+      const uint16_t* qp = q + ((int64_t)u * Hkv * G + (int64_t)g * G + gi) * D + kk * 16 + 4 * t4;
+      const uint2 w = *reinterpret_cast<const uint2*>(qp);
+      qa[kk][0] = mma::pack_f16(bf16lo(w.x), bf16hi(w.x));
+      qa[kk][1] = mma::pack_f16(bf16lo(w.y), bf16hi(w.y));
+    } else {
+      qa[kk][0] = qa[kk][1] = 0u;
+    }
+  }
+  // o[s]: heads 2t, 2t+1 (columns) at dims 16s + 2g (c0, c1) and 16s + 2g + 1
+  // (c2, c3), g = lane / 4
+  float o[MT][4];
+#pragma unroll
+  for (int x = 0; x < MT; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.0f;
+  float m = -INFINITY, l = 0.0f;                  // for head lane / 4 (lanes of a quad agree)
+  const int r8 = lane & 7, mi = lane >> 3;        // ldmatrix: row r8 of matrix mi
+
+  for (int st = 0; st < nst; ++st) {
+    mma::cp_wait<STG - 2>();
+    __syncthreads();                              // stage st landed; slot st-1 is free
+    if (st + STG - 1 < nst) issue(st + STG - 1);
+    mma::cp_commit();
+    const int slot = st % STG;
+    const uint32_t sk = sbase + (uint32_t)slot * kStageB, sv = sk + kCodeB;
+    const uint32_t spk = sv + kCodeB, spv = spk + kParB;
+    const int wr = warp * 16;                     // this warp's 16 rows of the stage
+    const int valid = nrows - st * mma::kRows - wr;   // rows of the 16 that exist
+
+    // ---- S = Q . K^T for 16 tokens (two 8-token tiles)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint4 pw = mma::lds128(spk + (uint32_t)((wr + 8 * nt + gi) * PB));   // token's pairs
+      uint32_t sc2[4], lo2[4];
+      sc2[0] = __byte_perm(pw.x, 0u, 0x1010u); lo2[0] = __byte_perm(pw.x, 0u, 0x3232u);
+      sc2[1] = __byte_perm(pw.y, 0u, 0x1010u); lo2[1] = __byte_perm(pw.y, 0u, 0x3232u);
+      sc2[2] = __byte_perm(pw.z, 0u, 0x1010u); lo2[2] = __byte_perm(pw.z, 0u, 0x3232u);
+      sc2[3] = __byte_perm(pw.w, 0u, 0x1010u); lo2[3] = __byte_perm(pw.w, 0u, 0x3232u);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t b[4];
+        mma::ldsm_x4(sk + (uint32_t)((wr + 8 * nt + r8) * RSB + (4 * half + mi) * 16), b);
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const int kk = 4 * half + m4;
+          mma::mma_f16(sacc[nt], qa[kk][0], qa[kk][1],
+                       mma::deq2(b[m4], 0x5140u, sc2[kk >> 1], lo2[kk >> 1]),
+                       mma::deq2(b[m4], 0x5342u, sc2[kk >> 1], lo2[kk >> 1]));
+        }
+      }
+    }
+    // ---- online softmax in base 2 over the 16 tokens (row = head lane / 4)
+    const int tcol = t4 * 2;
+    const float x0 = (tcol < valid) ? sacc[0][0] * scale_log2 : -INFINITY;
+    const float x1 = (tcol + 1 < valid) ? sacc[0][1] * scale_log2 : -INFINITY;
+    const float x2 = (8 + tcol < valid) ? sacc[1][0] * scale_log2 : -INFINITY;
+    const float x3 = (8 + tcol + 1 < valid) ? sacc[1][1] * scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    float alpha = 1.0f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    if (mn != -INFINITY) {
+      if (mn > m) alpha = mma::ex2(m - mn);       // m = -inf -> 0
+      p0 = mma::ex2(x0 - mn); p1 = mma::ex2(x1 - mn); p2 = mma::ex2(x2 - mn); p3 = mma::ex2(x3 - mn);
+      l = l * alpha + ((p0 + p1) + (p2 + p3));
+      m = mn;
+    }
+    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      // this lane's output columns are heads 2t and 2t+1
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t4);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);
+#pragma unroll
+      for (int x = 0; x < MT; ++x) {
+        o[x][0] *= a0; o[x][1] *= a1; o[x][2] *= a0; o[x][3] *= a1;
+      }
+    }
+    // ---- O^T += V^T . P^T: P (16 tokens x heads) is the B operand
+    const uint32_t pb0 = mma::pack_f16(p0, p1), pb1 = mma::pack_f16(p2, p3);
+    {
+      // pairs of tokens 2t, 2t+1 (k 2t, 2t+1) and 2t+8, 2t+9 (k 2t+8, 2t+9)
+      const uint4 wa4 = mma::lds128(spv + (uint32_t)((wr + 2 * t4) * PB));
+      const uint4 wb4 = mma::lds128(spv + (uint32_t)((wr + 2 * t4 + 1) * PB));
+      const uint4 wc4 = mma::lds128(spv + (uint32_t)((wr + 8 + 2 * t4) * PB));
+      const uint4 wd4 = mma::lds128(spv + (uint32_t)((wr + 9 + 2 * t4) * PB));
+      // matrix mi: tokens wr + 8 (mi & 1) + r8 of chunk 2sp + (mi >> 1)
+      const uint32_t vrow = sv + (uint32_t)((wr + 8 * (mi & 1) + r8) * RSB + (mi >> 1) * 16);
+#pragma unroll
+      for (int sp = 0; sp < D / 32; ++sp) {        // chunks 2sp, 2sp+1 share pair group sp
+        uint32_t b[4];
+        mma::ldsm_x4_t(vrow + (uint32_t)(sp * 32), b);
+        const uint32_t wa = sp == 0 ? wa4.x : sp == 1 ? wa4.y : sp == 2 ? wa4.z : wa4.w;
+        const uint32_t wb = sp == 0 ? wb4.x : sp == 1 ? wb4.y : sp == 2 ? wb4.z : wb4.w;
+        const uint32_t wc = sp == 0 ? wc4.x : sp == 1 ? wc4.y : sp == 2 ? wc4.z : wc4.w;
+        const uint32_t wd = sp == 0 ? wd4.x : sp == 1 ? wd4.y : sp == 2 ? wd4.z : wd4.w;
+        const uint32_t sc_a = __byte_perm(wa, wb, 0x5410u), lo_a = __byte_perm(wa, wb, 0x7632u);
+        const uint32_t sc_b = __byte_perm(wc, wd, 0x5410u), lo_b = __byte_perm(wc, wd, 0x7632u);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t r0 = b[2 * cc], r1 = b[2 * cc + 1];   // tokens 0-7 / 8-15
+          mma::mma_f16x4(o[2 * sp + cc],
+                         mma::deq2(r0, 0x5240u, sc_a, lo_a),     // rows 0-7: even dims
+                         mma::deq2(r0, 0x5341u, sc_a, lo_a),     // rows 8-15: odd dims
+                         mma::deq2(r1, 0x5240u, sc_b, lo_b),
+                         mma::deq2(r1, 0x5341u, sc_b, lo_b), pb0, pb1);
+        }
+      }
+    }
+  }
+  mma::cp_wait<0>();
+  __syncthreads();                                // every warp is done with the stages
+  // quad sum of l, then per-warp partials to shared memory (the stage area)
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  float (*acc_sm)[G][D] = reinterpret_cast<float (*)[G][D]>(smem_q8);
+  if (gi < G && t4 == 0) { m_sm[warp][gi] = m; l_sm[warp][gi] = l; }
+  {
+    const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+#pragma unroll
+    for (int x = 0; x < MT; ++x) {
+      const int dm = 16 * x + 2 * gi;
+      if (h0 < G) { acc_sm[warp][h0][dm] = o[x][0]; acc_sm[warp][h0][dm + 1] = o[x][2]; }
+      if (h1 < G) { acc_sm[warp][h1][dm] = o[x][1]; acc_sm[warp][h1][dm + 1] = o[x][3]; }
     }
   }
   __syncthreads();
@@ -1048,7 +1217,8 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
         const void* k_new, const void* v_new, int U, int Hkv, int max_len, float scale, void* out,
         float* lse, float* ws, const Dev& dev, cudaStream_t s) {
   const int n = U * Hkv;
-  const int max_chunks = (max_len + kChunk - 1) / kChunk;
+  const int chunk = qz.kq ? kQ8Chunk : kChunk;
+  const int max_chunks = (max_len + chunk - 1) / chunk;
   const float sl2 = scale * kLog2e;
   if (max_chunks > 0) {
     dim3 grid((unsigned)max_chunks, (unsigned)n);
@@ -1057,26 +1227,25 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
     if constexpr (sizeof(Tin) == 2 && G <= 8) {
       if (qz.kq) {
         if constexpr (D == 128) {
-          const size_t smem = mma::smem_bytes<D, true>();
-          auto kern = decode_partial_mma_kernel<D, G, true>;
+          const size_t smem = mma::q8_smem_bytes<D>();
+          auto kern = decode_partial_q8_kernel<D, G>;
           if (!(attr_done.load() & (bit << 32))) {
             KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
             attr_done.fetch_or(bit << 32);
           }
           if (int rc = prefer_max_shared(kern, dev.device)) return rc;
           if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
-                                  static_cast<const uint16_t*>(q), (const void*)qz.kq,
-                                  (const void*)qz.vq, (const uint32_t*)qz.kp,
+                                  static_cast<const uint16_t*>(q), (const uint8_t*)qz.kq,
+                                  (const uint8_t*)qz.vq, (const uint32_t*)qz.kp,
                                   (const uint32_t*)qz.vp, start, (const int32_t*)len, Hkv,
-                                  max_chunks, sl2, ws, (const int64_t*)nullptr,
-                                  (const int32_t*)nullptr))
+                                  max_chunks, sl2, ws))
             return rc;
         } else {
           return KVC_ERR_UNSUPPORTED;
         }
       } else {
         const size_t smem = mma::smem_bytes<D>();
-        auto kern = decode_partial_mma_kernel<D, G, false>;
+        auto kern = decode_partial_mma_kernel<D, G>;
         if (!(attr_done.load() & bit)) {
           KVC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
           attr_done.fetch_or(bit);
@@ -1084,8 +1253,7 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
         if (int rc = prefer_max_shared(kern, dev.device)) return rc;
         if (int rc = launch_pdl(kern, grid, dim3(kWarps * 32), smem, s,
                                 static_cast<const uint16_t*>(q), (const void*)kc, (const void*)vc,
-                                (const uint32_t*)nullptr, (const uint32_t*)nullptr, start,
-                                (const int32_t*)len, Hkv, max_chunks, sl2, ws,
+                                start, (const int32_t*)len, Hkv, max_chunks, sl2, ws,
                                 (const int64_t*)nullptr, (const int32_t*)nullptr))
           return rc;
       }
@@ -1110,7 +1278,7 @@ int run(const void* q, void* kc, void* vc, const QPool& qz, const int64_t* start
                     static_cast<const Tin*>(q), static_cast<Tin*>(kc), static_cast<Tin*>(vc),
                     start, len, static_cast<const Tin*>(k_new), static_cast<const Tin*>(v_new),
                     n, Hkv, max_chunks, sl2, (const float*)ws, static_cast<Tin*>(out), lse,
-                    dev.status, qz.kq, qz.kp, qz.vq, qz.vp);
+                    dev.status, qz.kq, qz.kp, qz.vq, qz.vp, chunk);
 }
 
 template <typename Tin, int D>
@@ -1137,7 +1305,7 @@ int run_vector(const void* q, void* kc, void* vc, const int64_t* kstart, int32_t
   const int max_chunks = (max_len + kChunk - 1) / kChunk + 1;
   const float sl2 = scale * kLog2e;
   const size_t smem = mma::smem_bytes<D>();
-  auto kern = decode_partial_mma_kernel<D, G, false>;
+  auto kern = decode_partial_mma_kernel<D, G>;
   static std::atomic<uint32_t> attr_done{0};            // one bit per device
   const uint32_t bit = 1u << (dev.device & 31);
   if (!(attr_done.load() & bit)) {
@@ -1147,8 +1315,7 @@ int run_vector(const void* q, void* kc, void* vc, const int64_t* kstart, int32_t
   if (int rc = prefer_max_shared(kern, dev.device)) return rc;
   if (int rc = launch_pdl(kern, dim3((unsigned)max_chunks, (unsigned)n), dim3(kWarps * 32), smem,
                           s, static_cast<const uint16_t*>(q), (const void*)kc, (const void*)vc,
-                          (const uint32_t*)nullptr, (const uint32_t*)nullptr, kstart,
-                          (const int32_t*)klen, Hkv, max_chunks, sl2, ws, vstart, napprox))
+                          kstart, (const int32_t*)klen, Hkv, max_chunks, sl2, ws, vstart, napprox))
     return rc;
   auto comb = decode_combine_vector_kernel<D, G>;
   if (int rc = prefer_max_shared(comb, dev.device)) return rc;
