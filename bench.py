@@ -6,9 +6,11 @@ Headline (one JSON line on rank 0): KV tokens/s scored + selected + compacted
 for one Llama-3-8B-shaped layer cache (U=1, 32 q / 8 kv heads, d=128,
 T=32768, bf16, observation window 64, global top-k across heads at keep
 ratio 0.10, 4 sinks + 64 recent always kept).  A step is one pass of
-kvc_score_attn -> kvc_select -> kvc_compact over that cache; inputs are
-resident in HBM; L2 is flushed (256 MiB write) between steps, outside the
-step's CUDA events.  The same JSON line also reports:
+kvc_score_attn -> kvc_select_compact (the selection and the compaction in
+one call, outputs identical to kvc_select -> kvc_compact, which is timed
+too: step_three_calls_us) over that cache; inputs are resident in HBM; L2
+is flushed (256 MiB write) between steps, outside the step's CUDA events.
+The same JSON line also reports:
 
 * roofline: the dominant kernel (tensor-core scoring) against the measured
   HBM copy bandwidth, and its tensor-pipe rate;
@@ -131,7 +133,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------- workloads
 class LayerWorkload:
-    """Device buffers of one score -> select -> compact pass."""
+    """Device buffers of one score -> select -> compact pass (two calls, or one for
+    the selection and the compaction together)."""
 
     def __init__(self, B, w, device):
         self.B, self.w = B, w
@@ -143,6 +146,9 @@ class LayerWorkload:
         self.score_ws = torch.empty(B.lib().kvc_score_attn_workspace(
             w.U, w.Hq, w.Hkv, w.T, w.W, w.d, B.KVC_BF16 if w.dtype == "bf16" else B.KVC_F32),
             dtype=torch.uint8, device=device)
+        self.sc_ws = torch.empty(B.lib().kvc_select_compact_workspace(w.U, w.Hkv, w.T,
+                                                                      B.MODES["global"]),
+                                 dtype=torch.uint8, device=device)
         self.kept = torch.empty((n, w.T), dtype=torch.int32, device=device)
         self.counts = torch.empty(n, dtype=torch.int32, device=device)
         self.offs = torch.empty(n + 1, dtype=torch.int64, device=device)
@@ -165,6 +171,13 @@ class LayerWorkload:
         self.B.kvc_compact(self.k, self.v, self.kept, self.counts, self.offs, self.kc, self.vc,
                            self.start, self.len, slack=self.w.slack)
 
+    def select_compact(self):
+        w = self.w
+        self.B.kvc_select_compact(self.scores, "global", self.k, self.v, self.kept, self.counts,
+                                  self.offs, self.kc, self.vc, self.start, self.len,
+                                  keep_ratio=w.keep_ratio, n_sink=w.n_sink, n_recent=w.n_recent,
+                                  slack=w.slack, workspace=self.sc_ws)
+
 
 def flush_l2(buf):
     buf.add_(1)          # 256 MiB read + write, larger than the 126 MB L2
@@ -172,37 +185,51 @@ def flush_l2(buf):
 
 def bench_layer(B, w, steps, warmup, device):
     """`warmup` untimed steps, then `steps` timed steps: each one score ->
-    select -> compact with CUDA events around the three launches only (the
-    L2 flush before it stays outside).  Nothing is recorded between the
-    kernels, so each may start while its predecessor drains (programmatic
-    dependent launch).  A second run of the same steps with events between
-    the kernels gives the per-stage split (it serialises the stages)."""
+    select + compact (kvc_select_compact, one call) with CUDA events around
+    the launches only (the L2 flush before it stays outside).  Nothing is
+    recorded between the kernels, so each may start while its predecessor
+    drains (programmatic dependent launch).  The same steps with kvc_select
+    and kvc_compact as two calls are timed next, then runs with events
+    between the calls give the per-stage split (they serialise the stages)."""
     L = LayerWorkload(B, w, device)
     flush = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)
     s = torch.cuda.current_stream()
-    for _ in range(warmup):
-        flush_l2(flush)
-        L.score(); L.select(); L.compact()
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    for i in range(steps):
-        flush_l2(flush)
-        ev[i][0].record(s); L.score(); L.select(); L.compact(); ev[i][1].record(s)
-    torch.cuda.synchronize()
-    t_step = [e[0].elapsed_time(e[1]) for e in ev]
-    # per-stage split (outside the timed steps)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    for i in range(steps):
-        flush_l2(flush)
-        e = ev[i]
-        e[0].record(s); L.score(); e[1].record(s); L.select(); e[2].record(s); L.compact()
-        e[3].record(s)
-    torch.cuda.synchronize()
-    t_score = [e[0].elapsed_time(e[1]) for e in ev]
-    t_sel = [e[1].elapsed_time(e[2]) for e in ev]
-    t_comp = [e[2].elapsed_time(e[3]) for e in ev]
+
+    def timed(calls):
+        for _ in range(warmup):
+            flush_l2(flush)
+            for f in calls:
+                f()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush_l2(flush)
+            ev[i][0].record(s)
+            for f in calls:
+                f()
+            ev[i][1].record(s)
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    def staged(calls):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+              for _ in range(steps)]
+        for i in range(steps):
+            flush_l2(flush)
+            ev[i][0].record(s)
+            for x, f in enumerate(calls):
+                f()
+                ev[i][x + 1].record(s)
+        torch.cuda.synchronize()
+        return [[e[x].elapsed_time(e[x + 1]) for e in ev] for x in range(len(calls))]
+
+    t_step = timed([L.score, L.select_compact])
+    t_step3 = timed([L.score, L.select, L.compact])
+    t_score, t_sel, t_comp = staged([L.score, L.select, L.compact])
+    _, t_selcomp = staged([L.score, L.select_compact])
     kept_rows = int(L.offs[-1].item())
     return L, dict(score_ms=t_score, select_ms=t_sel, compact_ms=t_comp, step_ms=t_step,
+                   step_three_calls_ms=t_step3, select_compact_ms=t_selcomp,
                    kept_rows=kept_rows)
 
 
@@ -251,7 +278,7 @@ def bench_kvzip_plus(B, L, steps, warmup):
 
 def bench_e2e(B, L, steps, warmup):
     """Same pass through the C ABI with host buffers: every step copies
-    q_win/K/V from pinned host memory, runs score -> select -> compact and
+    q_win/K/V from pinned host memory, runs score -> select + compact and
     copies the compacted cache + offsets back.  Steps alternate between two
     streams, each with its own device buffers, so one step's copies overlap
     the other's kernels (the copy engines, not the kernels, set the pace)."""
@@ -274,7 +301,7 @@ def bench_e2e(B, L, steps, warmup):
             Lp.q.copy_(hq, non_blocking=True)
             Lp.k.copy_(hk, non_blocking=True)
             Lp.v.copy_(hv, non_blocking=True)
-            Lp.score(); Lp.select(); Lp.compact()
+            Lp.score(); Lp.select_compact()
             oofs.copy_(Lp.offs, non_blocking=True)
             okc.copy_(Lp.kc[:rows], non_blocking=True)
             ovc.copy_(Lp.vc[:rows], non_blocking=True)
@@ -1034,7 +1061,9 @@ def main():
     if args.only == "layer":
         print(json.dumps({"value": value, "step_ms": step_ms, "score_ms": score_ms,
                           "select_ms": statistics.mean(r["select_ms"]),
-                          "compact_ms": statistics.mean(r["compact_ms"])}))
+                          "compact_ms": statistics.mean(r["compact_ms"]),
+                          "select_compact_ms": statistics.mean(r["select_compact_ms"]),
+                          "step_three_calls_ms": statistics.mean(r["step_three_calls_ms"])}))
         return
 
     # ---- sub-measurements (outside the headline timed region)
@@ -1070,9 +1099,12 @@ def main():
                    "parallelism": f"replicas x{world}"},
         # stage times from a separate run with events between the kernels
         "stages_us": {"score": score_ms * 1e3,
+                      "select_compact": statistics.mean(r["select_compact_ms"]) * 1e3,
                       "select": statistics.mean(r["select_ms"]) * 1e3,
                       "compact": statistics.mean(r["compact_ms"]) * 1e3,
                       "kept_rows": r["kept_rows"]},
+        # the same step with kvc_select and kvc_compact as two calls
+        "step_three_calls_us": statistics.mean(r["step_three_calls_ms"]) * 1e3,
         "roofline": {"kernel": "score_tc_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": src,

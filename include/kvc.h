@@ -266,11 +266,12 @@ int kvc_select(const float* scores, int U, int Hkv, int T, int mode,
  * kc, vc   [capacity_rows, d] dtype; capacity_rows must be at least
  *          offsets[U*Hkv] + U*Hkv*slack_per_head (the device checks every
  *          row and records KVC_ERR_RANGE instead of writing past it).
- * The device also checks the offsets against counts and T before it reads
- * an index: a row j of head i with j < 0, j >= counts[i] or j >= T (offsets
- * that disagree with counts), or a kept index outside [0, T), is skipped
- * and recorded as KVC_ERR_RANGE; an offsets total outside [0, U*Hkv*T]
- * copies nothing and records KVC_ERR_RANGE.
+ * The device also checks the offsets against counts and T: a row j of head
+ * i with j < 0 or j >= T is never looked up (its index would lie outside
+ * row i of kept_idx), and one with j >= counts[i] (offsets that disagree
+ * with counts), or with a kept index outside [0, T), is skipped; each is
+ * recorded as KVC_ERR_RANGE.  An offsets total outside [0, U*Hkv*T] copies
+ * nothing and records KVC_ERR_RANGE.
  * start    [U*Hkv] int64 (written), len [U*Hkv] int32 (written = counts).
  * Requires d * element size to be a multiple of 16 bytes and 16-byte aligned
  * k, v, kc, vc.
@@ -279,6 +280,32 @@ int kvc_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, 
                 const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
                 int slack_per_head, void* kc, void* vc, int64_t capacity_rows,
                 int64_t* start, int32_t* len, void* stream);
+
+/* Bytes of workspace kvc_select_compact uses to hand a single pool's
+ * decision from the selection to the emission (0: it then runs kvc_select
+ * and kvc_compact as they are). */
+size_t kvc_select_compact_workspace(int U, int Hkv, int T, int mode);
+
+/*
+ * kvc_select followed by kvc_compact on the same arguments, with the same
+ * outputs bit for bit (kept_idx, counts, offsets, start, len and the
+ * compacted rows of kc / vc) and the same argument rules and error
+ * behaviour.  A launch with one selection pool (GLOBAL_TOPK with U = 1, or
+ * one head) given at least kvc_select_compact_workspace() bytes of
+ * workspace ends the selection once the threshold is known and lets one
+ * kernel, a CTA per (token range, head), decide each token again from that
+ * threshold, write its index and copy its K / V rows (no separate pass over
+ * the kept indices, one launch and one dependent round trip fewer).  Other
+ * launches, or a smaller workspace, run the two calls back to back.
+ */
+int kvc_select_compact(const float* scores, int U, int Hkv, int T, int mode,
+                       double keep_ratio, float tau, const int32_t* head_budget,
+                       int n_sink, int n_recent,
+                       const void* k, const void* v, int dtype, int d, int slack_per_head,
+                       void* kc, void* vc, int64_t capacity_rows,
+                       int32_t* kept_idx, int32_t* counts, int64_t* offsets,
+                       int64_t* start, int32_t* len,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ----------------------------------------------------------------- decode */
 

@@ -44,6 +44,9 @@ SIGNATURES = {
     "kvc_select_workspace": (_SZ, [_I, _I, _I, _I]),
     "kvc_select": (_I, [_P, _I, _I, _I, _I, _D, _F, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "kvc_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I64, _P, _P, _P]),
+    "kvc_select_compact_workspace": (_SZ, [_I, _I, _I, _I]),
+    "kvc_select_compact": (_I, [_P, _I, _I, _I, _I, _D, _F, _P, _I, _I, _P, _P, _I, _I, _I, _P,
+                                _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "kvc_decode_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "kvc_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                              _P, _SZ, _P]),
@@ -221,6 +224,26 @@ def kvc_compact(k, v, kept_idx, counts, offsets, kc, vc, start, length, slack=0,
                            _ptr(counts), _ptr(offsets), int(slack), _ptr(kc), _ptr(vc),
                            kc.shape[0], _ptr(start), _ptr(length), _stream(stream))
     _check("kvc_compact", rc)
+
+
+def kvc_select_compact(scores, mode, k, v, kept_idx, counts, offsets, kc, vc, start, length,
+                       keep_ratio=0.0, tau=0.0, head_budget=None, n_sink=0, n_recent=0, slack=0,
+                       workspace=None, stream=None):
+    """kvc_select then kvc_compact in one call (see kvc.h); workspace None
+    allocates kvc_select_compact_workspace() bytes."""
+    U, Hkv, T = scores.shape
+    d = k.shape[-1]
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    if workspace is None:
+        workspace = _workspace(lib().kvc_select_compact_workspace(U, Hkv, T, m), scores.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().kvc_select_compact(_ptr(scores), U, Hkv, T, m, float(keep_ratio), float(tau),
+                                  _ptr(head_budget), int(n_sink), int(n_recent), _ptr(k), _ptr(v),
+                                  _dtype(k), d, int(slack), _ptr(kc), _ptr(vc), kc.shape[0],
+                                  _ptr(kept_idx), _ptr(counts), _ptr(offsets), _ptr(start),
+                                  _ptr(length), _ptr(workspace) if ws_bytes else None, ws_bytes,
+                                  _stream(stream))
+    _check("kvc_select_compact", rc)
 
 
 def kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype=KVC_BF16) -> int:

@@ -136,10 +136,14 @@ int kvc_score_linear(const void* hidden, const void* weight, const float* bias, 
 // ----------------------------------------------------------------- select
 size_t kvc_select_workspace(int U, int Hkv, int T, int mode) { return 0; }
 
-int kvc_select(const float* scores, int U, int Hkv, int T, int mode, double keep_ratio,
-               float tau, const int32_t* head_budget, int n_sink, int n_recent,
-               int32_t* kept_idx, int32_t* counts, int64_t* offsets, void* workspace,
-               size_t workspace_bytes, void* stream) {
+namespace {
+
+// kvc_select's argument rules; on success *need_out is the non-protected
+// budget, *ns_out / *nr_out the clamped sink and recent counts.
+int select_args(const float* scores, int U, int Hkv, int T, int mode, double keep_ratio,
+                const int32_t* head_budget, int n_sink, int n_recent, const int32_t* kept_idx,
+                const int32_t* counts, const int64_t* offsets, int64_t* need_out, int* ns_out,
+                int* nr_out) {
   if (!scores || !kept_idx || !counts || !offsets) return KVC_ERR_INVALID;
   if (U <= 0 || Hkv <= 0 || T <= 0 || n_sink < 0 || n_recent < 0) return KVC_ERR_INVALID;
   if (mode != KVC_SEL_GLOBAL_TOPK && mode != KVC_SEL_THRESHOLD && mode != KVC_SEL_PER_HEAD)
@@ -163,12 +167,61 @@ int kvc_select(const float* scores, int U, int Hkv, int T, int mode, double keep
     if (Beff > total) Beff = total;
     need = Beff - Hkv * nP;
   }
+  *need_out = need;
+  *ns_out = (int)ns;
+  *nr_out = (int)(T - rs);
+  return KVC_OK;
+}
+
+}  // namespace
+
+int kvc_select(const float* scores, int U, int Hkv, int T, int mode, double keep_ratio,
+               float tau, const int32_t* head_budget, int n_sink, int n_recent,
+               int32_t* kept_idx, int32_t* counts, int64_t* offsets, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  int64_t need = 0;
+  int ns = 0, nr = 0;
+  if (int rc = select_args(scores, U, Hkv, T, mode, keep_ratio, head_budget, n_sink, n_recent,
+                           kept_idx, counts, offsets, &need, &ns, &nr))
+    return rc;
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
-  return kvc::select_launch(scores, U, Hkv, T, mode, need, tau, head_budget, (int)ns,
-                            (int)(T - rs), kept_idx, counts, offsets, dev,
-                            kvc::as_stream(stream));
+  return kvc::select_launch(scores, U, Hkv, T, mode, need, tau, head_budget, ns, nr, kept_idx,
+                            counts, offsets, dev, kvc::as_stream(stream));
+}
+
+size_t kvc_select_compact_workspace(int U, int Hkv, int T, int mode) {
+  if (U <= 0 || Hkv <= 0 || T <= 0) return 0;
+  return kvc::select_compact_ws(U, Hkv, T, mode);
+}
+
+int kvc_select_compact(const float* scores, int U, int Hkv, int T, int mode, double keep_ratio,
+                       float tau, const int32_t* head_budget, int n_sink, int n_recent,
+                       const void* k, const void* v, int dtype, int d, int slack_per_head,
+                       void* kc, void* vc, int64_t capacity_rows, int32_t* kept_idx,
+                       int32_t* counts, int64_t* offsets, int64_t* start, int32_t* len,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  int64_t need = 0;
+  int ns = 0, nr = 0;
+  if (int rc = select_args(scores, U, Hkv, T, mode, keep_ratio, head_budget, n_sink, n_recent,
+                           kept_idx, counts, offsets, &need, &ns, &nr))
+    return rc;
+  if (!k || !v || !kc || !vc || !start || !len) return KVC_ERR_INVALID;
+  if (dtype != KVC_F32 && dtype != KVC_BF16) return KVC_ERR_INVALID;
+  if (d <= 0 || slack_per_head < 0 || capacity_rows < 0) return KVC_ERR_INVALID;
+  int64_t row_bytes = (int64_t)d * (int64_t)kvc::elt_size(dtype);
+  if (row_bytes % 16 || row_bytes > 4096) return KVC_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc))
+    return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::select_compact_launch(scores, U, Hkv, T, mode, need, tau, head_budget, ns, nr, k,
+                                    v, (int)row_bytes, slack_per_head, kc, vc, capacity_rows,
+                                    kept_idx, counts, offsets, start, len, workspace,
+                                    workspace ? workspace_bytes : 0, dev,
+                                    kvc::as_stream(stream));
 }
 
 // ---------------------------------------------------------------- compact

@@ -90,11 +90,15 @@ compact_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, int vpr
       // caller's error and are reported, never followed)
       const int64_t j = r - offs[i];
       const int64_t dst = r + (int64_t)i * slack;
-      if (j < 0 || j >= T || j >= __ldg(counts + i) || dst >= capacity_rows) {
+      if (j < 0 || j >= T || dst >= capacity_rows) {
         report(status, KVC_ERR_RANGE);
       } else {
+        // the head's count and the index are read together (row j < T of
+        // head i lies inside kept_idx whatever the count says); the index
+        // is used only if j is below the count
+        const int32_t cnt = __ldg(counts + i);
         const int32_t t = __ldg(kept_idx + (int64_t)i * T + j);
-        if (t < 0 || t >= T) {
+        if (j >= cnt || t < 0 || t >= T) {
           report(status, KVC_ERR_RANGE);
         } else {
           src_row = (int64_t)i * T + t;

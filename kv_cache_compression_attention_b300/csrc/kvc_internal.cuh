@@ -108,6 +108,16 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
                   int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
                   cudaStream_t s);
 
+// kvc_select followed by kvc_compact; a launch with one selection pool
+// hands the select's decision to a kernel that emits and copies in one go.
+size_t select_compact_ws(int U, int Hkv, int T, int mode);
+int select_compact_launch(const float* scores, int U, int Hkv, int T, int mode,
+                          int64_t need_global, float tau, const int32_t* head_budget, int n_sink,
+                          int n_recent, const void* k, const void* v, int row_bytes, int slack,
+                          void* kc, void* vc, int64_t capacity_rows, int32_t* kept_idx,
+                          int32_t* counts, int64_t* offsets, int64_t* start, int32_t* len,
+                          void* ws, size_t ws_bytes, const Dev& dev, cudaStream_t s);
+
 int select_stream_launch(const float* scores, int U, int Hkv, int T, int mode,
                          int64_t need_global, float tau, const int32_t* head_budget, int n_sink,
                          int n_recent, int nP, int32_t* kept_idx, int32_t* counts,

@@ -57,6 +57,8 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxHps = 8;                 // heads per pool kept in registers
 constexpr uint32_t kNoThr = 0xffffffffu;   // larger than every real key
+constexpr int kSubRange = 512;             // tokens per emission CTA of the hand-off
+constexpr int kMaxSub = 64;                // sub-ranges per CTA range at most
 
 struct Args {
   const float* scores;
@@ -69,6 +71,11 @@ struct Args {
   int32_t* counts;
   int64_t* offsets;   // written here when the launch has a single pool, else NULL
   int* status;
+  // non-NULL: hand the decision to emit_compact_kernel instead of emitting
+  // ([C][2 + hps * hand_sub] words: threshold key, tie cut, kept count per
+  // head and 512-token sub-range of the CTA's range)
+  uint32_t* hand;
+  int hand_sub;
 };
 
 struct Shared {
@@ -459,15 +466,34 @@ select_kernel(Args a) {
     }
   }
 
-  // ---- phase D: warp w emits the kept tokens of its slice [j_lo, j_hi) of
-  // the range, per head, ascending, into its staging segment
-  const int per_w = lay.per_w;
-  const int j_lo = min(nt, warp * per_w), j_hi = min(nt, j_lo + per_w);
   const bool thr_mode = a.mode == KVC_SEL_THRESHOLD;
   auto keep = [&](uint32_t key, int j, int hh) -> bool {
     return key == 0u || (thr_mode ? key >= thr
                                   : (key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut)));
   };
+  if (a.hand) {
+    // ---- hand-off: this range's threshold, tie cut and kept count per head
+    // (the placement and the row copies run in emit_compact_kernel)
+    const int S = a.hand_sub;
+    uint32_t* rec = a.hand + (size_t)rank * (2 + hps * S);
+    for (int q = warp; q < hps * S; q += kWarps) {
+      const int hh = q / S, sub = q - hh * S;
+      const int j1 = min(nt, (sub + 1) * kSubRange);
+      uint32_t n = 0;
+      for (int j = sub * kSubRange + lane; j < j1; j += 32) n += keep(keys[hh * nt + j], j, hh) ? 1u : 0u;
+      n = __reduce_add_sync(0xffffffffu, n);
+      if (lane == 0) rec[2 + q] = n;
+    }
+    if (tid == 0) { rec[0] = thr; rec[1] = ecut; }
+    // no CTA may leave while a peer can still read its shared memory
+    cl.sync();
+    return;
+  }
+
+  // ---- phase D: warp w emits the kept tokens of its slice [j_lo, j_hi) of
+  // the range, per head, ascending, into its staging segment
+  const int per_w = lay.per_w;
+  const int j_lo = min(nt, warp * per_w), j_hi = min(nt, j_lo + per_w);
 #pragma unroll 2
   for (int hh = 0; hh < hps; ++hh) {
     const uint32_t* __restrict__ kr = keys + hh * nt;                       // keys and staging
@@ -578,6 +604,171 @@ offsets_kernel(const int32_t* __restrict__ counts, int n, int64_t* __restrict__ 
   if (threadIdx.x == 0) offsets[n] = carry_s;
 }
 
+// Second half of kvc_select_compact for a launch with one selection pool:
+// CTA (rank * S + sub, hh) takes 512-token sub-range `sub` of the select
+// kernel's range `rank` of head hh, decides its tokens again with that
+// range's threshold and tie cut, places them after the kept tokens of the
+// head's lower ranges and sub-ranges (all counted in the hand-off record),
+// writes their indices and copies their K / V rows.  The rule and the
+// per-range tie cut are the select kernel's own, so the indices are the ones
+// kvc_select writes.
+constexpr int kEThreads = 256;
+constexpr int kEWarps = kEThreads / 32;
+constexpr int kEVec = 8;                 // 16-byte vectors in flight per thread and tensor
+static_assert(kSubRange == 2 * kEThreads, "two tokens per thread");
+static_assert(kMaxHps <= kEWarps, "a warp per head");
+
+struct EArgs {
+  const float* scores;
+  int T, hps, C, S, mode, n_sink, n_recent;
+  const uint32_t* hand;          // [C][2 + hps * S]
+  const uint4* k;
+  const uint4* v;
+  int vpr_shift, slack;
+  uint4* kc;
+  uint4* vc;
+  int64_t capacity_rows;
+  int32_t* kept;
+  int32_t* counts;
+  int64_t* offsets;
+  int64_t* start;
+  int32_t* len;
+  int* status;
+};
+
+__global__ void __launch_bounds__(kEThreads)
+emit_compact_kernel(EArgs e) {
+  __shared__ uint32_t htot[kMaxHps], base_s, wsum[kEWarps];
+  __shared__ int32_t lst_t[kSubRange], lst_p[kSubRange];
+  const int T = e.T, hps = e.hps, C = e.C, S = e.S;
+  const int rank = blockIdx.x / S, sub = blockIdx.x - rank * S, hh = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = (int)((int64_t)rank * T / C), t1 = (int)((int64_t)(rank + 1) * T / C);
+  const int a0 = t0 + sub * kSubRange, a1 = min(t1, a0 + kSubRange);
+  const int rs = T - e.n_recent;
+  const int stride = 2 + hps * S;
+  const float* row = e.scores + (int64_t)hh * T;
+  pdl_wait();
+  pdl_trigger();
+  // two consecutive tokens per thread, in flight while the record is read
+  const int tb = a0 + 2 * tid;
+  float sv[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) sv[x] = tb + x < a1 ? __ldg(row + tb + x) : 0.0f;
+  const uint32_t thr = e.hand[(size_t)rank * stride];
+  const uint32_t ecut = e.hand[(size_t)rank * stride + 1];
+  if (warp < hps) {
+    // warp h: head h's total; for head hh also the part ranked before this
+    // CTA (lower ranges, then lower sub-ranges of this range)
+    uint32_t tot = 0, below = 0;
+    for (int q = lane; q < C * S; q += 32) {
+      const int r = q / S, sb = q - r * S;
+      const uint32_t x = e.hand[(size_t)r * stride + 2 + warp * S + sb];
+      tot += x;
+      below += (r < rank || (r == rank && sb < sub)) ? x : 0u;
+    }
+    tot = __reduce_add_sync(0xffffffffu, tot);
+    below = __reduce_add_sync(0xffffffffu, below);
+    if (lane == 0) {
+      htot[warp] = tot;
+      if (warp == hh) base_s = below;
+    }
+  }
+  __syncthreads();
+  int64_t off_hh = 0, total = 0;
+  for (int h = 0; h < hps; ++h) {
+    if (h < hh) off_hh += htot[h];
+    total += htot[h];
+  }
+  if (blockIdx.x == 0 && hh == 0 && tid <= hps) {
+    int64_t o = 0;
+    for (int h = 0; h < tid; ++h) o += htot[h];
+    e.offsets[tid] = o;
+    if (tid < hps) {
+      e.counts[tid] = (int32_t)htot[tid];
+      e.start[tid] = o + (int64_t)tid * e.slack;
+      e.len[tid] = (int32_t)htot[tid];
+    }
+  }
+  (void)total;
+  const bool thr_mode = e.mode == KVC_SEL_THRESHOLD;
+  uint32_t flags = 0u;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int t = tb + x;
+    if (t < a1) {
+      const uint32_t key = (t < e.n_sink || t >= rs) ? 0u : score_key(sv[x]);
+      const uint32_t jl = (uint32_t)(t - t0);
+      const bool kp = key == 0u || (thr_mode ? key >= thr
+                                            : (key > thr || (key == thr && jl * hps + hh < ecut)));
+      flags |= (kp ? 1u : 0u) << x;
+    }
+  }
+  const uint32_t n = __popc(flags);
+  uint32_t incl = n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kEWarps; ++w) {
+    const uint32_t v = wsum[w];
+    if (w < warp) before += v;
+    all += v;
+  }
+  const uint32_t base = base_s;
+  int32_t* out = e.kept + (int64_t)hh * T;
+  uint32_t k = before + incl - n;              // this thread's first slot in the list
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if ((flags >> x) & 1u) {
+      const uint32_t pos = base + k;
+      lst_t[k] = tb + x;
+      lst_p[k] = (int32_t)pos;
+      if (pos < (uint32_t)T) out[pos] = tb + x;
+      else report(e.status, KVC_ERR_RANGE);
+      ++k;
+    }
+  }
+  __syncthreads();
+  // the kept rows: K and V, 16-byte vectors, kEVec in flight per tensor
+  const int64_t dst0 = off_hh + (int64_t)hh * e.slack;   // head's first compacted row
+  const int vpr = 1 << e.vpr_shift;
+  const int pairs = (int)all << e.vpr_shift;
+  for (int p0 = 0; p0 < pairs; p0 += kEThreads * kEVec) {
+    uint4 kv[kEVec], vv[kEVec];
+    int64_t dst[kEVec];
+#pragma unroll
+    for (int x = 0; x < kEVec; ++x) {
+      const int p = p0 + x * kEThreads + tid;
+      dst[x] = -1;
+      if (p < pairs) {
+        const int r = p >> e.vpr_shift, vec = p & (vpr - 1);
+        const int64_t src = (int64_t)hh * T + lst_t[r];
+        const int64_t d = dst0 + lst_p[r];
+        if (lst_p[r] < T && d < e.capacity_rows) {
+          kv[x] = __ldg(e.k + (src << e.vpr_shift) + vec);
+          vv[x] = __ldg(e.v + (src << e.vpr_shift) + vec);
+          dst[x] = (d << e.vpr_shift) + vec;
+        } else if (vec == 0) {
+          report(e.status, KVC_ERR_RANGE);
+        }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < kEVec; ++x) {
+      if (dst[x] >= 0) {
+        e.kc[dst[x]] = kv[x];
+        e.vc[dst[x]] = vv[x];
+      }
+    }
+  }
+}
+
 size_t shared_bytes(int nt, int hps, int V) {
   const Layout lay(nt, hps, V);
   return ((sizeof(Shared) + 15) & ~size_t(15)) + (lay.keys_words() + (size_t)lay.region) * 4;
@@ -585,10 +776,17 @@ size_t shared_bytes(int nt, int hps, int V) {
 
 }  // namespace
 
-int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t need_global,
-                  float tau, const int32_t* head_budget, int n_sink, int n_recent,
-                  int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
-                  cudaStream_t s) {
+namespace {
+
+// The cluster launch of kvc_select.  With `hand` (one pool only) the kernel
+// hands its decision over instead of emitting; *cluster receives the
+// cluster size then, or 0 when the pool took the streaming kernel (which
+// emits as usual).
+int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64_t need_global,
+                     float tau, const int32_t* head_budget, int n_sink, int n_recent,
+                     int32_t* kept_idx, int32_t* counts, int64_t* offsets, uint32_t* hand,
+                     int* cluster, int* sub, const Dev& dev, cudaStream_t s) {
+  if (cluster) *cluster = 0;
   const int hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1;
   const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
   const int64_t pool = (int64_t)hps * T;
@@ -631,6 +829,8 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   a.kept = kept_idx; a.counts = counts;
   a.offsets = (nseg == 1) ? offsets : nullptr;
   a.status = dev.status;
+  a.hand = (nseg == 1) ? hand : nullptr;
+  a.hand_sub = 0;
   static std::mutex mu;
   static bool attr_done[64];
   static std::map<std::tuple<int, int, size_t>, int> active_memo;
@@ -675,12 +875,72 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
     if (C == 1 || smem_for(C / 2) > smem_max) return stream();
     C /= 2;
   }
+  if (a.hand) {
+    // the emission takes 512-token sub-ranges of every CTA's range
+    a.hand_sub = (int)(((T + C - 1) / C + kSubRange - 1) / kSubRange);
+    if (a.hand_sub > kMaxSub) a.hand = nullptr;
+  }
   attr[1] = pdl_attr();
   cfg.numAttrs = 2;
   if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
   else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
+  if (a.hand) {
+    if (cluster) *cluster = C;
+    if (sub) *sub = a.hand_sub;
+    return launch_status();
+  }
   if (int rc = launch_offsets()) return rc;
   return launch_status();
+}
+
+}  // namespace
+
+int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t need_global,
+                  float tau, const int32_t* head_budget, int n_sink, int n_recent,
+                  int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
+                  cudaStream_t s) {
+  return select_launch_ex(scores, U, Hkv, T, mode, need_global, tau, head_budget, n_sink,
+                          n_recent, kept_idx, counts, offsets, nullptr, nullptr, nullptr, dev,
+                          s);
+}
+
+size_t select_compact_ws(int U, int Hkv, int T, int mode) {
+  const int hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1;
+  const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
+  if (nseg != 1 || hps > kMaxHps) return 0;
+  return (size_t)16 * (2 + hps * kMaxSub) * sizeof(uint32_t);
+}
+
+int select_compact_launch(const float* scores, int U, int Hkv, int T, int mode,
+                          int64_t need_global, float tau, const int32_t* head_budget, int n_sink,
+                          int n_recent, const void* k, const void* v, int row_bytes, int slack,
+                          void* kc, void* vc, int64_t capacity_rows, int32_t* kept_idx,
+                          int32_t* counts, int64_t* offsets, int64_t* start, int32_t* len,
+                          void* ws, size_t ws_bytes, const Dev& dev, cudaStream_t s) {
+  const int vpr = row_bytes / 16;
+  if (vpr <= 0 || (vpr & (vpr - 1)) || vpr > 32) return KVC_ERR_UNSUPPORTED;
+  const size_t need_ws = select_compact_ws(U, Hkv, T, mode);
+  uint32_t* hand = (need_ws && ws && ws_bytes >= need_ws) ? static_cast<uint32_t*>(ws) : nullptr;
+  int C = 0, S = 0;
+  if (int rc = select_launch_ex(scores, U, Hkv, T, mode, need_global, tau, head_budget, n_sink,
+                                n_recent, kept_idx, counts, offsets, hand, &C, &S, dev, s))
+    return rc;
+  if (!hand || C == 0)       // the select emitted: the plain compaction follows
+    return compact_launch(k, v, row_bytes, U, Hkv, T, kept_idx, counts, offsets, slack, kc, vc,
+                          capacity_rows, start, len, dev, s);
+  EArgs e;
+  e.scores = scores; e.T = T; e.hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1; e.C = C; e.S = S;
+  e.mode = mode; e.n_sink = n_sink; e.n_recent = n_recent; e.hand = hand;
+  e.k = static_cast<const uint4*>(k); e.v = static_cast<const uint4*>(v);
+  int sh = 0;
+  while ((16 << sh) < row_bytes) ++sh;
+  e.vpr_shift = sh; e.slack = slack;
+  e.kc = static_cast<uint4*>(kc); e.vc = static_cast<uint4*>(vc);
+  e.capacity_rows = capacity_rows;
+  e.kept = kept_idx; e.counts = counts; e.offsets = offsets; e.start = start; e.len = len;
+  e.status = dev.status;
+  return launch_pdl(emit_compact_kernel, dim3((unsigned)(C * S), (unsigned)e.hps),
+                    dim3(kEThreads), 0, s, e);
 }
 
 }  // namespace kvc

@@ -117,6 +117,34 @@ def test_select_rejects_bad_arguments(lib):
     assert call(Hkv=600, T=16) == -2               # more than 512 heads in one pool
 
 
+def test_select_compact_rejects_bad_arguments(lib):
+    f = lib.kvc_select_compact
+
+    def call(scores=P, U=1, Hkv=2, T=16, mode=0, ratio=0.5, tau=0.0, hb=None, ns=1, nr=1,
+             k=P, v=P, dtype=1, d=128, slack=0, kc=P, vc=P, cap=64, kept=P, counts=P, offs=P,
+             start=P, length=P):
+        return f(scores, U, Hkv, T, mode, ratio, tau, hb, ns, nr, k, v, dtype, d, slack, kc, vc,
+                 cap, kept, counts, offs, start, length, None, 0, None)
+
+    assert call(scores=None) == -1            # the select's rules
+    assert call(mode=3) == -1
+    assert call(ratio=1.5) == -1
+    assert call(T=(1 << 24) + 1, mode=1) == -2
+    assert call(k=None) == -1                 # the compaction's rules
+    assert call(length=None) == -1
+    assert call(dtype=7) == -1
+    assert call(slack=-1) == -1
+    assert call(d=100) == -2                  # 200-byte rows
+    assert call(d=4096) == -2                 # 8 KB rows
+    # the hand-off record: one pool only, up to 8 heads per pool
+    # (16 CTA ranges x (threshold, tie cut, a count per head and 512-token sub-range))
+    assert lib.kvc_select_compact_workspace(1, 8, 32768, 0) == 16 * (2 + 8 * 64) * 4
+    assert lib.kvc_select_compact_workspace(1, 1, 4096, 1) == 16 * (2 + 64) * 4
+    assert lib.kvc_select_compact_workspace(2, 8, 32768, 0) == 0
+    assert lib.kvc_select_compact_workspace(1, 9, 32768, 0) == 0
+    assert lib.kvc_select_compact_workspace(1, 4, 131072, 1) == 0     # four per-head pools
+
+
 def test_compact_and_decode_reject_bad_arguments(lib):
     c = lib.kvc_compact
     assert c(None, P, 1, 1, 1, 8, 128, P, P, P, 0, P, P, 8, P, P, None) == -1

@@ -287,3 +287,124 @@ def test_compact_rejects_offsets_that_disagree_with_counts(B, case):
     assert B.kvc_device_status() == 0             # cleared
     assert guard[cap:].abs().sum().item() == 0    # nothing written past the capacity
     assert vguard[cap:].abs().sum().item() == 0
+
+
+# --------------------------------------------------- select + compact in one call
+def fused_and_separate(B, s, k, v, mode, slack, workspace=None, **kw):
+    """Outputs of kvc_select_compact and of kvc_select + kvc_compact on the same
+    inputs, every output buffer pre-filled with the same sentinel."""
+    U, Hkv, T = s.shape
+    n = U * Hkv
+    hb = kw.pop("head_budget", None)
+    if hb is not None:
+        hb = torch.as_tensor(np.asarray(hb), dtype=torch.int32).cuda()
+    cap = n * T + n * slack
+    res = []
+    for fused in (True, False):
+        kept = torch.full((n, T), -7, dtype=torch.int32, device="cuda")
+        counts = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+        offs = torch.full((n + 1,), -7, dtype=torch.int64, device="cuda")
+        kc = torch.full((cap, k.shape[-1]), 3.0, dtype=k.dtype, device="cuda")
+        vc = torch.full_like(kc, -3.0)
+        start = torch.full((n,), -7, dtype=torch.int64, device="cuda")
+        length = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+        if fused:
+            B.kvc_select_compact(s, mode, k, v, kept, counts, offs, kc, vc, start, length,
+                                 head_budget=hb, slack=slack, workspace=workspace, **kw)
+        else:
+            B.kvc_select(s, mode, kept, counts, offs, head_budget=hb, **kw)
+            B.kvc_compact(k, v, kept, counts, offs, kc, vc, start, length, slack=slack)
+        torch.cuda.synchronize()
+        assert B.kvc_device_status() == 0
+        c = counts.cpu().numpy()
+        kn = kept.cpu().numpy()
+        res.append(([kn[i, : c[i]] for i in range(n)], c, offs.cpu().numpy(),
+                    start.cpu().numpy(), length.cpu().numpy(), as_bytes(kc), as_bytes(vc)))
+    return res
+
+
+def assert_same_outputs(a, b):
+    for x, y in zip(a[0], b[0]):
+        np.testing.assert_array_equal(x, y)
+    for x, y in zip(a[1:], b[1:]):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("shape,mode,dtype,d", [
+    ((1, 8, 32768), "global", torch.bfloat16, 128),   # the 32k layer's shape: hand-off path
+    ((1, 4, 5000), "global", torch.float32, 64),      # ragged ranges
+    ((1, 3, 777), "global", torch.bfloat16, 64),
+    ((1, 1, 70001), "per_head", torch.bfloat16, 128),
+    ((1, 1, 4099), "threshold", torch.float32, 128),
+    ((2, 8, 3000), "global", torch.bfloat16, 128),    # two pools: the two calls back to back
+    ((1, 8, 65536), "global", torch.bfloat16, 64),    # beyond one cluster: streaming select
+])
+@pytest.mark.parametrize("ties,specials", [(False, False), (True, True)])
+def test_select_compact_equals_the_two_calls(B, shape, mode, dtype, d, ties, specials):
+    s = inputs.random_scores(shape, seed=sum(shape) + 3, ties=ties, specials=specials).cuda()
+    U, Hkv, T = shape
+    g = torch.Generator().manual_seed(11)
+    k = torch.randn((U, Hkv, T, d), generator=g).to(dtype).cuda()
+    v = torch.randn((U, Hkv, T, d), generator=g).to(dtype).cuda()
+    if mode == "global":
+        cases = [dict(keep_ratio=r, n_sink=ns, n_recent=nr)
+                 for r, ns, nr in [(0.1, 4, 64), (0.0, 2, 2), (1.0, 1, 1), (0.37, 0, 0)]]
+    elif mode == "per_head":
+        cases = [dict(head_budget=[b] * (U * Hkv), n_sink=4, n_recent=64)
+                 for b in (0, 700, 7000, T + 5)]
+    else:
+        cases = [dict(tau=t, n_sink=1, n_recent=3) for t in (0.5, float("nan"), float("-inf"))]
+    for kw in cases:
+        for slack in (0, 5):
+            a, b = fused_and_separate(B, s, k, v, mode, slack, **dict(kw))
+            assert_same_outputs(a, b)
+
+
+def test_select_compact_llama32k_against_the_oracle(B):
+    """The 32k layer through the fused call on the oracle's scores: kept
+    indices, counts, offsets and the compacted rows equal the oracle's."""
+    w = inputs.WORKLOADS["c2_llama32k"]
+    q = inputs.window_queries(w, "cuda")
+    k, v = inputs.keys_values(w, q, "cuda")
+    s = O.score_attn(np64(q), np64(k), w.scale).astype(np.float32)
+    kw = dict(keep_ratio=w.keep_ratio, n_sink=w.n_sink, n_recent=w.n_recent)
+    a, _ = fused_and_separate(B, torch.from_numpy(s).cuda(), k, v, "global", 0, **kw)
+    rk, rc, ro = O.select(s, "global", **kw)
+    np.testing.assert_array_equal(a[1], rc)
+    np.testing.assert_array_equal(a[2], ro)
+    for i in range(len(rc)):
+        np.testing.assert_array_equal(a[0][i], rk[i, : rc[i]])
+    kh = k.cpu().view(torch.int16).numpy()
+    vh = v.cpu().view(torch.int16).numpy()
+    ck, cv, cs, cl = O.compact(kh, vh, rk, rc, ro, 0)
+    rows = int(ro[-1])
+    np.testing.assert_array_equal(a[3], cs)
+    np.testing.assert_array_equal(a[4], cl)
+    np.testing.assert_array_equal(a[5].reshape(-1, w.d * 2)[:rows], ck.view(np.uint8).reshape(rows, -1))
+    np.testing.assert_array_equal(a[6].reshape(-1, w.d * 2)[:rows], cv.view(np.uint8).reshape(rows, -1))
+
+
+def test_select_compact_without_workspace_and_capacity_overflow(B):
+    U, Hkv, T, d = 1, 2, 640, 128
+    s = inputs.random_scores((U, Hkv, T), seed=4).cuda()
+    k = torch.randn((U, Hkv, T, d), device="cuda").to(torch.bfloat16)
+    v = torch.randn_like(k)
+    # no workspace: the two calls, same outputs
+    a, b = fused_and_separate(B, s, k, v, "global", 2,
+                              workspace=torch.empty(0, dtype=torch.uint8, device="cuda"),
+                              keep_ratio=0.3, n_sink=4, n_recent=8)
+    assert_same_outputs(a, b)
+    # a cache too small: rows past it are skipped and reported
+    guard = torch.zeros((2 * T, d), dtype=torch.bfloat16, device="cuda")
+    kc = guard[:100]
+    vc = torch.zeros_like(guard)[:100]
+    kept = torch.empty((2, T), dtype=torch.int32, device="cuda")
+    counts = torch.empty(2, dtype=torch.int32, device="cuda")
+    offs = torch.empty(3, dtype=torch.int64, device="cuda")
+    start = torch.empty(2, dtype=torch.int64, device="cuda")
+    length = torch.empty(2, dtype=torch.int32, device="cuda")
+    B.kvc_select_compact(s, "global", k, v, kept, counts, offs, kc, vc, start, length,
+                         keep_ratio=0.5, n_sink=4, n_recent=8)
+    assert B.kvc_device_status() == -6            # KVC_ERR_RANGE
+    assert B.kvc_device_status() == 0
+    assert guard[100:].abs().sum().item() == 0
