@@ -575,6 +575,49 @@ def bench_decode(B, steps, warmup, device):
     return out_d
 
 
+def bench_decode_q8_small(B, units, steps, warmup, device):
+    """A cut of the decode workload for profiling: `units` sequences of
+    N(0, 1) rows at the workload's per-head lengths, quantised with
+    kvc_quantize_rows, then `steps` timed kvc_decode_attn_q8 calls without
+    appends (the same cache every call)."""
+    import dataclasses
+    w = dataclasses.replace(inputs.WORKLOADS[DECODE_WORKLOAD], U=units)
+    lens = inputs.head_budgets(w, "cpu")
+    kc, vc, start, length = inputs.compressed_pool(w, lens, device)
+    kq = torch.empty(kc.shape, dtype=torch.uint8, device=device)
+    vq = torch.empty_like(kq)
+    kp = torch.empty((kc.shape[0], w.d // 32, 2), dtype=torch.float16, device=device)
+    vp = torch.empty_like(kp)
+    B.kvc_quantize_rows(kc, kq, kp)
+    B.kvc_quantize_rows(vc, vq, vp)
+    del kc, vc
+    max_len = int(lens.max()) + 8
+    ws = torch.empty(B.kvc_decode_workspace(w.U, w.Hq, w.Hkv, w.d, max_len), dtype=torch.uint8,
+                     device=device)
+    q, _, _ = inputs.decode_step_inputs(w, 0, device)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.U, w.Hq), device=device)
+
+    def run():
+        B.kvc_decode_attn_q8(q, kq, kp, vq, vp, start, length, out, lse, max_len=max_len,
+                             scale=w.scale, workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        run()
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / max(steps, 1) * 1e3
+    rows = int(lens.sum())
+    nbytes = 2 * rows * (w.d + (w.d // 32) * 4)
+    return {"workload": f"{w.name} cut to U={units}", "rows": rows, "bytes": nbytes,
+            "us_per_step": us, "gbs": nbytes / (us * 1e-6) / 1e9}
+
+
 def bench_vector(B, w, steps, warmup, device):
     """VECTOR three-way routing on the 32k layer (p_c = 0.9, p_a = 0.05): score ->
     pool select (1 - p_c + p_a, global top-k) -> reconstruction-error keys ->
@@ -994,7 +1037,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "decode", "c4", "c3", "vector"], default=None,
+    ap.add_argument("--units", type=int, default=16,
+                    help="--only decode_q8: batch size of the decode workload's cut")
+    ap.add_argument("--only", choices=["layer", "decode", "decode_q8", "c4", "c3", "vector"],
+                    default=None,
                     help="profiling runs: time only one workload")
     args = ap.parse_args()
     world, rank, local = dist_setup(args.gpus)
@@ -1038,6 +1084,9 @@ def main():
     if args.only == "decode":
         dec = bench_decode(B, args.steps, args.warmup, device)
         print(json.dumps({"decode": dec, "frac": dec["gbs"] / hbm}))
+        return
+    if args.only == "decode_q8":
+        print(json.dumps(bench_decode_q8_small(B, args.units, args.steps, args.warmup, device)))
         return
     if args.only == "c4":
         print(json.dumps(bench_c4(B, args.steps, args.warmup, device)))

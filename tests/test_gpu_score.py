@@ -169,6 +169,26 @@ def test_score_linear_small(B, dtype, U, Hkv, Dh, T):
     assert row_rel_err(np64(out), ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("U,Hkv,Dh,T", [
+    (1, 4, 3584, 4099),    # the 128k layer's width, ragged last stage of whole rows
+    (3, 4, 128, 2001),     # one 8-dim chunk per warp slice: most lanes idle
+    (1, 2, 6144, 1500),    # two chunks per lane
+    (2, 2, 384, 1029),
+])
+def test_score_linear_streamed_rows(B, U, Hkv, Dh, T):
+    """Many bf16 rows of widths from one 128-dim block to 6144, ragged row
+    counts; compared with the oracle on every row."""
+    h = rand((U, T, Dh), torch.bfloat16, 15)
+    wt = rand((Dh, Hkv), torch.bfloat16, 16, scale=Dh ** -0.5)
+    bias = rand((Hkv,), torch.float32, 17)
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda")
+    B.kvc_score_linear(h, wt, bias, out)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    ref = O.score_linear(np64(h), np64(wt), np64(bias))
+    assert row_rel_err(np64(out), ref) <= TOL[torch.bfloat16]
+
+
 def test_score_linear_qwen128k_sampled_rows(B):
     w = inputs.WORKLOADS["c4_qwen128k"]
     hid, wt, bias = inputs.linear_scorer(w, "cuda")
