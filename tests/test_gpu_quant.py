@@ -100,6 +100,36 @@ def test_decode_q8_small(B, G, append):
         np.testing.assert_array_equal(vp.cpu().numpy()[rows].view(np.uint16), avp.view(np.uint16))
 
 
+@pytest.mark.parametrize("G", [1, 3, 8])
+def test_decode_q8_chunk_edges(B, G):
+    """Lengths around the quantised kernel's 1024-row chunks and 64-row
+    stages, with appends, against the oracle's decode over the dequantised pool."""
+    U, Hkv, d = 1, 6, 128
+    kc, vc, start, lens = pool([63, 64, 1023, 1024, 1025, 2049], 2, d, 4)
+    g = torch.Generator().manual_seed(34 + G)
+    q = torch.randn((U, Hkv * G, d), generator=g).to(torch.bfloat16)
+    kn = torch.randn((U, Hkv, d), generator=g).to(torch.bfloat16)
+    vn = torch.randn((U, Hkv, d), generator=g).to(torch.bfloat16)
+    kq, kp = gpu_quantize(B, kc.cuda())
+    vq, vp = gpu_quantize(B, vc.cuda())
+    st, ln = torch.from_numpy(start).cuda(), torch.from_numpy(lens).cuda()
+    out = torch.full((U, Hkv * G, d), float("nan"), device="cuda").to(torch.bfloat16)
+    lse = torch.full((U, Hkv * G), float("nan"), device="cuda")
+    B.kvc_decode_attn_q8(q.cuda(), kq, kp, vq, vp, st, ln, out, lse, k_new=kn.cuda(),
+                         v_new=vn.cuda(), max_len=int(lens.max()) + 1)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    rkq, rkp = O.quantize_rows(kc.float().numpy())
+    rvq, rvp = O.quantize_rows(vc.float().numpy())
+    kd, vd = O.dequantize_rows(rkq, rkp), O.dequantize_rows(rvq, rvp)
+    # the new token is attended exactly (it is appended quantised afterwards)
+    ro, rl, _, _, rlen = O.decode_attn(np64(q), kd, vd, start, lens, np64(kn), np64(vn),
+                                       d ** -0.5)
+    assert row_rel_err(np64(out).reshape(-1, d), ro.reshape(-1, d)) <= 2e-2
+    assert lse_err(np64(lse), rl) <= 2e-2
+    np.testing.assert_array_equal(ln.cpu().numpy(), rlen)
+
+
 def test_decode_q8_batch64_sampled(B):
     """The batch-64 compressed caches: quantised once, four decode steps
     (appends quantised), sampled sequences against the oracle at steps 0 and 3."""
