@@ -49,6 +49,8 @@ SHAPES = [
     (torch.bfloat16, 128, 4, 64, 1000),   # tcgen05, R = 256, ragged tail
     (torch.bfloat16, 128, 2, 64, 1300),   # tcgen05, R = 128
     (torch.bfloat16, 128, 4, 64, 300),    # tcgen05, fewer tiles than cluster ranks
+    (torch.bfloat16, 128, 16, 8, 900),    # tcgen05, R = 128 of 8-row query heads
+    (torch.bfloat16, 128, 8, 32, 640),    # tcgen05, R = 256, an odd count of whole tiles
     (torch.bfloat16, 64, 4, 16, 500),     # SIMT bf16
 ]
 
