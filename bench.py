@@ -653,8 +653,7 @@ def bench_vector(B, w, steps, warmup, device):
                                    n_sink=w.n_sink, n_recent=w.n_recent)
         yield lambda: B.kvc_vector_residual(L.k, v, W, L.kept, L.counts, key, w.n_sink,
                                             w.n_recent)
-        yield lambda: B.kvc_select(key, "global", apos, acnt, aoff,
-                                   keep_ratio=(A + 0.5) / (w.Hkv * w.T))
+        yield lambda: B.kvc_vector_select(key, L.counts, A, apos, acnt, aoff)
         yield lambda: B.kvc_vector_compact(L.k, v, L.kept, L.counts, L.offs, apos, acnt, aoff,
                                            kc, vc, ks, kl, vs, na, slack=w.slack)
 

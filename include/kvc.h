@@ -498,6 +498,29 @@ int kvc_vector_residual(const void* k, const void* v, const void* W, int dtype, 
                         int n_sink, int n_recent, float* key, void* stream);
 
 /*
+ * Step 3's choice of the approximated tokens, reading only the pool's
+ * positions: per unit u, the n_approx positions of highest key among
+ * positions j < counts[u*Hkv + g] of its heads g, ranked by (key desc,
+ * position asc, head asc), NaN below every number.  Positions at or past a
+ * head's count are neither read as candidates nor chosen; when n_approx
+ * exceeds the candidates, every candidate is chosen.  With the keys of
+ * kvc_vector_residual and an n_approx of at most the pool's non-protected
+ * tokens (the pages' budgets), no NaN key is chosen and the result equals
+ * kvc_select(key, KVC_SEL_GLOBAL_TOPK) with no protected set and a budget of
+ * n_approx, which sweeps all Hkv * T positions.
+ * key [U, Hkv, T] fp32 (16-byte aligned rows take bulk copies); counts
+ * [U*Hkv] int32 (the pool's, from kvc_select); outputs as kvc_select's:
+ * approx_pos [U*Hkv, T] (the first approx_counts[i] entries of row i,
+ * ascending), approx_counts [U*Hkv], approx_offsets [U*Hkv + 1].
+ * Errors: KVC_ERR_INVALID for NULL pointers, non-positive sizes or n_approx
+ * outside [0, Hkv*T]; KVC_ERR_UNSUPPORTED for more than 8 heads per unit or
+ * a pool beyond 2^24 positions.  Device-side counts are clamped to [0, T].
+ */
+int kvc_vector_select(const float* key, int U, int Hkv, int T, const int32_t* counts,
+                      int64_t n_approx, int32_t* approx_pos, int32_t* approx_counts,
+                      int64_t* approx_offsets, void* stream);
+
+/*
  * Step 3 as a cache layout.  Head i keeps the K rows of all counts[i] pool
  * tokens and the V rows of the exact ones:
  *   kc rows [kstart_i, kstart_i + counts_i + slack): the approximated tokens

@@ -59,6 +59,7 @@ SIGNATURES = {
     "kvc_score_mlp_workspace": (_SZ, [_I, _I]),
     "kvc_score_mlp": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_vector_residual": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, _P]),
+    "kvc_vector_select": (_I, [_P, _I, _I, _I, _P, _I64, _P, _P, _P, _P]),
     "kvc_vector_compact": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I64,
                                 _P, _I64, _P, _P, _P, _P, _P]),
     "kvc_decode_vector_workspace": (_SZ, [_I, _I, _I, _I, _I]),
@@ -312,6 +313,17 @@ def kvc_vector_residual(k, v, W, kept_idx, counts, key, n_sink=0, n_recent=0, st
                                    _ptr(kept_idx), _ptr(counts), int(n_sink), int(n_recent),
                                    _ptr(key), _stream(stream))
     _check("kvc_vector_residual", rc)
+
+
+def kvc_vector_select(key, counts, n_approx, approx_pos, approx_counts, approx_offsets,
+                      stream=None):
+    """VECTOR step 3's choice: per unit, the n_approx highest keys among the
+    pool positions j < counts[i] of its heads.  key [U, Hkv, T] fp32."""
+    U, Hkv, T = key.shape
+    rc = lib().kvc_vector_select(_ptr(key), U, Hkv, T, _ptr(counts), int(n_approx),
+                                 _ptr(approx_pos), _ptr(approx_counts), _ptr(approx_offsets),
+                                 _stream(stream))
+    _check("kvc_vector_select", rc)
 
 
 def kvc_vector_compact(k, v, kept_idx, counts, offsets, approx_pos, approx_counts,

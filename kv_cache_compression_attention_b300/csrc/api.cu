@@ -440,6 +440,20 @@ int kvc_vector_residual(const void* k, const void* v, const void* W, int dtype, 
                                      dev, kvc::as_stream(stream));
 }
 
+int kvc_vector_select(const float* key, int U, int Hkv, int T, const int32_t* counts,
+                      int64_t n_approx, int32_t* approx_pos, int32_t* approx_counts,
+                      int64_t* approx_offsets, void* stream) {
+  if (!key || !counts || !approx_pos || !approx_counts || !approx_offsets) return KVC_ERR_INVALID;
+  if (U <= 0 || Hkv <= 0 || T <= 0 || n_approx < 0 || n_approx > (int64_t)Hkv * T)
+    return KVC_ERR_INVALID;
+  if ((int64_t)Hkv * T > (1ll << 24) || (int64_t)U * Hkv > (1ll << 24)) return KVC_ERR_UNSUPPORTED;
+  Dev dev;
+  int rc = kvc::device_info(&dev);
+  if (rc) return rc;
+  return kvc::select_lens_launch(key, U, Hkv, T, counts, n_approx, approx_pos, approx_counts,
+                                 approx_offsets, dev, kvc::as_stream(stream));
+}
+
 int kvc_vector_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, int d,
                        const int32_t* kept_idx, const int32_t* counts, const int64_t* offsets,
                        const int32_t* approx_pos, const int32_t* approx_counts,

@@ -108,6 +108,12 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
                   int32_t* kept_idx, int32_t* counts, int64_t* offsets, const Dev& dev,
                   cudaStream_t s);
 
+// Global top-k of `need` keys per unit in which head i's candidates are its
+// positions t < lens[i] (no protected set); the cluster kernel only.
+int select_lens_launch(const float* keys, int U, int Hkv, int T, const int32_t* lens,
+                       int64_t need, int32_t* kept_idx, int32_t* counts, int64_t* offsets,
+                       const Dev& dev, cudaStream_t s);
+
 // kvc_select followed by kvc_compact; a launch with one selection pool
 // hands the select's decision to a kernel that emits and copies in one go.
 size_t select_compact_ws(int U, int Hkv, int T, int mode);

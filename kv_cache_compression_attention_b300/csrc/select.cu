@@ -76,6 +76,10 @@ struct Args {
   // head and 512-token sub-range of the CTA's range)
   uint32_t* hand;
   int hand_sub;
+  // non-NULL (global top-k, no protected set): head i's candidates are its
+  // positions t < lens[i]; the rest are neither candidates nor kept, and the
+  // CTAs split only the pool's longest head length, not T
+  const int32_t* lens;
 };
 
 struct Shared {
@@ -92,6 +96,7 @@ struct Shared {
   uint32_t xall[16][kMaxHps];         // every CTA's per-head counts
   uint32_t head_base[kMaxHps];
   uint32_t head_total[kMaxHps];
+  int lenh[kMaxHps];                  // per-head lengths (Args::lens)
   uint32_t sel_bin, sel_above, sel_count, ecut, tie_base;
   uint64_t bar;                       // completion of the bulk score copies
 };
@@ -205,20 +210,12 @@ select_kernel(Args a) {
   const int hps = a.hps;
   const int T = a.T;
   const int head0 = seg * hps;
-  const int t0 = (int)((int64_t)rank * T / C);
-  const int t1 = (int)((int64_t)(rank + 1) * T / C);
-  const int nt = t1 - t0;
-  const Layout lay(nt, hps, V);
-  const int nloc = lay.nloc;
-  const int nvec = nloc / V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   int sbuf = 0;
 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
-  uint32_t* region = keys + lay.keys_words();
 
   for (int i = tid; i < 4 * 256; i += kThreads) (&sh.tot[0][0])[i] = 0u;
   for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.whist[0][0])[i] = 0u;
@@ -233,9 +230,39 @@ select_kernel(Args a) {
   // the scores (and every output) belong to the previous kernel until here
   pdl_wait();
 
+  // the positions the cluster splits: all of T, or the pool's longest head
+  // (Args::lens), in ranges of whole 4-token groups when V = 4
+  int Te = T;
+  int64_t n_cand = 0;
+  if (a.lens) {
+    Te = 0;
+    for (int hh = 0; hh < hps; ++hh) {
+      const int L = min(T, max(0, a.lens[head0 + hh]));
+      Te = max(Te, L);
+      n_cand += L;
+      if (tid == 0) sh.lenh[hh] = L;
+    }
+  }
+  int t0, t1;
+  if (V == 4) {
+    const int q = (Te + 3) >> 2;
+    t0 = 4 * (int)((int64_t)rank * q / C);
+    t1 = 4 * (int)((int64_t)(rank + 1) * q / C);
+  } else {
+    t0 = (int)((int64_t)rank * Te / C);
+    t1 = (int)((int64_t)(rank + 1) * Te / C);
+  }
+  const int nt = t1 - t0;
+  const Layout lay(nt, hps, V);
+  const int nloc = lay.nloc;
+  const int nvec = nloc / V;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
+  uint32_t* region = keys + lay.keys_words();
+
   int64_t need = 0;
   if (a.mode == KVC_SEL_GLOBAL_TOPK) {
     need = a.need_global;
+    if (a.lens && need > n_cand) need = n_cand;   // every candidate kept
   } else if (a.mode == KVC_SEL_PER_HEAD) {
     int64_t b = a.head_budget[head0];
     if (b < a.nP) b = a.nP;
@@ -301,6 +328,20 @@ select_kernel(Args a) {
       const uint32_t key = *kp;
       *kp = 0u;
       if (radix) atomicSub(&sh.whist[0][key >> 24], 1u);
+    }
+  }
+  if (a.lens) {
+    // positions at or past their head's length: key 0 like a protected
+    // token (keep() drops them), taken back out of the first histogram
+    for (int hh = 0; hh < hps; ++hh) {
+      for (int t = max(t0, sh.lenh[hh]) + tid; t < t1; t += kThreads) {
+        uint32_t* kp = keys + hh * nt + (t - t0);
+        const uint32_t key = *kp;
+        if (key) {
+          *kp = 0u;
+          if (radix) atomicSub(&sh.whist[0][key >> 24], 1u);
+        }
+      }
     }
   }
   __syncthreads();
@@ -467,7 +508,9 @@ select_kernel(Args a) {
   }
 
   const bool thr_mode = a.mode == KVC_SEL_THRESHOLD;
+  const bool has_lens = a.lens != nullptr;
   auto keep = [&](uint32_t key, int j, int hh) -> bool {
+    if (has_lens && t0 + j >= sh.lenh[hh]) return false;
     return key == 0u || (thr_mode ? key >= thr
                                   : (key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut)));
   };
@@ -785,7 +828,8 @@ namespace {
 int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64_t need_global,
                      float tau, const int32_t* head_budget, int n_sink, int n_recent,
                      int32_t* kept_idx, int32_t* counts, int64_t* offsets, uint32_t* hand,
-                     int* cluster, int* sub, const Dev& dev, cudaStream_t s) {
+                     int* cluster, int* sub, const Dev& dev, cudaStream_t s,
+                     const int32_t* lens = nullptr) {
   if (cluster) *cluster = 0;
   const int hps = (mode == KVC_SEL_GLOBAL_TOPK) ? Hkv : 1;
   const int nseg = (mode == KVC_SEL_GLOBAL_TOPK) ? U : U * Hkv;
@@ -811,7 +855,9 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
       return rc;
     return launch_offsets();
   };
-  if (hps > kMaxHps) return stream();
+  // per-head lengths need the cluster kernel (the streaming one reads all of T)
+  if (lens && (mode != KVC_SEL_GLOBAL_TOPK || n_sink || n_recent || hand)) return KVC_ERR_INVALID;
+  if (hps > kMaxHps) return lens ? KVC_ERR_UNSUPPORTED : stream();
   const size_t smem_max = (size_t)dev.max_smem_optin;
   const bool aligned = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
   // four keys per thread and step when every CTA's range is a multiple of 4
@@ -821,7 +867,7 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   int C = 1;
   while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
   while (C < 16 && smem_for(C) > smem_max) C *= 2;
-  if (smem_for(C) > smem_max) return stream();
+  if (smem_for(C) > smem_max) return lens ? KVC_ERR_UNSUPPORTED : stream();
   Args a;
   a.scores = scores; a.T = T; a.hps = hps; a.mode = mode; a.need_global = need_global;
   a.tau = tau; a.head_budget = head_budget; a.n_sink = n_sink; a.n_recent = n_recent;
@@ -831,6 +877,7 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   a.status = dev.status;
   a.hand = (nseg == 1) ? hand : nullptr;
   a.hand_sub = 0;
+  a.lens = lens;
   static std::mutex mu;
   static bool attr_done[64];
   static std::map<std::tuple<int, int, size_t>, int> active_memo;
@@ -872,7 +919,7 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
       active_memo[key] = active;
     }
     if (active > 0) break;
-    if (C == 1 || smem_for(C / 2) > smem_max) return stream();
+    if (C == 1 || smem_for(C / 2) > smem_max) return lens ? KVC_ERR_UNSUPPORTED : stream();
     C /= 2;
   }
   if (a.hand) {
@@ -902,6 +949,13 @@ int select_launch(const float* scores, int U, int Hkv, int T, int mode, int64_t 
   return select_launch_ex(scores, U, Hkv, T, mode, need_global, tau, head_budget, n_sink,
                           n_recent, kept_idx, counts, offsets, nullptr, nullptr, nullptr, dev,
                           s);
+}
+
+int select_lens_launch(const float* keys, int U, int Hkv, int T, const int32_t* lens,
+                       int64_t need, int32_t* kept_idx, int32_t* counts, int64_t* offsets,
+                       const Dev& dev, cudaStream_t s) {
+  return select_launch_ex(keys, U, Hkv, T, KVC_SEL_GLOBAL_TOPK, need, 0.0f, nullptr, 0, 0,
+                          kept_idx, counts, offsets, nullptr, nullptr, nullptr, dev, s, lens);
 }
 
 size_t select_compact_ws(int U, int Hkv, int T, int mode) {

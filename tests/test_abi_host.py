@@ -236,6 +236,12 @@ def test_vector_entry_points_reject_bad_arguments(lib):
         assert r(*bad) == want, (k, v)
     bad = list(ok); bad[2] = ctypes.c_void_p(24)
     assert r(*bad) == -2                                        # unaligned W
+    sv = lib.kvc_vector_select
+    oks = [P, 1, 8, 32768, P, 3932, P, P, P, None]
+    for k, v, want in [(0, None, -1), (4, None, -1), (8, None, -1), (1, 0, -1), (3, -5, -1),
+                       (5, -1, -1), (5, 8 * 32768 + 1, -1), (3, 1 << 22, -2)]:
+        bad = list(oks); bad[k] = v
+        assert sv(*bad) == want, (k, v)
     c = lib.kvc_vector_compact
     okc = [P, P, 1, 1, 8, 64, 128, P, P, P, P, P, P, 0, P, 100, P, 100, P, P, P, P, None]
     bad = list(okc); bad[9] = None

@@ -59,7 +59,9 @@ def small_case(seed, U=2, Hkv=3, T=300, d=128, keep=0.4, n_sink=4, n_recent=16):
 
 
 def run_gpu_routing(B, k, v, W, kept, counts, offsets, A, n_sink, n_recent, slack):
-    """residual -> global top-A of the keys -> VECTOR compaction, all on the GPU."""
+    """residual -> top-A of the keys over the pool positions -> VECTOR
+    compaction, all on the GPU; the choice is also made by the plain global
+    select over all positions, which must agree bit for bit."""
     U, Hkv, T, d = k.shape
     n = U * Hkv
     kept_t, counts_t = torch.as_tensor(kept).cuda(), torch.as_tensor(counts).cuda()
@@ -69,7 +71,14 @@ def run_gpu_routing(B, k, v, W, kept, counts, offsets, A, n_sink, n_recent, slac
     apos = torch.empty((n, T), dtype=torch.int32, device="cuda")
     acnt = torch.empty(n, dtype=torch.int32, device="cuda")
     aoff = torch.empty(n + 1, dtype=torch.int64, device="cuda")
-    B.kvc_select(key, "global", apos, acnt, aoff, keep_ratio=(A + 0.5) / (Hkv * T))
+    B.kvc_vector_select(key, counts_t, A, apos, acnt, aoff)
+    apos2, acnt2, aoff2 = torch.empty_like(apos), torch.empty_like(acnt), torch.empty_like(aoff)
+    B.kvc_select(key, "global", apos2, acnt2, aoff2, keep_ratio=(A + 0.5) / (Hkv * T))
+    torch.cuda.synchronize()
+    assert torch.equal(acnt, acnt2) and torch.equal(aoff, aoff2)
+    for i in range(n):
+        c = int(acnt[i])
+        assert torch.equal(apos[i, :c], apos2[i, :c]), i
     rows_k = int(np.sum(counts)) + n * slack
     rows_v = int(np.sum(counts)) - U * A + n * slack
     kc = torch.zeros((rows_k, d), dtype=torch.bfloat16, device="cuda")
@@ -113,6 +122,63 @@ def test_vector_routing_small(B):
         np.testing.assert_array_equal(gkc[r], rkc[r])
         r = slice(int(rvs[i]), int(rvs[i] + rkl[i] - rna[i]))
         np.testing.assert_array_equal(gvc[r], rvc[r])
+
+
+def vselect(B, key, counts, A):
+    U, Hkv, T = key.shape
+    n = U * Hkv
+    apos = torch.full((n, T), -7, dtype=torch.int32, device="cuda")
+    acnt = torch.empty(n, dtype=torch.int32, device="cuda")
+    aoff = torch.empty(n + 1, dtype=torch.int64, device="cuda")
+    B.kvc_vector_select(key.cuda(), torch.as_tensor(counts, dtype=torch.int32).cuda(), A, apos,
+                        acnt, aoff)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    return apos.cpu().numpy(), acnt.cpu().numpy(), aoff.cpu().numpy()
+
+
+@pytest.mark.parametrize("U,Hkv,T", [(1, 8, 32768), (3, 8, 1000), (2, 5, 997), (4, 1, 4096)])
+def test_vector_select_pool_positions(B, U, Hkv, T):
+    """The choice over pool positions j < counts[i] against the oracle's
+    choice on keys that hold NaN from counts[i] on (as the residual writes
+    them), with ties, +-0, +-inf and NaN inside the pools; heads with empty
+    and full pools; budgets up to every number-valued key."""
+    g = torch.Generator().manual_seed(U * 1000 + Hkv * 10 + T)
+    n = U * Hkv
+    counts = torch.randint(0, max(2, T // 5), (n,), generator=g).to(torch.int32)
+    counts[0] = 0
+    counts[-1] = T
+    key = -torch.rand((U, Hkv, T), generator=g).square()
+    key = torch.where(torch.rand((U, Hkv, T), generator=g) < 0.3, key.round(decimals=2), key)
+    flat = key.view(n, T)
+    flat[-1, :4] = torch.tensor([0.0, -0.0, float("inf"), -float("inf")])
+    flat[-1, 4:9] = float("nan")
+    pos = torch.arange(T)
+    flat[pos[None, :] >= counts[:, None].long()] = float("nan")
+    kn = key.numpy()
+    valid = np.array([int((~np.isnan(kn[u])).sum()) for u in range(U)])
+    for A in sorted({0, 1, int(valid.min()) // 3, int(valid.min())}):
+        apos, acnt, aoff = vselect(B, key, counts.numpy(), A)
+        rpos, rcnt = O.vector_approx(kn, A)
+        np.testing.assert_array_equal(acnt, rcnt)
+        np.testing.assert_array_equal(aoff, np.concatenate([[0], np.cumsum(rcnt)]))
+        for i in range(n):
+            np.testing.assert_array_equal(apos[i, :rcnt[i]], rpos[i, :rcnt[i]])
+
+
+def test_vector_select_budget_beyond_the_pool(B):
+    """A budget above the candidates keeps every pool position, NaN or not,
+    and nothing past a head's count."""
+    U, Hkv, T = 2, 4, 640
+    g = torch.Generator().manual_seed(5)
+    counts = np.array([0, 7, 640, 300, 1, 64, 0, 129], dtype=np.int32)
+    key = torch.randn((U, Hkv, T), generator=g)
+    key.view(-1)[::7] = float("nan")
+    for A in (int(counts[:4].sum()), int(counts[:4].sum()) + 5, Hkv * T):
+        apos, acnt, _ = vselect(B, key, counts, A)
+        np.testing.assert_array_equal(acnt, counts)
+        for i in range(U * Hkv):
+            np.testing.assert_array_equal(apos[i, :counts[i]], np.arange(counts[i]))
 
 
 def test_vector_residual_edges(B):
