@@ -76,9 +76,10 @@ struct Args {
   // head and 512-token sub-range of the CTA's range)
   uint32_t* hand;
   int hand_sub;
-  // non-NULL (global top-k, no protected set): head i's candidates are its
-  // positions t < lens[i]; the rest are neither candidates nor kept, and the
-  // CTAs split only the pool's longest head length, not T
+  // select_kernel<V, true> (global top-k, no protected set): head i's
+  // candidates are its positions t < lens[i]; the rest are neither
+  // candidates nor kept, and the CTAs split only the pool's longest head
+  // length, not T
   const int32_t* lens;
 };
 
@@ -96,7 +97,6 @@ struct Shared {
   uint32_t xall[16][kMaxHps];         // every CTA's per-head counts
   uint32_t head_base[kMaxHps];
   uint32_t head_total[kMaxHps];
-  int lenh[kMaxHps];                  // per-head lengths (Args::lens)
   uint32_t sel_bin, sel_above, sel_count, ecut, tie_base;
   uint64_t bar;                       // completion of the bulk score copies
 };
@@ -198,9 +198,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Offset of the keys in dynamic shared memory; with per-head lengths they
+// sit after Shared and the lengths.
+template <bool kLens>
+__host__ __device__ constexpr size_t keys_offset() {
+  return (sizeof(Shared) + (kLens ? kMaxHps * sizeof(int) : 0) + 15) & ~size_t(15);
+}
+
 // V = 4 requires every CTA's range to start and end on a multiple of 4
 // tokens and 16-byte aligned score rows (then the rows are bulk-copied).
-template <int V>
+template <int V, bool kLens>
 __global__ void __launch_bounds__(kThreads, 1)
 select_kernel(Args a) {
   cg::cluster_group cl = cg::this_cluster();
@@ -213,9 +220,16 @@ select_kernel(Args a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   int sbuf = 0;
+  // this CTA's token range: of T, or (kLens) of the pool's longest head
+  int t0 = 0, t1 = 0;
+  if constexpr (!kLens) {
+    t0 = (int)((int64_t)rank * T / C);
+    t1 = (int)((int64_t)(rank + 1) * T / C);
+  }
 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  int* lenh = reinterpret_cast<int*>(smem_raw + sizeof(Shared));   // kLens: [hps]
 
   for (int i = tid; i < 4 * 256; i += kThreads) (&sh.tot[0][0])[i] = 0u;
   for (int i = tid; i < kWarps * 256; i += kThreads) (&sh.whist[0][0])[i] = 0u;
@@ -230,39 +244,32 @@ select_kernel(Args a) {
   // the scores (and every output) belong to the previous kernel until here
   pdl_wait();
 
-  // the positions the cluster splits: all of T, or the pool's longest head
-  // (Args::lens), in ranges of whole 4-token groups when V = 4
-  int Te = T;
   int64_t n_cand = 0;
-  if (a.lens) {
-    Te = 0;
+  if constexpr (kLens) {
+    // the cluster splits the pool's longest head, in whole 4-token groups
+    // when V = 4
+    int Te = 0;
     for (int hh = 0; hh < hps; ++hh) {
       const int L = min(T, max(0, a.lens[head0 + hh]));
       Te = max(Te, L);
       n_cand += L;
-      if (tid == 0) sh.lenh[hh] = L;
+      if (tid == 0) lenh[hh] = L;
     }
-  }
-  int t0, t1;
-  if (V == 4) {
-    const int q = (Te + 3) >> 2;
-    t0 = 4 * (int)((int64_t)rank * q / C);
-    t1 = 4 * (int)((int64_t)(rank + 1) * q / C);
-  } else {
-    t0 = (int)((int64_t)rank * Te / C);
-    t1 = (int)((int64_t)(rank + 1) * Te / C);
+    const int q = V == 4 ? (Te + 3) >> 2 : Te;
+    t0 = V * (int)((int64_t)rank * q / C);
+    t1 = V * (int)((int64_t)(rank + 1) * q / C);
   }
   const int nt = t1 - t0;
   const Layout lay(nt, hps, V);
   const int nloc = lay.nloc;
   const int nvec = nloc / V;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(Shared) + 15) & ~size_t(15)));
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + keys_offset<kLens>());
   uint32_t* region = keys + lay.keys_words();
 
   int64_t need = 0;
   if (a.mode == KVC_SEL_GLOBAL_TOPK) {
     need = a.need_global;
-    if (a.lens && need > n_cand) need = n_cand;   // every candidate kept
+    if (kLens && need > n_cand) need = n_cand;   // every candidate kept
   } else if (a.mode == KVC_SEL_PER_HEAD) {
     int64_t b = a.head_budget[head0];
     if (b < a.nP) b = a.nP;
@@ -330,11 +337,11 @@ select_kernel(Args a) {
       if (radix) atomicSub(&sh.whist[0][key >> 24], 1u);
     }
   }
-  if (a.lens) {
+  if constexpr (kLens) {
     // positions at or past their head's length: key 0 like a protected
     // token (keep() drops them), taken back out of the first histogram
     for (int hh = 0; hh < hps; ++hh) {
-      for (int t = max(t0, sh.lenh[hh]) + tid; t < t1; t += kThreads) {
+      for (int t = max(t0, lenh[hh]) + tid; t < t1; t += kThreads) {
         uint32_t* kp = keys + hh * nt + (t - t0);
         const uint32_t key = *kp;
         if (key) {
@@ -508,9 +515,10 @@ select_kernel(Args a) {
   }
 
   const bool thr_mode = a.mode == KVC_SEL_THRESHOLD;
-  const bool has_lens = a.lens != nullptr;
   auto keep = [&](uint32_t key, int j, int hh) -> bool {
-    if (has_lens && t0 + j >= sh.lenh[hh]) return false;
+    if constexpr (kLens) {
+      if (t0 + j >= lenh[hh]) return false;
+    }
     return key == 0u || (thr_mode ? key >= thr
                                   : (key > thr || (key == thr && (uint32_t)(j * hps + hh) < ecut)));
   };
@@ -812,9 +820,10 @@ emit_compact_kernel(EArgs e) {
   }
 }
 
-size_t shared_bytes(int nt, int hps, int V) {
+size_t shared_bytes(int nt, int hps, int V, bool lens) {
   const Layout lay(nt, hps, V);
-  return ((sizeof(Shared) + 15) & ~size_t(15)) + (lay.keys_words() + (size_t)lay.region) * 4;
+  return (lens ? keys_offset<true>() : keys_offset<false>()) +
+         (lay.keys_words() + (size_t)lay.region) * 4;
 }
 
 }  // namespace
@@ -862,7 +871,9 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   const bool aligned = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0;
   // four keys per thread and step when every CTA's range is a multiple of 4
   auto vec_for = [&](int c) { return (aligned && T % (4 * c) == 0) ? 4 : 1; };
-  auto smem_for = [&](int c) { return shared_bytes((T + c - 1) / c, hps, vec_for(c)); };
+  auto smem_for = [&](int c) {
+    return shared_bytes((T + c - 1) / c, hps, vec_for(c), lens != nullptr);
+  };
   // the smallest cluster that keeps <= 16K keys per CTA, else the smallest that fits
   int C = 1;
   while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
@@ -883,15 +894,17 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   static std::map<std::tuple<int, int, size_t>, int> active_memo;
   std::lock_guard<std::mutex> lock(mu);
   if (!attr_done[dev.device & 63]) {
-    for (auto fn : {select_kernel<1>, select_kernel<4>}) {
+    for (auto fn : {select_kernel<1, false>, select_kernel<4, false>, select_kernel<1, true>,
+                    select_kernel<4, true>}) {
       KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
       KVC_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         dev.max_smem_optin));
     }
     attr_done[dev.device & 63] = true;
   }
-  if (int rc = prefer_max_shared(select_kernel<1>, dev.device)) return rc;
-  if (int rc = prefer_max_shared(select_kernel<4>, dev.device)) return rc;
+  for (auto fn : {select_kernel<1, false>, select_kernel<4, false>, select_kernel<1, true>,
+                  select_kernel<4, true>})
+    if (int rc = prefer_max_shared(fn, dev.device)) return rc;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   // a cluster must fit one GPC: shrink it (while the keys still fit) until
@@ -915,7 +928,7 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
     if (it != active_memo.end()) {
       active = it->second;
     } else {
-      KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel<1>, &cfg));
+      KVC_CUDA_TRY(cudaOccupancyMaxActiveClusters(&active, select_kernel<1, false>, &cfg));
       active_memo[key] = active;
     }
     if (active > 0) break;
@@ -929,8 +942,12 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   }
   attr[1] = pdl_attr();
   cfg.numAttrs = 2;
-  if (vec_for(C) == 4) KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<4>, a));
-  else KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, select_kernel<1>, a));
+  {
+    const bool v4 = vec_for(C) == 4;
+    auto kern = lens ? (v4 ? select_kernel<4, true> : select_kernel<1, true>)
+                     : (v4 ? select_kernel<4, false> : select_kernel<1, false>);
+    KVC_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, a));
+  }
   if (a.hand) {
     if (cluster) *cluster = C;
     if (sub) *sub = a.hand_sub;
