@@ -32,7 +32,7 @@ namespace kvc {
 namespace {
 
 constexpr int kChunk = 512;     // rows per partial CTA
-constexpr int kQ8Chunk = 1024;  // rows per partial CTA over a quantised pool
+constexpr int kQ8Chunk = 2048;  // rows per partial CTA over a quantised pool
 constexpr int kWarps = 4;       // compute warps per partial CTA
 constexpr int kStageRows = 32;  // rows per shared-memory stage (8 per compute warp)
 constexpr int kStages = 4;

@@ -37,6 +37,7 @@ decode_prune_kernel(PrunePools pools, float* __restrict__ rscore,
                     const float* __restrict__ s_new, int window, int n_sink, float tau,
                     int64_t capacity_rows, int* status) {
   pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int64_t s0 = start[i];
   const int L = len[i];
@@ -123,6 +124,7 @@ decode_prune_ring_kernel(PrunePools pools, float* __restrict__ rscore,
                          const float* __restrict__ s_new, int n_heads, int window, int n_sink,
                          float tau, int64_t capacity_rows, int* status) {
   pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * kRingWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= n_heads) return;
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kThreads)
 prune_ring_init_kernel(const int32_t* __restrict__ len, int n_heads, int window, int64_t t_next,
                        int32_t* __restrict__ ring, int* status) {
   pdl_wait();
+  pdl_trigger();
   (void)status;
   const int64_t x = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   if (x >= (int64_t)n_heads * window) return;
@@ -190,6 +193,7 @@ gather_scores_kernel(const float* __restrict__ scores, int T,
                      const int64_t* __restrict__ start, float* __restrict__ rscore,
                      int64_t capacity_rows, int* status) {
   pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.y;
   const int j = blockIdx.x * kThreads + threadIdx.x;
   if (j >= T || j >= counts[i]) return;

@@ -193,7 +193,10 @@ linear_row_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight
                   const float* __restrict__ bias, int T, int Dh, float* __restrict__ scores) {
   constexpr int E = Vec<Tin>::E;
   __shared__ float part[kRowThreads / 32][HK];
-  pdl_wait();
+  // The row and the weights are read before waiting on the previous kernel
+  // of the stream (no kernel of this library writes hidden states, weights or
+  // biases), so that this work overlaps its tail; the scores are written
+  // after the wait (the previous kernel may still read the last ones).
   pdl_trigger();
   const int64_t row = blockIdx.x;
   const int NC = Dh / E;
@@ -232,6 +235,7 @@ linear_row_kernel(const Tin* __restrict__ hidden, const Tin* __restrict__ weight
     if (lane == 0) part[warp][g] = v;
   }
   __syncthreads();
+  pdl_wait();
   if (threadIdx.x < HK) {
     const int g = threadIdx.x;
     float v = 0.0f;

@@ -102,10 +102,10 @@ def test_decode_q8_small(B, G, append):
 
 @pytest.mark.parametrize("G", [1, 3, 8])
 def test_decode_q8_chunk_edges(B, G):
-    """Lengths around the quantised kernel's 1024-row chunks and 64-row
+    """Lengths around the quantised kernel's 2048-row chunks and 64-row
     stages, with appends, against the oracle's decode over the dequantised pool."""
     U, Hkv, d = 1, 6, 128
-    kc, vc, start, lens = pool([63, 64, 1023, 1024, 1025, 2049], 2, d, 4)
+    kc, vc, start, lens = pool([63, 1025, 2047, 2048, 2049, 4097], 2, d, 4)
     g = torch.Generator().manual_seed(34 + G)
     q = torch.randn((U, Hkv * G, d), generator=g).to(torch.bfloat16)
     kn = torch.randn((U, Hkv, d), generator=g).to(torch.bfloat16)
