@@ -1206,7 +1206,7 @@ def main():
              "achieved_gbs": c3["compact_gbs"], "frac": c3["compact_gbs"] / hbm},
             {"kernel": "decode_partial_kernel+decode_combine_kernel", "workload": DECODE_WORKLOAD,
              "bound": "hbm", "achieved_gbs": dec["gbs"], "frac": dec["gbs"] / hbm},
-            {"kernel": "decode_partial_mma_kernel<q8>+decode_combine_kernel (group-quantised pool)",
+            {"kernel": "decode_partial_q8_kernel+decode_combine_kernel (group-quantised pool)",
              "workload": DECODE_WORKLOAD, "bound": "hbm", "time_us": dec["q8"]["us_per_step"],
              "achieved_gbs": dec["q8"]["gbs"], "frac": dec["q8"]["gbs"] / hbm},
             {"kernel": "vector_residual_kernel", "workload": WORKLOAD + " (VECTOR p_c 0.9, p_a 0.05)",
