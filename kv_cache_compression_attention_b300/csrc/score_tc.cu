@@ -257,19 +257,28 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (item >= 2) mbar_wait(&sm.tmem_empty[b], ((item >> 1) - 1) & 1, p.status, abort_flag);
             tc::fence_after_sync();
             const uint32_t dcol = tmem + (uint32_t)b * 256u;
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t kh = kk >> 2, ko = (kk & 3) * 32u;
-              uint64_t a, bd;
-              if (i < ns) {
-                a = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + x * 128u * 128u + ko);
-                bd = tc::smem_desc_sw128(kst + kh * kHalfBytes + ko);
-                tc::mma_bf16(dcol, a, bd, nti == 2 ? idesc1 : idesc1h, kk > 0);
-              } else {
-                a = tc::smem_desc_sw128(kst + kh * kHalfBytes + x * kBoxBytes + ko);
-                bd = tc::smem_desc_sw128(q_smem + kh * q_half_bytes + ko);
-                tc::mma_bf16(dcol, a, bd, idesc2, kk > 0);
-              }
+            // operand descriptors of the item's first k step, for each 64-dim
+            // half; a 16-wide k step adds 32 bytes (2 in the descriptor's
+            // address field, which cannot carry below 256 KiB)
+            uint32_t a_lo, b_lo, id;
+            if (i < ns) {
+              a_lo = q_smem + x * 128u * 128u;
+              b_lo = kst;
+              id = nti == 2 ? idesc1 : idesc1h;
+            } else {
+              a_lo = kst + x * kBoxBytes;
+              b_lo = q_smem;
+              id = idesc2;
             }
+            const uint32_t a_hstep = i < ns ? q_half_bytes : kHalfBytes;
+            const uint32_t b_hstep = i < ns ? kHalfBytes : q_half_bytes;
+            const uint64_t ad0 = tc::smem_desc_sw128(a_lo), bd0 = tc::smem_desc_sw128(b_lo);
+            const uint64_t ad1 = tc::smem_desc_sw128(a_lo + a_hstep);
+            const uint64_t bd1 = tc::smem_desc_sw128(b_lo + b_hstep);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(dcol, ad0 + 2u * kk, bd0 + 2u * kk, id, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(dcol, ad1 + 2u * kk, bd1 + 2u * kk, id, 1u);
             tc::mma_commit(&sm.tmem_full[b]);
           }
           tc::mma_commit(&sm.empty[s]);

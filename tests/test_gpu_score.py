@@ -223,6 +223,7 @@ def test_score_attn_rejects_non_positive_temperature_on_device(B, dtype, d, G, W
     (4, 3584, 448, 257),      # the 128k layer's widths: two MMAs of N = 224, ragged row tile
     (3, 200, 520, 129),       # Dh not a multiple of the 64-wide k-block; two passes of 288
     (8, 1024, 1000, 333),     # two passes of 512 columns, padded rows of W1t
+    (2, 256, 64, 50),         # one 128-row tile: a single CTA instead of a pair
 ])
 def test_score_mlp_small(B, Hkv, Dh, Dm, T):
     U = 2
@@ -252,6 +253,30 @@ def test_score_mlp_qwen128k_sampled_rows(B):
     ref = O.score_mlp(np64(hid[:, rows]), np64(w1), np64(b1), np64(w2), np64(b2))
     assert row_rel_err(np64(out[:, :, rows]), ref) <= 2e-2
     assert torch.isfinite(out).all()
+
+
+def test_score_mlp_gelu_against_the_oracle(B):
+    """The epilogue's GELU alone: W1 = I (z = h exactly, already bf16), b1 = 0
+    and one-hot W2 columns make score[g, t] = GELU(h[t, m_g]); its erf
+    (Abramowitz & Stegun 7.1.26, absolute error <= 1.5e-7) against the
+    oracle's exact GELU over [-8, 8], zeros and tiny values."""
+    U, T, Dh, Hkv = 1, 384, 64, 4
+    g = torch.Generator().manual_seed(5)
+    h = (16 * torch.rand((U, T, Dh), generator=g) - 8).to(torch.bfloat16)
+    h[0, :8, 0] = torch.tensor([0.0, -0.0, 1e-30, -1e-30, 1e-3, -1e-3, 8.0, -8.0])
+    w1 = torch.eye(Dh).to(torch.bfloat16)
+    b1 = torch.zeros(Dh)
+    cols = [0, 1, 17, 63]
+    w2 = torch.zeros((Dh, Hkv))
+    for k, m in enumerate(cols):
+        w2[m, k] = 1.0
+    out = torch.full((U, Hkv, T), float("nan"), device="cuda")
+    B.kvc_score_mlp(h.cuda(), w1.cuda(), b1.cuda(), w2.to(torch.bfloat16).cuda(), None, out)
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
+    ref = O.gelu(np64(h)[0][:, cols].T)                      # [Hkv, T]
+    # |error| <= |z| / 2 * (1.5e-7 + two fp32 ulps of 1) <= 1.1e-6 on [-8, 8]
+    np.testing.assert_allclose(np64(out)[0], ref, rtol=2e-6, atol=1.5e-6)
 
 
 def kvzip_case(seed, U, Hq, Hkv, W, T, d=128):
