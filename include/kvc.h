@@ -260,7 +260,12 @@ int kvc_select(const float* scores, int U, int Hkv, int T, int mode,
  *   kc[start[i] + j, :] = k[u, g, kept_idx[i, j], :]  (same for v), j < counts[i].
  * Slack rows are not written: decode appends new tokens there.
  *
- * k, v     [U, Hkv, T, d] dtype (a byte copy: any dtype of the enum)
+ * k, v     [U, Hkv, T, d] dtype (a byte copy: any dtype of the enum), in
+ *          device memory or in pinned host memory mapped at the same address
+ *          (cudaHostAlloc under unified addressing): the kernel then reads
+ *          only the kept rows across the bus (a cache held on the host need
+ *          not be copied whole to be compacted).  Host memory the device
+ *          cannot read is refused with KVC_ERR_INVALID before any launch.
  * kept_idx [U*Hkv, T] int32, counts [U*Hkv] int32, offsets [U*Hkv+1] int64
  *          as written by kvc_select.
  * kc, vc   [capacity_rows, d] dtype; capacity_rows must be at least

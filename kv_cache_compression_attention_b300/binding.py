@@ -117,6 +117,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _src_ptr(t: torch.Tensor):
+    """A source the compaction reads in place: a CUDA tensor, or a host tensor
+    (the library accepts pinned host memory the device can read at the same
+    address, and refuses any other with KVC_ERR_INVALID before launching)."""
+    if not t.is_contiguous():
+        raise ValueError("kvc kernels take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _dtype(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return KVC_F32
@@ -221,7 +230,7 @@ def kvc_select(scores, mode, kept_idx, counts, offsets, keep_ratio=0.0, tau=0.0,
 
 def kvc_compact(k, v, kept_idx, counts, offsets, kc, vc, start, length, slack=0, stream=None):
     U, Hkv, T, d = k.shape
-    rc = lib().kvc_compact(_ptr(k), _ptr(v), _dtype(k), U, Hkv, T, d, _ptr(kept_idx),
+    rc = lib().kvc_compact(_src_ptr(k), _src_ptr(v), _dtype(k), U, Hkv, T, d, _ptr(kept_idx),
                            _ptr(counts), _ptr(offsets), int(slack), _ptr(kc), _ptr(vc),
                            kc.shape[0], _ptr(start), _ptr(length), _stream(stream))
     _check("kvc_compact", rc)
@@ -239,7 +248,7 @@ def kvc_select_compact(scores, mode, k, v, kept_idx, counts, offsets, kc, vc, st
         workspace = _workspace(lib().kvc_select_compact_workspace(U, Hkv, T, m), scores.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().kvc_select_compact(_ptr(scores), U, Hkv, T, m, float(keep_ratio), float(tau),
-                                  _ptr(head_budget), int(n_sink), int(n_recent), _ptr(k), _ptr(v),
+                                  _ptr(head_budget), int(n_sink), int(n_recent), _src_ptr(k), _src_ptr(v),
                                   _dtype(k), d, int(slack), _ptr(kc), _ptr(vc), kc.shape[0],
                                   _ptr(kept_idx), _ptr(counts), _ptr(offsets), _ptr(start),
                                   _ptr(length), _ptr(workspace) if ws_bytes else None, ws_bytes,

@@ -15,6 +15,22 @@ bool g_dev_ready[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A source the compaction kernels may read in place: device (or managed)
+// memory, or pinned host memory that the device sees at the same address
+// (page-locked with the mapped property, which unified addressing gives
+// cudaHostAlloc memory).  Anything else would fault on the device, so it is
+// refused here.
+int device_readable(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVC_ERR_INVALID;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return KVC_OK;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == p) return KVC_OK;
+  return KVC_ERR_INVALID;
+}
+
 }  // namespace
 
 namespace kvc {
@@ -217,6 +233,7 @@ int kvc_select_compact(const float* scores, int U, int Hkv, int T, int mode, dou
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
+  if ((rc = device_readable(k)) || (rc = device_readable(v))) return rc;
   return kvc::select_compact_launch(scores, U, Hkv, T, mode, need, tau, head_budget, ns, nr, k,
                                     v, (int)row_bytes, slack_per_head, kc, vc, capacity_rows,
                                     kept_idx, counts, offsets, start, len, workspace,
@@ -241,6 +258,7 @@ int kvc_compact(const void* k, const void* v, int dtype, int U, int Hkv, int T, 
   Dev dev;
   int rc = kvc::device_info(&dev);
   if (rc) return rc;
+  if ((rc = device_readable(k)) || (rc = device_readable(v))) return rc;
   return kvc::compact_launch(k, v, (int)row_bytes, U, Hkv, T, kept_idx, counts, offsets,
                              slack_per_head, kc, vc, capacity_rows, start, len, dev,
                              kvc::as_stream(stream));

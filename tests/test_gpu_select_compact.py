@@ -408,3 +408,48 @@ def test_select_compact_without_workspace_and_capacity_overflow(B):
     assert B.kvc_device_status() == -6            # KVC_ERR_RANGE
     assert B.kvc_device_status() == 0
     assert guard[100:].abs().sum().item() == 0
+
+
+@pytest.mark.parametrize("shape,mode", [((1, 8, 32768), "global"), ((2, 3, 777), "global"),
+                                        ((1, 1, 4099), "threshold")])
+def test_compaction_reads_a_cache_held_in_pinned_host_memory(B, shape, mode):
+    """K and V left in pinned host memory (mapped at the same address under
+    unified addressing): both compaction calls read only the kept rows across
+    the bus and write the same outputs, bit for bit, as from device copies."""
+    s = inputs.random_scores(shape, seed=sum(shape) + 17).cuda()
+    U, Hkv, T = shape
+    g = torch.Generator().manual_seed(19)
+    k = torch.randn((U, Hkv, T, 128), generator=g).to(torch.bfloat16)
+    v = torch.randn((U, Hkv, T, 128), generator=g).to(torch.bfloat16)
+    hk, hv = k.pin_memory(), v.pin_memory()
+    kw = dict(keep_ratio=0.1, n_sink=4, n_recent=64) if mode == "global" else dict(tau=0.5)
+    on_device = fused_and_separate(B, s, k.cuda(), v.cuda(), mode, 3, **dict(kw))
+    on_host = fused_and_separate(B, s, hk, hv, mode, 3, **dict(kw))
+    for a, b in zip(on_device, on_host):
+        assert_same_outputs(a, b)
+
+
+def test_compaction_refuses_host_memory_the_device_cannot_read(B):
+    """Pageable host memory would fault on the device: both calls refuse it
+    on the host (KVC_ERR_INVALID) and launch nothing."""
+    shape = (1, 2, 256)
+    s = inputs.random_scores(shape, seed=3).cuda()
+    n, T = 2, 256
+    k = torch.zeros((1, 2, T, 128), dtype=torch.bfloat16)       # pageable
+    v_dev = torch.zeros((1, 2, T, 128), dtype=torch.bfloat16, device="cuda")
+    kept = torch.zeros((n, T), dtype=torch.int32, device="cuda")
+    counts = torch.zeros(n, dtype=torch.int32, device="cuda")
+    offs = torch.zeros(n + 1, dtype=torch.int64, device="cuda")
+    kc = torch.zeros((n * T, 128), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    start = torch.zeros(n, dtype=torch.int64, device="cuda")
+    length = torch.zeros(n, dtype=torch.int32, device="cuda")
+    with pytest.raises(B.KvcError) as e:
+        B.kvc_compact(k, v_dev, kept, counts, offs, kc, vc, start, length)
+    assert e.value.status == -1
+    with pytest.raises(B.KvcError) as e:
+        B.kvc_select_compact(s, "global", v_dev, k, kept, counts, offs, kc, vc, start, length,
+                             keep_ratio=0.5)
+    assert e.value.status == -1
+    torch.cuda.synchronize()
+    assert B.kvc_device_status() == 0
