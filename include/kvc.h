@@ -584,7 +584,7 @@ int kvc_decode_attn_vector(const void* q, void* kc, void* vc, const int64_t* kst
  *  - Limit: sizes with kvc_decode_workspace(U, Hq, Hkv, d, max_len, dtype) >
  *    KVC_DECODE_NOALLOC_SCRATCH_BYTES are refused with KVC_ERR_WORKSPACE
  *    before any CUDA call (e.g. 64 x 8 kv heads, G = 4, d = 128 fit up to
- *    max_len = 7680).
+ *    max_len = 15360).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current.  With CUDA's lazy
  *    module loading (the default) that lookup is also what loads the module

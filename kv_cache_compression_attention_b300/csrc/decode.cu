@@ -9,7 +9,7 @@
 // The step streams every cached K/V row once from HBM (bandwidth bound; the
 // G query heads of a kv head share each row, 4*d flops per 2*d bytes at
 // G = 4), so it runs on the SIMT cores:
-//   partial  grid (chunks of 512 rows, heads): each CTA's 4 warps take
+//   partial  grid (chunks of 1024 rows, heads): each CTA's 4 warps take
 //            16-row groups; K rows are read by 8-lane teams (16-byte
 //            coalesced loads), the 8 partial dot products are reduced by
 //            xor-shuffles, an online softmax (base 2) keeps (m, l) per head,
@@ -31,7 +31,7 @@
 namespace kvc {
 namespace {
 
-constexpr int kChunk = 512;     // rows per partial CTA
+constexpr int kChunk = 1024;    // rows per partial CTA (512 measured 3 % slower on the batch-64 step)
 constexpr int kQ8Chunk = 2048;  // rows per partial CTA over a quantised pool
 constexpr int kWarps = 4;       // compute warps per partial CTA
 constexpr int kStageRows = 32;  // rows per shared-memory stage (8 per compute warp)
@@ -130,7 +130,7 @@ constexpr size_t partial_smem_bytes() {
   return 2ull * kStages * kStageRows * D * sizeof(Tin);
 }
 
-// One CTA per (kv head, 512-row chunk).  A producer warp streams the chunk's
+// One CTA per (kv head, 1024-row chunk).  A producer warp streams the chunk's
 // K and V rows (contiguous in the pool) into a 4-stage shared-memory ring
 // with bulk asynchronous copies; four compute warps take 8 rows of every
 // stage each.
@@ -543,7 +543,7 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
   int na = napprox[i];
   if (na < 0 || na > L) { if (x == 0) report(status, KVC_ERR_RANGE); na = na < 0 ? 0 : L; }
   const int ne = L - na;
-  const int cha = (na + 2 * kChunk - 1) / (2 * kChunk);    // chunks of 1024 approximated rows
+  const int cha = (na + 2 * kChunk - 1) / (2 * kChunk);    // chunks of 2048 approximated rows
   int nch = cha + (ne + kChunk - 1) / kChunk;
   if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
   const bool append = k_new != nullptr;

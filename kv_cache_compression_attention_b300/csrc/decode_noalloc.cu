@@ -2,7 +2,7 @@
 // callers that cannot allocate device memory.
 //
 // kvc_decode_attn takes its split-K scratch (one (acc[d], max, sum) record
-// per q head and 512-row chunk) from a workspace the caller allocates.  Some
+// per q head and 1024-row chunk) from a workspace the caller allocates.  Some
 // callers have no way to do that: a plug-in loaded into a host engine that
 // owns every device allocation and hands its plug-ins no allocator and no
 // workspace, or a caller whose device-memory budget is fixed at start-up and

@@ -167,7 +167,7 @@ def test_compact_and_decode_reject_bad_arguments(lib):
 def test_workspace_queries_are_pure_host(lib):
     assert lib.kvc_select_workspace(1, 8, 32768, 0) == 0
     n = lib.kvc_decode_workspace(64, 32, 8, 128, 10086, 1)
-    chunks = (10086 + 511) // 512
+    chunks = (10086 + 1023) // 1024
     assert n == 64 * 8 * chunks * 4 * (128 + 2) * 4
     # tensor-core scoring path: per-CTA row partials (2 buffers x 1024 CTAs x G*W rows,
     # each (max, sum) as two tagged 64-bit words), independent of U and T; the SIMT
@@ -263,7 +263,7 @@ def test_vector_entry_points_reject_bad_arguments(lib):
     # one more split-K chunk than the plain decode: approximated and exact rows
     # are chunked apart
     assert lib.kvc_decode_vector_workspace(64, 32, 8, 128, 10086) == \
-        64 * 8 * (20 + 1) * 4 * 130 * 4
+        64 * 8 * (10 + 1) * 4 * 130 * 4
 
 
 def test_score_mlp_rejects_bad_arguments(lib):

@@ -234,9 +234,9 @@ def test_bounded_wait_times_out_and_context_survives(B):
 
 
 def test_decode_more_chunks_than_the_combine_stages(B):
-    """A head of 140 000 rows has 274 chunks of 512, more than the combine
+    """A head of 280 000 rows has 274 chunks of 1024, more than the combine
     kernel stages in shared memory (256): the second merge path runs."""
-    L = 140000
+    L = 280000
     kc, vc, start, lens = pool([L], 1, 128, torch.bfloat16, 17)
     g = torch.Generator().manual_seed(18)
     q = torch.randn((1, 2, 128), generator=g).to(torch.bfloat16)

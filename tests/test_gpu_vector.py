@@ -203,7 +203,8 @@ def test_vector_residual_edges(B):
 @pytest.mark.parametrize("append", [True, False])
 def test_decode_vector_small(B, G, append):
     n_sink, n_recent, slack = 4, 16, 2
-    # a long pool so that heads span several 512-row chunks of both kinds
+    # a long pool so that heads span several chunks of both kinds (1024 exact,
+    # 2048 approximated rows)
     k, v, W, kept, counts, offsets = small_case(83 + G, U=2, Hkv=2, T=2600, keep=0.9,
                                                 n_sink=n_sink, n_recent=n_recent)
     U, Hkv, T, d = k.shape
@@ -347,8 +348,8 @@ def test_decode_vector_batch64_sampled(B):
 
 def test_decode_vector_many_chunks(B):
     """A head with more split-K chunks than the merge stages in shared memory
-    (36 000 approximated + 36 000 exact rows: 36 + 71 chunks)."""
-    d, G, na, ne = 128, 2, 36000, 36000
+    (72 000 approximated + 72 000 exact rows: 36 + 71 chunks)."""
+    d, G, na, ne = 128, 2, 72000, 72000
     g = torch.Generator().manual_seed(95)
     kc = torch.randn((na + ne + 1, d), generator=g).to(torch.bfloat16)
     vc = torch.randn((ne + 1, d), generator=g).to(torch.bfloat16)

@@ -35,10 +35,10 @@ def test_noalloc_refuses_on_the_host():
     assert limit == 16 << 20
     P = ctypes.c_void_p(16)
     f = lib.kvc_decode_attn_noalloc
-    # 64 x 8 kv heads, G = 4, d = 128: 7680 rows fit, 7681 rows do not
-    ok_need = lib.kvc_decode_workspace(64, 32, 8, 128, 7680, 1)
-    assert ok_need <= limit < lib.kvc_decode_workspace(64, 32, 8, 128, 7681, 1)
-    assert f(P, P, P, P, P, None, None, 1, 64, 32, 8, 128, 7681, 0.1, P, P, None) == -3
+    # 64 x 8 kv heads, G = 4, d = 128: 15360 rows fit, 15361 rows do not
+    ok_need = lib.kvc_decode_workspace(64, 32, 8, 128, 15360, 1)
+    assert ok_need <= limit < lib.kvc_decode_workspace(64, 32, 8, 128, 15361, 1)
+    assert f(P, P, P, P, P, None, None, 1, 64, 32, 8, 128, 15361, 0.1, P, P, None) == -3
     assert f(None, P, P, P, P, None, None, 1, 64, 32, 8, 128, 64, 0.1, P, P, None) == -1
     assert f(P, P, P, P, P, None, None, 1, 0, 32, 8, 128, 64, 0.1, P, P, None) == -1
 
