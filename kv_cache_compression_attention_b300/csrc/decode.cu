@@ -365,21 +365,14 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
                       uint8_t* __restrict__ kq, uint32_t* __restrict__ kp,
                       uint8_t* __restrict__ vq, uint32_t* __restrict__ vp, int chunk) {
   __shared__ float red[D / 32][G];
-  pdl_wait();
-  pdl_trigger();
   const int i = blockIdx.x;
   const int u = i / Hkv, g = i - u * Hkv;
   const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
-  const int L = len[i];
-  int nch = (L + chunk - 1) / chunk;
-  if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
   const bool append = k_new != nullptr;
-  bool room = append;
-  if (append && i + 1 < n_heads && start[i] + L >= start[i + 1]) {
-    if (x == 0) report(status, KVC_ERR_RANGE);
-    room = false;
-  }
   const int64_t nrow = (int64_t)u * Hkv + g;
+  // The step's own inputs (q, k_new, v_new: no kernel writes them) are read
+  // and the appended token's scores formed before waiting on the partial
+  // kernel, so that this work overlaps its tail.
   const float kn = append ? Elt<Tin>::get(k_new + nrow * D, x) : 0.0f;
   const float vn = append ? Elt<Tin>::get(v_new + nrow * D, x) : 0.0f;
   // appended-token scores for the G heads
@@ -399,6 +392,20 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
     for (int w = 0; w < D / 32; ++w) a += red[w][h];
     snew[h] = a * scale_log2;
   }
+  // the head's length too: the previous kernels that write it (this
+  // library's appends and prunes of earlier steps) completed before the
+  // partial kernel let this one start, so it is final (read from L2, past
+  // any line an earlier kernel left in this SM's L1)
+  const int L = __ldcg(len + i);
+  int nch = (L + chunk - 1) / chunk;
+  if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
+  bool room = append;
+  if (append && i + 1 < n_heads && start[i] + L >= start[i + 1]) {
+    if (x == 0) report(status, KVC_ERR_RANGE);
+    room = false;
+  }
+  pdl_wait();
+  pdl_trigger();
   const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
   if (nch <= kStagedChunks) {
     // every chunk's (max, sum) of every head into shared memory (all loads
@@ -411,6 +418,14 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
       s_w[e] = pc[D];
       s_l[e] = pc[D + 1];
     }
+    // column x of the first kEarly chunks, in flight with the statistics
+    constexpr int kEarly = 8;
+    float pe[kEarly][G];
+#pragma unroll
+    for (int c = 0; c < kEarly; ++c)
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        pe[c][h] = c < nch ? base[(int64_t)(c * G + h) * (D + 2) + x] : 0.0f;
     __syncthreads();
     for (int h = warp; h < G; h += D / 32) {
       float M = append ? snew[h] : -INFINITY;
@@ -438,8 +453,14 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
     float acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kEarly; ++c)
+      if (c < nch) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(s_w[c * G + h], pe[c][h], acc[h]);
+      }
 #pragma unroll 4
-    for (int c = 0; c < nch; ++c) {
+    for (int c = kEarly; c < nch; ++c) {
       float pv[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) pv[h] = base[(int64_t)(c * G + h) * (D + 2) + x];
