@@ -400,7 +400,7 @@ decode_combine_kernel(const Tin* __restrict__ q, Tin* __restrict__ kc, Tin* __re
   int nch = (L + chunk - 1) / chunk;
   if (nch > max_chunks) { if (x == 0) report(status, KVC_ERR_RANGE); nch = max_chunks; }
   bool room = append;
-  if (append && i + 1 < n_heads && start[i] + L >= start[i + 1]) {
+  if (append && i + 1 < n_heads && __ldcg(start + i) + L >= __ldcg(start + i + 1)) {
     if (x == 0) report(status, KVC_ERR_RANGE);
     room = false;
   }
@@ -558,10 +558,12 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
     mmasync::cp_async16(smem_u32(w_sm + r * WS + ch * 8), W + ((int64_t)g * D + r) * D + ch * 8, 16u);
   }
   mmasync::cp_commit();
-  pdl_wait();
-  pdl_trigger();
-  const int L = klen[i];
-  int na = napprox[i];
+  // nor do the step's inputs (q, k_new, v_new) or the head's lengths: the
+  // kernels that write klen (appends of earlier steps) completed before the
+  // partial kernel let this one start (read from L2, past any line an
+  // earlier kernel left in this SM's L1)
+  const int L = __ldcg(klen + i);
+  int na = __ldcg(napprox + i);
   if (na < 0 || na > L) { if (x == 0) report(status, KVC_ERR_RANGE); na = na < 0 ? 0 : L; }
   const int ne = L - na;
   const int cha = (na + 2 * kChunk - 1) / (2 * kChunk);    // chunks of 2048 approximated rows
@@ -570,7 +572,8 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
   const bool append = k_new != nullptr;
   bool room = append;
   if (append && i + 1 < n_heads &&
-      (kstart[i] + L >= kstart[i + 1] || vstart[i] + ne >= vstart[i + 1])) {
+      (__ldcg(kstart + i) + L >= __ldcg(kstart + i + 1) ||
+       __ldcg(vstart + i) + ne >= __ldcg(vstart + i + 1))) {
     if (x == 0) report(status, KVC_ERR_RANGE);
     room = false;
   }
@@ -593,6 +596,8 @@ decode_combine_vector_kernel(const uint16_t* __restrict__ q, uint16_t* __restric
     for (int w = 0; w < D / 32; ++w) a += red[w][h];
     snew[h] = a * scale_log2;
   }
+  pdl_wait();
+  pdl_trigger();
   const float* base = ws + (int64_t)i * max_chunks * G * (D + 2);
   float av[G], M[G], lsum[G];
   if (nch <= kVecStaged) {
