@@ -874,9 +874,15 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   auto smem_for = [&](int c) {
     return shared_bytes((T + c - 1) / c, hps, vec_for(c), lens != nullptr);
   };
-  // the smallest cluster that keeps <= 16K keys per CTA, else the smallest that fits
+  // the smallest cluster that keeps <= per_cta keys per CTA, else the smallest that fits
   int C = 1;
-  while (C < 16 && (pool + C - 1) / C > 16384) C *= 2;
+  // keys per CTA: a threshold pool has no radix passes, so a wider cluster
+  // only divides its sweep (16 CTAs of <= 4096 keys: 14.8 -> 12.7 us on four
+  // 131 072-key pools); the radix passes of the other modes pay a cluster
+  // exchange each, and more, smaller clusters keep more SMs busy (16-CTA
+  // clusters for the 32-layer pools: 181 -> 320 us)
+  const int64_t per_cta = mode == KVC_SEL_THRESHOLD ? 4096 : 16384;
+  while (C < 16 && (pool + C - 1) / C > per_cta) C *= 2;
   while (C < 16 && smem_for(C) > smem_max) C *= 2;
   if (smem_for(C) > smem_max) return lens ? KVC_ERR_UNSUPPORTED : stream();
   Args a;
