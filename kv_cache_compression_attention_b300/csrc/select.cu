@@ -877,8 +877,9 @@ int select_launch_ex(const float* scores, int U, int Hkv, int T, int mode, int64
   // the smallest cluster that keeps <= per_cta keys per CTA, else the smallest that fits
   int C = 1;
   // keys per CTA: a threshold pool has no radix passes, so a wider cluster
-  // only divides its sweep (16 CTAs of <= 4096 keys: 14.8 -> 12.7 us on four
-  // 131 072-key pools); the radix passes of the other modes pay a cluster
+  // only divides its sweep (four 131 072-key pools in 16-CTA clusters of 8192
+  // keys per CTA instead of 8-CTA clusters of 16 K: 14.8 -> 12.7 us); the
+  // radix passes of the other modes pay a cluster
   // exchange each, and more, smaller clusters keep more SMs busy (16-CTA
   // clusters for the 32-layer pools: 181 -> 320 us)
   const int64_t per_cta = mode == KVC_SEL_THRESHOLD ? 4096 : 16384;
