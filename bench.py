@@ -9,7 +9,9 @@ ratio 0.10, 4 sinks + 64 recent always kept).  A step is one pass of
 kvc_score_attn -> kvc_select_compact (the selection and the compaction in
 one call, outputs identical to kvc_select -> kvc_compact, which is timed
 too: step_three_calls_us) over that cache; inputs are resident in HBM; L2
-is flushed (256 MiB write) between steps, outside the step's CUDA events.
+is flushed between steps, outside the step's CUDA events (a 256 MiB
+read + write, then a 256 MiB read that writes the flush's own dirty lines
+back before the step).
 The same JSON line also reports:
 
 * roofline: the dominant kernel (tensor-core scoring) against the measured
@@ -183,8 +185,27 @@ class LayerWorkload:
 RAMP_STEPS = 200      # untimed steps (~30 ms of GPU time) before a layer bench's warm-up
 
 
+_CLEAN = {}
+
+
 def flush_l2(buf):
-    buf.add_(1)          # 256 MiB read + write, larger than the 126 MB L2
+    """Evict everything from L2 between timed steps.  A 256 MiB read + write
+    (larger than the 126 MB L2) leaves L2 full of dirty lines of `buf`; a
+    256 MiB read of a second buffer then writes those back here, so that the
+    next step's timed region does not pay the flush's write-backs (≈ 126 MB
+    of DRAM writes: 5.2 against 5.65 TB/s on the 940 MB linear scorer).
+    Either way no input of the step is left in L2.
+
+    Last, the stream is held for 10^6 GPU cycles (≈ 0.5 ms, a bounded spin)
+    so that the host has queued the whole step before the GPU reaches it:
+    the step's CUDA events then time its kernels, not the Python launch path
+    (which, on a busy host, fell behind the five-launch VECTOR step)."""
+    buf.add_(1)
+    c = _CLEAN.get(buf.device)
+    if c is None:
+        c = _CLEAN[buf.device] = (torch.zeros_like(buf), torch.empty(1, device=buf.device))
+    torch.sum(c[0], dim=0, keepdim=True, out=c[1])
+    torch.cuda._sleep(1_000_000)
 
 
 def bench_layer(B, w, steps, warmup, device):
@@ -1156,7 +1177,8 @@ def main():
         "data": "synthetic (seeded; Llama-3-8B-shaped layer cache at 32k tokens)",
         "config": {"workload": WORKLOAD, "U": w.U, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
                    "T": w.T, "W": w.W, "keep_ratio": w.keep_ratio, "n_sink": w.n_sink,
-                   "n_recent": w.n_recent, "l2": "flushed between steps (256 MiB write)",
+                   "n_recent": w.n_recent,
+                   "l2": "flushed between steps (256 MiB read + write, then a 256 MiB read)",
                    "clock_ramp_steps": RAMP_STEPS,
                    "parallelism": f"replicas x{world}"},
         # stage times from a separate run with events between the kernels
