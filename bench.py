@@ -95,6 +95,7 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.first = ""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
@@ -102,6 +103,13 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+        # nvidia-smi takes a moment to start: the timed work begins only once
+        # its first sample is in (waiting 10 s at most)
+        import select
+        ready, _, _ = select.select([self.proc.stdout], [], [], 10.0)
+        if ready:
+            self.first = self.proc.stdout.readline()
         return self
 
     def __exit__(self, *exc):
@@ -109,7 +117,8 @@ class ClockSampler:
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                rest, _ = self.proc.communicate(timeout=5)
+                self.out = self.first + (rest or "")
             except Exception:
                 self.proc.kill()
                 self.out = ""
