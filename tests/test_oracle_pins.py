@@ -360,6 +360,29 @@ def test_select_per_head_matches_brute_force(seed):
     assert kept_lists(kept, counts) == brute_select_per_head(s, budgets, 1, 4)
 
 
+def test_protected_mask_closed_forms():
+    """The always-kept tokens: the first n_sink and the last n_recent
+    positions, with the two ranges overlapping when they cover T."""
+    T_, F_ = True, False
+    assert O.protected_mask(10, 2, 3).tolist() == [T_, T_, F_, F_, F_, F_, F_, T_, T_, T_]
+    assert O.protected_mask(5, 3, 4).all()
+    assert not O.protected_mask(6, 0, 0).any()
+    assert O.protected_mask(4, 0, 1).tolist() == [F_, F_, F_, T_]
+    assert O.protected_mask(4, 1, 0).tolist() == [T_, F_, F_, F_]
+
+
+def test_global_budget_one_double_rounding():
+    """B = floor(ratio * Hkv * T), the product rounded once in IEEE double:
+    0.1 of 8 x 32768 keys is 26214.4 -> 26214; 0.29 * 100 is
+    28.999999999999996 in double -> 28 (not 29); exact products stay exact."""
+    assert O.global_budget(0.10, 8, 32768) == 26214
+    assert O.global_budget(0.25, 4, 1024) == 1024
+    assert O.global_budget(0.29, 1, 100) == 28
+    assert O.global_budget(0.7, 1, 10) == 7
+    assert O.global_budget(0.0, 8, 32768) == 0
+    assert O.global_budget(1.0, 8, 32768) == 8 * 32768
+
+
 def test_select_threshold_exact_set():
     from kv_cache_compression_attention_b300 import inputs
     s = inputs.random_scores((2, 2, 40), seed=3, ties=True, specials=True).numpy()
