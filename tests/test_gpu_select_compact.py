@@ -62,6 +62,18 @@ def test_select_global_small(B, shape, ties, specials):
         check_same(got, ref)
 
 
+def test_select_global_budget_rounds_once_in_double(B):
+    """The library's budget is floor(ratio * Hkv * T) with the product
+    rounded once in double, as the oracle's: 0.29 of 100 keys is
+    28.999999999999996 there, so 28 keys are kept, not 29 (and 0.57 of them
+    56.99999999999999: 56 kept)."""
+    s = inputs.random_scores((2, 1, 100), seed=29)
+    for ratio, want in [(0.29, 28), (0.57, 56), (0.1, 10)]:
+        got = gpu_select(B, s.cuda(), "global", keep_ratio=ratio)
+        assert (got[1] == want).all()
+        check_same(got, O.select(s.numpy(), "global", keep_ratio=ratio))
+
+
 @pytest.mark.parametrize("shape", [(2, 3, 777), (1, 8, 4096)])
 def test_select_per_head_and_threshold_small(B, shape):
     s = inputs.random_scores(shape, seed=5, ties=True, specials=True)
