@@ -423,9 +423,10 @@ size_t head_bytes(int Hkv) { return sizeof(SmemHead) + 3 * 128 * (size_t)Hkv * 4
 // CTAs per cluster.  The kernel can run as pairs that share every W1t slab
 // (each CTA loads half of it and multicasts it to both), which halves the L2
 // reads of the first-layer weight; on the 128k layer that measured 406 us
-// against 392 us for single CTAs: the kernel is held by the latency of each
-// stage's loads, not by L2 bandwidth (ncu: L2 29 %, DRAM 32 %, tensor pipe
-// 48 %), so single CTAs are launched.
+// against 392 us for single CTAs (ncu: L2 29 %, DRAM 32 %, tensor pipe 48 %),
+// so single CTAs are launched.  Neither L2 bandwidth nor the DRAM latency of
+// the hidden rows holds the kernel: fetching each stage's hidden rows into L2
+// eight k-blocks ahead of their load made it slower (324 against 314 us).
 int cluster_size(int n_tiles, int sms) {
   (void)n_tiles;
   (void)sms;
